@@ -1,0 +1,137 @@
+"""Pins for the oracle's quantizers (CPU only)."""
+import numpy as np
+import pytest
+
+from oracle import formats as F
+from oracle import quant as Q
+from oracle import products as P
+from tests.conftest import load_golden, golden_float
+import synth
+
+
+def _golden_W(name):
+    g = load_golden(name)
+    W = np.array([[golden_float(v) for v in row] for row in g["W"]], dtype=np.float32)
+    return g, W
+
+
+def test_nvfp4_hand_example():
+    g, W = _golden_W("nvfp4_hand.json")
+    codes, scales, s_t = Q.nvfp4_quantize(W)
+    assert s_t == np.float32(g["s_t"])
+    assert codes.tolist() == g["codes"]
+    assert scales.tolist() == g["scales"]
+    w_hat = P.nvfp4_dequantize(codes, scales, s_t)
+    assert list(w_hat[1]) == g["w_hat_row1"]
+
+
+def test_mxfp4_hand_example():
+    g, W = _golden_W("mxfp4_hand.json")
+    codes, scales = Q.mxfp4_quantize(W)
+    assert scales.tolist() == g["scales"]
+    assert codes.tolist() == g["codes"]
+
+
+def test_fp8_hand_example():
+    g, W = _golden_W("fp8_hand.json")
+    codes, s_r = Q.fp8_rowwise_quantize(W)
+    assert s_r.tolist() == g["row_scale"]
+    assert codes.tolist() == g["codes"]
+
+
+@pytest.fixture(scope="module")
+def W_rand():
+    W = synth.weight_fp32((96, 512), seed=7, index=0).numpy()
+    W[3, :16] = 0.0                            # an all-zero block
+    W[5, 16:32] *= 1e-6                        # a block far below the others
+    W[7, 40] = 0.5                             # an outlier
+    return W
+
+
+def test_nvfp4_invariants(W_rand):
+    codes, scales, s_t = Q.nvfp4_quantize(W_rand)
+    assert codes.shape == (96, 256) and scales.shape == (96, 32)
+    q = F.e2m1_decode(Q.unpack_nibbles(codes)).reshape(96, 32, 16)
+    sb = F.e4m3_decode(scales)
+    amax_b = np.abs(W_rand.reshape(96, 32, 16)).max(axis=2)
+    normal = (scales & 0x78) != 0
+    # the largest weight of every block with a normal scale maps to |q| = 6
+    assert np.all(np.abs(q).max(axis=2)[normal & (amax_b > 0)] == 6.0)
+    assert np.nanmax(sb) <= 448.0
+    # the block holding the tensor amax gets the top of E4M3's range
+    r, c = np.unravel_index(np.argmax(np.abs(W_rand)), W_rand.shape)
+    assert sb[r, c // 16] >= 416.0
+    # zero block -> zero scale code and zero codes
+    assert scales[3, 0] == 0 and np.all(q[3, 0] == 0)
+    # |w - w_hat| <= d_b for blocks with a normal scale
+    w_hat = P.nvfp4_dequantize(codes, scales, s_t).reshape(96, 32, 16)
+    d_b = (sb.astype(np.float32) * s_t).astype(np.float64)
+    err = np.abs(W_rand.reshape(96, 32, 16) - w_hat)
+    assert np.all(err[normal] <= d_b[normal][:, None])
+    # byte count: 4 + 8/16 bits per weight
+    assert codes.nbytes + scales.nbytes == 96 * 512 * 4.5 / 8
+
+
+def test_nvfp4_requantize_is_identity(W_rand):
+    codes, scales, s_t = Q.nvfp4_quantize(W_rand)
+    w_hat = P.nvfp4_dequantize(codes, scales, s_t).astype(np.float32)
+    # re-encode w_hat under the same scales: w_hat / d_b is the grid value
+    d_b = (F.e4m3_decode(scales).astype(np.float32) * s_t).astype(np.float32)
+    ratio = (w_hat.reshape(96, 32, 16) / d_b[..., None]).astype(np.float32)
+    q2 = np.where((d_b > 0)[..., None], F.e2m1_encode(ratio), 0)
+    q1 = Q.unpack_nibbles(codes).reshape(96, 32, 16)
+    same = (q1 & 7) == (q2 & 7)
+    assert np.all(same)
+
+
+def test_nvfp4_outlier_only_coarsens_its_block():
+    W = synth.weight_fp32((1, 64), seed=3).numpy()
+    c0, s0, t0 = Q.nvfp4_quantize(W, s_t=np.float32(1.0 / 2688))
+    W2 = W.copy()
+    W2[0, 5] = 50 * np.abs(W).max()
+    c1, s1, t1 = Q.nvfp4_quantize(W2, s_t=np.float32(1.0 / 2688))
+    assert np.array_equal(s0[0, 1:], s1[0, 1:])
+    assert np.array_equal(c0[0, 8:], c1[0, 8:])
+
+
+def test_nvfp4_zero_tensor():
+    codes, scales, s_t = Q.nvfp4_quantize(np.zeros((4, 32), np.float32))
+    assert s_t == 1.0 and not codes.any() and not scales.any()
+
+
+def test_mxfp4_grid_roundtrip():
+    rng = np.random.default_rng(5)
+    grid = F.e2m1_decode(np.arange(16))
+    for k in (-20, -3, 0, 7, 100):
+        vals = rng.choice(grid, size=(4, 64)).astype(np.float64)
+        vals[:, ::32] = 6.0                    # pin amax = 6*2^k
+        W = np.ldexp(vals, k).astype(np.float32)
+        codes, scales = Q.mxfp4_quantize(W)
+        assert np.all(scales == 127 + k)
+        assert np.array_equal(P.mxfp4_dequantize(codes, scales), W.astype(np.float64))
+
+
+def test_mxfp4_scale_rule(W_rand):
+    codes, scales = Q.mxfp4_quantize(W_rand)
+    amax = np.abs(W_rand.reshape(96, 16, 32)).max(axis=2)
+    e = scales.astype(np.int64) - 127
+    nz = amax > 0
+    # 2^(e+2) <= amax < 2^(e+3): the block amax lands in [4, 8) before clipping
+    assert np.all(np.ldexp(1.0, e[nz] + 2) <= amax[nz])
+    assert np.all(amax[nz] < np.ldexp(1.0, e[nz] + 3))
+    w_hat = P.mxfp4_dequantize(codes, scales)
+    assert np.all(np.abs(w_hat) <= np.ldexp(6.0, e).repeat(32, axis=1) + 0)
+
+
+def test_fp8_row_max_encodes_near_448(W_rand):
+    codes, s_r = Q.fp8_rowwise_quantize(W_rand)
+    W = W_rand
+    for i in range(W.shape[0]):
+        j = np.argmax(np.abs(W[i]))
+        c = codes[i, j] & 0x7F
+        # 0x7E unless fl32 rounding of s_r pushes amax/s_r just above 448
+        assert c == 0x7E
+    w_hat = P.fp8_dequantize(codes, s_r)
+    rel = np.abs(W - w_hat) / np.maximum(np.abs(W), 1e-30)
+    normal = np.abs(W) >= (2.0 ** -6) * s_r[:, None]
+    assert np.all(rel[normal] <= 2.0 ** -4 + 1e-7)
