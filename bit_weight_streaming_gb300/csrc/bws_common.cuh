@@ -1,0 +1,161 @@
+// Shared device helpers of the weight-stream kernels (sm_103a).
+#pragma once
+#include <cuda_runtime.h>
+#include <cuda_fp16.h>
+#include <cuda_bf16.h>
+#include <stdint.h>
+
+#define BWS_DEV __device__ __forceinline__
+
+namespace bws {
+
+// ---- programmatic dependent launch ---------------------------------------
+// A kernel calls pdl_launch_dependents() early so the next kernel in the
+// stream may be scheduled while it runs, and pdl_wait() before it reads
+// anything an earlier kernel wrote (it returns once the preceding grid has
+// completed and its writes are visible).
+BWS_DEV void pdl_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+BWS_DEV void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+// ---- loads ----------------------------------------------------------------
+// Weights are read exactly once per step: stream them past L1.
+BWS_DEV uint4 ld_stream_v4(const void* p) {
+  uint4 v;
+  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "l"(p));
+  return v;
+}
+BWS_DEV uint2 ld_stream_v2(const void* p) {
+  uint2 v;
+  asm volatile("ld.global.nc.L1::no_allocate.v2.u32 {%0,%1}, [%2];"
+               : "=r"(v.x), "=r"(v.y) : "l"(p));
+  return v;
+}
+BWS_DEV uint32_t ld_stream_u16(const void* p) {
+  unsigned short v;
+  asm volatile("ld.global.nc.L1::no_allocate.u16 %0, [%1];" : "=h"(v) : "l"(p));
+  return v;
+}
+BWS_DEV uint32_t ld_stream_u8(const void* p) {
+  unsigned short v;
+  asm volatile("ld.global.nc.L1::no_allocate.u8 %0, [%1];" : "=h"(v) : "l"(p));
+  return v;
+}
+// Activations are small and shared by every warp: keep them in L1.
+BWS_DEV uint4 ld_act_v4(const void* p) {
+  uint4 v;
+  asm volatile("ld.global.nc.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "l"(p));
+  return v;
+}
+// L2 prefetch of a 16-byte aligned range whose size is a multiple of 16.
+BWS_DEV void prefetch_l2_bulk(const void* p, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" :: "l"(p), "r"(bytes) : "memory");
+}
+// Coherent (L1-bypassing) load of data another SM wrote in this grid.
+BWS_DEV float4 ld_cg_f4(const float4* p) {
+  float4 v;
+  asm volatile("ld.global.cg.v4.f32 {%0,%1,%2,%3}, [%4];"
+               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w) : "l"(p));
+  return v;
+}
+
+// ---- conversions (hardware, exact for these inputs) ------------------------
+// Two E2M1 codes in one byte -> f16x2. Every E2M1 value is exact in f16.
+BWS_DEV uint32_t e2m1x2_to_f16x2(uint32_t byte_in_low8) {
+  uint32_t r;
+  asm("{ .reg .b8 b; cvt.u8.u32 b, %1; cvt.rn.f16x2.e2m1x2 %0, b; }" : "=r"(r) : "r"(byte_in_low8));
+  return r;
+}
+// Two E4M3 codes in 16 bits -> f16x2. Every E4M3 value is exact in f16.
+BWS_DEV uint32_t e4m3x2_to_f16x2(uint32_t two_bytes_in_low16) {
+  uint32_t r;
+  asm("{ .reg .b16 h; cvt.u16.u32 h, %1; cvt.rn.f16x2.e4m3x2 %0, h; }" : "=r"(r) : "r"(two_bytes_in_low16));
+  return r;
+}
+// Unpack the 4 bytes of a word, and convert each byte's two E2M1 codes.
+BWS_DEV void e2m1x8_to_f16x2x4(uint32_t w, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
+  asm("{ .reg .b8 b0, b1, b2, b3;\n"
+      "  mov.b32 {b0, b1, b2, b3}, %4;\n"
+      "  cvt.rn.f16x2.e2m1x2 %0, b0;\n"
+      "  cvt.rn.f16x2.e2m1x2 %1, b1;\n"
+      "  cvt.rn.f16x2.e2m1x2 %2, b2;\n"
+      "  cvt.rn.f16x2.e2m1x2 %3, b3; }"
+      : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3) : "r"(w));
+}
+BWS_DEV void e4m3x4_to_f16x2x2(uint32_t w, uint32_t& r0, uint32_t& r1) {
+  asm("{ .reg .b16 h0, h1;\n"
+      "  mov.b32 {h0, h1}, %2;\n"
+      "  cvt.rn.f16x2.e4m3x2 %0, h0;\n"
+      "  cvt.rn.f16x2.e4m3x2 %1, h1; }"
+      : "=r"(r0), "=r"(r1) : "r"(w));
+}
+// Encoders with round-to-nearest-even and saturation to the largest finite
+// value. The first source operand lands in the upper part of the result.
+BWS_DEV uint32_t f32x2_to_e2m1x2(float hi, float lo) {
+  uint32_t r;
+  asm("{ .reg .b8 b; cvt.rn.satfinite.e2m1x2.f32 b, %1, %2; cvt.u32.u8 %0, b; }"
+      : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+BWS_DEV uint32_t f32x2_to_e4m3x2(float hi, float lo) {
+  unsigned short r;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+BWS_DEV float e4m3_to_f32(uint32_t code) {
+  uint32_t h = e4m3x2_to_f16x2(code & 0xFF);
+  return __half2float(__ushort_as_half((unsigned short)(h & 0xFFFF)));
+}
+
+BWS_DEV uint32_t hmul2_u32(uint32_t a, uint32_t b) {
+  uint32_t r;
+  asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+  return r;
+}
+// Broadcast the low / high f16 of a pair to both halves.
+BWS_DEV uint32_t bcast_lo(uint32_t x) { return __byte_perm(x, 0, 0x1010); }
+BWS_DEV uint32_t bcast_hi(uint32_t x) { return __byte_perm(x, 0, 0x3232); }
+
+// D += A * B, A 16x16 f16 (row), B 16x8 f16 (col), D 16x8 f32.
+BWS_DEV void mma_f16_16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                           uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// Exact power of two as FP32 (e in [-149, 127]); 0 below.
+BWS_DEV float exp2i(int e) {
+  if (e >= -126) return __int_as_float((e + 127) << 23);
+  if (e >= -149) return __int_as_float(1 << (e + 149));
+  return 0.0f;
+}
+// x * 2^e exactly (up to the final rounding of an out-of-range result).
+BWS_DEV float ldexp_exact(float x, int e) {
+  int a = e > 127 ? 127 : (e < -126 ? -126 : e);
+  int b = e - a;
+  b = b > 127 ? 127 : (b < -126 ? -126 : b);
+  return __fmul_rn(__fmul_rn(x, exp2i(a)), exp2i(b));
+}
+// floor(log2 |x|) for finite x != 0, exact for subnormals.
+BWS_DEV int floor_log2_abs(float x) {
+  uint32_t b = __float_as_uint(x) & 0x7FFFFFFFu;
+  int e = (int)(b >> 23);
+  if (e > 0) return e - 127;
+  return (31 - __clz((int)b)) - 149;
+}
+
+BWS_DEV float warp_max(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+  return v;
+}
+BWS_DEV float warp_sum(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+
+}  // namespace bws

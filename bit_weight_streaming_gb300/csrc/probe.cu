@@ -1,0 +1,45 @@
+// Measurement kernels: an HBM read probe and an L2 flush.
+#include "bws_common.cuh"
+#include "bws_internal.h"
+
+namespace bws {
+
+// Streaming read of every 16-byte word, XOR-folded so the loads cannot be
+// dropped; one atomic per CTA.
+__global__ void __launch_bounds__(512) hbm_read_probe_kernel(const uint4* __restrict__ src, size_t n16,
+                                                             uint32_t* __restrict__ out) {
+  uint32_t acc = 0;
+  size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x;
+  const size_t stride = (size_t)gridDim.x * blockDim.x;
+  for (; i + 3 * stride < n16; i += 4 * stride) {
+    const uint4 a = ld_stream_v4(src + i);
+    const uint4 b = ld_stream_v4(src + i + stride);
+    const uint4 c = ld_stream_v4(src + i + 2 * stride);
+    const uint4 d = ld_stream_v4(src + i + 3 * stride);
+    acc ^= a.x ^ a.y ^ a.z ^ a.w ^ b.x ^ b.y ^ b.z ^ b.w ^ c.x ^ c.y ^ c.z ^ c.w ^ d.x ^ d.y ^ d.z ^ d.w;
+  }
+  for (; i < n16; i += stride) {
+    const uint4 a = ld_stream_v4(src + i);
+    acc ^= a.x ^ a.y ^ a.z ^ a.w;
+  }
+  acc = __reduce_xor_sync(0xffffffffu, acc);
+  if ((threadIdx.x & 31) == 0) atomicXor(out, acc);
+}
+
+__global__ void __launch_bounds__(512) l2_flush_kernel(uint4* __restrict__ buf, size_t n16, uint32_t salt) {
+  for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n16; i += (size_t)gridDim.x * blockDim.x)
+    buf[i] = make_uint4(salt, (uint32_t)i, salt, (uint32_t)(i >> 32));
+}
+
+cudaError_t launch_hbm_read_probe(const void* src, size_t n_bytes, uint32_t* out, cudaStream_t st) {
+  hbm_read_probe_kernel<<<num_sms() * 4, 512, 0, st>>>(reinterpret_cast<const uint4*>(src), n_bytes / 16, out);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_l2_flush(void* buf, size_t n_bytes, cudaStream_t st) {
+  static uint32_t salt = 1;
+  l2_flush_kernel<<<num_sms() * 4, 512, 0, st>>>(reinterpret_cast<uint4*>(buf), n_bytes / 16, salt++);
+  return cudaGetLastError();
+}
+
+}  // namespace bws

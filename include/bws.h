@@ -1,0 +1,173 @@
+/*
+ * bws.h -- C ABI of the decode-step weight stream (GB300 / sm_103a).
+ *
+ * The library streams block-scaled 4-bit (NVFP4, MXFP4) and 8-bit (FP8 E4M3)
+ * weights against BF16 activations with FP32 accumulation: the batch-1 and
+ * speculative-verify (N <= 8 token) decode step whose time is set by the
+ * bytes of weights read ([Spark27B] "Decode speed is bytes divided by
+ * bandwidth"; [LingMoE] sections 4 and 5).
+ *
+ * Page names used in the citations below:
+ *   [Spark27B] mdjawad.com, DGX Spark post on Qwen3.8-27B NVFP4 decoding
+ *   [LingMoE]  magicnetworld.com, reading of NVIDIA's "3 Ways to Boost MoE
+ *              Inference on NVIDIA DGX Spark" (Ling-3.0-flash)
+ *
+ * Conventions for every entry point
+ *   - Tensor pointers are DEVICE pointers unless a parameter says "host".
+ *     The caller owns every buffer; the library never allocates device memory
+ *     on these paths and never frees a caller pointer.
+ *   - BF16 data is passed as its 16-bit patterns (uint16_t).
+ *   - `stream` is a cudaStream_t (NULL = legacy default stream). Calls are
+ *     asynchronous on that stream; argument checks are synchronous.
+ *   - Matrices are row-major. NVFP4 / MXFP4 codes are packed two per byte,
+ *     element 2k in the low nibble; an E2M1 code is sign:1 exp:2 mant:1.
+ *   - Scratch memory ("workspace") is passed by the caller; the size needed is
+ *     returned by the matching *_workspace_size() function. Its contents need
+ *     no initialisation and are overwritten by every call. Two calls that use
+ *     the same workspace must not run concurrently.
+ *   - Return value: BWS_OK or a BWS_ERR_* code; bws_last_error() returns a
+ *     thread-local message for the last failing call on this host thread.
+ *     Invalid arguments are reported before anything is enqueued.
+ */
+#ifndef BWS_H
+#define BWS_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+enum bws_status {
+  BWS_OK = 0,
+  BWS_ERR_INVALID_ARG = 1,      /* null pointer, N out of range, bad enum  */
+  BWS_ERR_UNSUPPORTED_SHAPE = 2,/* a dimension the kernels do not support  */
+  BWS_ERR_MISALIGNED = 3,       /* a pointer below its required alignment  */
+  BWS_ERR_FORMAT = 4,           /* wrong or inconsistent format tag        */
+  BWS_ERR_CUDA = 5,             /* a CUDA runtime call failed              */
+  BWS_ERR_TIMEOUT = 6,          /* a bounded device wait ran out           */
+  BWS_ERR_WORKSPACE = 7         /* workspace smaller than required         */
+};
+
+/* Weight formats of a matrix (the ABI carries the tag explicitly so that a
+ * tensor can never be read in a format it was not written in: [LingMoE]
+ * section 11 describes FP8 weights silently read as BF16). */
+enum bws_format {
+  BWS_FMT_NVFP4 = 1,   /* E2M1 codes, E4M3 scale per 16 along d_in, FP32 tensor scale */
+  BWS_FMT_MXFP4 = 2,   /* E2M1 codes, E8M0 scale per 32 along d_in                    */
+  BWS_FMT_FP8_ROW = 3  /* E4M3 codes, FP32 scale per row                              */
+};
+
+/* Bits of the device status word (bws_status_word). */
+enum bws_status_bits {
+  BWS_STATUS_X_TWO_BANDS = 1u,  /* an activation needed the second f16 band  */
+  BWS_STATUS_X_FLUSHED = 2u     /* an activation below 2^-57 of its token's
+                                   largest magnitude was treated as zero     */
+};
+
+/* Library version (major*10000 + minor*100 + patch). */
+int bws_version(void);
+
+/* Message describing the last error on the calling host thread ("" if none). */
+const char* bws_last_error(void);
+
+/* ------------------------------------------------------------------------ */
+/* Quantizers (set-up work: they run once per weight tensor, not per step)  */
+/* ------------------------------------------------------------------------ */
+
+/* NVFP4 quantization ([Spark27B] "Fewer bytes per weight: NVFP4": E2M1
+ * elements, one E4M3 scale per 16 consecutive weights chosen so the block's
+ * largest magnitude maps to 6, one FP32 scale per tensor bringing the block
+ * scales into E4M3's range).
+ *   W        fp32 [d_out][d_in], 16-byte aligned
+ *   codes    u8   [d_out][d_in/2]   out
+ *   scales   u8   [d_out][d_in/16]  out (E4M3 codes)
+ *   tensor_scale  fp32 [1]          out: s_t = amax(|W|) / (6*448), 1 if that is 0
+ * Per block b, in FP32 with round-to-nearest-even:
+ *   code_b = E4M3(amax_b / 6 / s_t), d_b = dec(code_b) * s_t,
+ *   q = E2M1(w / d_b) (zero codes where d_b == 0); both encoders saturate.
+ * d_in % 16 == 0, d_out >= 1. Workspace: bws_nvfp4_quantize_workspace_size(). */
+size_t bws_nvfp4_quantize_workspace_size(int d_out, int d_in);
+int bws_nvfp4_quantize(const float* W, int d_out, int d_in, uint8_t* codes,
+                       uint8_t* scales, float* tensor_scale, void* workspace,
+                       size_t workspace_bytes, void* stream);
+
+/* MXFP4 quantization ([LingMoE] section 17: 4-bit micro-scaling floats whose
+ * small blocks share a scale; block size 32, E8M0 scale and clipping follow
+ * the OCP MX definition): e = clamp(floor(log2 amax_b) - 2, -127, 127),
+ * scale code e + 127, q = E2M1(w * 2^-e) saturating; a zero block gets code 0
+ * and zero codes.
+ *   W fp32 [rows][d_in]; codes u8 [rows][d_in/2]; scales u8 [rows][d_in/32].
+ * d_in % 32 == 0. */
+int bws_mxfp4_quantize(const float* W, int rows, int d_in, uint8_t* codes,
+                       uint8_t* scales, void* stream);
+
+/* Row-wise FP8 E4M3 quantization of an output layer ([LingMoE] section 7:
+ * the BF16 head is quantized to FP8 when the model loads):
+ * s_r = amax_r / 448, code = E4M3(w / s_r) saturating; s_r = 0 and zero codes
+ * for a row whose s_r is 0.
+ *   W fp32 [rows][cols]; codes u8 [rows][cols]; row_scale fp32 [rows]. */
+int bws_fp8_rowwise_quantize(const float* W, int rows, int cols, uint8_t* codes,
+                             float* row_scale, void* stream);
+
+/* ------------------------------------------------------------------------ */
+/* Weight-stream products                                                    */
+/* ------------------------------------------------------------------------ */
+
+/* Workspace bytes for one product call over a weight tensor with d_out_total
+ * output rows (all matrices of the call together) and d_in columns, N tokens. */
+size_t bws_gemv_workspace_size(int N, int d_out_total, int d_in);
+
+/* NVFP4 GEMV / skinny GEMM: y[n][i] = s_t * sum_j dec(s_b(i,j)) * q_ij * x[n][j]
+ * for N = 1..8 token rows (N = 1 is the plain decode step, N = K+1 the
+ * speculative verify pass of [Spark27B] "More tokens per weight read").
+ * Products are exact and accumulate in FP32; y is rounded to BF16.
+ *   codes/scales/tensor_scale as written by bws_nvfp4_quantize
+ *   x  bf16 [N][d_in]; y bf16 [N][d_out]
+ * d_in % 32 == 0; codes, scales, x, y 16-byte aligned. N == 0 or d_out == 0
+ * is a no-op that returns BWS_OK. */
+int bws_nvfp4_gemv(const uint8_t* codes, const uint8_t* scales,
+                   const float* tensor_scale, const uint16_t* x, int N,
+                   int d_out, int d_in, uint16_t* y, void* workspace,
+                   size_t workspace_bytes, void* stream);
+
+/* Fused MLP front half: h[n][i] = BF16( SiLU(g) * u ) with g = W_gate x,
+ * u = W_up x, both NVFP4 [d_inter][d_in], computed in FP32 and never written
+ * out ([Spark27B] flow figure: gate, up, SiLU, then down). SiLU(g) =
+ * g / (1 + exp(-g)).  h bf16 [N][d_inter]. Same constraints as bws_nvfp4_gemv. */
+int bws_nvfp4_gate_up_silu(const uint8_t* gate_codes, const uint8_t* gate_scales,
+                           const float* gate_tensor_scale,
+                           const uint8_t* up_codes, const uint8_t* up_scales,
+                           const float* up_tensor_scale, const uint16_t* x,
+                           int N, int d_inter, int d_in, uint16_t* h,
+                           void* workspace, size_t workspace_bytes, void* stream);
+
+/* FP8 output layer: logits[n][v] = s_v * sum_j dec(W[v][j]) * x[n][j], FP32
+ * out ([Spark27B]: the 248,320 x 5,120 output layer is read in full every
+ * step; [LingMoE] section 7).
+ *   W u8 [V][d] E4M3; row_scale fp32 [V]; x bf16 [N][d]; logits fp32 [N][V].
+ * d % 32 == 0. */
+int bws_fp8_lmhead_gemv(const uint8_t* W, const float* row_scale,
+                        const uint16_t* x, int N, int V, int d, float* logits,
+                        void* workspace, size_t workspace_bytes, void* stream);
+
+/* ------------------------------------------------------------------------ */
+/* Status and measurement                                                    */
+/* ------------------------------------------------------------------------ */
+
+/* Copies the device status word of a workspace (an OR of bws_status_bits set
+ * by the calls that used it) into *status (host); synchronises the stream. */
+int bws_status_word(const void* workspace, uint32_t* status, void* stream);
+
+/* Read-only streaming sum over n_bytes (% 16 == 0) of src; writes one u32
+ * checksum to out. Used to measure the achievable HBM read bandwidth. */
+int bws_hbm_read_probe(const void* src, size_t n_bytes, uint32_t* out, void* stream);
+
+/* Overwrites n_bytes of buf (e.g. 2 x L2) so the next kernel starts cold. */
+int bws_l2_flush(void* buf, size_t n_bytes, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* BWS_H */
