@@ -69,7 +69,8 @@ int run_product(int fmt, int epi, GemvParams& p, const uint16_t* x, int N, int d
   p.partials = reinterpret_cast<float*>(w + L.off_partials);
   p.out = out;
   p.out_ld = out_ld;
-  p.prefetch_units = 8;
+  p.prefetch_units = fmt == kFmtFP8 ? 4 : 8;
+  p.prefetch_ahead = 0;
   cudaError_t e = launch_prep_x(x, N, d_in, p.d_in_pad, xhi, xlo, xexp, xflags, hdr, p.counters,
                                 p.n_tiles, st, true);
   if (e != cudaSuccess) return cuda_status(e, name);

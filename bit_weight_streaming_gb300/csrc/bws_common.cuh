@@ -60,6 +60,19 @@ BWS_DEV float4 ld_cg_f4(const float4* p) {
   return v;
 }
 
+// ---- async global -> shared copies (per thread, 16 bytes, bypassing L1) ---
+BWS_DEV void cp_async16(uint32_t smem_addr, const void* g) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" :: "r"(smem_addr), "l"(g) : "memory");
+}
+BWS_DEV void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+BWS_DEV void cp_async_wait() { asm volatile("cp.async.wait_group %0;" :: "n"(N) : "memory"); }
+BWS_DEV uint4 lds_v4(uint32_t smem_addr) {
+  uint4 v;
+  asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(smem_addr));
+  return v;
+}
+
 // ---- conversions (hardware, exact for these inputs) ------------------------
 // Two E2M1 codes in one byte -> f16x2. Every E2M1 value is exact in f16.
 BWS_DEV uint32_t e2m1x2_to_f16x2(uint32_t byte_in_low8) {

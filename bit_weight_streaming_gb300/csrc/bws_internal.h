@@ -54,7 +54,8 @@ struct GemvParams {
   int out_ld;
   float* partials;         // [(n_tiles + n_warps) * kSlotFloats]
   uint32_t* counters;      // [n_tiles], zero on entry, left zero on exit
-  int prefetch_units;
+  int prefetch_units;       // units pulled into L2 before waiting on the inputs
+  int prefetch_ahead;       // rolling L2 prefetch distance in units (0 = off)
 };
 
 // Workspace layout of one product call (all offsets 256-byte aligned).

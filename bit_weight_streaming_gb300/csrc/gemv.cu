@@ -27,11 +27,13 @@ namespace bws {
 
 namespace {
 
+// In-flight data of one unit for one lane.
+template <int FMT, bool LO>
 struct Frag {
-  uint4 c[2][2][2];   // [sub][row g / g+8][two 16-byte pieces (FP8 uses both)]
-  uint32_t sc[2][2];  // [sub][row g / g+8] block scale bytes
-  uint4 xh[4];        // this lane's 32 f16 activations (token g), hi band
-  uint4 xl[4];        // lo band
+  uint4 c[2][2][FMT == kFmtFP8 ? 2 : 1];   // [sub][row g / g+8][16-byte pieces]
+  uint32_t sc[2][2];                        // [sub][row g / g+8] block scale bytes
+  uint4 xh[4];                              // this lane's 32 f16 activations, hi band
+  uint4 xl[LO ? 4 : 1];                     // lo band
 };
 
 struct TileRows {
@@ -58,47 +60,71 @@ BWS_DEV TileRows tile_rows(const GemvParams& p, int tile) {
   return tr;
 }
 
-template <int FMT, bool LO>
-BWS_DEV void load_unit(const GemvParams& p, const TileRows& tr, int seg, int g, int t, Frag& f) {
-  const int k0 = seg * kSegK + 32 * t;
-  const bool kval = k0 < p.d_in;
+// Per-tile lane pointers: computed once per piece, advanced per unit.
+template <int FMT>
+struct LanePtrs {
+  const uint8_t* c[2][2];
+  const uint8_t* sc[2][2];
+  const uint16_t* xh;
+  const uint16_t* xl;
+  uint32_t rowmask;   // bit 2*s+h: row valid
+};
+
+template <int FMT, int EPI>
+BWS_DEV LanePtrs<FMT> lane_ptrs(const GemvParams& p, const TileRows& tr, int g, int t) {
+  LanePtrs<FMT> L;
+  L.rowmask = 0u;
 #pragma unroll
   for (int s = 0; s < 2; ++s) {
     const GemvMat& M = p.mats[tr.mat[s]];
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
       const int row = tr.row0[s] + g + 8 * h;
-      const bool ok = kval && row < M.d_out;
+      const int rr = row < M.d_out ? row : 0;
+      if (row < M.d_out) L.rowmask |= 1u << (2 * s + h);
       if (FMT == kFmtFP8) {
-        const uint8_t* src = M.codes + (size_t)row * p.d_in + k0;
-        f.c[s][h][0] = ok ? ld_stream_v4(src) : make_uint4(0, 0, 0, 0);
-        f.c[s][h][1] = ok ? ld_stream_v4(src + 16) : make_uint4(0, 0, 0, 0);
-        f.sc[s][h] = 0;
+        L.c[s][h] = M.codes + (size_t)rr * p.d_in + 32 * t;
+        L.sc[s][h] = nullptr;
       } else {
-        const uint8_t* src = M.codes + (size_t)row * (p.d_in >> 1) + (k0 >> 1);
-        f.c[s][h][0] = ok ? ld_stream_v4(src) : make_uint4(0, 0, 0, 0);
-        if (FMT == kFmtNVFP4)
-          f.sc[s][h] = ok ? ld_stream_u16(M.scales + (size_t)row * (p.d_in >> 4) + (k0 >> 4)) : 0u;
-        else
-          f.sc[s][h] = ok ? ld_stream_u8(M.scales + (size_t)row * (p.d_in >> 5) + (k0 >> 5)) : 0u;
+        L.c[s][h] = M.codes + (size_t)rr * (p.d_in >> 1) + 16 * t;
+        L.sc[s][h] = FMT == kFmtNVFP4 ? M.scales + (size_t)rr * (p.d_in >> 4) + 2 * t
+                                      : M.scales + (size_t)rr * (p.d_in >> 5) + t;
       }
     }
   }
-  if (g < p.N) {
-    const uint16_t* xs = p.x.hi + (size_t)g * p.d_in_pad + seg * kSegK + 32 * t;
+  // token rows g >= N read the all-zero row kept after the N real rows
+  const size_t xo = (size_t)(g < p.N ? g : p.N) * p.d_in_pad + 32 * t;
+  L.xh = p.x.hi + xo;
+  L.xl = p.x.lo + xo;
+  return L;
+}
+
+// Loads are unpredicated: rows past d_out read row 0 (their outputs are never
+// stored) and lanes past d_in read the row's last 32 weights, which meet the
+// zero padding of the activations, so they add nothing.
+template <int FMT, bool LO>
+BWS_DEV void load_unit(const GemvParams& p, const LanePtrs<FMT>& L, int seg, int g, int t, Frag<FMT, LO>& f) {
+  const int k0 = min(seg * kSegK + 32 * t, p.d_in - 32) - 32 * t;   // lane offset added in L
+  const int cb = FMT == kFmtFP8 ? k0 : (k0 >> 1);
 #pragma unroll
-    for (int i = 0; i < 4; ++i) f.xh[i] = ld_act_v4(xs + 8 * i);
-    if (LO) {
-      const uint16_t* xl = p.x.lo + (size_t)g * p.d_in_pad + seg * kSegK + 32 * t;
+  for (int s = 0; s < 2; ++s)
 #pragma unroll
-      for (int i = 0; i < 4; ++i) f.xl[i] = ld_act_v4(xl + 8 * i);
+    for (int h = 0; h < 2; ++h) {
+      f.c[s][h][0] = ld_stream_v4(L.c[s][h] + cb);
+      if constexpr (FMT == kFmtFP8) {
+        f.c[s][h][FMT == kFmtFP8 ? 1 : 0] = ld_stream_v4(L.c[s][h] + cb + 16);
+        f.sc[s][h] = 0u;
+      } else if constexpr (FMT == kFmtNVFP4) {
+        f.sc[s][h] = ld_stream_u16(L.sc[s][h] + (k0 >> 4));
+      } else {
+        f.sc[s][h] = ld_stream_u8(L.sc[s][h] + (k0 >> 5));
+      }
     }
-  } else {
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      f.xh[i] = make_uint4(0, 0, 0, 0);
-      if (LO) f.xl[i] = make_uint4(0, 0, 0, 0);
-    }
+  for (int i = 0; i < 4; ++i) f.xh[i] = ld_act_v4(L.xh + seg * kSegK + 8 * i);
+  if (LO) {
+#pragma unroll
+    for (int i = 0; i < 4; ++i) f.xl[i] = ld_act_v4(L.xl + seg * kSegK + 8 * i);
   }
 }
 
@@ -115,12 +141,15 @@ BWS_DEV uint32_t f16x2_pow2(int k) {
   return h | (h << 16);
 }
 
-// Accumulate one unit into acc[sub][4] (and accl for the lo band).
+// Accumulators: [sub][chain][4].
+constexpr int kChains = 1;
+typedef float Acc[2][kChains][4];
+
 template <int FMT, bool LO>
-BWS_DEV void compute_unit(const Frag& f, float (&acc)[2][4], float (&accl)[2][4]) {
+BWS_DEV void compute_unit(const Frag<FMT, LO>& f, Acc& acc, Acc& accl) {
 #pragma unroll
   for (int s = 0; s < 2; ++s) {
-    if (FMT == kFmtFP8) {
+    if constexpr (FMT == kFmtFP8) {
 #pragma unroll
       for (int j = 0; j < 8; ++j) {
         uint32_t a0, a2, a1, a3;
@@ -128,39 +157,37 @@ BWS_DEV void compute_unit(const Frag& f, float (&acc)[2][4], float (&accl)[2][4]
         e4m3x4_to_f16x2x2(word_of(f.c[s][1][j >> 2], j & 3), a1, a3);
         const uint32_t b0 = word_of(f.xh[j >> 1], 2 * (j & 1));
         const uint32_t b1 = word_of(f.xh[j >> 1], 2 * (j & 1) + 1);
-        mma_f16_16816(acc[s], a0, a1, a2, a3, b0, b1);
+        mma_f16_16816(acc[s][(j & 1) % kChains], a0, a1, a2, a3, b0, b1);
         if (LO) {
           const uint32_t c0 = word_of(f.xl[j >> 1], 2 * (j & 1));
           const uint32_t c1 = word_of(f.xl[j >> 1], 2 * (j & 1) + 1);
-          mma_f16_16816(accl[s], a0, a1, a2, a3, c0, c1);
+          mma_f16_16816(accl[s][(j & 1) % kChains], a0, a1, a2, a3, c0, c1);
         }
       }
     } else {
-      uint32_t mg[2], m8[2];   // per 16-element half of the lane's 32 weights
-      if (FMT == kFmtNVFP4) {
+      uint32_t mg[2], m8[2];   // multipliers for the two 16-weight halves
+      float sref_g = 0.f, sref_8 = 0.f;
+      if constexpr (FMT == kFmtNVFP4) {
         const uint32_t sg = e4m3x2_to_f16x2(f.sc[s][0]);
         const uint32_t s8 = e4m3x2_to_f16x2(f.sc[s][1]);
         mg[0] = bcast_lo(sg); mg[1] = bcast_hi(sg);
         m8[0] = bcast_lo(s8); m8[1] = bcast_hi(s8);
-      }
-      float sref_g = 0.f, sref_8 = 0.f;
-      if (FMT == kFmtMXFP4) {
+      } else {
+        // MXFP4: the lane's 32 weights are one E8M0 block; scale relative to
+        // the largest block of the row in this unit, rescale the sum in FP32.
         const int eg = (int)f.sc[s][0] - 127;
         const int e8 = (int)f.sc[s][1] - 127;
-        int rg = eg, r8 = e8;
-        rg = max(rg, __shfl_xor_sync(0xffffffffu, rg, 1));
+        int rg = max(eg, __shfl_xor_sync(0xffffffffu, eg, 1));
         rg = max(rg, __shfl_xor_sync(0xffffffffu, rg, 2));
-        r8 = max(r8, __shfl_xor_sync(0xffffffffu, r8, 1));
+        int r8 = max(e8, __shfl_xor_sync(0xffffffffu, e8, 1));
         r8 = max(r8, __shfl_xor_sync(0xffffffffu, r8, 2));
         mg[0] = mg[1] = f16x2_pow2(eg - rg);
         m8[0] = m8[1] = f16x2_pow2(e8 - r8);
         sref_g = exp2i(rg);
         sref_8 = exp2i(r8);
       }
-      // NVFP4 accumulates straight into acc; MXFP4 forms the unit's sum at
-      // the unit's reference scale first and rescales it in FP32.
-      float dm[4] = {0.f, 0.f, 0.f, 0.f};
-      float dml[4] = {0.f, 0.f, 0.f, 0.f};
+      float dm[kChains][4] = {};
+      float dml[kChains][4] = {};
 #pragma unroll
       for (int w = 0; w < 4; ++w) {
         uint32_t p0, p1, p2, p3, q0, q1, q2, q3;
@@ -169,32 +196,30 @@ BWS_DEV void compute_unit(const Frag& f, float (&acc)[2][4], float (&accl)[2][4]
         const uint32_t sa = mg[w >> 1], sb = m8[w >> 1];
         p0 = hmul2_u32(p0, sa); p1 = hmul2_u32(p1, sa); p2 = hmul2_u32(p2, sa); p3 = hmul2_u32(p3, sa);
         q0 = hmul2_u32(q0, sb); q1 = hmul2_u32(q1, sb); q2 = hmul2_u32(q2, sb); q3 = hmul2_u32(q3, sb);
-        if constexpr (FMT == kFmtMXFP4) {
-          mma_f16_16816(dm, p0, q0, p1, q1, f.xh[w].x, f.xh[w].y);
-          mma_f16_16816(dm, p2, q2, p3, q3, f.xh[w].z, f.xh[w].w);
-          if (LO) {
-            mma_f16_16816(dml, p0, q0, p1, q1, f.xl[w].x, f.xl[w].y);
-            mma_f16_16816(dml, p2, q2, p3, q3, f.xl[w].z, f.xl[w].w);
-          }
-        } else {
-          mma_f16_16816(acc[s], p0, q0, p1, q1, f.xh[w].x, f.xh[w].y);
-          mma_f16_16816(acc[s], p2, q2, p3, q3, f.xh[w].z, f.xh[w].w);
-          if (LO) {
-            mma_f16_16816(accl[s], p0, q0, p1, q1, f.xl[w].x, f.xl[w].y);
-            mma_f16_16816(accl[s], p2, q2, p3, q3, f.xl[w].z, f.xl[w].w);
-          }
+        float(&D0)[4] = FMT == kFmtMXFP4 ? dm[0] : acc[s][0];
+        float(&D1)[4] = FMT == kFmtMXFP4 ? dm[1 % kChains] : acc[s][1 % kChains];
+        mma_f16_16816(D0, p0, q0, p1, q1, f.xh[w].x, f.xh[w].y);
+        mma_f16_16816(D1, p2, q2, p3, q3, f.xh[w].z, f.xh[w].w);
+        if (LO) {
+          float(&L0)[4] = FMT == kFmtMXFP4 ? dml[0] : accl[s][0];
+          float(&L1)[4] = FMT == kFmtMXFP4 ? dml[1 % kChains] : accl[s][1 % kChains];
+          mma_f16_16816(L0, p0, q0, p1, q1, f.xl[w].x, f.xl[w].y);
+          mma_f16_16816(L1, p2, q2, p3, q3, f.xl[w].z, f.xl[w].w);
         }
       }
       if constexpr (FMT == kFmtMXFP4) {
-        acc[s][0] = __fmaf_rn(dm[0], sref_g, acc[s][0]);
-        acc[s][1] = __fmaf_rn(dm[1], sref_g, acc[s][1]);
-        acc[s][2] = __fmaf_rn(dm[2], sref_8, acc[s][2]);
-        acc[s][3] = __fmaf_rn(dm[3], sref_8, acc[s][3]);
-        if (LO) {
-          accl[s][0] = __fmaf_rn(dml[0], sref_g, accl[s][0]);
-          accl[s][1] = __fmaf_rn(dml[1], sref_g, accl[s][1]);
-          accl[s][2] = __fmaf_rn(dml[2], sref_8, accl[s][2]);
-          accl[s][3] = __fmaf_rn(dml[3], sref_8, accl[s][3]);
+#pragma unroll
+        for (int c = 0; c < kChains; ++c) {
+          acc[s][c][0] = __fmaf_rn(dm[c][0], sref_g, acc[s][c][0]);
+          acc[s][c][1] = __fmaf_rn(dm[c][1], sref_g, acc[s][c][1]);
+          acc[s][c][2] = __fmaf_rn(dm[c][2], sref_8, acc[s][c][2]);
+          acc[s][c][3] = __fmaf_rn(dm[c][3], sref_8, acc[s][c][3]);
+          if (LO) {
+            accl[s][c][0] = __fmaf_rn(dml[c][0], sref_g, accl[s][c][0]);
+            accl[s][c][1] = __fmaf_rn(dml[c][1], sref_g, accl[s][c][1]);
+            accl[s][c][2] = __fmaf_rn(dml[c][2], sref_8, accl[s][c][2]);
+            accl[s][c][3] = __fmaf_rn(dml[c][3], sref_8, accl[s][c][3]);
+          }
         }
       }
     }
@@ -303,53 +328,122 @@ BWS_DEV void end_piece(const GemvParams& p, int tile, long long warp_id, bool wh
   if (lane == 0) p.counters[tile] = 0u;
 }
 
-template <int FMT, int EPI, bool LO>
-BWS_DEV void run_range(const GemvParams& p, long long u, long long u_end, long long warp_id, int lane,
-                       const int (&xexp)[2]) {
-  const int g = lane >> 2, t = lane & 3;
-  const int nseg = p.nseg;
-  float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-  float accl[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-  int tile = (int)(u / nseg);
-  int seg = (int)(u % nseg);
-  int piece_first = seg;
-  TileRows tr = tile_rows<EPI>(p, tile);
-  Frag fa, fb;
-  load_unit<FMT, LO>(p, tr, seg, g, t, fa);
-  for (;;) {
-    // issue the next unit's loads before computing this one
-    const long long un = u + 1;
-    int tile_n = tile, seg_n = seg + 1;
-    if (seg_n == nseg) { seg_n = 0; tile_n = tile + 1; }
-    TileRows trn = tr;
-    if (un < u_end) {
-      if (tile_n != tile) trn = tile_rows<EPI>(p, tile_n);
-      load_unit<FMT, LO>(p, trn, seg_n, g, t, fb);
-    }
-    compute_unit<FMT, LO>(fa, acc, accl);
-    const bool tile_done = (seg == nseg - 1) || (un == u_end);
-    if (tile_done) {
-      float v[2][4];
-#pragma unroll
-      for (int s = 0; s < 2; ++s)
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          v[s][i] = LO ? __fmaf_rn(accl[s][i], 0x1p-29f, acc[s][i]) : acc[s][i];
-          acc[s][i] = 0.f;
-          accl[s][i] = 0.f;
-        }
-      const bool whole = piece_first == 0 && seg == nseg - 1;
-      end_piece<FMT, EPI>(p, tile, warp_id, whole, v, xexp, lane);
-      piece_first = 0;
-    }
-    if (un >= u_end) break;
-    u = un; tile = tile_n; seg = seg_n; tr = trn;
-    fa = fb;
+// Pull unit u's weights of this warp's 32 rows towards L2 (lane l: row l).
+template <int FMT, int EPI>
+BWS_DEV void prefetch_unit(const GemvParams& p, long long u, int lane) {
+  const int tile = (int)(u / p.nseg);
+  const int seg = (int)(u % p.nseg);
+  const TileRows tr = tile_rows<EPI>(p, tile);
+  const int s = lane >> 4;
+  const GemvMat& M = p.mats[tr.mat[s]];
+  const int row = tr.row0[s] + (lane & 15);
+  if (row >= M.d_out) return;
+  if (FMT == kFmtFP8) {
+    const uint8_t* a = M.codes + (size_t)row * p.d_in + seg * kSegK;
+    const int nb = min(kSegK, p.d_in - seg * kSegK);
+    if (nb >= 16) prefetch_l2_bulk(a, (uint32_t)(nb & ~15));
+  } else {
+    const uint8_t* a = M.codes + (size_t)row * (p.d_in >> 1) + seg * (kSegK / 2);
+    const int nb = min(kSegK / 2, (p.d_in >> 1) - seg * (kSegK / 2));
+    if (nb >= 16) prefetch_l2_bulk(a, (uint32_t)(nb & ~15));
+    const uint8_t* sa = FMT == kFmtNVFP4 ? M.scales + (size_t)row * (p.d_in >> 4) + seg * (kSegK / 16)
+                                         : M.scales + (size_t)row * (p.d_in >> 5) + seg * (kSegK / 32);
+    asm volatile("prefetch.global.L2 [%0];" :: "l"(sa));
   }
 }
 
+// Lane l pulls row l's bytes of units [sa, sb] of a tile into L2 (one op).
+template <int FMT>
+BWS_DEV void prefetch_rows(const GemvParams& p, const TileRows& tr, int sa, int sb, int lane) {
+  const int sub = lane >> 4;
+  const GemvMat& M = p.mats[tr.mat[sub]];
+  const int row = tr.row0[sub] + (lane & 15);
+  if (row >= M.d_out || sb < sa) return;
+  const int per = FMT == kFmtFP8 ? kSegK : kSegK / 2;
+  const size_t row_bytes = FMT == kFmtFP8 ? (size_t)p.d_in : (size_t)(p.d_in >> 1);
+  const size_t kb0 = (size_t)sa * per;
+  size_t nb = (size_t)(sb - sa + 1) * per;
+  if (kb0 + nb > row_bytes) nb = row_bytes - kb0;
+  if (nb >= 16) prefetch_l2_bulk(M.codes + (size_t)row * row_bytes + kb0, (uint32_t)(nb & ~(size_t)15));
+}
+
+// One piece: units [seg0, seg1] of one tile, software-pipelined two deep.
+template <int FMT, int EPI, bool LO>
+BWS_DEV void run_piece(const GemvParams& p, int tile, int seg0, int seg1, long long warp_id, int lane,
+                       const int (&xexp)[2]) {
+  const int g = lane >> 2, t = lane & 3;
+  const TileRows tr = tile_rows<EPI>(p, tile);
+  const LanePtrs<FMT> L = lane_ptrs<FMT, EPI>(p, tr, g, t);
+  Acc acc = {}, accl = {};
+  if (LO) {
+    // rare path (two activation bands): one unit at a time
+    for (int seg = seg0; seg <= seg1; ++seg) {
+      Frag<FMT, true> f;
+      load_unit<FMT, true>(p, L, seg, g, t, f);
+      compute_unit<FMT, true>(f, acc, accl);
+    }
+  } else {
+    Frag<FMT, false> fa, fb;
+    const int P = p.prefetch_ahead;           // L2 prefetch window in units
+    if (P > 0) prefetch_rows<FMT>(p, tr, seg0, min(seg1, seg0 + P - 1), lane);
+    load_unit<FMT, false>(p, L, seg0, g, t, fa);
+    for (int seg = seg0; seg <= seg1; seg += 2) {
+      if (seg + 1 <= seg1) load_unit<FMT, false>(p, L, seg + 1, g, t, fb);
+      // every P/2 units, extend the prefetched window to P units ahead
+      if (P > 0 && ((seg - seg0) % (P >> 1)) < 2 && ((seg - seg0) % (P >> 1)) == 0 && seg + P <= seg1)
+        prefetch_rows<FMT>(p, tr, seg + P - (P >> 1) + 1, min(seg1, seg + P), lane);
+      compute_unit<FMT, false>(fa, acc, accl);
+      if (seg + 1 > seg1) break;
+      if (seg + 2 <= seg1) load_unit<FMT, false>(p, L, seg + 2, g, t, fa);
+      compute_unit<FMT, false>(fb, acc, accl);
+    }
+  }
+  float v[2][4];
+#pragma unroll
+  for (int s = 0; s < 2; ++s)
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      float a = acc[s][0][i], al = accl[s][0][i];
+#pragma unroll
+      for (int c = 1; c < kChains; ++c) { a = __fadd_rn(a, acc[s][c][i]); al = __fadd_rn(al, accl[s][c][i]); }
+      v[s][i] = LO ? __fmaf_rn(al, 0x1p-29f, a) : a;
+    }
+  const bool whole = seg0 == 0 && seg1 == p.nseg - 1;
+  end_piece<FMT, EPI>(p, tile, warp_id, whole, v, xexp, lane);
+}
+
+// The two-band path is rare; keep it out of line so that its register
+// needs do not constrain the common path.
+template <int FMT, int EPI, bool LO>
+__device__ __noinline__ void run_range_lo(const GemvParams& p, long long u, long long u_end, long long warp_id,
+                                          int lane, int xe0, int xe1);
+
+template <int FMT, int EPI, bool LO>
+BWS_DEV void run_range(const GemvParams& p, long long u, long long u_end, long long warp_id, int lane,
+                       const int (&xexp)[2]) {
+  while (u < u_end) {
+    const int tile = (int)(u / p.nseg);
+    const int seg0 = (int)(u % p.nseg);
+    const long long left = u_end - u;
+    const int seg1 = (long long)(p.nseg - 1 - seg0) < left ? p.nseg - 1 : seg0 + (int)left - 1;
+    run_piece<FMT, EPI, LO>(p, tile, seg0, seg1, warp_id, lane, xexp);
+    u += seg1 - seg0 + 1;
+  }
+}
+
+template <int FMT, int EPI, bool LO>
+__device__ __noinline__ void run_range_lo(const GemvParams& p, long long u, long long u_end, long long warp_id,
+                                          int lane, int xe0, int xe1) {
+  const int xexp[2] = {xe0, xe1};
+  run_range<FMT, EPI, true>(p, u, u_end, warp_id, lane, xexp);
+}
+
+#ifndef BWS_GEMV_MIN_BLOCKS
+#define BWS_GEMV_MIN_BLOCKS 2
+#endif
+
 template <int FMT, int EPI>
-__global__ void __launch_bounds__(kWarpsPerCta * 32, 2) gemv_kernel(const __grid_constant__ GemvParams p) {
+__global__ void __launch_bounds__(kWarpsPerCta * 32, BWS_GEMV_MIN_BLOCKS) gemv_kernel(const __grid_constant__ GemvParams p) {
   const int lane = threadIdx.x & 31;
   const long long warp_id = (long long)blockIdx.x * kWarpsPerCta + (threadIdx.x >> 5);
   pdl_launch_dependents();
@@ -358,25 +452,26 @@ __global__ void __launch_bounds__(kWarpsPerCta * 32, 2) gemv_kernel(const __grid
   const long long u0 = range_begin(warp_id, U, W);
   const long long u1 = range_begin(warp_id + 1, U, W);
 
-  // Weights do not depend on earlier kernels: start pulling this warp's first
-  // units into L2 before waiting for the activations.
+  // Weights do not depend on earlier kernels: start pulling the first units
+  // of this warp's range into L2 before waiting for the activations (one bulk
+  // prefetch per lane, lane l covering row l of the first tile piece).
   if (p.prefetch_units > 0) {
     const int tile = (int)(u0 / p.nseg);
     const int seg = (int)(u0 % p.nseg);
-    int nsegs = p.nseg - seg;
-    if (nsegs > p.prefetch_units) nsegs = p.prefetch_units;
-    if ((long long)nsegs > u1 - u0) nsegs = (int)(u1 - u0);
+    long long nu = p.nseg - seg;
+    if (nu > p.prefetch_units) nu = p.prefetch_units;
+    if (nu > u1 - u0) nu = u1 - u0;
     const TileRows tr = tile_rows<EPI>(p, tile);
-    const int s = lane >> 4, r = lane & 15;
-    const GemvMat& M = p.mats[tr.mat[s]];
-    const int row = tr.row0[s] + r;
-    if (row < M.d_out && nsegs > 0) {
-      const int bytes_per_seg = FMT == kFmtFP8 ? kSegK : kSegK / 2;
+    const int sub = lane >> 4;
+    const GemvMat& M = p.mats[tr.mat[sub]];
+    const int row = tr.row0[sub] + (lane & 15);
+    if (row < M.d_out && nu > 0) {
+      const int per = FMT == kFmtFP8 ? kSegK : kSegK / 2;
       const size_t row_bytes = FMT == kFmtFP8 ? (size_t)p.d_in : (size_t)(p.d_in >> 1);
-      const int kb0 = seg * bytes_per_seg;
-      int nb = nsegs * bytes_per_seg;
-      if ((size_t)(kb0 + nb) > row_bytes) nb = (int)(row_bytes - kb0);
-      if (nb >= 16) prefetch_l2_bulk(M.codes + (size_t)row * row_bytes + kb0, (uint32_t)(nb & ~15));
+      const size_t kb0 = (size_t)seg * per;
+      size_t nb = (size_t)nu * per;
+      if (kb0 + nb > row_bytes) nb = row_bytes - kb0;
+      if (nb >= 16) prefetch_l2_bulk(M.codes + (size_t)row * row_bytes + kb0, (uint32_t)(nb & ~(size_t)15));
     }
   }
   pdl_wait();
@@ -390,65 +485,97 @@ __global__ void __launch_bounds__(kWarpsPerCta * 32, 2) gemv_kernel(const __grid
   }
   for (int tok = 0; tok < p.N; ++tok) flags |= __ldg(p.x.flags + tok);
   if (flags & 1u)
-    run_range<FMT, EPI, true>(p, u0, u1, warp_id, lane, xexp);
+    run_range_lo<FMT, EPI, true>(p, u0, u1, warp_id, lane, xexp[0], xexp[1]);
   else
     run_range<FMT, EPI, false>(p, u0, u1, warp_id, lane, xexp);
 }
 
 // ---- activation prep ----------------------------------------------------------
 
-// One CTA per token: E = floor(log2 max|x|), then the two f16 bands.
-// Also zeroes the counters of the product that follows.
-__global__ void __launch_bounds__(256) prep_x_kernel(const uint16_t* __restrict__ x, int N, int d_in,
-                                                     int d_in_pad, uint16_t* __restrict__ xhi,
-                                                     uint16_t* __restrict__ xlo, int* __restrict__ xexp,
-                                                     uint32_t* __restrict__ xflags, uint32_t* __restrict__ hdr,
-                                                     uint32_t* __restrict__ zero_ptr, int zero_words) {
+// One CTA per token: E = floor(log2 max|x|), then the two f16 bands. Each
+// thread handles 8-element chunks (d_in % 32 == 0, so a chunk never straddles
+// d_in). Also zeroes the counters of the product that follows.
+constexpr int kPrepThreads = 1024;
+__global__ void __launch_bounds__(kPrepThreads) prep_x_kernel(const uint16_t* __restrict__ x, int N, int d_in,
+                                                              int d_in_pad, uint16_t* __restrict__ xhi,
+                                                              uint16_t* __restrict__ xlo, int* __restrict__ xexp,
+                                                              uint32_t* __restrict__ xflags, uint32_t* __restrict__ hdr,
+                                                              uint32_t* __restrict__ zero_ptr, int zero_words) {
   pdl_launch_dependents();
   pdl_wait();
   for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < zero_words; i += gridDim.x * blockDim.x)
     zero_ptr[i] = 0u;
+  if (blockIdx.x == 0) {   // the all-zero token row N read by unused MMA columns
+    uint4* zh = reinterpret_cast<uint4*>(xhi + (size_t)N * d_in_pad);
+    uint4* zl = reinterpret_cast<uint4*>(xlo + (size_t)N * d_in_pad);
+    for (int c = threadIdx.x; c < (d_in_pad >> 3); c += blockDim.x) {
+      zh[c] = make_uint4(0, 0, 0, 0);
+      zl[c] = make_uint4(0, 0, 0, 0);
+    }
+  }
   const int tok = blockIdx.x;
   if (tok >= N) return;
   if (tok == 0 && threadIdx.x == 0) hdr[0] = (uint32_t)N;
-  const uint16_t* xr = x + (size_t)tok * d_in;
+  const uint4* xr = reinterpret_cast<const uint4*>(x + (size_t)tok * d_in);
+  const int nchunk = d_in >> 3, nchunk_pad = d_in_pad >> 3;
   float m = 0.0f;
-  for (int k = threadIdx.x; k < d_in; k += blockDim.x)
-    m = fmaxf(m, fabsf(__uint_as_float((uint32_t)xr[k] << 16)));
+  for (int c = threadIdx.x; c < nchunk; c += blockDim.x) {
+    const uint4 v = __ldg(xr + c);
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+      m = fmaxf(m, fmaxf(fabsf(__uint_as_float(w[i] << 16)), fabsf(__uint_as_float(w[i] & 0xFFFF0000u))));
+  }
   m = warp_max(m);
-  __shared__ float sm[8];
-  __shared__ uint32_t sf[8];
+  __shared__ float sm[kPrepThreads / 32];
+  __shared__ uint32_t sf[kPrepThreads / 32];
   if ((threadIdx.x & 31) == 0) sm[threadIdx.x >> 5] = m;
   __syncthreads();
   float mx = 0.0f;
-#pragma unroll
-  for (int i = 0; i < 8; ++i) mx = fmaxf(mx, sm[i]);
+#pragma unroll 8
+  for (int i = 0; i < kPrepThreads / 32; ++i) mx = fmaxf(mx, sm[i]);
   const int E = mx > 0.0f ? floor_log2_abs(mx) : 0;
   uint32_t flags = 0u;
-  for (int k = threadIdx.x; k < d_in_pad; k += blockDim.x) {
-    const float v = k < d_in ? __uint_as_float((uint32_t)xr[k] << 16) : 0.0f;
-    const float hi = ldexp_exact(v, 14 - E);
-    uint16_t h = 0, l = 0;
-    if (fabsf(hi) >= 0x1p-14f) {
-      h = __half_as_ushort(__float2half_rn(hi));
-    } else if (v != 0.0f) {
-      const float lo = ldexp_exact(v, 43 - E);
-      if (fabsf(lo) >= 0x1p-14f) {
-        l = __half_as_ushort(__float2half_rn(lo));
-        flags |= 1u;
-      } else {
-        flags |= 2u;
+  uint4* hi4 = reinterpret_cast<uint4*>(xhi + (size_t)tok * d_in_pad);
+  uint4* lo4 = reinterpret_cast<uint4*>(xlo + (size_t)tok * d_in_pad);
+  for (int c = threadIdx.x; c < nchunk_pad; c += blockDim.x) {
+    uint4 v = make_uint4(0, 0, 0, 0);
+    if (c < nchunk) v = __ldg(xr + c);
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+    uint32_t h[4], l[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      uint32_t hh[2], ll[2];
+#pragma unroll
+      for (int j = 0; j < 2; ++j) {
+        const float f = __uint_as_float(j == 0 ? (w[i] << 16) : (w[i] & 0xFFFF0000u));
+        const float a = ldexp_exact(f, 14 - E);
+        hh[j] = 0u;
+        ll[j] = 0u;
+        if (fabsf(a) >= 0x1p-14f) {
+          hh[j] = __half_as_ushort(__float2half_rn(a));
+        } else if (f != 0.0f) {
+          const float b = ldexp_exact(f, 43 - E);
+          if (fabsf(b) >= 0x1p-14f) {
+            ll[j] = __half_as_ushort(__float2half_rn(b));
+            flags |= 1u;
+          } else {
+            flags |= 2u;
+          }
+        }
       }
+      h[i] = hh[0] | (hh[1] << 16);
+      l[i] = ll[0] | (ll[1] << 16);
     }
-    xhi[(size_t)tok * d_in_pad + k] = h;
-    xlo[(size_t)tok * d_in_pad + k] = l;
+    hi4[c] = make_uint4(h[0], h[1], h[2], h[3]);
+    lo4[c] = make_uint4(l[0], l[1], l[2], l[3]);
   }
   flags = __reduce_or_sync(0xffffffffu, flags);
   if ((threadIdx.x & 31) == 0) sf[threadIdx.x >> 5] = flags;
   __syncthreads();
   if (threadIdx.x == 0) {
     uint32_t f = 0u;
-    for (int i = 0; i < 8; ++i) f |= sf[i];
+    for (int i = 0; i < kPrepThreads / 32; ++i) f |= sf[i];
     xexp[tok] = E;
     xflags[tok] = f;
   }
@@ -461,6 +588,7 @@ cudaError_t launch_one(const GemvParams& p, cudaStream_t st, bool pdl) {
   cfg.gridDim = dim3((unsigned)ctas);
   cfg.blockDim = dim3(kWarpsPerCta * 32);
   cfg.stream = st;
+
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
@@ -482,7 +610,7 @@ int num_sms() {
   return n;
 }
 
-long long gemv_max_warps() { return (long long)num_sms() * 2 * kWarpsPerCta; }
+long long gemv_max_warps() { return (long long)num_sms() * BWS_GEMV_MIN_BLOCKS * kWarpsPerCta; }
 
 static size_t align256(size_t v) { return (v + 255) & ~(size_t)255; }
 
@@ -493,8 +621,8 @@ GemvWorkspace gemv_workspace_layout(int N, int d_in, int n_tiles, long long max_
   w.off_hdr = o; o += 256;
   w.off_exp = o; o += align256(sizeof(int) * kMaxTokens);
   w.off_flags = o; o += align256(sizeof(uint32_t) * kMaxTokens);
-  w.off_hi = o; o += align256(2 * d_pad * N);
-  w.off_lo = o; o += align256(2 * d_pad * N);
+  w.off_hi = o; o += align256(2 * d_pad * (N + 1));   // N tokens + one zero row
+  w.off_lo = o; o += align256(2 * d_pad * (N + 1));
   w.off_counters = o; o += align256(sizeof(uint32_t) * (size_t)n_tiles);
   w.off_partials = o; o += align256(sizeof(float) * kSlotFloats * ((size_t)n_tiles + max_warps));
   w.total = o;
@@ -506,7 +634,7 @@ cudaError_t launch_prep_x(const uint16_t* x, int N, int d_in, int d_in_pad, uint
                           cudaStream_t st, bool pdl) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)N);
-  cfg.blockDim = dim3(256);
+  cfg.blockDim = dim3(kPrepThreads);
   cfg.stream = st;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;

@@ -36,9 +36,17 @@ cudaError_t launch_hbm_read_probe(const void* src, size_t n_bytes, uint32_t* out
   return cudaGetLastError();
 }
 
+// Writes the first half of buf, then streams through the second half: the
+// write evicts whatever the cache held, and the read evicts the dirty lines
+// that write left, so the next kernel starts with a cold L2 holding only
+// clean lines and pays no write-back.
 cudaError_t launch_l2_flush(void* buf, size_t n_bytes, cudaStream_t st) {
   static uint32_t salt = 1;
-  l2_flush_kernel<<<num_sms() * 4, 512, 0, st>>>(reinterpret_cast<uint4*>(buf), n_bytes / 16, salt++);
+  const size_t half16 = n_bytes / 32;
+  l2_flush_kernel<<<num_sms() * 4, 512, 0, st>>>(reinterpret_cast<uint4*>(buf), half16, salt++);
+  // the checksum of the read lands in the (already overwritten) first word
+  hbm_read_probe_kernel<<<num_sms() * 4, 512, 0, st>>>(reinterpret_cast<const uint4*>(buf) + half16,
+                                                         half16, reinterpret_cast<uint32_t*>(buf));
   return cudaGetLastError();
 }
 

@@ -164,7 +164,8 @@ int bws_status_word(const void* workspace, uint32_t* status, void* stream);
  * checksum to out. Used to measure the achievable HBM read bandwidth. */
 int bws_hbm_read_probe(const void* src, size_t n_bytes, uint32_t* out, void* stream);
 
-/* Overwrites n_bytes of buf (e.g. 2 x L2) so the next kernel starts cold. */
+/* Leaves L2 cold and clean for the next kernel: writes the first half of buf,
+ * then streams through the second half (n_bytes should be >= 4 x L2). */
 int bws_l2_flush(void* buf, size_t n_bytes, void* stream);
 
 #ifdef __cplusplus
