@@ -18,6 +18,11 @@ from .api import (  # noqa: F401
     hbm_read_probe,
     l2_flush,
     Workspace,
+    MoeLayer,
+    MoeWeights,
+    mxfp4_moe_workspace_size,
+    mxfp4_moe_gemv,
+    mxfp4_moe_inspect,
 )
 
 BWS_STATUS_X_TWO_BANDS = 1

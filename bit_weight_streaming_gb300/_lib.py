@@ -24,6 +24,7 @@ SIGNATURES = {
     "bws_fp8_lmhead_gemv": (I, [P, P, P, I, I, I, P, P, Z, P]),
     "bws_mxfp4_moe_workspace_size": (Z, [P, I, I]),
     "bws_mxfp4_moe_gemv": (I, [P, P, P, I, I, P, P, P, Z, P]),
+    "bws_mxfp4_moe_inspect": (I, [P, P, I, I, P, P, P, P, P]),
     "bws_decode_step_workspace_size": (Z, [P, I]),
     "bws_decode_step_plan_create": (I, [P, I, P]),
     "bws_decode_step_plan_destroy": (None, [P]),

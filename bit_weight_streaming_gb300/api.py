@@ -143,3 +143,82 @@ def hbm_read_probe(src, out):
 def l2_flush(buf):
     _need_cuda(buf)
     check(lib().bws_l2_flush(_ptr(buf), buf.numel() * buf.element_size(), _stream(buf.device)), "bws_l2_flush")
+
+
+# ---- MoE -------------------------------------------------------------------
+
+import ctypes as _C
+
+
+class MoeLayer(_C.Structure):
+    """Mirror of struct bws_moe_layer (include/bws.h)."""
+    _fields_ = [
+        ("n_experts", _C.c_int), ("hidden", _C.c_int), ("inter", _C.c_int),
+        ("gate_up_codes", _C.c_void_p), ("gate_up_codes_stride", _C.c_size_t),
+        ("gate_up_scales", _C.c_void_p), ("gate_up_scales_stride", _C.c_size_t),
+        ("down_codes", _C.c_void_p), ("down_codes_stride", _C.c_size_t),
+        ("down_scales", _C.c_void_p), ("down_scales_stride", _C.c_size_t),
+        ("shared_gate_up_codes", _C.c_void_p), ("shared_gate_up_scales", _C.c_void_p),
+        ("shared_down_codes", _C.c_void_p), ("shared_down_scales", _C.c_void_p),
+    ]
+
+
+class MoeWeights:
+    """Device tensors of one MXFP4 MoE layer, laid out as bws_moe_layer wants:
+    gate_up codes [E, 2*inter, hidden/2], scales [E, 2*inter, hidden/32],
+    down codes [E, hidden, inter/2], scales [E, hidden, inter/32], and the
+    shared expert's four tensors (or None)."""
+
+    def __init__(self, gate_up_codes, gate_up_scales, down_codes, down_scales, shared=None):
+        self.gu_c, self.gu_s, self.dn_c, self.dn_s = gate_up_codes, gate_up_scales, down_codes, down_scales
+        self.shared = shared
+        E, two_i, _ = gate_up_codes.shape
+        self.n_experts, self.inter, self.hidden = E, two_i // 2, down_codes.shape[1]
+
+    def descriptor(self):
+        d = MoeLayer()
+        d.n_experts, d.hidden, d.inter = self.n_experts, self.hidden, self.inter
+        d.gate_up_codes, d.gate_up_codes_stride = self.gu_c.data_ptr(), self.gu_c[0].numel()
+        d.gate_up_scales, d.gate_up_scales_stride = self.gu_s.data_ptr(), self.gu_s[0].numel()
+        d.down_codes, d.down_codes_stride = self.dn_c.data_ptr(), self.dn_c[0].numel()
+        d.down_scales, d.down_scales_stride = self.dn_s.data_ptr(), self.dn_s[0].numel()
+        if self.shared is not None:
+            sgc, sgs, sdc, sds = self.shared
+            d.shared_gate_up_codes, d.shared_gate_up_scales = sgc.data_ptr(), sgs.data_ptr()
+            d.shared_down_codes, d.shared_down_scales = sdc.data_ptr(), sds.data_ptr()
+        return d
+
+
+def mxfp4_moe_workspace_size(layer, N, topk):
+    d = layer.descriptor()
+    return int(lib().bws_mxfp4_moe_workspace_size(_C.addressof(d), N, topk))
+
+
+def mxfp4_moe_gemv(layer, ids, route_w, x, y=None, ws=None):
+    """y bf16 [N, hidden] = shared(x) + sum_k route_w[:, k] * expert_{ids[:, k]}(x)."""
+    _need_cuda(ids, route_w, x, y)
+    N, hidden = x.shape
+    topk = ids.shape[1]
+    if y is None:
+        y = torch.empty((N, hidden), dtype=torch.bfloat16, device=x.device)
+    d = layer.descriptor()
+    buf = _ws(ws, lib().bws_mxfp4_moe_workspace_size(_C.addressof(d), N, topk), x.device)
+    check(lib().bws_mxfp4_moe_gemv(_C.addressof(d), _ptr(ids), _ptr(route_w), N, topk, _ptr(x), _ptr(y),
+                                   _ptr(buf), buf.numel(), _stream(x.device)), "bws_mxfp4_moe_gemv")
+    return y
+
+
+def mxfp4_moe_inspect(layer, ws, N, topk):
+    """(n_slots, slot experts, h bf16 [slots, N, inter], status) of the last call."""
+    import numpy as np
+    d = layer.descriptor()
+    buf = ws.buf if isinstance(ws, Workspace) else ws
+    max_slots = N * topk + (1 if layer.shared is not None else 0)
+    n_slots = _C.c_int(0)
+    status = _C.c_uint32(0)
+    experts = np.zeros(max_slots, dtype=np.int32)
+    h = np.zeros((max_slots, N, layer.inter), dtype=np.uint16)
+    check(lib().bws_mxfp4_moe_inspect(_ptr(buf), _C.addressof(d), N, topk, _C.addressof(n_slots),
+                                      experts.ctypes.data, h.ctypes.data, _C.addressof(status),
+                                      _stream(buf.device)), "bws_mxfp4_moe_inspect")
+    return n_slots.value, experts, h, status.value

@@ -6,13 +6,14 @@
 #include <string.h>
 
 #include "../../include/bws.h"
+#include "bws_abi_util.h"
 #include "bws_internal.h"
 
-using namespace bws;
-
 namespace {
-
 thread_local char g_err[512] = "";
+}
+
+namespace bws {
 
 int fail(int code, const char* fmt, ...) {
   va_list ap;
@@ -30,16 +31,19 @@ int cuda_status(cudaError_t e, const char* what) {
   return fail(BWS_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
 }
 
-bool aligned(const void* p, size_t a) { return ((uintptr_t)p % a) == 0; }
+void clear_error() { g_err[0] = 0; }
 
-cudaStream_t as_stream(void* s) { return reinterpret_cast<cudaStream_t>(s); }
+}  // namespace bws
+
+using namespace bws;
+
+namespace {
 
 int check_tokens(int N) {
   if (N < 1 || N > kMaxTokens) return fail(BWS_ERR_INVALID_ARG, "N = %d must be in [1, %d]", N, kMaxTokens);
   return BWS_OK;
 }
 
-int nseg_of(int d_in) { return (d_in + kSegK - 1) / kSegK; }
 
 // Shared body of every product call: prep the activations, then the product.
 int run_product(int fmt, int epi, GemvParams& p, const uint16_t* x, int N, int d_in, void* ws,
@@ -56,23 +60,32 @@ int run_product(int fmt, int epi, GemvParams& p, const uint16_t* x, int N, int d
     return fail(BWS_ERR_WORKSPACE, "%s: workspace of %zu bytes needed, %zu given", name, L.total, ws_bytes);
   if (!aligned(ws, 256)) return fail(BWS_ERR_MISALIGNED, "%s: workspace must be 256-byte aligned", name);
   char* w = static_cast<char*>(ws);
-  uint16_t* xhi = reinterpret_cast<uint16_t*>(w + L.off_hi);
-  uint16_t* xlo = reinterpret_cast<uint16_t*>(w + L.off_lo);
-  int* xexp = reinterpret_cast<int*>(w + L.off_exp);
-  uint32_t* xflags = reinterpret_cast<uint32_t*>(w + L.off_flags);
-  uint32_t* hdr = reinterpret_cast<uint32_t*>(w + L.off_hdr);
-  p.x.hi = xhi;
-  p.x.lo = xlo;
-  p.x.exp = xexp;
-  p.x.flags = xflags;
-  p.counters = reinterpret_cast<uint32_t*>(w + L.off_counters);
+  PrepParams q = {};
+  q.mode = kPrepCopy;
+  q.x = x;
+  q.ld = d_in;
+  q.N = N;
+  q.d_in = d_in;
+  q.d_in_pad = p.d_in_pad;
+  q.hi = reinterpret_cast<uint16_t*>(w + L.off_hi);
+  q.lo = reinterpret_cast<uint16_t*>(w + L.off_lo);
+  q.exp = reinterpret_cast<int*>(w + L.off_exp);
+  q.flags = reinterpret_cast<uint32_t*>(w + L.off_flags);
+  q.hdr = reinterpret_cast<uint32_t*>(w + L.off_hdr);
+  q.zero_ptr = reinterpret_cast<uint32_t*>(w + L.off_counters);
+  q.zero_words = p.n_tiles;
+  p.x.hi = q.hi;
+  p.x.lo = q.lo;
+  p.x.exp = q.exp;
+  p.x.flags = q.flags;
+  p.x.shared = 1;
+  p.counters = q.zero_ptr;
   p.partials = reinterpret_cast<float*>(w + L.off_partials);
   p.out = out;
   p.out_ld = out_ld;
+  p.out_slot_stride = 0;
   p.prefetch_units = fmt == kFmtFP8 ? 4 : 8;
-  p.prefetch_ahead = 0;
-  cudaError_t e = launch_prep_x(x, N, d_in, p.d_in_pad, xhi, xlo, xexp, xflags, hdr, p.counters,
-                                p.n_tiles, st, true);
+  cudaError_t e = launch_prep(q, st, true);
   if (e != cudaSuccess) return cuda_status(e, name);
   e = launch_gemv(fmt, epi, p, st, true);
   return cuda_status(e, name);

@@ -1,4 +1,4 @@
-// Internal launch interface between the C ABI (abi.cu) and the kernels.
+// Internal launch interface between the C ABI (abi.cu, stack.cu) and the kernels.
 #pragma once
 #include <cuda_runtime.h>
 #include <stddef.h>
@@ -14,10 +14,11 @@ constexpr int kFmtFP8 = 3;
 constexpr int kEpiStoreBF16 = 0;   // y bf16 [N][out_ld]
 constexpr int kEpiStoreF32 = 1;    // y fp32 [N][out_ld]
 constexpr int kEpiResidF32 = 2;    // r fp32 [N][out_ld] += y
-constexpr int kEpiSwiGLU = 3;      // h bf16 = SiLU(gate) * up, mats[0]=gate, mats[1]=up
+constexpr int kEpiSwiGLU = 3;      // h bf16 = SiLU(gate) * up
 
 constexpr int kMaxMats = 4;
 constexpr int kMaxTokens = 8;
+constexpr int kMaxTopk = 8;
 constexpr int kSegK = 128;          // k values per work unit
 constexpr int kWarpsPerCta = 8;
 constexpr int kTileRows = 32;       // two m16 sub-tiles per work unit
@@ -32,44 +33,107 @@ struct GemvMat {
   int tile_begin;          // first tile of this matrix
 };
 
-// Activations as the product kernels read them: per token t, f16 values
-// x * 2^(14 - E_t) ("hi band") and, for elements below 2^-14 after that
-// scaling, x * 2^(43 - E_t) ("lo band"); E_t = floor(log2 max|x_t|).
+// Expert ("slot") mode: the matrices of a product are experts picked on the
+// device. Slot s uses expert slot_expert[s] (-1: the shared expert). Tiles are
+// numbered slot-major; the number of live slots is read from n_slots.
+struct SlotMode {
+  const int* n_slots;          // device [1]; nullptr: plain mode
+  const int* slot_expert;      // device [max_slots]
+  const uint8_t* codes;        // routed expert e starts at codes + e * codes_stride
+  size_t codes_stride;
+  const uint8_t* scales;
+  size_t scales_stride;
+  const uint8_t* shared_codes;
+  const uint8_t* shared_scales;
+  int rows;                    // rows of one matrix (one half for SwiGLU)
+  int up_row_off;              // SwiGLU: first row of the up half in the expert tensor
+  int tiles_per_slot;
+  int max_slots;
+  int n_experts;
+};
+
+// Activations as the product kernels read them. Row (slot, tok) holds, for
+// token tok of slot s, f16 values x * 2^(14 - E) ("hi band") and, for elements
+// below 2^-14 after that scaling, x * 2^(43 - E) ("lo band"), with
+// E = floor(log2 max|x|) of that row. Each slot block has N + 1 rows, the
+// last all zero (read by the MMA columns of absent tokens).
 struct XPrep {
-  const uint16_t* hi;      // f16 [N][d_in_pad]
-  const uint16_t* lo;      // f16 [N][d_in_pad]
-  const int* exp;          // [N]
-  const uint32_t* flags;   // [N] bws_status_bits
+  const uint16_t* hi;      // f16 [slots][N + 1][d_in_pad]
+  const uint16_t* lo;
+  const int* exp;          // [slots][N]
+  const uint32_t* flags;   // [slots][N] bws_status_bits
+  int shared;              // 1: every slot reads slot 0's activations
 };
 
 struct GemvParams {
   GemvMat mats[kMaxMats];
   int n_mats;
+  SlotMode slots;
   int N, d_in, d_in_pad, nseg;
-  int n_tiles;
-  long long n_units;
-  long long n_warps;       // warps that share the units (<= n_units)
+  int n_tiles;             // plain mode: all tiles; slot mode: tiles_per_slot * max_slots
+  long long n_units;       // plain mode only
+  long long n_warps;       // plain mode: warps sharing the units; slot mode: warps launched
   XPrep x;
   void* out;
   int out_ld;
-  float* partials;         // [(n_tiles + n_warps) * kSlotFloats]
+  size_t out_slot_stride;  // elements between slots' outputs
+  float* partials;         // [(n_tiles + warps) * kSlotFloats]
   uint32_t* counters;      // [n_tiles], zero on entry, left zero on exit
-  int prefetch_units;       // units pulled into L2 before waiting on the inputs
-  int prefetch_ahead;       // rolling L2 prefetch distance in units (0 = off)
+  int prefetch_units;      // units pulled into L2 before waiting on the inputs
 };
 
-// Workspace layout of one product call (all offsets 256-byte aligned).
+// Input of the activation prep kernel.
+constexpr int kPrepCopy = 0;      // x bf16 -> bands
+constexpr int kPrepRmsNorm = 1;   // r fp32 -> BF16(RMSNorm(r)) -> bands
+struct PrepParams {
+  int mode;
+  const uint16_t* x;       // kPrepCopy: row (slot, tok) at x + slot * x_slot_stride + tok * ld
+  int ld;
+  size_t x_slot_stride;
+  float* r;                // kPrepRmsNorm: residual [N][d_in]
+  const uint16_t* x0;      // kPrepRmsNorm, optional: r = x0 first
+  float eps;
+  int N, d_in, d_in_pad;
+  const int* n_slots;      // device; nullptr: one slot
+  int max_slots;
+  uint16_t* hi;
+  uint16_t* lo;
+  int* exp;
+  uint32_t* flags;
+  uint32_t* hdr;           // [0] = N (status reads), may be null
+  uint32_t* zero_ptr;      // counters of the next product, zeroed
+  int zero_words;
+};
+
+// Workspace of one product call (all offsets 256-byte aligned).
 struct GemvWorkspace {
   size_t off_hdr, off_exp, off_flags, off_hi, off_lo, off_counters, off_partials, total;
 };
-GemvWorkspace gemv_workspace_layout(int N, int d_in, int n_tiles, long long max_warps);
+GemvWorkspace gemv_workspace_layout(int N, int d_in, int n_tiles, long long max_warps, int slots = 1);
+size_t align256(size_t v);
 int num_sms();
 long long gemv_max_warps();
 
-cudaError_t launch_prep_x(const uint16_t* x, int N, int d_in, int d_in_pad, uint16_t* xhi,
-                          uint16_t* xlo, int* xexp, uint32_t* xflags, uint32_t* hdr,
-                          uint32_t* zero_ptr, int zero_words, cudaStream_t st, bool pdl);
+cudaError_t launch_prep(const PrepParams& q, cudaStream_t st, bool pdl);
 cudaError_t launch_gemv(int fmt, int epi, const GemvParams& p, cudaStream_t st, bool pdl);
+
+// MoE helpers.
+struct MoeRoute {
+  const int32_t* ids;      // [N][topk]
+  const float* route_w;    // [N][topk]
+  int N, topk, n_experts;
+  int has_shared;
+  int max_slots;
+  int* n_slots;            // out [1]
+  int* slot_expert;        // out [max_slots]
+  float* cw;               // out [max_slots][N] combine weights
+  uint32_t* status;        // out [1]: bit 4 set if an id was out of range
+};
+cudaError_t launch_moe_route(const MoeRoute& m, cudaStream_t st, bool pdl);
+// y[tok][i] (+)= sum over live slots s of cw[s][tok] * ys[s][tok][i]
+cudaError_t launch_moe_combine(const float* ys, const float* cw, const int* n_slots, int N, int d,
+                               void* out, int out_mode /* kEpiStoreBF16 or kEpiResidF32 */, cudaStream_t st,
+                               bool pdl);
 
 cudaError_t launch_nvfp4_quantize(const float* W, int d_out, int d_in, uint8_t* codes,
                                   uint8_t* scales, float* tensor_scale, void* ws, cudaStream_t st);

@@ -36,64 +36,105 @@ struct Frag {
   uint4 xl[LO ? 4 : 1];                     // lo band
 };
 
-struct TileRows {
-  int mat[2];
-  int row0[2];        // first row of each sub-tile within its matrix
+// Where a tile's two sub-tiles live.
+struct TileInfo {
+  const uint8_t* codes[2];
+  const uint8_t* scales[2];
+  const float* scale32[2];
+  int d_out[2];        // rows of the matrix (rows >= d_out are padding)
+  int row0[2];         // first row of the sub-tile within its matrix
+  int out_row_off[2];  // output row of the matrix's row 0
+  int slot;
 };
 
-template <int EPI>
-BWS_DEV TileRows tile_rows(const GemvParams& p, int tile) {
-  TileRows tr;
-  if (EPI == kEpiSwiGLU) {
-    tr.mat[0] = 0; tr.mat[1] = 1;
-    tr.row0[0] = tr.row0[1] = tile * 16;
-  } else {
-    int m = 0;
+template <int FMT, int EPI>
+BWS_DEV TileInfo tile_info(const GemvParams& p, int tile) {
+  TileInfo ti;
+  if (p.slots.n_slots != nullptr) {
+    const SlotMode& S = p.slots;
+    const int slot = tile / S.tiles_per_slot;
+    const int rt = tile - slot * S.tiles_per_slot;
+    const int e = __ldg(S.slot_expert + slot);
+    const uint8_t* c = e < 0 ? S.shared_codes : S.codes + (size_t)e * S.codes_stride;
+    const uint8_t* sc = e < 0 ? S.shared_scales : S.scales + (size_t)e * S.scales_stride;
+    const size_t row_bytes = FMT == kFmtFP8 ? (size_t)p.d_in : (size_t)(p.d_in >> 1);
+    const size_t srow_bytes = FMT == kFmtNVFP4 ? (size_t)(p.d_in >> 4) : (size_t)(p.d_in >> 5);
+    ti.slot = slot;
 #pragma unroll
-    for (int i = 1; i < kMaxMats; ++i)
-      if (i < p.n_mats && tile >= p.mats[i].tile_begin) m = i;
-    const int local = tile - p.mats[m].tile_begin;
-    tr.mat[0] = tr.mat[1] = m;
-    tr.row0[0] = local * 32;
-    tr.row0[1] = local * 32 + 16;
+    for (int s = 0; s < 2; ++s) {
+      const int half = (EPI == kEpiSwiGLU && s == 1) ? S.up_row_off : 0;
+      ti.codes[s] = c + (size_t)half * row_bytes;
+      ti.scales[s] = sc + (size_t)half * srow_bytes;
+      ti.scale32[s] = nullptr;
+      ti.d_out[s] = S.rows;
+      ti.row0[s] = EPI == kEpiSwiGLU ? rt * 16 : rt * 32 + 16 * s;
+      ti.out_row_off[s] = 0;
+    }
+    return ti;
   }
-  return tr;
+  ti.slot = 0;
+  if (EPI == kEpiSwiGLU) {
+#pragma unroll
+    for (int s = 0; s < 2; ++s) {
+      ti.codes[s] = p.mats[s].codes;
+      ti.scales[s] = p.mats[s].scales;
+      ti.scale32[s] = p.mats[s].scale32;
+      ti.d_out[s] = p.mats[s].d_out;
+      ti.row0[s] = tile * 16;
+      ti.out_row_off[s] = 0;
+    }
+    return ti;
+  }
+  int m = 0;
+#pragma unroll
+  for (int i = 1; i < kMaxMats; ++i)
+    if (i < p.n_mats && tile >= p.mats[i].tile_begin) m = i;
+  const GemvMat& M = p.mats[m];
+  const int local = tile - M.tile_begin;
+#pragma unroll
+  for (int s = 0; s < 2; ++s) {
+    ti.codes[s] = M.codes;
+    ti.scales[s] = M.scales;
+    ti.scale32[s] = M.scale32;
+    ti.d_out[s] = M.d_out;
+    ti.row0[s] = local * 32 + 16 * s;
+    ti.out_row_off[s] = M.out_row_off;
+  }
+  return ti;
 }
 
-// Per-tile lane pointers: computed once per piece, advanced per unit.
+BWS_DEV int x_block(const GemvParams& p, int slot) { return p.x.shared ? 0 : slot; }
+
+// Per-piece lane pointers.
 template <int FMT>
 struct LanePtrs {
   const uint8_t* c[2][2];
   const uint8_t* sc[2][2];
   const uint16_t* xh;
   const uint16_t* xl;
-  uint32_t rowmask;   // bit 2*s+h: row valid
 };
 
-template <int FMT, int EPI>
-BWS_DEV LanePtrs<FMT> lane_ptrs(const GemvParams& p, const TileRows& tr, int g, int t) {
+template <int FMT>
+BWS_DEV LanePtrs<FMT> lane_ptrs(const GemvParams& p, const TileInfo& ti, int g, int t) {
   LanePtrs<FMT> L;
-  L.rowmask = 0u;
 #pragma unroll
   for (int s = 0; s < 2; ++s) {
-    const GemvMat& M = p.mats[tr.mat[s]];
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
-      const int row = tr.row0[s] + g + 8 * h;
-      const int rr = row < M.d_out ? row : 0;
-      if (row < M.d_out) L.rowmask |= 1u << (2 * s + h);
+      const int row = ti.row0[s] + g + 8 * h;
+      const int rr = row < ti.d_out[s] ? row : 0;   // padding rows read row 0
       if (FMT == kFmtFP8) {
-        L.c[s][h] = M.codes + (size_t)rr * p.d_in + 32 * t;
+        L.c[s][h] = ti.codes[s] + (size_t)rr * p.d_in + 32 * t;
         L.sc[s][h] = nullptr;
       } else {
-        L.c[s][h] = M.codes + (size_t)rr * (p.d_in >> 1) + 16 * t;
-        L.sc[s][h] = FMT == kFmtNVFP4 ? M.scales + (size_t)rr * (p.d_in >> 4) + 2 * t
-                                      : M.scales + (size_t)rr * (p.d_in >> 5) + t;
+        L.c[s][h] = ti.codes[s] + (size_t)rr * (p.d_in >> 1) + 16 * t;
+        L.sc[s][h] = FMT == kFmtNVFP4 ? ti.scales[s] + (size_t)rr * (p.d_in >> 4) + 2 * t
+                                      : ti.scales[s] + (size_t)rr * (p.d_in >> 5) + t;
       }
     }
   }
-  // token rows g >= N read the all-zero row kept after the N real rows
-  const size_t xo = (size_t)(g < p.N ? g : p.N) * p.d_in_pad + 32 * t;
+  // token rows g >= N read the all-zero row after the N real rows
+  const size_t xo = ((size_t)x_block(p, ti.slot) * (p.N + 1) + (g < p.N ? g : p.N)) * p.d_in_pad + 32 * t;
   L.xh = p.x.hi + xo;
   L.xl = p.x.lo + xo;
   return L;
@@ -103,8 +144,8 @@ BWS_DEV LanePtrs<FMT> lane_ptrs(const GemvParams& p, const TileRows& tr, int g, 
 // stored) and lanes past d_in read the row's last 32 weights, which meet the
 // zero padding of the activations, so they add nothing.
 template <int FMT, bool LO>
-BWS_DEV void load_unit(const GemvParams& p, const LanePtrs<FMT>& L, int seg, int g, int t, Frag<FMT, LO>& f) {
-  const int k0 = min(seg * kSegK + 32 * t, p.d_in - 32) - 32 * t;   // lane offset added in L
+BWS_DEV void load_unit(const GemvParams& p, const LanePtrs<FMT>& L, int seg, int t, Frag<FMT, LO>& f) {
+  const int k0 = min(seg * kSegK + 32 * t, p.d_in - 32) - 32 * t;   // lane offset is in L
   const int cb = FMT == kFmtFP8 ? k0 : (k0 >> 1);
 #pragma unroll
   for (int s = 0; s < 2; ++s)
@@ -141,9 +182,7 @@ BWS_DEV uint32_t f16x2_pow2(int k) {
   return h | (h << 16);
 }
 
-// Accumulators: [sub][chain][4].
-constexpr int kChains = 1;
-typedef float Acc[2][kChains][4];
+typedef float Acc[2][4];   // [sub][4 accumulator registers]
 
 template <int FMT, bool LO>
 BWS_DEV void compute_unit(const Frag<FMT, LO>& f, Acc& acc, Acc& accl) {
@@ -157,11 +196,11 @@ BWS_DEV void compute_unit(const Frag<FMT, LO>& f, Acc& acc, Acc& accl) {
         e4m3x4_to_f16x2x2(word_of(f.c[s][1][j >> 2], j & 3), a1, a3);
         const uint32_t b0 = word_of(f.xh[j >> 1], 2 * (j & 1));
         const uint32_t b1 = word_of(f.xh[j >> 1], 2 * (j & 1) + 1);
-        mma_f16_16816(acc[s][(j & 1) % kChains], a0, a1, a2, a3, b0, b1);
+        mma_f16_16816(acc[s], a0, a1, a2, a3, b0, b1);
         if (LO) {
           const uint32_t c0 = word_of(f.xl[j >> 1], 2 * (j & 1));
           const uint32_t c1 = word_of(f.xl[j >> 1], 2 * (j & 1) + 1);
-          mma_f16_16816(accl[s][(j & 1) % kChains], a0, a1, a2, a3, c0, c1);
+          mma_f16_16816(accl[s], a0, a1, a2, a3, c0, c1);
         }
       }
     } else {
@@ -186,8 +225,8 @@ BWS_DEV void compute_unit(const Frag<FMT, LO>& f, Acc& acc, Acc& accl) {
         sref_g = exp2i(rg);
         sref_8 = exp2i(r8);
       }
-      float dm[kChains][4] = {};
-      float dml[kChains][4] = {};
+      float dm[4] = {0.f, 0.f, 0.f, 0.f};
+      float dml[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
       for (int w = 0; w < 4; ++w) {
         uint32_t p0, p1, p2, p3, q0, q1, q2, q3;
@@ -196,30 +235,25 @@ BWS_DEV void compute_unit(const Frag<FMT, LO>& f, Acc& acc, Acc& accl) {
         const uint32_t sa = mg[w >> 1], sb = m8[w >> 1];
         p0 = hmul2_u32(p0, sa); p1 = hmul2_u32(p1, sa); p2 = hmul2_u32(p2, sa); p3 = hmul2_u32(p3, sa);
         q0 = hmul2_u32(q0, sb); q1 = hmul2_u32(q1, sb); q2 = hmul2_u32(q2, sb); q3 = hmul2_u32(q3, sb);
-        float(&D0)[4] = FMT == kFmtMXFP4 ? dm[0] : acc[s][0];
-        float(&D1)[4] = FMT == kFmtMXFP4 ? dm[1 % kChains] : acc[s][1 % kChains];
-        mma_f16_16816(D0, p0, q0, p1, q1, f.xh[w].x, f.xh[w].y);
-        mma_f16_16816(D1, p2, q2, p3, q3, f.xh[w].z, f.xh[w].w);
+        float(&D)[4] = FMT == kFmtMXFP4 ? dm : acc[s];
+        mma_f16_16816(D, p0, q0, p1, q1, f.xh[w].x, f.xh[w].y);
+        mma_f16_16816(D, p2, q2, p3, q3, f.xh[w].z, f.xh[w].w);
         if (LO) {
-          float(&L0)[4] = FMT == kFmtMXFP4 ? dml[0] : accl[s][0];
-          float(&L1)[4] = FMT == kFmtMXFP4 ? dml[1 % kChains] : accl[s][1 % kChains];
-          mma_f16_16816(L0, p0, q0, p1, q1, f.xl[w].x, f.xl[w].y);
-          mma_f16_16816(L1, p2, q2, p3, q3, f.xl[w].z, f.xl[w].w);
+          float(&DL)[4] = FMT == kFmtMXFP4 ? dml : accl[s];
+          mma_f16_16816(DL, p0, q0, p1, q1, f.xl[w].x, f.xl[w].y);
+          mma_f16_16816(DL, p2, q2, p3, q3, f.xl[w].z, f.xl[w].w);
         }
       }
       if constexpr (FMT == kFmtMXFP4) {
-#pragma unroll
-        for (int c = 0; c < kChains; ++c) {
-          acc[s][c][0] = __fmaf_rn(dm[c][0], sref_g, acc[s][c][0]);
-          acc[s][c][1] = __fmaf_rn(dm[c][1], sref_g, acc[s][c][1]);
-          acc[s][c][2] = __fmaf_rn(dm[c][2], sref_8, acc[s][c][2]);
-          acc[s][c][3] = __fmaf_rn(dm[c][3], sref_8, acc[s][c][3]);
-          if (LO) {
-            accl[s][c][0] = __fmaf_rn(dml[c][0], sref_g, accl[s][c][0]);
-            accl[s][c][1] = __fmaf_rn(dml[c][1], sref_g, accl[s][c][1]);
-            accl[s][c][2] = __fmaf_rn(dml[c][2], sref_8, accl[s][c][2]);
-            accl[s][c][3] = __fmaf_rn(dml[c][3], sref_8, accl[s][c][3]);
-          }
+        acc[s][0] = __fmaf_rn(dm[0], sref_g, acc[s][0]);
+        acc[s][1] = __fmaf_rn(dm[1], sref_g, acc[s][1]);
+        acc[s][2] = __fmaf_rn(dm[2], sref_8, acc[s][2]);
+        acc[s][3] = __fmaf_rn(dm[3], sref_8, acc[s][3]);
+        if (LO) {
+          accl[s][0] = __fmaf_rn(dml[0], sref_g, accl[s][0]);
+          accl[s][1] = __fmaf_rn(dml[1], sref_g, accl[s][1]);
+          accl[s][2] = __fmaf_rn(dml[2], sref_8, accl[s][2]);
+          accl[s][3] = __fmaf_rn(dml[3], sref_8, accl[s][3]);
         }
       }
     }
@@ -231,73 +265,73 @@ BWS_DEV float silu_mul(float g, float u) {
   return __fmul_rn(sg, u);
 }
 
-// Scale raw sums v[sub][4] to outputs and store them.
+// Scale raw sums v[sub][4] to outputs and store them. Register i of a lane
+// holds (row g + 8*(i>>1), token 2t + (i&1)).
 template <int FMT, int EPI>
-BWS_DEV void finish_tile(const GemvParams& p, const TileRows& tr, int g, int t,
-                         const float (&v)[2][4], const int (&xexp)[2]) {
+BWS_DEV void finish_tile(const GemvParams& p, const TileInfo& ti, int g, int t, const float (&v)[2][4]) {
+  const int xb = x_block(p, ti.slot);
+  int xexp[2];
+#pragma unroll
+  for (int i = 0; i < 2; ++i) {
+    const int tok = 2 * t + i;
+    xexp[i] = tok < p.N ? __ldg(p.x.exp + xb * p.N + tok) : 0;
+  }
   float val[2][4];
 #pragma unroll
   for (int s = 0; s < 2; ++s) {
-    const GemvMat& M = p.mats[tr.mat[s]];
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
-      const int row = tr.row0[s] + g + 8 * (i >> 1);
+      const int row = ti.row0[s] + g + 8 * (i >> 1);
       float sc = 1.0f;
-      if (FMT == kFmtNVFP4) sc = __ldg(M.scale32);
-      if (FMT == kFmtFP8) sc = row < M.d_out ? __ldg(M.scale32 + row) : 0.0f;
+      if (FMT == kFmtNVFP4 && ti.scale32[s] != nullptr) sc = __ldg(ti.scale32[s]);
+      if (FMT == kFmtFP8) sc = row < ti.d_out[s] ? __ldg(ti.scale32[s] + row) : 0.0f;
       val[s][i] = ldexp_exact(__fmul_rn(v[s][i], sc), xexp[i & 1] - 14);
     }
   }
+  char* out = reinterpret_cast<char*>(p.out);
   if constexpr (EPI == kEpiSwiGLU) {
-    const int d_out = p.mats[0].d_out;
+    __nv_bfloat16* h = reinterpret_cast<__nv_bfloat16*>(out) + (size_t)ti.slot * p.out_slot_stride;
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
-      const int row = tr.row0[0] + g + 8 * (i >> 1);
+      const int row = ti.row0[0] + g + 8 * (i >> 1);
       const int tok = 2 * t + (i & 1);
-      if (row < d_out && tok < p.N) {
-        const float h = silu_mul(val[0][i], val[1][i]);
-        reinterpret_cast<__nv_bfloat16*>(p.out)[(size_t)tok * p.out_ld + row] = __float2bfloat16_rn(h);
-      }
+      if (row < ti.d_out[0] && tok < p.N)
+        h[(size_t)tok * p.out_ld + row] = __float2bfloat16_rn(silu_mul(val[0][i], val[1][i]));
     }
   } else {
 #pragma unroll
-  for (int s = 0; s < 2; ++s) {
-    const GemvMat& M = p.mats[tr.mat[s]];
+    for (int s = 0; s < 2; ++s) {
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const int row = tr.row0[s] + g + 8 * (i >> 1);
-      const int tok = 2 * t + (i & 1);
-      if (row < M.d_out && tok < p.N) {
-        const size_t o = (size_t)tok * p.out_ld + M.out_row_off + row;
-        if (EPI == kEpiStoreBF16)
-          reinterpret_cast<__nv_bfloat16*>(p.out)[o] = __float2bfloat16_rn(val[s][i]);
-        else if (EPI == kEpiStoreF32)
-          reinterpret_cast<float*>(p.out)[o] = val[s][i];
-        else
-          reinterpret_cast<float*>(p.out)[o] = __fadd_rn(reinterpret_cast<float*>(p.out)[o], val[s][i]);
+      for (int i = 0; i < 4; ++i) {
+        const int row = ti.row0[s] + g + 8 * (i >> 1);
+        const int tok = 2 * t + (i & 1);
+        if (row < ti.d_out[s] && tok < p.N) {
+          const size_t o = (size_t)ti.slot * p.out_slot_stride + (size_t)tok * p.out_ld + ti.out_row_off[s] + row;
+          if (EPI == kEpiStoreBF16)
+            reinterpret_cast<__nv_bfloat16*>(out)[o] = __float2bfloat16_rn(val[s][i]);
+          else if (EPI == kEpiStoreF32)
+            reinterpret_cast<float*>(out)[o] = val[s][i];
+          else
+            reinterpret_cast<float*>(out)[o] = __fadd_rn(reinterpret_cast<float*>(out)[o], val[s][i]);
+        }
       }
     }
   }
-  }
 }
 
-BWS_DEV long long owner_warp(long long u, long long U, long long W) {
-  return ((u + 1) * W - 1) / U;
-}
+BWS_DEV long long owner_warp(long long u, long long U, long long W) { return ((u + 1) * W - 1) / U; }
 BWS_DEV long long range_begin(long long w, long long U, long long W) { return w * U / W; }
 
 // End of a warp's piece of a tile: finish directly, or deposit the partial
 // sums and let the last contributor finish the tile.
 template <int FMT, int EPI>
-BWS_DEV void end_piece(const GemvParams& p, int tile, long long warp_id, bool whole,
-                       float (&v)[2][4], const int (&xexp)[2], int lane) {
+BWS_DEV void end_piece(const GemvParams& p, const TileInfo& ti, int tile, long long warp_id, bool whole,
+                       const float (&v)[2][4], long long U, long long W, int lane) {
   const int g = lane >> 2, t = lane & 3;
-  const TileRows tr = tile_rows<EPI>(p, tile);
   if (whole) {
-    finish_tile<FMT, EPI>(p, tr, g, t, v, xexp);
+    finish_tile<FMT, EPI>(p, ti, g, t, v);
     return;
   }
-  const long long U = p.n_units, W = p.n_warps;
   float4* slot = reinterpret_cast<float4*>(p.partials) + (size_t)(tile + warp_id) * (kSlotFloats / 4);
   slot[lane] = make_float4(v[0][0], v[0][1], v[0][2], v[0][3]);
   slot[32 + lane] = make_float4(v[1][0], v[1][1], v[1][2], v[1][3]);
@@ -312,89 +346,45 @@ BWS_DEV void end_piece(const GemvParams& p, int tile, long long warp_id, bool wh
   __threadfence();
   float s[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
   for (long long w = w0; w <= w1; ++w) {
-    const float4* o = reinterpret_cast<const float4*>(p.partials) + (size_t)(tile + w) * (kSlotFloats / 4);
     float4 a, b;
     if (w == warp_id) {
       a = make_float4(v[0][0], v[0][1], v[0][2], v[0][3]);
       b = make_float4(v[1][0], v[1][1], v[1][2], v[1][3]);
     } else {
+      const float4* o = reinterpret_cast<const float4*>(p.partials) + (size_t)(tile + w) * (kSlotFloats / 4);
       a = ld_cg_f4(o + lane);
       b = ld_cg_f4(o + 32 + lane);
     }
     s[0][0] += a.x; s[0][1] += a.y; s[0][2] += a.z; s[0][3] += a.w;
     s[1][0] += b.x; s[1][1] += b.y; s[1][2] += b.z; s[1][3] += b.w;
   }
-  finish_tile<FMT, EPI>(p, tr, g, t, s, xexp);
+  finish_tile<FMT, EPI>(p, ti, g, t, s);
   if (lane == 0) p.counters[tile] = 0u;
 }
 
-// Pull unit u's weights of this warp's 32 rows towards L2 (lane l: row l).
-template <int FMT, int EPI>
-BWS_DEV void prefetch_unit(const GemvParams& p, long long u, int lane) {
-  const int tile = (int)(u / p.nseg);
-  const int seg = (int)(u % p.nseg);
-  const TileRows tr = tile_rows<EPI>(p, tile);
-  const int s = lane >> 4;
-  const GemvMat& M = p.mats[tr.mat[s]];
-  const int row = tr.row0[s] + (lane & 15);
-  if (row >= M.d_out) return;
-  if (FMT == kFmtFP8) {
-    const uint8_t* a = M.codes + (size_t)row * p.d_in + seg * kSegK;
-    const int nb = min(kSegK, p.d_in - seg * kSegK);
-    if (nb >= 16) prefetch_l2_bulk(a, (uint32_t)(nb & ~15));
-  } else {
-    const uint8_t* a = M.codes + (size_t)row * (p.d_in >> 1) + seg * (kSegK / 2);
-    const int nb = min(kSegK / 2, (p.d_in >> 1) - seg * (kSegK / 2));
-    if (nb >= 16) prefetch_l2_bulk(a, (uint32_t)(nb & ~15));
-    const uint8_t* sa = FMT == kFmtNVFP4 ? M.scales + (size_t)row * (p.d_in >> 4) + seg * (kSegK / 16)
-                                         : M.scales + (size_t)row * (p.d_in >> 5) + seg * (kSegK / 32);
-    asm volatile("prefetch.global.L2 [%0];" :: "l"(sa));
-  }
-}
-
-// Lane l pulls row l's bytes of units [sa, sb] of a tile into L2 (one op).
-template <int FMT>
-BWS_DEV void prefetch_rows(const GemvParams& p, const TileRows& tr, int sa, int sb, int lane) {
-  const int sub = lane >> 4;
-  const GemvMat& M = p.mats[tr.mat[sub]];
-  const int row = tr.row0[sub] + (lane & 15);
-  if (row >= M.d_out || sb < sa) return;
-  const int per = FMT == kFmtFP8 ? kSegK : kSegK / 2;
-  const size_t row_bytes = FMT == kFmtFP8 ? (size_t)p.d_in : (size_t)(p.d_in >> 1);
-  const size_t kb0 = (size_t)sa * per;
-  size_t nb = (size_t)(sb - sa + 1) * per;
-  if (kb0 + nb > row_bytes) nb = row_bytes - kb0;
-  if (nb >= 16) prefetch_l2_bulk(M.codes + (size_t)row * row_bytes + kb0, (uint32_t)(nb & ~(size_t)15));
-}
-
-// One piece: units [seg0, seg1] of one tile, software-pipelined two deep.
+// One piece: units [seg0, seg1] of one tile, software-pipelined two deep
+// (one unit at a time on the rare two-band path).
 template <int FMT, int EPI, bool LO>
-BWS_DEV void run_piece(const GemvParams& p, int tile, int seg0, int seg1, long long warp_id, int lane,
-                       const int (&xexp)[2]) {
+BWS_DEV void run_piece(const GemvParams& p, int tile, int seg0, int seg1, long long warp_id, long long U,
+                       long long W, int lane) {
   const int g = lane >> 2, t = lane & 3;
-  const TileRows tr = tile_rows<EPI>(p, tile);
-  const LanePtrs<FMT> L = lane_ptrs<FMT, EPI>(p, tr, g, t);
+  const TileInfo ti = tile_info<FMT, EPI>(p, tile);
+  const LanePtrs<FMT> L = lane_ptrs<FMT>(p, ti, g, t);
   Acc acc = {}, accl = {};
   if (LO) {
-    // rare path (two activation bands): one unit at a time
     for (int seg = seg0; seg <= seg1; ++seg) {
       Frag<FMT, true> f;
-      load_unit<FMT, true>(p, L, seg, g, t, f);
+      load_unit<FMT, true>(p, L, seg, t, f);
       compute_unit<FMT, true>(f, acc, accl);
     }
   } else {
     Frag<FMT, false> fa, fb;
-    const int P = p.prefetch_ahead;           // L2 prefetch window in units
-    if (P > 0) prefetch_rows<FMT>(p, tr, seg0, min(seg1, seg0 + P - 1), lane);
-    load_unit<FMT, false>(p, L, seg0, g, t, fa);
+    load_unit<FMT, false>(p, L, seg0, t, fa);
     for (int seg = seg0; seg <= seg1; seg += 2) {
-      if (seg + 1 <= seg1) load_unit<FMT, false>(p, L, seg + 1, g, t, fb);
-      // every P/2 units, extend the prefetched window to P units ahead
-      if (P > 0 && ((seg - seg0) % (P >> 1)) < 2 && ((seg - seg0) % (P >> 1)) == 0 && seg + P <= seg1)
-        prefetch_rows<FMT>(p, tr, seg + P - (P >> 1) + 1, min(seg1, seg + P), lane);
+      if (seg + 1 <= seg1) load_unit<FMT, false>(p, L, seg + 1, t, fb);
       compute_unit<FMT, false>(fa, acc, accl);
       if (seg + 1 > seg1) break;
-      if (seg + 2 <= seg1) load_unit<FMT, false>(p, L, seg + 2, g, t, fa);
+      if (seg + 2 <= seg1) load_unit<FMT, false>(p, L, seg + 2, t, fa);
       compute_unit<FMT, false>(fb, acc, accl);
     }
   }
@@ -402,40 +392,26 @@ BWS_DEV void run_piece(const GemvParams& p, int tile, int seg0, int seg1, long l
 #pragma unroll
   for (int s = 0; s < 2; ++s)
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      float a = acc[s][0][i], al = accl[s][0][i];
-#pragma unroll
-      for (int c = 1; c < kChains; ++c) { a = __fadd_rn(a, acc[s][c][i]); al = __fadd_rn(al, accl[s][c][i]); }
-      v[s][i] = LO ? __fmaf_rn(al, 0x1p-29f, a) : a;
-    }
+    for (int i = 0; i < 4; ++i) v[s][i] = LO ? __fmaf_rn(accl[s][i], 0x1p-29f, acc[s][i]) : acc[s][i];
   const bool whole = seg0 == 0 && seg1 == p.nseg - 1;
-  end_piece<FMT, EPI>(p, tile, warp_id, whole, v, xexp, lane);
+  end_piece<FMT, EPI>(p, ti, tile, warp_id, whole, v, U, W, lane);
 }
 
-// The two-band path is rare; keep it out of line so that its register
-// needs do not constrain the common path.
-template <int FMT, int EPI, bool LO>
-__device__ __noinline__ void run_range_lo(const GemvParams& p, long long u, long long u_end, long long warp_id,
-                                          int lane, int xe0, int xe1);
-
-template <int FMT, int EPI, bool LO>
-BWS_DEV void run_range(const GemvParams& p, long long u, long long u_end, long long warp_id, int lane,
-                       const int (&xexp)[2]) {
-  while (u < u_end) {
-    const int tile = (int)(u / p.nseg);
-    const int seg0 = (int)(u % p.nseg);
-    const long long left = u_end - u;
-    const int seg1 = (long long)(p.nseg - 1 - seg0) < left ? p.nseg - 1 : seg0 + (int)left - 1;
-    run_piece<FMT, EPI, LO>(p, tile, seg0, seg1, warp_id, lane, xexp);
-    u += seg1 - seg0 + 1;
-  }
+// The two-band path is rare; keep it out of line so that its register needs
+// do not constrain the common path.
+template <int FMT, int EPI>
+__device__ __noinline__ void run_piece_lo(const GemvParams& p, int tile, int seg0, int seg1, long long warp_id,
+                                          long long U, long long W, int lane) {
+  run_piece<FMT, EPI, true>(p, tile, seg0, seg1, warp_id, U, W, lane);
 }
 
-template <int FMT, int EPI, bool LO>
-__device__ __noinline__ void run_range_lo(const GemvParams& p, long long u, long long u_end, long long warp_id,
-                                          int lane, int xe0, int xe1) {
-  const int xexp[2] = {xe0, xe1};
-  run_range<FMT, EPI, true>(p, u, u_end, warp_id, lane, xexp);
+template <int FMT, int EPI>
+BWS_DEV bool piece_needs_lo(const GemvParams& p, int tile) {
+  const int slot = p.slots.n_slots != nullptr ? tile / p.slots.tiles_per_slot : 0;
+  const int xb = x_block(p, slot);
+  uint32_t f = 0u;
+  for (int tok = 0; tok < p.N; ++tok) f |= __ldg(p.x.flags + xb * p.N + tok);
+  return (f & 1u) != 0u;
 }
 
 #ifndef BWS_GEMV_MIN_BLOCKS
@@ -447,108 +423,187 @@ __global__ void __launch_bounds__(kWarpsPerCta * 32, BWS_GEMV_MIN_BLOCKS) gemv_k
   const int lane = threadIdx.x & 31;
   const long long warp_id = (long long)blockIdx.x * kWarpsPerCta + (threadIdx.x >> 5);
   pdl_launch_dependents();
-  if (warp_id >= p.n_warps) { pdl_wait(); return; }
-  const long long U = p.n_units, W = p.n_warps;
-  const long long u0 = range_begin(warp_id, U, W);
-  const long long u1 = range_begin(warp_id + 1, U, W);
-
-  // Weights do not depend on earlier kernels: start pulling the first units
-  // of this warp's range into L2 before waiting for the activations (one bulk
-  // prefetch per lane, lane l covering row l of the first tile piece).
-  if (p.prefetch_units > 0) {
-    const int tile = (int)(u0 / p.nseg);
-    const int seg = (int)(u0 % p.nseg);
-    long long nu = p.nseg - seg;
-    if (nu > p.prefetch_units) nu = p.prefetch_units;
-    if (nu > u1 - u0) nu = u1 - u0;
-    const TileRows tr = tile_rows<EPI>(p, tile);
-    const int sub = lane >> 4;
-    const GemvMat& M = p.mats[tr.mat[sub]];
-    const int row = tr.row0[sub] + (lane & 15);
-    if (row < M.d_out && nu > 0) {
-      const int per = FMT == kFmtFP8 ? kSegK : kSegK / 2;
-      const size_t row_bytes = FMT == kFmtFP8 ? (size_t)p.d_in : (size_t)(p.d_in >> 1);
-      const size_t kb0 = (size_t)seg * per;
-      size_t nb = (size_t)nu * per;
-      if (kb0 + nb > row_bytes) nb = row_bytes - kb0;
-      if (nb >= 16) prefetch_l2_bulk(M.codes + (size_t)row * row_bytes + kb0, (uint32_t)(nb & ~(size_t)15));
+  long long U, W;
+  if (p.slots.n_slots == nullptr) {
+    U = p.n_units;
+    W = p.n_warps;
+    if (warp_id >= W) {
+      pdl_wait();
+      return;
     }
+    // Weights do not depend on earlier kernels: start pulling the first units
+    // of this warp's range into L2 before waiting for the activations (one
+    // bulk prefetch per lane, lane l covering row l of the first piece).
+    const long long u0 = range_begin(warp_id, U, W), u1 = range_begin(warp_id + 1, U, W);
+    if (p.prefetch_units > 0) {
+      const int tile = (int)(u0 / p.nseg);
+      const int seg = (int)(u0 % p.nseg);
+      long long nu = p.nseg - seg;
+      if (nu > p.prefetch_units) nu = p.prefetch_units;
+      if (nu > u1 - u0) nu = u1 - u0;
+      const TileInfo ti = tile_info<FMT, EPI>(p, tile);
+      const int sub = lane >> 4;
+      const int row = ti.row0[sub] + (lane & 15);
+      if (row < ti.d_out[sub] && nu > 0) {
+        const int per = FMT == kFmtFP8 ? kSegK : kSegK / 2;
+        const size_t row_bytes = FMT == kFmtFP8 ? (size_t)p.d_in : (size_t)(p.d_in >> 1);
+        const size_t kb0 = (size_t)seg * per;
+        size_t nb = (size_t)nu * per;
+        if (kb0 + nb > row_bytes) nb = row_bytes - kb0;
+        if (nb >= 16) prefetch_l2_bulk(ti.codes[sub] + (size_t)row * row_bytes + kb0, (uint32_t)(nb & ~(size_t)15));
+      }
+    }
+    pdl_wait();
+  } else {
+    pdl_wait();
+    const long long n_slots = __ldg(p.slots.n_slots);
+    U = n_slots * p.slots.tiles_per_slot * p.nseg;
+    W = p.n_warps < U ? p.n_warps : U;
+    if (warp_id >= W) return;
   }
-  pdl_wait();
-
-  int xexp[2];
-  uint32_t flags = 0u;
-#pragma unroll
-  for (int i = 0; i < 2; ++i) {
-    const int tok = 2 * (lane & 3) + i;
-    xexp[i] = tok < p.N ? __ldg(p.x.exp + tok) : 0;
+  long long u = range_begin(warp_id, U, W);
+  const long long u_end = range_begin(warp_id + 1, U, W);
+  while (u < u_end) {
+    const int tile = (int)(u / p.nseg);
+    const int seg0 = (int)(u % p.nseg);
+    const long long left = u_end - u;
+    const int seg1 = (long long)(p.nseg - 1 - seg0) < left ? p.nseg - 1 : seg0 + (int)left - 1;
+    if (piece_needs_lo<FMT, EPI>(p, tile))
+      run_piece_lo<FMT, EPI>(p, tile, seg0, seg1, warp_id, U, W, lane);
+    else
+      run_piece<FMT, EPI, false>(p, tile, seg0, seg1, warp_id, U, W, lane);
+    u += seg1 - seg0 + 1;
   }
-  for (int tok = 0; tok < p.N; ++tok) flags |= __ldg(p.x.flags + tok);
-  if (flags & 1u)
-    run_range_lo<FMT, EPI, true>(p, u0, u1, warp_id, lane, xexp[0], xexp[1]);
-  else
-    run_range<FMT, EPI, false>(p, u0, u1, warp_id, lane, xexp);
 }
 
 // ---- activation prep ----------------------------------------------------------
 
-// One CTA per token: E = floor(log2 max|x|), then the two f16 bands. Each
-// thread handles 8-element chunks (d_in % 32 == 0, so a chunk never straddles
-// d_in). Also zeroes the counters of the product that follows.
+// One CTA per (slot, token) row: optionally RMSNorm, then E = floor(log2
+// max|x|) and the two f16 bands. Each thread handles 8-element chunks
+// (d_in % 32 == 0, so a chunk never straddles d_in). Also zeroes the counters
+// of the product that follows.
 constexpr int kPrepThreads = 1024;
-__global__ void __launch_bounds__(kPrepThreads) prep_x_kernel(const uint16_t* __restrict__ x, int N, int d_in,
-                                                              int d_in_pad, uint16_t* __restrict__ xhi,
-                                                              uint16_t* __restrict__ xlo, int* __restrict__ xexp,
-                                                              uint32_t* __restrict__ xflags, uint32_t* __restrict__ hdr,
-                                                              uint32_t* __restrict__ zero_ptr, int zero_words) {
+
+BWS_DEV float block_reduce_max(float v, float* sm) {
+  v = warp_max(v);
+  __syncthreads();
+  if ((threadIdx.x & 31) == 0) sm[threadIdx.x >> 5] = v;
+  __syncthreads();
+  float r = 0.0f;
+#pragma unroll 8
+  for (int i = 0; i < kPrepThreads / 32; ++i) r = fmaxf(r, sm[i]);
+  return r;
+}
+BWS_DEV float block_reduce_sum(float v, float* sm) {
+  v = warp_sum(v);
+  __syncthreads();
+  if ((threadIdx.x & 31) == 0) sm[threadIdx.x >> 5] = v;
+  __syncthreads();
+  float r = 0.0f;
+  for (int i = 0; i < kPrepThreads / 32; ++i) r += sm[i];   // fixed order
+  return r;
+}
+
+BWS_DEV float bf16_bits_to_f32(uint32_t b) { return __uint_as_float(b << 16); }
+
+// The row's values as BF16 bit patterns, chunk c (8 values).
+BWS_DEV void prep_chunk(const PrepParams& q, int c, int nchunk, const float* rr, const uint4* xr, float inv_rms,
+                        uint32_t (&w)[4]) {
+  if (c >= nchunk) {
+    w[0] = w[1] = w[2] = w[3] = 0u;
+  } else if (q.mode == kPrepRmsNorm) {
+    const float4 a = reinterpret_cast<const float4*>(rr)[2 * c];
+    const float4 b = reinterpret_cast<const float4*>(rr)[2 * c + 1];
+    const float v[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const uint32_t lo = __bfloat16_as_ushort(__float2bfloat16_rn(__fmul_rn(v[2 * i], inv_rms)));
+      const uint32_t hi = __bfloat16_as_ushort(__float2bfloat16_rn(__fmul_rn(v[2 * i + 1], inv_rms)));
+      w[i] = lo | (hi << 16);
+    }
+  } else {
+    const uint4 b = __ldg(xr + c);
+    w[0] = b.x; w[1] = b.y; w[2] = b.z; w[3] = b.w;
+  }
+}
+
+__global__ void __launch_bounds__(kPrepThreads) prep_kernel(const __grid_constant__ PrepParams q) {
   pdl_launch_dependents();
   pdl_wait();
-  for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < zero_words; i += gridDim.x * blockDim.x)
-    zero_ptr[i] = 0u;
-  if (blockIdx.x == 0) {   // the all-zero token row N read by unused MMA columns
-    uint4* zh = reinterpret_cast<uint4*>(xhi + (size_t)N * d_in_pad);
-    uint4* zl = reinterpret_cast<uint4*>(xlo + (size_t)N * d_in_pad);
-    for (int c = threadIdx.x; c < (d_in_pad >> 3); c += blockDim.x) {
+  for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < q.zero_words; i += gridDim.x * blockDim.x)
+    q.zero_ptr[i] = 0u;
+  const int slot = blockIdx.x / q.N;
+  const int tok = blockIdx.x - slot * q.N;
+  const int n_slots = q.n_slots != nullptr ? __ldg(q.n_slots) : 1;
+  if (slot >= n_slots) return;
+  if (blockIdx.x == 0 && threadIdx.x == 0 && q.hdr != nullptr) q.hdr[0] = (uint32_t)q.N;
+  __shared__ float sm[kPrepThreads / 32];
+  __shared__ uint32_t sf[kPrepThreads / 32];
+  const size_t rowbase = ((size_t)slot * (q.N + 1)) * q.d_in_pad;
+  if (tok == 0) {   // this slot's all-zero row
+    uint4* zh = reinterpret_cast<uint4*>(q.hi + rowbase + (size_t)q.N * q.d_in_pad);
+    uint4* zl = reinterpret_cast<uint4*>(q.lo + rowbase + (size_t)q.N * q.d_in_pad);
+    for (int c = threadIdx.x; c < (q.d_in_pad >> 3); c += blockDim.x) {
       zh[c] = make_uint4(0, 0, 0, 0);
       zl[c] = make_uint4(0, 0, 0, 0);
     }
   }
-  const int tok = blockIdx.x;
-  if (tok >= N) return;
-  if (tok == 0 && threadIdx.x == 0) hdr[0] = (uint32_t)N;
-  const uint4* xr = reinterpret_cast<const uint4*>(x + (size_t)tok * d_in);
-  const int nchunk = d_in >> 3, nchunk_pad = d_in_pad >> 3;
+  const int nchunk = q.d_in >> 3, nchunk_pad = q.d_in_pad >> 3;
+  float inv_rms = 1.0f;
+  const uint4* xr = nullptr;
+  float* rr = nullptr;
+  if (q.mode == kPrepRmsNorm) {
+    rr = q.r + (size_t)tok * q.d_in;
+    const uint4* x0 = q.x0 != nullptr ? reinterpret_cast<const uint4*>(q.x0 + (size_t)tok * q.d_in) : nullptr;
+    float ss = 0.0f;
+    for (int c = threadIdx.x; c < nchunk; c += blockDim.x) {
+      float v[8];
+      if (x0 != nullptr) {
+        const uint4 b = __ldg(x0 + c);
+        const uint32_t w[4] = {b.x, b.y, b.z, b.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          v[2 * i] = bf16_bits_to_f32(w[i] & 0xFFFF);
+          v[2 * i + 1] = bf16_bits_to_f32(w[i] >> 16);
+        }
+        reinterpret_cast<float4*>(rr)[2 * c] = make_float4(v[0], v[1], v[2], v[3]);
+        reinterpret_cast<float4*>(rr)[2 * c + 1] = make_float4(v[4], v[5], v[6], v[7]);
+      } else {
+        const float4 a = reinterpret_cast<const float4*>(rr)[2 * c];
+        const float4 b = reinterpret_cast<const float4*>(rr)[2 * c + 1];
+        v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w; v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
+      }
+#pragma unroll
+      for (int i = 0; i < 8; ++i) ss = __fmaf_rn(v[i], v[i], ss);
+    }
+    const float ms = __fdiv_rn(block_reduce_sum(ss, sm), (float)q.d_in);
+    inv_rms = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(ms, q.eps)));
+  } else {
+    xr = reinterpret_cast<const uint4*>(q.x + (size_t)slot * q.x_slot_stride + (size_t)tok * q.ld);
+  }
   float m = 0.0f;
   for (int c = threadIdx.x; c < nchunk; c += blockDim.x) {
-    const uint4 v = __ldg(xr + c);
-    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+    uint32_t w[4];
+    prep_chunk(q, c, nchunk, rr, xr, inv_rms, w);
 #pragma unroll
     for (int i = 0; i < 4; ++i)
-      m = fmaxf(m, fmaxf(fabsf(__uint_as_float(w[i] << 16)), fabsf(__uint_as_float(w[i] & 0xFFFF0000u))));
+      m = fmaxf(m, fmaxf(fabsf(bf16_bits_to_f32(w[i] & 0xFFFF)), fabsf(bf16_bits_to_f32(w[i] >> 16))));
   }
-  m = warp_max(m);
-  __shared__ float sm[kPrepThreads / 32];
-  __shared__ uint32_t sf[kPrepThreads / 32];
-  if ((threadIdx.x & 31) == 0) sm[threadIdx.x >> 5] = m;
-  __syncthreads();
-  float mx = 0.0f;
-#pragma unroll 8
-  for (int i = 0; i < kPrepThreads / 32; ++i) mx = fmaxf(mx, sm[i]);
+  const float mx = block_reduce_max(m, sm);
   const int E = mx > 0.0f ? floor_log2_abs(mx) : 0;
   uint32_t flags = 0u;
-  uint4* hi4 = reinterpret_cast<uint4*>(xhi + (size_t)tok * d_in_pad);
-  uint4* lo4 = reinterpret_cast<uint4*>(xlo + (size_t)tok * d_in_pad);
+  uint4* hi4 = reinterpret_cast<uint4*>(q.hi + rowbase + (size_t)tok * q.d_in_pad);
+  uint4* lo4 = reinterpret_cast<uint4*>(q.lo + rowbase + (size_t)tok * q.d_in_pad);
   for (int c = threadIdx.x; c < nchunk_pad; c += blockDim.x) {
-    uint4 v = make_uint4(0, 0, 0, 0);
-    if (c < nchunk) v = __ldg(xr + c);
-    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+    uint32_t w[4];
+    prep_chunk(q, c, nchunk, rr, xr, inv_rms, w);
     uint32_t h[4], l[4];
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
       uint32_t hh[2], ll[2];
 #pragma unroll
       for (int j = 0; j < 2; ++j) {
-        const float f = __uint_as_float(j == 0 ? (w[i] << 16) : (w[i] & 0xFFFF0000u));
+        const float f = bf16_bits_to_f32(j == 0 ? (w[i] & 0xFFFF) : (w[i] >> 16));
         const float a = ldexp_exact(f, 14 - E);
         hh[j] = 0u;
         ll[j] = 0u;
@@ -571,30 +626,108 @@ __global__ void __launch_bounds__(kPrepThreads) prep_x_kernel(const uint16_t* __
     lo4[c] = make_uint4(l[0], l[1], l[2], l[3]);
   }
   flags = __reduce_or_sync(0xffffffffu, flags);
+  __syncthreads();
   if ((threadIdx.x & 31) == 0) sf[threadIdx.x >> 5] = flags;
   __syncthreads();
   if (threadIdx.x == 0) {
     uint32_t f = 0u;
     for (int i = 0; i < kPrepThreads / 32; ++i) f |= sf[i];
-    xexp[tok] = E;
-    xflags[tok] = f;
+    q.exp[slot * q.N + tok] = E;
+    q.flags[slot * q.N + tok] = f;
   }
+}
+
+cudaLaunchConfig_t make_cfg(dim3 grid, dim3 block, size_t smem, cudaStream_t st, bool pdl,
+                            cudaLaunchAttribute* attr) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  return cfg;
 }
 
 template <int FMT, int EPI>
 cudaError_t launch_one(const GemvParams& p, cudaStream_t st, bool pdl) {
   const long long ctas = (p.n_warps + kWarpsPerCta - 1) / kWarpsPerCta;
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((unsigned)ctas);
-  cfg.blockDim = dim3(kWarpsPerCta * 32);
-  cfg.stream = st;
-
+  if (ctas <= 0) return cudaSuccess;
   cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = pdl ? 1 : 0;
+  cudaLaunchConfig_t cfg = make_cfg(dim3((unsigned)ctas), dim3(kWarpsPerCta * 32), 0, st, pdl, attr);
   return cudaLaunchKernelEx(&cfg, gemv_kernel<FMT, EPI>, p);
+}
+
+// ---- MoE routing and combine -------------------------------------------------
+
+// One CTA of 128 threads (N * topk <= 64 routed entries): the shared expert in
+// slot 0, then the distinct routed experts in ascending id order, and the
+// combine weight of every (slot, token) pair.
+__global__ void __launch_bounds__(128) moe_route_kernel(const MoeRoute m) {
+  pdl_launch_dependents();
+  pdl_wait();
+  __shared__ int ids[kMaxTokens * kMaxTopk];
+  __shared__ int first[kMaxTokens * kMaxTopk];
+  const int n = m.N * m.topk;
+  const int i = threadIdx.x;
+  int bad = 0;
+  if (i < n) {
+    int e = m.ids[i];
+    if (e < 0 || e >= m.n_experts) {
+      bad = 1;
+      e = -1;
+    }
+    ids[i] = e;
+  }
+  bad = __syncthreads_or(bad);
+  if (i == 0) m.status[0] = bad ? 4u : 0u;
+  for (int s = i; s < m.max_slots * m.N; s += blockDim.x) m.cw[s] = 0.0f;
+  __syncthreads();
+  if (i < n) {
+    int is_first = ids[i] >= 0 ? 1 : 0;
+    for (int j = 0; j < i; ++j) is_first &= ids[j] != ids[i];
+    first[i] = is_first;
+  }
+  __syncthreads();
+  int rank = 0;
+  if (i < n && ids[i] >= 0)
+    for (int j = 0; j < n; ++j) rank += (first[j] && ids[j] < ids[i]) ? 1 : 0;
+  const int slot = m.has_shared + rank;
+  if (i < n && first[i]) m.slot_expert[slot] = ids[i];
+  if (i == 0) {
+    int c = 0;
+    for (int j = 0; j < n; ++j) c += first[j];
+    if (m.has_shared) m.slot_expert[0] = -1;
+    m.n_slots[0] = c + m.has_shared;
+  }
+  __syncthreads();   // cw zeroing above is complete
+  // ids are distinct per token, so each (slot, token) cell gets one weight
+  if (i < n && ids[i] >= 0) m.cw[slot * m.N + i / m.topk] = m.route_w[i];
+  if (m.has_shared && i < m.N) m.cw[i] = 1.0f;
+}
+
+// y[tok][i] (+)= sum over slots, in slot order, of cw[s][tok] * ys[s][tok][i]
+__global__ void __launch_bounds__(256) moe_combine_kernel(const float* __restrict__ ys, const float* __restrict__ cw,
+                                                          const int* __restrict__ n_slots_p, int N, int d,
+                                                          void* __restrict__ out, int out_mode) {
+  pdl_launch_dependents();
+  pdl_wait();
+  const int tok = blockIdx.y;
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= d) return;
+  const int ns = __ldg(n_slots_p);
+  float acc = 0.0f;
+  for (int s = 0; s < ns; ++s) {
+    const float w = __ldg(cw + s * N + tok);
+    if (w != 0.0f) acc = __fmaf_rn(w, __ldg(ys + ((size_t)s * N + tok) * d + i), acc);
+  }
+  if (out_mode == kEpiStoreBF16)
+    reinterpret_cast<__nv_bfloat16*>(out)[(size_t)tok * d + i] = __float2bfloat16_rn(acc);
+  else
+    reinterpret_cast<float*>(out)[(size_t)tok * d + i] =
+        __fadd_rn(reinterpret_cast<float*>(out)[(size_t)tok * d + i], acc);
 }
 
 }  // namespace
@@ -612,37 +745,28 @@ int num_sms() {
 
 long long gemv_max_warps() { return (long long)num_sms() * BWS_GEMV_MIN_BLOCKS * kWarpsPerCta; }
 
-static size_t align256(size_t v) { return (v + 255) & ~(size_t)255; }
+size_t align256(size_t v) { return (v + 255) & ~(size_t)255; }
 
-GemvWorkspace gemv_workspace_layout(int N, int d_in, int n_tiles, long long max_warps) {
+GemvWorkspace gemv_workspace_layout(int N, int d_in, int n_tiles, long long max_warps, int slots) {
   GemvWorkspace w;
   const size_t d_pad = (size_t)((d_in + kSegK - 1) / kSegK) * kSegK;
   size_t o = 0;
   w.off_hdr = o; o += 256;
-  w.off_exp = o; o += align256(sizeof(int) * kMaxTokens);
-  w.off_flags = o; o += align256(sizeof(uint32_t) * kMaxTokens);
-  w.off_hi = o; o += align256(2 * d_pad * (N + 1));   // N tokens + one zero row
-  w.off_lo = o; o += align256(2 * d_pad * (N + 1));
+  w.off_exp = o; o += align256(sizeof(int) * (size_t)kMaxTokens * slots);
+  w.off_flags = o; o += align256(sizeof(uint32_t) * (size_t)kMaxTokens * slots);
+  w.off_hi = o; o += align256(2 * d_pad * (size_t)(N + 1) * slots);
+  w.off_lo = o; o += align256(2 * d_pad * (size_t)(N + 1) * slots);
   w.off_counters = o; o += align256(sizeof(uint32_t) * (size_t)n_tiles);
   w.off_partials = o; o += align256(sizeof(float) * kSlotFloats * ((size_t)n_tiles + max_warps));
   w.total = o;
   return w;
 }
 
-cudaError_t launch_prep_x(const uint16_t* x, int N, int d_in, int d_in_pad, uint16_t* xhi, uint16_t* xlo,
-                          int* xexp, uint32_t* xflags, uint32_t* hdr, uint32_t* zero_ptr, int zero_words,
-                          cudaStream_t st, bool pdl) {
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((unsigned)N);
-  cfg.blockDim = dim3(kPrepThreads);
-  cfg.stream = st;
+cudaError_t launch_prep(const PrepParams& q, cudaStream_t st, bool pdl) {
   cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = pdl ? 1 : 0;
-  return cudaLaunchKernelEx(&cfg, prep_x_kernel, x, N, d_in, d_in_pad, xhi, xlo, xexp, xflags, hdr,
-                            zero_ptr, zero_words);
+  const int slots = q.n_slots != nullptr ? q.max_slots : 1;
+  cudaLaunchConfig_t cfg = make_cfg(dim3((unsigned)(slots * q.N)), dim3(kPrepThreads), 0, st, pdl, attr);
+  return cudaLaunchKernelEx(&cfg, prep_kernel, q);
 }
 
 cudaError_t launch_gemv(int fmt, int epi, const GemvParams& p, cudaStream_t st, bool pdl) {
@@ -660,6 +784,19 @@ cudaError_t launch_gemv(int fmt, int epi, const GemvParams& p, cudaStream_t st, 
   BWS_CASE(kFmtFP8, kEpiStoreBF16)
 #undef BWS_CASE
   return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_moe_route(const MoeRoute& m, cudaStream_t st, bool pdl) {
+  cudaLaunchAttribute attr[1];
+  cudaLaunchConfig_t cfg = make_cfg(dim3(1), dim3(128), 0, st, pdl, attr);
+  return cudaLaunchKernelEx(&cfg, moe_route_kernel, m);
+}
+
+cudaError_t launch_moe_combine(const float* ys, const float* cw, const int* n_slots, int N, int d, void* out,
+                               int out_mode, cudaStream_t st, bool pdl) {
+  cudaLaunchAttribute attr[1];
+  cudaLaunchConfig_t cfg = make_cfg(dim3((unsigned)((d + 255) / 256), (unsigned)N), dim3(256), 0, st, pdl, attr);
+  return cudaLaunchKernelEx(&cfg, moe_combine_kernel, ys, cw, n_slots, N, d, out, out_mode);
 }
 
 }  // namespace bws

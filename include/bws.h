@@ -152,6 +152,50 @@ int bws_fp8_lmhead_gemv(const uint8_t* W, const float* row_scale,
                         const uint16_t* x, int N, int V, int d, float* logits,
                         void* workspace, size_t workspace_bytes, void* stream);
 
+/* One MXFP4 mixture-of-experts layer ([LingMoE] sections 3, 4 and 8: each
+ * token is routed to top-k of n_experts routed experts plus one shared
+ * expert; only the activated experts' weights are read; N tokens of a
+ * verify pass widen the set of distinct experts).
+ * Expert e's weights: gate_up rows [0, inter) are the gate, rows
+ * [inter, 2*inter) the up projection, both [.][hidden]; down is
+ * [hidden][inter]. Expert e's tensors start at base + e * stride bytes. */
+typedef struct bws_moe_layer {
+  int n_experts;           /* routed experts (e.g. 512)                      */
+  int hidden;              /* model width (e.g. 2560), % 32 == 0             */
+  int inter;               /* expert intermediate width (e.g. 768), % 32 == 0*/
+  const uint8_t* gate_up_codes;  size_t gate_up_codes_stride;  /* [2*inter][hidden/2] */
+  const uint8_t* gate_up_scales; size_t gate_up_scales_stride; /* [2*inter][hidden/32] */
+  const uint8_t* down_codes;     size_t down_codes_stride;     /* [hidden][inter/2]    */
+  const uint8_t* down_scales;    size_t down_scales_stride;    /* [hidden][inter/32]   */
+  /* shared expert (weight 1), same shapes; NULL codes = no shared expert */
+  const uint8_t* shared_gate_up_codes; const uint8_t* shared_gate_up_scales;
+  const uint8_t* shared_down_codes;    const uint8_t* shared_down_scales;
+} bws_moe_layer;
+
+/* y[n] = shared(x[n]) + sum_k route_w[n][k] * expert_{ids[n][k]}(x[n]) with
+ * expert(x) = W_down BF16(SiLU(W_gate x) * W_up x); FP32 accumulation, y BF16.
+ *   L host pointer to the layer descriptor (copied during the call)
+ *   ids int32 [N][topk] device, distinct per token, in [0, n_experts)
+ *   route_w fp32 [N][topk] device; x bf16 [N][hidden]; y bf16 [N][hidden]
+ * N in [1, 8], topk in [1, 8]. Ids are read on the device; an id out of range
+ * is skipped and flagged in the status word (see bws_mxfp4_moe_inspect). */
+size_t bws_mxfp4_moe_workspace_size(const bws_moe_layer* L, int N, int topk);
+int bws_mxfp4_moe_gemv(const bws_moe_layer* L, const int32_t* ids,
+                       const float* route_w, int N, int topk, const uint16_t* x,
+                       uint16_t* y, void* workspace, size_t workspace_bytes,
+                       void* stream);
+
+/* Verification tap: copies to HOST memory, from the workspace of the last
+ * bws_mxfp4_moe_gemv call with the same (L, N, topk), the number of live
+ * expert slots, the expert of every slot (-1 = shared expert; shared first,
+ * then the distinct routed experts in ascending id order), the SwiGLU
+ * activations h bf16 [N*topk + has_shared][N][inter] in slot order (rows of
+ * slots >= *n_slots are stale) and the status word (bit 4: an id was out of
+ * range). Synchronises the stream. */
+int bws_mxfp4_moe_inspect(const void* workspace, const bws_moe_layer* L, int N,
+                          int topk, int* n_slots, int32_t* slot_expert,
+                          uint16_t* h, uint32_t* status, void* stream);
+
 /* ------------------------------------------------------------------------ */
 /* Status and measurement                                                    */
 /* ------------------------------------------------------------------------ */
