@@ -25,5 +25,7 @@ from .api import (  # noqa: F401
     mxfp4_moe_inspect,
 )
 
+from . import stack, workloads  # noqa: F401,E402
+
 BWS_STATUS_X_TWO_BANDS = 1
 BWS_STATUS_X_FLUSHED = 2

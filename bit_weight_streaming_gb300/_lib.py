@@ -25,10 +25,11 @@ SIGNATURES = {
     "bws_mxfp4_moe_workspace_size": (Z, [P, I, I]),
     "bws_mxfp4_moe_gemv": (I, [P, P, P, I, I, P, P, P, Z, P]),
     "bws_mxfp4_moe_inspect": (I, [P, P, I, I, P, P, P, P, P]),
-    "bws_decode_step_workspace_size": (Z, [P, I]),
+    "bws_decode_step_workspace_size": (Z, [P]),
     "bws_decode_step_plan_create": (I, [P, I, P]),
     "bws_decode_step_plan_destroy": (None, [P]),
     "bws_decode_step_stream": (I, [P, P, P, P, Z, P]),
+    "bws_decode_step_kernel_count": (I, [P]),
     "bws_status_word": (I, [P, P, P]),
     "bws_hbm_read_probe": (I, [P, Z, P, P]),
     "bws_l2_flush": (I, [P, Z, P]),

@@ -4,7 +4,19 @@
 #include <stddef.h>
 #include <stdint.h>
 
+#include "../../include/bws.h"
+
 namespace bws {
+
+struct XPrep;
+
+// MoE layer pieces used by the decode stream (moe.cu).
+size_t moe_workspace_bytes(const bws_moe_layer* L, int N, int topk);
+void moe_counter_span(const bws_moe_layer* L, int N, int topk, size_t* offset, int* words);
+int check_moe_layer(const bws_moe_layer* L, int N, int topk, const char* name);
+int enqueue_moe(const bws_moe_layer* L, const int32_t* ids, const float* route_w, int N, int topk,
+                const uint16_t* x, void* y, int out_mode, void* ws, cudaStream_t st, const XPrep* x_prepped,
+                const char* name);
 
 // Records a message for bws_last_error() and returns code.
 int fail(int code, const char* fmt, ...);

@@ -782,6 +782,8 @@ cudaError_t launch_gemv(int fmt, int epi, const GemvParams& p, cudaStream_t st, 
   BWS_CASE(kFmtMXFP4, kEpiStoreF32)
   BWS_CASE(kFmtFP8, kEpiStoreF32)
   BWS_CASE(kFmtFP8, kEpiStoreBF16)
+  BWS_CASE(kFmtFP8, kEpiResidF32)
+  BWS_CASE(kFmtFP8, kEpiSwiGLU)
 #undef BWS_CASE
   return cudaErrorInvalidValue;
 }

@@ -220,6 +220,14 @@ int enqueue_moe(const bws_moe_layer* L, const int32_t* ids, const float* route_w
 
 size_t moe_workspace_bytes(const bws_moe_layer* L, int N, int topk) { return moe_layout(L, N, topk).total; }
 
+void moe_counter_span(const bws_moe_layer* L, int N, int topk, size_t* offset, int* words) {
+  const MoeLayout m = moe_layout(L, N, topk);
+  *offset = m.off_counters;
+  *words = m.n_tiles;
+}
+
+int check_moe_layer(const bws_moe_layer* L, int N, int topk, const char* name) { return check_moe(L, N, topk, name); }
+
 }  // namespace bws
 
 using namespace bws;

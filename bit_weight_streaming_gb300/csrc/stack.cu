@@ -1,0 +1,349 @@
+// C ABI of the whole decode step: a validated layer stack whose kernels are
+// enqueued in order on one stream, chained with programmatic dependent launch
+// (each product kernel starts pulling its weights into L2 while the kernel
+// before it finishes), and recorded once as a CUDA graph.
+#include <cuda_runtime.h>
+
+#include <new>
+#include <vector>
+
+#include "../../include/bws.h"
+#include "bws_abi_util.h"
+#include "bws_internal.h"
+
+using namespace bws;
+
+struct bws_stack_plan {
+  int N, hidden;
+  float eps;
+  std::vector<bws_layer> layers;
+  bws_matrix head;
+  // workspace layout
+  size_t off_r, off_xp, off_u, off_vp, off_h, off_hp, off_moe, off_counters, off_partials, total;
+  GemvWorkspace xw, vw, hw;    // prep-block offsets (relative to their block)
+  int max_u, max_dv, max_inter, max_tiles;
+  int kernels;
+  // recorded graph
+  cudaGraphExec_t exec;
+  const void* key[4];
+};
+
+namespace {
+
+int check_matrix(const bws_matrix& m, int d_in, const char* what, int layer) {
+  const char* name = "bws_decode_step_plan_create";
+  if (m.format != BWS_FMT_NVFP4 && m.format != BWS_FMT_MXFP4 && m.format != BWS_FMT_FP8_ROW)
+    return fail(BWS_ERR_FORMAT, "%s: layer %d %s: unknown format %d", name, layer, what, m.format);
+  if (m.d_in != d_in || m.d_out < 1 || m.d_in % 32)
+    return fail(BWS_ERR_UNSUPPORTED_SHAPE, "%s: layer %d %s: %d x %d (d_in %d expected, %% 32)", name, layer, what,
+                m.d_out, m.d_in, d_in);
+  if (!m.codes || !aligned(m.codes, 16))
+    return fail(BWS_ERR_MISALIGNED, "%s: layer %d %s: codes null or not 16-byte aligned", name, layer, what);
+  if (m.format != BWS_FMT_FP8_ROW && !m.scales)
+    return fail(BWS_ERR_INVALID_ARG, "%s: layer %d %s: null block scales", name, layer, what);
+  if (m.format != BWS_FMT_MXFP4 && !m.scale32)
+    return fail(BWS_ERR_INVALID_ARG, "%s: layer %d %s: null FP32 scale", name, layer, what);
+  return BWS_OK;
+}
+
+int fmt_of(const bws_matrix& m) {
+  return m.format == BWS_FMT_NVFP4 ? kFmtNVFP4 : (m.format == BWS_FMT_MXFP4 ? kFmtMXFP4 : kFmtFP8);
+}
+
+GemvMat gm(const bws_matrix& m, int out_row_off, int tile_begin) {
+  GemvMat g;
+  g.codes = m.codes;
+  g.scales = m.scales;
+  g.scale32 = m.scale32;
+  g.d_out = m.d_out;
+  g.out_row_off = out_row_off;
+  g.tile_begin = tile_begin;
+  return g;
+}
+
+struct Ctx {
+  const bws_stack_plan* P;
+  char* w;
+  cudaStream_t st;
+};
+
+XPrep xprep_of(const Ctx& c, size_t block, const GemvWorkspace& L) {
+  XPrep x;
+  x.hi = reinterpret_cast<uint16_t*>(c.w + block + L.off_hi);
+  x.lo = reinterpret_cast<uint16_t*>(c.w + block + L.off_lo);
+  x.exp = reinterpret_cast<int*>(c.w + block + L.off_exp);
+  x.flags = reinterpret_cast<uint32_t*>(c.w + block + L.off_flags);
+  x.shared = 1;
+  return x;
+}
+
+// prep into a block; zeroes `zero_words` counters at zero_ptr
+cudaError_t prep(const Ctx& c, int mode, const uint16_t* x, int ld, const uint16_t* x0, int d_in, size_t block,
+                 const GemvWorkspace& L, uint32_t* zero_ptr, int zero_words) {
+  PrepParams q = {};
+  q.mode = mode;
+  q.x = x;
+  q.ld = ld;
+  q.r = reinterpret_cast<float*>(c.w + c.P->off_r);
+  q.x0 = x0;
+  q.eps = c.P->eps;
+  q.N = c.P->N;
+  q.d_in = d_in;
+  q.d_in_pad = nseg_of(d_in) * 128;
+  const XPrep xp = xprep_of(c, block, L);
+  q.hi = const_cast<uint16_t*>(xp.hi);
+  q.lo = const_cast<uint16_t*>(xp.lo);
+  q.exp = const_cast<int*>(xp.exp);
+  q.flags = const_cast<uint32_t*>(xp.flags);
+  q.hdr = nullptr;
+  q.zero_ptr = zero_ptr;
+  q.zero_words = zero_words;
+  return launch_prep(q, c.st, true);
+}
+
+int tiles_for(const bws_matrix* mats, int nm, int epi) {
+  if (epi == kEpiSwiGLU) return (mats[0].d_out + 15) / 16;
+  int t = 0;
+  for (int i = 0; i < nm; ++i) t += (mats[i].d_out + 31) / 32;
+  return t;
+}
+
+cudaError_t product(const Ctx& c, const bws_matrix* mats, int nm, int epi, int d_in, const XPrep& x, void* out,
+                    int out_ld) {
+  GemvParams p = {};
+  p.n_mats = nm;
+  int tile = 0, row = 0;
+  for (int i = 0; i < nm; ++i) {
+    p.mats[i] = gm(mats[i], epi == kEpiSwiGLU ? 0 : row, tile);
+    row += mats[i].d_out;
+    tile += (mats[i].d_out + 31) / 32;
+  }
+  p.n_tiles = tiles_for(mats, nm, epi);
+  p.N = c.P->N;
+  p.d_in = d_in;
+  p.nseg = nseg_of(d_in);
+  p.d_in_pad = p.nseg * 128;
+  p.n_units = (long long)p.n_tiles * p.nseg;
+  const long long maxw = gemv_max_warps();
+  p.n_warps = p.n_units < maxw ? p.n_units : maxw;
+  p.x = x;
+  p.out = out;
+  p.out_ld = out_ld;
+  p.counters = reinterpret_cast<uint32_t*>(c.w + c.P->off_counters);
+  p.partials = reinterpret_cast<float*>(c.w + c.P->off_partials);
+  p.prefetch_units = fmt_of(mats[0]) == kFmtFP8 ? 4 : 8;
+  return launch_gemv(fmt_of(mats[0]), epi, p, c.st, true);
+}
+
+int enqueue_step(const bws_stack_plan* P, const uint16_t* x0, float* logits, void* ws, cudaStream_t st) {
+  const char* name = "bws_decode_step_stream";
+  Ctx c{P, static_cast<char*>(ws), st};
+  float* r = reinterpret_cast<float*>(c.w + P->off_r);
+  uint32_t* counters = reinterpret_cast<uint32_t*>(c.w + P->off_counters);
+  uint16_t* u = reinterpret_cast<uint16_t*>(c.w + P->off_u);
+  uint16_t* h = reinterpret_cast<uint16_t*>(c.w + P->off_h);
+  const XPrep xa = xprep_of(c, P->off_xp, P->xw);
+  const XPrep xv = xprep_of(c, P->off_vp, P->vw);
+  const XPrep xh = xprep_of(c, P->off_hp, P->hw);
+  const int H = P->hidden;
+  const uint16_t* init = x0;   // the first RMSNorm also sets r = x0
+  cudaError_t e = cudaSuccess;
+#define BWS_TRY(call)                          \
+  do {                                         \
+    e = (call);                                \
+    if (e != cudaSuccess) return cuda_status(e, name); \
+  } while (0)
+  for (size_t li = 0; li < P->layers.size(); ++li) {
+    const bws_layer& L = P->layers[li];
+    if (L.kind == BWS_LAYER_MIXER_MLP) {
+      int sum_out = 0;
+      for (int i = 0; i < L.n_mixer_in; ++i) sum_out += L.mixer_in[i].d_out;
+      BWS_TRY(prep(c, kPrepRmsNorm, nullptr, 0, init, H, P->off_xp, P->xw, counters,
+                   tiles_for(L.mixer_in, L.n_mixer_in, kEpiStoreBF16)));
+      init = nullptr;
+      BWS_TRY(product(c, L.mixer_in, L.n_mixer_in, kEpiStoreBF16, H, xa, u, sum_out));
+      const int dv = L.mixer_out.d_in;
+      BWS_TRY(prep(c, kPrepCopy, u, sum_out, nullptr, dv, P->off_vp, P->vw, counters, tiles_for(&L.mixer_out, 1, kEpiResidF32)));
+      BWS_TRY(product(c, &L.mixer_out, 1, kEpiResidF32, dv, xv, r, H));
+    }
+    if (L.kind == BWS_LAYER_MIXER_MLP || L.kind == BWS_LAYER_MLP) {
+      const bws_matrix gu[2] = {L.gate, L.up};
+      BWS_TRY(prep(c, kPrepRmsNorm, nullptr, 0, init, H, P->off_xp, P->xw, counters, tiles_for(gu, 2, kEpiSwiGLU)));
+      init = nullptr;
+      BWS_TRY(product(c, gu, 2, kEpiSwiGLU, H, xa, h, L.gate.d_out));
+      const int I = L.down.d_in;
+      BWS_TRY(prep(c, kPrepCopy, h, I, nullptr, I, P->off_hp, P->hw, counters, tiles_for(&L.down, 1, kEpiResidF32)));
+      BWS_TRY(product(c, &L.down, 1, kEpiResidF32, I, xh, r, H));
+    }
+    if (L.kind == BWS_LAYER_MOE) {
+      size_t coff;
+      int cwords;
+      moe_counter_span(&L.moe, P->N, L.topk, &coff, &cwords);
+      BWS_TRY(prep(c, kPrepRmsNorm, nullptr, 0, init, H, P->off_xp, P->xw,
+                   reinterpret_cast<uint32_t*>(c.w + P->off_moe + coff), cwords));
+      init = nullptr;
+      const int rc = enqueue_moe(&L.moe, L.ids, L.route_w, P->N, L.topk, nullptr, r, kEpiResidF32,
+                                 c.w + P->off_moe, st, &xa, name);
+      if (rc != BWS_OK) return rc;
+    }
+  }
+  BWS_TRY(prep(c, kPrepRmsNorm, nullptr, 0, init, H, P->off_xp, P->xw, counters, tiles_for(&P->head, 1, kEpiStoreF32)));
+  BWS_TRY(product(c, &P->head, 1, kEpiStoreF32, H, xa, logits, P->head.d_out));
+#undef BWS_TRY
+  return BWS_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int bws_decode_step_plan_create(const bws_stack* S, int N, bws_stack_plan** plan) {
+  const char* name = "bws_decode_step_plan_create";
+  if (!S || !plan) return fail(BWS_ERR_INVALID_ARG, "%s: null pointer", name);
+  *plan = nullptr;
+  if (N < 1 || N > kMaxTokens) return fail(BWS_ERR_INVALID_ARG, "%s: N = %d must be in [1, %d]", name, N, kMaxTokens);
+  if (S->hidden < 32 || S->hidden % 32) return fail(BWS_ERR_UNSUPPORTED_SHAPE, "%s: hidden %% 32 != 0", name);
+  if (S->n_layers < 0 || (S->n_layers > 0 && !S->layers)) return fail(BWS_ERR_INVALID_ARG, "%s: bad layer array", name);
+  if (!(S->rms_eps >= 0.0f)) return fail(BWS_ERR_INVALID_ARG, "%s: rms_eps must be >= 0", name);
+  const int H = S->hidden;
+  int rc;
+  bws_stack_plan* P = new (std::nothrow) bws_stack_plan();
+  if (!P) return fail(BWS_ERR_INVALID_ARG, "%s: out of host memory", name);
+  P->N = N;
+  P->hidden = H;
+  P->eps = S->rms_eps;
+  P->head = S->head;
+  P->max_u = P->max_dv = P->max_inter = 32;
+  P->max_tiles = 1;
+  P->kernels = 2;
+  size_t moe_bytes = 0;
+  auto bad = [&](int code) {
+    delete P;
+    return code;
+  };
+  for (int li = 0; li < S->n_layers; ++li) {
+    const bws_layer& L = S->layers[li];
+    if (L.kind == BWS_LAYER_MIXER_MLP) {
+      if (L.n_mixer_in < 1 || L.n_mixer_in > 4)
+        return bad(fail(BWS_ERR_INVALID_ARG, "%s: layer %d: n_mixer_in must be 1..4", name, li));
+      int sum_out = 0, tiles = 0;
+      for (int i = 0; i < L.n_mixer_in; ++i) {
+        if ((rc = check_matrix(L.mixer_in[i], H, "mixer_in", li))) return bad(rc);
+        if (L.mixer_in[i].format != L.mixer_in[0].format)
+          return bad(fail(BWS_ERR_FORMAT, "%s: layer %d: mixer inputs must share one format", name, li));
+        sum_out += L.mixer_in[i].d_out;
+        tiles += (L.mixer_in[i].d_out + 31) / 32;
+      }
+      if ((rc = check_matrix(L.mixer_out, L.mixer_out.d_in, "mixer_out", li))) return bad(rc);
+      if (L.mixer_out.d_out != H || L.mixer_out.d_in > sum_out)
+        return bad(fail(BWS_ERR_UNSUPPORTED_SHAPE, "%s: layer %d: mixer_out must be [hidden][d_v], d_v <= %d", name, li, sum_out));
+      if (sum_out % 8) return bad(fail(BWS_ERR_UNSUPPORTED_SHAPE, "%s: layer %d: mixer outputs %% 8 != 0", name, li));
+      P->max_u = sum_out > P->max_u ? sum_out : P->max_u;
+      P->max_dv = L.mixer_out.d_in > P->max_dv ? L.mixer_out.d_in : P->max_dv;
+      P->max_tiles = tiles > P->max_tiles ? tiles : P->max_tiles;
+      const int t2 = (H + 31) / 32;
+      P->max_tiles = t2 > P->max_tiles ? t2 : P->max_tiles;
+      P->kernels += 4;
+    }
+    if (L.kind == BWS_LAYER_MIXER_MLP || L.kind == BWS_LAYER_MLP) {
+      if ((rc = check_matrix(L.gate, H, "gate", li)) || (rc = check_matrix(L.up, H, "up", li))) return bad(rc);
+      if ((rc = check_matrix(L.down, L.gate.d_out, "down", li))) return bad(rc);
+      if (L.up.d_out != L.gate.d_out || L.up.format != L.gate.format || L.down.d_out != H)
+        return bad(fail(BWS_ERR_UNSUPPORTED_SHAPE, "%s: layer %d: gate/up/down shapes or formats disagree", name, li));
+      const int I = L.gate.d_out;
+      P->max_inter = I > P->max_inter ? I : P->max_inter;
+      const int t1 = (I + 15) / 16, t2 = (H + 31) / 32;
+      P->max_tiles = t1 > P->max_tiles ? t1 : P->max_tiles;
+      P->max_tiles = t2 > P->max_tiles ? t2 : P->max_tiles;
+      P->kernels += 4;
+    } else if (L.kind == BWS_LAYER_MOE) {
+      if ((rc = check_moe_layer(&L.moe, N, L.topk, name))) return bad(rc);
+      if (L.moe.hidden != H) return bad(fail(BWS_ERR_UNSUPPORTED_SHAPE, "%s: layer %d: MoE hidden != stack hidden", name, li));
+      if (!L.ids || !L.route_w) return bad(fail(BWS_ERR_INVALID_ARG, "%s: layer %d: null routing", name, li));
+      const size_t b = moe_workspace_bytes(&L.moe, N, L.topk);
+      moe_bytes = b > moe_bytes ? b : moe_bytes;
+      P->kernels += 6;
+    } else if (L.kind != BWS_LAYER_MIXER_MLP) {
+      return bad(fail(BWS_ERR_INVALID_ARG, "%s: layer %d: unknown kind %d", name, li, L.kind));
+    }
+    P->layers.push_back(L);
+  }
+  if ((rc = check_matrix(S->head, H, "head", -1))) return bad(rc);
+  const int th = (S->head.d_out + 31) / 32;
+  P->max_tiles = th > P->max_tiles ? th : P->max_tiles;
+  // workspace layout
+  size_t o = 0;
+  P->off_r = o; o += align256(sizeof(float) * (size_t)N * H);
+  P->xw = gemv_workspace_layout(N, H, 0, 0, 1);
+  P->off_xp = o; o += P->xw.off_counters;
+  P->off_u = o; o += align256(2 * (size_t)N * P->max_u);
+  P->vw = gemv_workspace_layout(N, P->max_dv, 0, 0, 1);
+  P->off_vp = o; o += P->vw.off_counters;
+  P->off_h = o; o += align256(2 * (size_t)N * P->max_inter);
+  P->hw = gemv_workspace_layout(N, P->max_inter, 0, 0, 1);
+  P->off_hp = o; o += P->hw.off_counters;
+  P->off_moe = o; o += align256(moe_bytes);
+  P->off_counters = o; o += align256(sizeof(uint32_t) * (size_t)P->max_tiles);
+  P->off_partials = o; o += align256(sizeof(float) * kSlotFloats * ((size_t)P->max_tiles + gemv_max_warps()));
+  P->total = o;
+  P->exec = nullptr;
+  for (auto& k : P->key) k = nullptr;
+  *plan = P;
+  clear_error();
+  return BWS_OK;
+}
+
+void bws_decode_step_plan_destroy(bws_stack_plan* plan) {
+  if (!plan) return;
+  if (plan->exec) cudaGraphExecDestroy(plan->exec);
+  delete plan;
+}
+
+size_t bws_decode_step_workspace_size(const bws_stack_plan* plan) { return plan ? plan->total : 0; }
+
+int bws_decode_step_kernel_count(const bws_stack_plan* plan) { return plan ? plan->kernels : 0; }
+
+int bws_decode_step_stream(bws_stack_plan* P, const uint16_t* x0, float* logits, void* ws, size_t ws_bytes,
+                           void* stream) {
+  const char* name = "bws_decode_step_stream";
+  if (!P || !x0 || !logits || !ws) return fail(BWS_ERR_INVALID_ARG, "%s: null pointer", name);
+  if (ws_bytes < P->total) return fail(BWS_ERR_WORKSPACE, "%s: workspace of %zu bytes needed, %zu given", name, P->total, ws_bytes);
+  if (!aligned(ws, 256) || !aligned(x0, 16) || !aligned(logits, 4))
+    return fail(BWS_ERR_MISALIGNED, "%s: workspace 256-byte, x0 16-byte, logits 4-byte alignment needed", name);
+  cudaStream_t st = as_stream(stream);
+  cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+  if (st != nullptr) {
+    cudaError_t e = cudaStreamIsCapturing(st, &cs);
+    if (e != cudaSuccess) return cuda_status(e, name);
+  }
+  if (st == nullptr || cs != cudaStreamCaptureStatusNone) return enqueue_step(P, x0, logits, ws, st);
+  const void* key[4] = {x0, logits, ws, st};
+  bool same = P->exec != nullptr;
+  for (int i = 0; i < 4; ++i) same = same && key[i] == P->key[i];
+  if (!same) {
+    if (P->exec) {
+      cudaGraphExecDestroy(P->exec);
+      P->exec = nullptr;
+    }
+    cudaError_t e = cudaStreamBeginCapture(st, cudaStreamCaptureModeThreadLocal);
+    if (e != cudaSuccess) return cuda_status(e, name);
+    const int rc = enqueue_step(P, x0, logits, ws, st);
+    cudaGraph_t g = nullptr;
+    e = cudaStreamEndCapture(st, &g);
+    if (rc != BWS_OK) {
+      if (g) cudaGraphDestroy(g);
+      return rc;
+    }
+    if (e != cudaSuccess) return cuda_status(e, name);
+    e = cudaGraphInstantiate(&P->exec, g, 0);
+    cudaGraphDestroy(g);
+    if (e != cudaSuccess) {
+      P->exec = nullptr;
+      return cuda_status(e, name);
+    }
+    for (int i = 0; i < 4; ++i) P->key[i] = key[i];
+  }
+  return cuda_status(cudaGraphLaunch(P->exec, st), name);
+}
+
+}  // extern "C"

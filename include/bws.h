@@ -197,6 +197,76 @@ int bws_mxfp4_moe_inspect(const void* workspace, const bws_moe_layer* L, int N,
                           uint16_t* h, uint32_t* status, void* stream);
 
 /* ------------------------------------------------------------------------ */
+/* Whole decode step                                                         */
+/* ------------------------------------------------------------------------ */
+
+/* One weight matrix of a layer stack, in the layout its quantizer writes. */
+typedef struct bws_matrix {
+  int format;              /* enum bws_format                                  */
+  int d_out, d_in;         /* d_in % 32 == 0                                   */
+  const uint8_t* codes;    /* 16-byte aligned                                  */
+  const uint8_t* scales;   /* NVFP4: E4M3 [d_out][d_in/16]; MXFP4: E8M0 [d_out][d_in/32]; FP8: NULL */
+  const float* scale32;    /* NVFP4: tensor scale [1]; FP8: row scales [d_out]; MXFP4: NULL */
+} bws_matrix;
+
+enum bws_layer_kind {
+  BWS_LAYER_MIXER_MLP = 1, /* token mixer (weight-free op) + SwiGLU MLP        */
+  BWS_LAYER_MLP = 2,       /* SwiGLU MLP only                                  */
+  BWS_LAYER_MOE = 3        /* MXFP4 mixture of experts                         */
+};
+
+/* One layer. [Spark27B] "Decode speed is bytes divided by bandwidth": each
+ * layer is a token-mixing block then the MLP, and the mixing operation itself
+ * (attention over the cache, or the Gated DeltaNet state update) reads no
+ * weights. Its stand-in here takes the first mixer_out.d_in entries of the
+ * concatenated input projections. */
+typedef struct bws_layer {
+  int kind;                      /* enum bws_layer_kind                        */
+  int n_mixer_in;                /* MIXER_MLP: 1..4 input projections          */
+  bws_matrix mixer_in[4];        /* MIXER_MLP: same format and d_in = hidden   */
+  bws_matrix mixer_out;          /* MIXER_MLP: [hidden][d_v]                   */
+  bws_matrix gate, up, down;     /* MIXER_MLP, MLP: gate/up [inter][hidden], down [hidden][inter] */
+  bws_moe_layer moe;             /* MOE                                         */
+  const int32_t* ids;            /* MOE: device [N][topk]                       */
+  const float* route_w;          /* MOE: device [N][topk]                       */
+  int topk;                      /* MOE                                         */
+} bws_layer;
+
+typedef struct bws_stack {
+  int hidden;                    /* residual width, % 32 == 0                  */
+  int n_layers;
+  const bws_layer* layers;       /* host array [n_layers], read at plan creation */
+  bws_matrix head;               /* output layer [vocab][hidden], FP8 row-scaled */
+  float rms_eps;                 /* weightless RMSNorm epsilon (e.g. 1e-6)     */
+} bws_stack;
+
+/* A validated stack with its launch sequence. Create once, run many times;
+ * the plan copies the descriptors and owns no device memory. */
+typedef struct bws_stack_plan bws_stack_plan;
+
+int bws_decode_step_plan_create(const bws_stack* S, int N, bws_stack_plan** plan);
+void bws_decode_step_plan_destroy(bws_stack_plan* plan);
+size_t bws_decode_step_workspace_size(const bws_stack_plan* plan);
+
+/* Runs the whole decode step for the plan's N tokens:
+ *   r = x0
+ *   MIXER_MLP: a = BF16(RMSNorm(r)); u = BF16([W_in1 a, W_in2 a, ...]);
+ *              r += W_out u[:d_v]; then the MLP
+ *   MLP:       m = BF16(RMSNorm(r)); r += W_down BF16(SiLU(W_gate m) * W_up m)
+ *   MOE:       m = BF16(RMSNorm(r)); r += MoE(m)
+ *   logits = head(BF16(RMSNorm(r)))
+ * RMSNorm is weightless: r / sqrt(mean(r^2) + eps). The residual r is FP32.
+ *   x0 bf16 [N][hidden]; logits fp32 [N][vocab].
+ * With a non-default stream the first call records the step as a CUDA graph
+ * and later calls with the same (x0, logits, workspace, stream) replay it; on
+ * the legacy default stream the kernels are launched directly. */
+int bws_decode_step_stream(bws_stack_plan* plan, const uint16_t* x0, float* logits,
+                           void* workspace, size_t workspace_bytes, void* stream);
+
+/* Number of kernels one decode step launches. */
+int bws_decode_step_kernel_count(const bws_stack_plan* plan);
+
+/* ------------------------------------------------------------------------ */
 /* Status and measurement                                                    */
 /* ------------------------------------------------------------------------ */
 

@@ -1,0 +1,72 @@
+"""Whole decode step on the GPU against the oracle's stack.
+
+Each product inside is pinned at 1e-4 by the product tests; end to end the
+logits must meet |dl| <= 1e-4 * sum|w x| + 1/2 ulp + STACK_SLACK * rms(logits)
+(STACK_SLACK: see tests/stack_util.py and test_oracle_stack_sensitivity)."""
+import numpy as np
+import pytest
+import torch
+
+from oracle import tolerance as T, formats as F
+from tests.gpu_util import device, bws, f64
+from tests.stack_util import oracle_quantizers, oracle_logits, STACK_SLACK
+import synth
+
+pytestmark = pytest.mark.gpu
+
+
+def _dense_small(N, n_layers=4):
+    from bit_weight_streaming_gb300 import workloads as W
+    bws()
+    return W.dense_27b(N, seed=3, n_layers=n_layers, hidden=256, inter=512, vocab=1000, attn=(384, 64, 64, 192),
+                       gdn=(640, 192), quant=oracle_quantizers(device()), device=device())
+
+
+def _check(stack, N, seed):
+    x0 = synth.activation_bf16(N, stack.hidden, seed=seed, device=device())
+    logits = stack.step(x0)
+    torch.cuda.synchronize()
+    ref, A, _ = oracle_logits(stack, F.round_bf16(f64(x0)))
+    rms = np.sqrt(np.mean(ref ** 2, axis=1, keepdims=True))
+    ok, worst, at = T.check(ref, f64(logits), A, extra=STACK_SLACK * rms)
+    assert ok, (worst, at)
+    return logits
+
+
+@pytest.mark.parametrize("N", [1, 4, 8])
+def test_dense_stack_parity(N):
+    stack = _dense_small(N)
+    _check(stack, N, seed=N)
+
+
+def test_dense_stack_graph_replay_is_deterministic():
+    stack = _dense_small(2)
+    x0 = synth.activation_bf16(2, 256, seed=1, device=device())
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        a = stack.step(x0).clone()     # records the graph
+        b = stack.step(x0).clone()     # replays it
+        c = stack.step(x0).clone()
+    s.synchronize()
+    assert torch.equal(a, b) and torch.equal(b, c)
+    d = stack.step(x0)                 # default stream: direct launches
+    torch.cuda.synchronize()
+    assert torch.equal(a, d)
+
+
+def test_zero_layer_stack_is_the_head():
+    stack = _dense_small(3, n_layers=0)
+    _check(stack, 3, seed=5)
+    assert stack.kernel_count == 2
+
+
+def test_moe_stack_parity():
+    from bit_weight_streaming_gb300 import workloads as W
+    bws()
+    for N in (1, 4):
+        layers = W.moe_stack_layers(N, seed=4, n_dense=1, n_moe=2, hidden=256, inter=64, n_experts=32, topk=4,
+                                    dense_inter=384, quant=oracle_quantizers(device()), device=device())
+        head = W.make_matrix(3, (900, 256), 4, 7, oracle_quantizers(device()), device())
+        stack = bws().stack.DecodeStack(256, layers, head, N, device=device())
+        assert stack.kernel_count == 4 + 2 * 6 + 2
+        _check(stack, N, seed=10 + N)
