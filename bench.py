@@ -1,0 +1,436 @@
+"""Decode-step weight-stream benchmark.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+
+One step = one whole decode step (bws_decode_step_stream) of the 27B-shape
+dense stack: 64 NVFP4 layers (17.82 GB) plus the FP8 248320x5120 output layer,
+19.097 GB of weights read per step, for 1 token (the headline) and, as a
+second line of the same JSON object, for 8 tokens (speculative verify). The
+MoE stack (Ling-shape, MXFP4, N=1 and N=4) is measured too unless --no-moe.
+
+The metric is the decode-step weight bandwidth: algorithmic weight bytes per
+step / step time, in GB/s (1 GB = 1e9 B). Inputs are synthetic (seeded
+N(0, 0.02) weights quantized on the GPU, N(0, 1) BF16 activations). The
+weights of one step (19 GB) are far larger than L2, so no flush is needed
+between steps.
+
+Under torchrun (--gpus N > 1) each rank runs an independent replica of the
+step on its own GPU (the path has no exchange step); value is the sum of all
+ranks' bytes over the slowest rank's time.
+"""
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "decode-step weight GB/s"
+UNIT = "GB/s"
+
+
+# ---- multi-process plumbing (testable on CPU) -------------------------------
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def aggregate(bytes_per_rank, seconds_per_rank):
+    """Whole-job throughput: all ranks' bytes over the slowest rank's time."""
+    t = max(seconds_per_rank)
+    return sum(bytes_per_rank) / t if t > 0 else 0.0, t
+
+
+def all_gather_floats(vals, world):
+    import torch
+    import torch.distributed as dist
+    if world == 1:
+        return [list(vals)]
+    t = torch.tensor(vals, dtype=torch.float64)
+    if dist.get_backend() == "nccl":
+        t = t.cuda()
+    out = [torch.zeros_like(t) for _ in range(world)]
+    dist.all_gather(out, t)
+    return [o.cpu().tolist() for o in out]
+
+
+# ---- clocks -----------------------------------------------------------------
+
+CLOCK_QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+
+class ClockSampler:
+    """Samples nvidia-smi every 100 ms while running (in a background process)."""
+
+    def __init__(self, gpu_index=0):
+        self.gpu_index = gpu_index
+        self.lines = []
+        self.proc = None
+        self.thread = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu_index}", f"--query-gpu={CLOCK_QUERY}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except (OSError, ValueError):
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *a):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            self.thread.join(timeout=5)
+
+    def summary(self):
+        return parse_clock_lines(self.lines)
+
+
+def parse_clock_lines(lines):
+    sm, mx, reasons = [], [], set()
+    names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+    for ln in lines:
+        f = [x.strip() for x in ln.split(",")]
+        if len(f) < 9:
+            continue
+        try:
+            sm.append(float(f[1]))
+            mx.append(float(f[2]))
+        except ValueError:
+            continue
+        for n, v in zip(names, f[5:9]):
+            if v.lower().startswith("active"):
+                reasons.add(n)
+    if not sm:
+        return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0}
+    return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ---- CPU baseline (the oracle) ------------------------------------------------
+
+def cpu_oracle_rate(sample_matrices, budget_s=12.0):
+    """Times the oracle's NVFP4 product on host copies of some of the step's
+    matrices (N = 1), as algorithmic bytes per second of wall time. Returns
+    (GB/s, threads used, description)."""
+    import numpy as np
+    from oracle import products as P
+    rng = np.random.default_rng(0)
+    done_bytes = 0
+    t0, c0 = time.perf_counter(), sum(os.times()[:2])
+    n = 0
+    for codes, scales, ts in sample_matrices:
+        x = rng.standard_normal((1, codes.shape[1] * 2)).astype(np.float32)
+        P.nvfp4_gemv(codes, scales, ts, x)
+        done_bytes += codes.nbytes + scales.nbytes
+        n += 1
+        if time.perf_counter() - t0 > budget_s:
+            break
+    wall = time.perf_counter() - t0
+    cpu = sum(os.times()[:2]) - c0
+    cores = max(1, round(cpu / wall)) if wall > 0 else 1
+    return done_bytes / wall / 1e9, cores, f"oracle NVFP4 GEMV (FP64, numpy) on {n} of the step's matrices, N=1, {done_bytes/1e9:.3f} GB"
+
+
+def host_copies(stack, max_bytes):
+    out, total = [], 0
+    for L in stack.layers_py:
+        for name in ("gate", "up", "down"):
+            m = L.get(name)
+            if m is None or m.fmt != 1:
+                continue
+            out.append((m.codes.cpu().numpy(), m.scales.cpu().numpy(), float(m.scale32.item())))
+            total += m.nbytes()
+            if total >= max_bytes:
+                return out
+    return out
+
+
+# ---- the GPU arm ------------------------------------------------------------------
+
+def peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return 6800.0, "fallback"
+
+
+def time_steps(fn, steps, warmup, stream):
+    import torch
+    for _ in range(warmup):
+        fn()
+    stream.synchronize()
+    s = torch.cuda.Event(enable_timing=True)
+    e = torch.cuda.Event(enable_timing=True)
+    s.record(stream)
+    for _ in range(steps):
+        fn()
+    e.record(stream)
+    e.synchronize()
+    return s.elapsed_time(e) / 1e3 / steps
+
+
+def time_dominant_kernel(stack, stream, reps=3):
+    """Average duration of the NVFP4 weight-stream product on the stack's own
+    matrices (one call per matrix, rotating through all MLP and mixer
+    matrices, so every launch reads cold weights), timed with CUDA events on
+    the launching stream. Each call is the activation prep (one small kernel)
+    plus the product kernel, so the rate is a lower bound for the product."""
+    import torch
+    import bit_weight_streaming_gb300 as bws
+    mats = []
+    for L in stack.layers_py:
+        for m in [L.get("gate"), L.get("up"), L.get("down")] + list(L.get("mixer_in", [])):
+            if m is not None and m.fmt == 1:
+                mats.append(m)
+    xs = {}
+    ws = bws.Workspace(stack.device)
+    ys = {}
+    for m in mats:
+        if m.d_in not in xs:
+            xs[m.d_in] = torch.randn((1, m.d_in), device=stack.device).to(torch.bfloat16)
+        if m.d_out not in ys:
+            ys[m.d_out] = torch.empty((1, m.d_out), dtype=torch.bfloat16, device=stack.device)
+    with torch.cuda.stream(stream):
+        for m in mats[:8]:   # warm-up
+            bws.nvfp4_gemv(m.codes, m.scales, m.scale32, xs[m.d_in], y=ys[m.d_out], ws=ws)
+        stream.synchronize()
+        events = []
+        for _ in range(reps):
+            for m in mats:
+                a = torch.cuda.Event(enable_timing=True)
+                b = torch.cuda.Event(enable_timing=True)
+                a.record(stream)
+                bws.nvfp4_gemv(m.codes, m.scales, m.scale32, xs[m.d_in], y=ys[m.d_out], ws=ws)
+                b.record(stream)
+                events.append((m.nbytes(), a, b))
+        stream.synchronize()
+    nbytes = sum(n for n, _, _ in events)
+    secs = sum(a.elapsed_time(b) for _, a, b in events) / 1e3
+    return nbytes / len(events), secs / len(events), len(events)
+
+
+def run_gpu(args):
+    import torch
+    import torch.distributed as dist
+    world, rank, local = dist_env()
+    if world > 1:
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    import __graft_entry__ as g
+    if rank == 0:
+        g.build()
+    if world > 1:
+        dist.barrier()
+    import bit_weight_streaming_gb300 as bws
+    from bit_weight_streaming_gb300 import workloads as W
+    import synth
+
+    stream = torch.cuda.Stream(dev)
+    t_build = time.time()
+    with torch.cuda.stream(stream):
+        stack1 = W.dense_27b(1, seed=args.seed, device=dev)
+    stream.synchronize()
+    t_build = time.time() - t_build
+    nbytes = stack1.weight_bytes()
+    x1 = synth.activation_bf16(1, stack1.hidden, seed=args.seed, device=dev)
+    logits1 = torch.empty((1, stack1.head.d_out), dtype=torch.float32, device=dev)
+
+    def step1():
+        stack1.step(x1, logits1)
+
+    with torch.cuda.stream(stream):
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize()
+        with ClockSampler(local) as clocks:
+            t_step = time_steps(step1, args.steps, args.warmup, stream)
+        torch.cuda.synchronize()
+    clk = clocks.summary()
+    per_rank = all_gather_floats([nbytes, t_step], world)
+    value, t_max = aggregate([r[0] for r in per_rank], [r[1] for r in per_rank])
+    value /= 1e9
+
+    # end to end through the public API, host buffers: H2D x0, step, D2H logits
+    x_host = x1.cpu().pin_memory()
+    out_host = torch.empty_like(logits1, device="cpu").pin_memory()
+    x_dev = torch.empty_like(x1)
+
+    def step_e2e():
+        x_dev.copy_(x_host, non_blocking=True)
+        stack1.step(x_dev, logits1)
+        out_host.copy_(logits1, non_blocking=True)
+
+    with torch.cuda.stream(stream):
+        t_e2e = time_steps(step_e2e, args.steps, args.warmup, stream)
+    per_rank_e2e = all_gather_floats([nbytes, t_e2e], world)
+    e2e_val, _ = aggregate([r[0] for r in per_rank_e2e], [r[1] for r in per_rank_e2e])
+
+    # the speculative-verify shape (8 tokens) on the same weights
+    with torch.cuda.stream(stream):
+        stack8 = bws.stack.DecodeStack(stack1.hidden, stack1.layers_py, stack1.head, 8, device=dev)
+        x8 = synth.activation_bf16(8, stack1.hidden, seed=args.seed, device=dev)
+        logits8 = torch.empty((8, stack1.head.d_out), dtype=torch.float32, device=dev)
+        t_step8 = time_steps(lambda: stack8.step(x8, logits8), args.steps, args.warmup, stream)
+
+    # dominant kernel: the NVFP4 product
+    with torch.cuda.stream(stream):
+        dk_bytes, dk_secs, dk_n = time_dominant_kernel(stack1, stream)
+    peak, peak_kind = peaks()
+
+    moe = None
+    if not args.no_moe:
+        del stack8
+        moe = run_moe(args, dev, stream)
+
+    cpu = None
+    if rank == 0:
+        sample = host_copies(stack1, 600e6)
+        gbs, cores, desc = cpu_oracle_rate(sample)
+        cpu = {"value": round(gbs, 4), "unit": UNIT, "cores": cores, "kind": "oracle", "sample": desc}
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": round(t_max * 1e3, 4), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "nvfp4/fp8 weights, bf16 activations, fp32 accumulate",
+            "data": "synthetic: seeded N(0,0.02) weights quantized on the GPU, N(0,1) bf16 activations",
+            "config": {"workload": "27B-shape dense decode step: 64 NVFP4 layers (48 linear-attention, 16 full-attention, "
+                                   "MLP 17408x5120) + FP8 248320x5120 output layer, N=1 token",
+                       "weight_bytes_per_step": nbytes, "tokens": 1, "l2": "not flushed: 19.1 GB per step >> 129 MB L2",
+                       "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+                       "graph": "one CUDA graph per step, kernels chained with programmatic dependent launch",
+                       "build_s": round(t_build, 1)},
+            "us_per_step": round(t_max * 1e6, 1),
+            "tokens_per_s": round(world * 1 / t_max, 2),
+            "frac_of_hbm_peak": round(value / world / peak, 4),
+            "n8": {"value": round(nbytes / t_step8 / 1e9, 2), "unit": UNIT, "us_per_step": round(t_step8 * 1e6, 1),
+                   "tokens_per_s": round(8 / t_step8, 1), "frac_of_hbm_peak": round(nbytes / t_step8 / 1e9 / peak, 4)},
+            "moe": moe,
+            "e2e": {"value": round(e2e_val / 1e9, 2), "unit": UNIT, "h2d_bytes_per_step": x_host.numel() * 2,
+                    "d2h_bytes_per_step": out_host.numel() * 4},
+            "gpu_launches": stack1.kernel_count * args.steps,
+            "roofline": {"bound": "hbm", "achieved": round(dk_bytes / dk_secs / 1e9, 1), "peak": peak,
+                         "unit": "GB/s", "frac": round(dk_bytes / dk_secs / 1e9 / peak, 4), "traffic": None,
+                         "kernel": "NVFP4 weight-stream product (activation prep + product per call), N=1",
+                         "launches_timed": dk_n, "bytes_per_launch": round(dk_bytes), "peak_kind": peak_kind},
+            "clocks": clk,
+            "cpu_baseline": cpu,
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+def run_moe(args, dev, stream):
+    import torch
+    from bit_weight_streaming_gb300 import workloads as W
+    import synth
+    out = {}
+    for N in (1, 4):
+        t0 = time.time()
+        with torch.cuda.stream(stream):
+            st = W.moe_ling(N, seed=args.seed, device=dev)
+        stream.synchronize()
+        tb = time.time() - t0
+        distinct = W.distinct_per_moe_layer(st)
+        nbytes = st.weight_bytes(distinct)
+        x = synth.activation_bf16(N, st.hidden, seed=args.seed, device=dev)
+        lg = torch.empty((N, st.head.d_out), dtype=torch.float32, device=dev)
+
+        def step():   # 1.6 GB (N=1) to 4.5 GB (N=4) of weights per step: no L2 flush needed
+            st.step(x, lg)
+
+        with torch.cuda.stream(stream):
+            t = time_steps(step, args.steps, args.warmup, stream)
+        out[f"n{N}"] = {"value": round(nbytes / t / 1e9, 2), "unit": UNIT, "us_per_step": round(t * 1e6, 1),
+                        "weight_bytes_per_step": nbytes, "distinct_experts_mean": round(sum(distinct) / len(distinct), 2),
+                        "build_s": round(tb, 1)}
+        del st
+        torch.cuda.empty_cache()
+    out["workload"] = ("Ling-shape MoE decode step: 2 dense MXFP4 MLP layers (6912) + 40 MoE layers (512 experts, "
+                       "inter 768, top-8 + 1 shared, MXFP4) + FP8 157184x2560 output layer")
+    return out
+
+
+# ---- the reference arm: the oracle on the host cores -------------------------------
+
+def run_reference(args):
+    world, rank, _ = dist_env()
+    if rank != 0:
+        return
+    import numpy as np
+    import synth
+    from oracle import quant as Q
+    # A bounded sample of the same workload: MLP matrices of the 27B-shape
+    # stack (gate/up 17408x5120, down 5120x17408), quantized by the oracle.
+    mats = []
+    shapes = [(17408, 5120)]
+    for i, s in enumerate(shapes):
+        W = synth.weight_fp32(s, seed=args.seed, index=i).numpy()
+        mats.append(Q.nvfp4_quantize(W))
+    rates = []
+    for _ in range(args.warmup):
+        cpu_oracle_rate(mats[:1], budget_s=0.0)
+    t_all = []
+    for _ in range(args.steps):
+        gbs, cores, desc = cpu_oracle_rate(mats, budget_s=1e9)
+        rates.append(gbs)
+    value = statistics.median(rates)
+    nbytes = sum(c.nbytes + s.nbytes for c, s, _ in mats)
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(nbytes / (value * 1e9) * 1e3, 2),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic: seeded N(0,0.02) weights, N(0,1) bf16 activations",
+        "config": {"workload": "27B-shape dense decode step, bounded sample: the MLP gate projection "
+                               f"(17408x5120 NVFP4, {nbytes/1e9:.4f} GB) per step, N=1 token", "sample_bytes_per_step": nbytes},
+        "cpu_baseline": {"kind": "oracle", "cores": cores, "sample": desc, "value": round(value, 4)},
+        "e2e": {"value": round(value, 4), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=100)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--seed", type=int, default=0)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-moe", action="store_true")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_gpu(args)
+
+
+if __name__ == "__main__":
+    main()

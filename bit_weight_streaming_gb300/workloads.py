@@ -85,20 +85,26 @@ def dense_27b(N, seed=0, n_layers=64, hidden=5120, inter=17408, vocab=248320, at
 
 # ---- the MoE stack ------------------------------------------------------------------
 
-def moe_weights(n_experts, hidden, inter, seed, layer, with_shared=True, quant=None, device="cuda"):
-    """Stacked MXFP4 expert tensors of one MoE layer (gate rows then up rows)."""
+def moe_weights(n_experts, hidden, inter, seed, layer, with_shared=True, quant=None, device="cuda",
+                batch=64):
+    """Stacked MXFP4 expert tensors of one MoE layer (gate rows then up rows).
+    Experts are drawn and quantized `batch` at a time (one FP32 draw per
+    batch and tensor kind; MXFP4 rows are independent, so quantizing the
+    stacked rows equals quantizing each expert)."""
     quant = quant or gpu_quantizers()
     n = n_experts + (1 if with_shared else 0)
     gu_c = torch.empty((n, 2 * inter, hidden // 2), dtype=torch.uint8, device=device)
     gu_s = torch.empty((n, 2 * inter, hidden // 32), dtype=torch.uint8, device=device)
     dn_c = torch.empty((n, hidden, inter // 2), dtype=torch.uint8, device=device)
     dn_s = torch.empty((n, hidden, inter // 32), dtype=torch.uint8, device=device)
-    for e in range(n):
+    for e0 in range(0, n, batch):
+        nb = min(batch, n - e0)
         for k, (shape, c_dst, s_dst) in enumerate([((2 * inter, hidden), gu_c, gu_s), ((hidden, inter), dn_c, dn_s)]):
-            W = synth.weight_fp32(shape, seed=seed, index=1000000 + 4096 * layer + 2 * e + k, device=device)
+            W = synth.weight_fp32((nb * shape[0], shape[1]), seed=seed, index=1000000 + 4096 * layer + 2 * e0 + k,
+                                  device=device)
             c, s = quant[FMT_MXFP4](W)
-            c_dst[e].copy_(c)
-            s_dst[e].copy_(s)
+            c_dst[e0:e0 + nb].copy_(c.view(nb, shape[0], -1))
+            s_dst[e0:e0 + nb].copy_(s.view(nb, shape[0], -1))
             del W
     shared = (gu_c[n_experts], gu_s[n_experts], dn_c[n_experts], dn_s[n_experts]) if with_shared else None
     return api.MoeWeights(gu_c[:n_experts], gu_s[:n_experts], dn_c[:n_experts], dn_s[:n_experts], shared)
