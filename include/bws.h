@@ -132,6 +132,28 @@ int bws_nvfp4_gemv(const uint8_t* codes, const uint8_t* scales,
                    int d_out, int d_in, uint16_t* y, void* workspace,
                    size_t workspace_bytes, void* stream);
 
+/* bws_nvfp4_gemv for callers that cannot allocate device memory (a caller
+ * whose framework owns the whole device pool, a plugin called from a runtime
+ * that forbids allocation during a step, a latency-critical path that must
+ * not enter an allocator). The pages have no counterpart: this is a property
+ * of the library, not of the method. Same arguments and results as
+ * bws_nvfp4_gemv, without the workspace: the call uses an 8 MiB scratch array
+ * that the library defines as static device memory, which every GPU that
+ * loads the library holds until the process exits.
+ *   - Sizes whose scratch exceeds 8 MiB (about N * d_in * 8 bytes plus
+ *     (d_out/32 + 16 * SMs) KiB) are rejected with BWS_ERR_WORKSPACE and a
+ *     message; the call allocates nothing (no cudaMalloc, no allocating
+ *     library routine).
+ *   - The first call on a device looks up the scratch's device address (once
+ *     per device, with that device current); make that first call before any
+ *     stream capture.
+ *   - All calls on a device share the one scratch array and it keeps the last
+ *     call's contents: calls that overlap on the GPU (different streams, or
+ *     host threads without ordering) race with each other. Order them. */
+int bws_nvfp4_gemv_noalloc(const uint8_t* codes, const uint8_t* scales,
+                           const float* tensor_scale, const uint16_t* x, int N,
+                           int d_out, int d_in, uint16_t* y, void* stream);
+
 /* Fused MLP front half: h[n][i] = BF16( SiLU(g) * u ) with g = W_gate x,
  * u = W_up x, both NVFP4 [d_inter][d_in], computed in FP32 and never written
  * out ([Spark27B] flow figure: gate, up, SiLU, then down). SiLU(g) =
