@@ -415,6 +415,35 @@ def run_reference(args):
     print(json.dumps(line), flush=True)
 
 
+def run_product_only(args):
+    """Times repeated calls of one NVFP4 product (a small, single-kernel
+    workload for profiler captures): --product ROWSxCOLS --tokens N."""
+    import torch
+    import __graft_entry__ as g
+    g.build()
+    import bit_weight_streaming_gb300 as bws
+    from bit_weight_streaming_gb300 import workloads as W
+    import synth
+    rows, cols = (int(v) for v in args.product.lower().split("x"))
+    dev = torch.device("cuda", 0)
+    mats = [W.make_matrix(1, (rows, cols), args.seed, i, device=dev) for i in range(args.copies)]
+    x = synth.activation_bf16(args.tokens, cols, seed=args.seed, device=dev)
+    y = torch.empty((args.tokens, rows), dtype=torch.bfloat16, device=dev)
+    ws = bws.Workspace(dev)
+    k = [0]
+
+    def call():
+        m = mats[k[0] % len(mats)]
+        k[0] += 1
+        bws.nvfp4_gemv(m.codes, m.scales, m.scale32, x, y=y, ws=ws)
+
+    stream = torch.cuda.current_stream(dev)
+    t = time_steps(call, args.steps, args.warmup, stream)
+    nb = mats[0].nbytes()
+    print(json.dumps({"product": f"{rows}x{cols}", "tokens": args.tokens, "copies": args.copies,
+                      "us_per_call": round(t * 1e6, 2), "GB/s": round(nb / t / 1e9, 1)}), flush=True)
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
@@ -423,10 +452,15 @@ def main(argv=None):
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-moe", action="store_true")
+    ap.add_argument("--product", default=None, help="ROWSxCOLS: time one NVFP4 product only (profiling)")
+    ap.add_argument("--tokens", type=int, default=1)
+    ap.add_argument("--copies", type=int, default=4, help="--product: distinct weight copies to rotate")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         args.warmup = 3
-    if args.impl == "reference":
+    if args.product:
+        run_product_only(args)
+    elif args.impl == "reference":
         run_reference(args)
     else:
         run_gpu(args)

@@ -72,6 +72,7 @@ int run_product(int fmt, int epi, GemvParams& p, const uint16_t* x, int N, int d
   q.exp = reinterpret_cast<int*>(w + L.off_exp);
   q.flags = reinterpret_cast<uint32_t*>(w + L.off_flags);
   q.hdr = reinterpret_cast<uint32_t*>(w + L.off_hdr);
+  q.status_clear = q.hdr + 1;
   q.zero_ptr = reinterpret_cast<uint32_t*>(w + L.off_counters);
   q.zero_words = p.n_tiles;
   p.x.hi = q.hi;
@@ -85,9 +86,10 @@ int run_product(int fmt, int epi, GemvParams& p, const uint16_t* x, int N, int d
   p.out_ld = out_ld;
   p.out_slot_stride = 0;
   p.prefetch_units = fmt == kFmtFP8 ? 4 : 8;
+  q.interleave = gemv_tma_eligible(fmt, p) ? tma_interleave(fmt) : 0;   // the layout its product reads
   cudaError_t e = launch_prep(q, st, true);
   if (e != cudaSuccess) return cuda_status(e, name);
-  e = launch_gemv(fmt, epi, p, st, true);
+  e = launch_product(fmt, epi, p, q.hdr + 1, st, true);
   return cuda_status(e, name);
 }
 
@@ -227,17 +229,17 @@ int bws_fp8_lmhead_gemv(const uint8_t* W, const float* row_scale, const uint16_t
 int bws_status_word(const void* workspace, uint32_t* status, void* stream) {
   if (!workspace || !status) return fail(BWS_ERR_INVALID_ARG, "bws_status_word: null pointer");
   const GemvWorkspace L = gemv_workspace_layout(1, 32, 1, 1);
-  uint32_t hdr = 0, flags[kMaxTokens] = {0};
+  uint32_t hdr2[2] = {0, 0}, flags[kMaxTokens] = {0};
   cudaStream_t st = as_stream(stream);
-  cudaError_t e = cudaMemcpyAsync(&hdr, static_cast<const char*>(workspace) + L.off_hdr, 4,
+  cudaError_t e = cudaMemcpyAsync(hdr2, static_cast<const char*>(workspace) + L.off_hdr, 8,
                                   cudaMemcpyDeviceToHost, st);
   if (e == cudaSuccess)
     e = cudaMemcpyAsync(flags, static_cast<const char*>(workspace) + L.off_flags, sizeof(flags),
                         cudaMemcpyDeviceToHost, st);
   if (e == cudaSuccess) e = cudaStreamSynchronize(st);
   if (e != cudaSuccess) return cuda_status(e, "bws_status_word");
-  uint32_t s = 0;
-  for (uint32_t i = 0; i < hdr && i < (uint32_t)kMaxTokens; ++i) s |= flags[i];
+  uint32_t s = hdr2[1];
+  for (uint32_t i = 0; i < hdr2[0] && i < (uint32_t)kMaxTokens; ++i) s |= flags[i];
   *status = s;
   g_err[0] = 0;
   return BWS_OK;

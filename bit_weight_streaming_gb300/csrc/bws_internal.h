@@ -101,8 +101,11 @@ struct PrepParams {
   int* exp;
   uint32_t* flags;
   uint32_t* hdr;           // [0] = N (status reads), may be null
+  uint32_t* status_clear;  // zeroed by the prep (the status word of the call), may be null
   uint32_t* zero_ptr;      // counters of the next product, zeroed
   int zero_words;
+  int interleave;          // 0: linear rows; else the unit size in k (256 NVFP4, 128 FP8) of
+                           // the TMA kernel's layout (see gemv_tma.cu)
 };
 
 // Workspace of one product call (all offsets 256-byte aligned).
@@ -116,6 +119,17 @@ long long gemv_max_warps();
 
 cudaError_t launch_prep(const PrepParams& q, cudaStream_t st, bool pdl);
 cudaError_t launch_gemv(int fmt, int epi, const GemvParams& p, cudaStream_t st, bool pdl);
+// The TMA-fed product kernel (gemv_tma.cu) for plain-mode NVFP4 (d_in % 256
+// == 0) and FP8 (d_in % 128 == 0) products with 16-byte aligned tensors.
+bool gemv_tma_eligible(int fmt, const GemvParams& p);
+// Activation layout the TMA kernel reads for this format (PrepParams::interleave).
+inline int tma_interleave(int fmt) { return fmt == kFmtFP8 ? 128 : 256; }
+cudaError_t launch_gemv_tma(int fmt, int epi, const GemvParams& p, uint32_t* status, cudaStream_t st, bool pdl);
+// Product with the best kernel for its shape.
+inline cudaError_t launch_product(int fmt, int epi, const GemvParams& p, uint32_t* status, cudaStream_t st,
+                                  bool pdl) {
+  return gemv_tma_eligible(fmt, p) ? launch_gemv_tma(fmt, epi, p, status, st, pdl) : launch_gemv(fmt, epi, p, st, pdl);
+}
 
 // MoE helpers.
 struct MoeRoute {

@@ -536,7 +536,10 @@ __global__ void __launch_bounds__(kPrepThreads) prep_kernel(const __grid_constan
   const int tok = blockIdx.x - slot * q.N;
   const int n_slots = q.n_slots != nullptr ? __ldg(q.n_slots) : 1;
   if (slot >= n_slots) return;
-  if (blockIdx.x == 0 && threadIdx.x == 0 && q.hdr != nullptr) q.hdr[0] = (uint32_t)q.N;
+  if (blockIdx.x == 0 && threadIdx.x == 0) {
+    if (q.hdr != nullptr) q.hdr[0] = (uint32_t)q.N;
+    if (q.status_clear != nullptr) q.status_clear[0] = 0u;
+  }
   __shared__ float sm[kPrepThreads / 32];
   __shared__ uint32_t sf[kPrepThreads / 32];
   const size_t rowbase = ((size_t)slot * (q.N + 1)) * q.d_in_pad;
@@ -594,7 +597,17 @@ __global__ void __launch_bounds__(kPrepThreads) prep_kernel(const __grid_constan
   uint32_t flags = 0u;
   uint4* hi4 = reinterpret_cast<uint4*>(q.hi + rowbase + (size_t)tok * q.d_in_pad);
   uint4* lo4 = reinterpret_cast<uint4*>(q.lo + rowbase + (size_t)tok * q.d_in_pad);
+  // TMA-kernel layout: within each unit of K_u values, the 8-value chunk j of
+  // lane chunk cl (cl = 0..7, lane chunks of K_u/8 values) moves to chunk
+  // position j * 8 + cl, so that the 8 lanes of a shared-memory phase read 8
+  // different banks.
+  const int ku8 = q.interleave / 8, lk8 = q.interleave / 64;
   for (int c = threadIdx.x; c < nchunk_pad; c += blockDim.x) {
+    int dst = c;
+    if (q.interleave) {
+      const int u = c / ku8, r8 = c - u * ku8;
+      dst = u * ku8 + (r8 % lk8) * 8 + r8 / lk8;
+    }
     uint32_t w[4];
     prep_chunk(q, c, nchunk, rr, xr, inv_rms, w);
     uint32_t h[4], l[4];
@@ -622,8 +635,8 @@ __global__ void __launch_bounds__(kPrepThreads) prep_kernel(const __grid_constan
       h[i] = hh[0] | (hh[1] << 16);
       l[i] = ll[0] | (ll[1] << 16);
     }
-    hi4[c] = make_uint4(h[0], h[1], h[2], h[3]);
-    lo4[c] = make_uint4(l[0], l[1], l[2], l[3]);
+    hi4[dst] = make_uint4(h[0], h[1], h[2], h[3]);
+    lo4[dst] = make_uint4(l[0], l[1], l[2], l[3]);
   }
   flags = __reduce_or_sync(0xffffffffu, flags);
   __syncthreads();

@@ -1,0 +1,601 @@
+// Weight-stream products fed by TMA: one producer warp per CTA streams weight
+// tiles into a ring of shared-memory stages with cp.async.bulk.tensor; eight
+// consumer warps decode them and run the MMAs. The producer starts before the
+// kernel waits on its inputs (weights never depend on earlier kernels), so the
+// ring fills while the previous kernel finishes.
+//
+// Tiles and units. A tile is 128 output rows (8 MMA sub-tiles of 16): rows
+// [128i, 128i+128) of one matrix, or, for the fused SwiGLU, 64 gate rows and
+// the same 64 up rows. A unit is a tile x 128 bytes of each row (256 NVFP4
+// weights, 128 FP8 weights) and arrives as four 32-row TMA boxes with 128-byte
+// swizzle (plus four 32 x 16-byte boxes of E4M3 block scales for NVFP4) and,
+// through 1D bulk copies, the unit's activations of every token. Units are
+// dealt to CTAs in equal contiguous ranges (stream-K); a tile cut between CTAs
+// is finished by the last CTA to arrive, adding partial sums in CTA order.
+//
+// Consumer warp w takes box b = w%4 (two sub-tiles) and half h = w/4 of every
+// unit's 128 bytes: lane (g, t) reads the 16-byte chunk c = 2t + h of rows g,
+// g+8, g+16, g+24 of the box, which puts the 8 lanes of each shared-memory
+// access phase on 8 distinct swizzled chunks (no bank conflicts). A chunk is
+// 32 NVFP4 weights (two 16-weight blocks) or 16 FP8 weights; MMA j takes its
+// 4 consecutive weights 4j..4j+3 as logical k {2t, 2t+1, 2t+8, 2t+9}, and the
+// activations, laid out by the prep kernel so that chunk c's pieces sit at
+// c * 16 + q * 128, are read with the same mapping. The two halves of a
+// sub-tile are added through shared memory at the end of each tile piece.
+#include <cuda.h>
+
+#include <cstring>
+
+#include "bws_common.cuh"
+#include "bws_internal.h"
+
+namespace bws {
+
+namespace {
+
+constexpr int kConsumerWarps = 8;
+constexpr int kThreadsTma = (kConsumerWarps + 1) * 32;
+constexpr int kMaxStages = 16;
+constexpr int kBoxRows = 32;
+constexpr int kBoxes = 4;                          // boxes per unit
+constexpr int kBoxBytes = kBoxRows * 128;          // one code box
+constexpr int kCodeBytes = kBoxes * kBoxBytes;     // code bytes of a unit
+constexpr int kScaleBoxBytes = kBoxRows * 16;      // one NVFP4 scale box
+constexpr int kSmemBudget = 100 * 1024;            // stages per CTA: two CTAs share an SM
+constexpr uint32_t kMaxPolls = 1u << 24;           // bounded waits (seconds)
+constexpr uint32_t kStatusTimeout = 0x100u;
+constexpr int kPartialBytes = kBoxes * 2 * 32 * 16;   // one (tile, CTA) slot of partial sums
+
+struct TmaMat {
+  CUtensorMap codes;    // u8 [d_out][row_bytes], box {128, 32}, 128B swizzle
+  CUtensorMap scales;   // u8 [d_out][d_in/16], box {16, 32} (NVFP4)
+  const float* scale32;
+  int d_out;
+  int out_row_off;
+  int tile_begin;
+};
+
+struct TmaParams {
+  TmaMat mats[kMaxMats];
+  int n_mats;
+  int N, d_in, d_in_pad, nks;   // nks: units per tile (128-byte steps of a row)
+  int n_tiles;
+  long long n_units;
+  int n_ctas;
+  XPrep x;
+  void* out;
+  int out_ld;
+  float* partials;
+  uint32_t* counters;
+  uint32_t* status;
+  // shared-memory stage layout: code boxes at 0, scale boxes at kCodeBytes
+  // (NVFP4), one activation block per token at x_off + tok * x_blk
+  int n_stages, stage_bytes, x_off, x_blk, x_bytes;
+};
+
+// Shared memory after the stages.
+struct Tail {
+  float4 red[kBoxes][2][32];   // half-pair reduction (box, sub-tile, lane)
+  float4 swi[2][2][32];        // SwiGLU: up sums handed to the gate warps
+  uint64_t full[kMaxStages];
+  uint64_t empty[kMaxStages];
+  uint32_t flag;
+};
+
+// Matrix and first row of box b of a tile.
+template <int EPI>
+BWS_DEV void box_of(const TmaParams& p, int tile, int b, int& m, int& row) {
+  if (EPI == kEpiSwiGLU) {
+    m = b >> 1;
+    row = tile * 64 + 32 * (b & 1);
+    return;
+  }
+  m = 0;
+#pragma unroll
+  for (int i = 1; i < kMaxMats; ++i)
+    if (i < p.n_mats && tile >= p.mats[i].tile_begin) m = i;
+  row = (tile - p.mats[m].tile_begin) * 128 + 32 * b;
+}
+
+BWS_DEV long long owner(long long u, long long U, long long G) { return ((u + 1) * G - 1) / U; }
+BWS_DEV long long begin_of(long long c, long long U, long long G) { return c * U / G; }
+
+BWS_DEV float silu_mul_t(float g, float u) {
+  const float sg = __fdiv_rn(g, __fadd_rn(1.0f, expf(-g)));
+  return __fmul_rn(sg, u);
+}
+
+// Store v (raw sums of sub-tile s of box b; register i = row g + 8*(i>>1),
+// token 2t + (i&1)). SwiGLU: b is a gate box and vu the matching up sums.
+template <int FMT, int EPI>
+BWS_DEV void store_sub(const TmaParams& p, int tile, int b, int s, int g, int t, const float (&v)[4],
+                       const float (&vu)[4]) {
+  int mi, row_b;
+  box_of<EPI>(p, tile, b, mi, row_b);
+  const TmaMat& M = p.mats[mi];
+  const int row0 = row_b + 16 * s;
+  int xexp[2];
+#pragma unroll
+  for (int i = 0; i < 2; ++i) {
+    const int tok = 2 * t + i;
+    xexp[i] = tok < p.N ? __ldg(p.x.exp + tok) : 0;
+  }
+  float su = 1.0f;
+  if (EPI == kEpiSwiGLU) su = __ldg(p.mats[1].scale32);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int row = row0 + g + 8 * (i >> 1);
+    const int tok = 2 * t + (i & 1);
+    if (row >= M.d_out || tok >= p.N) continue;
+    float sc = 1.0f;
+    if (FMT == kFmtNVFP4) sc = __ldg(M.scale32);
+    if (FMT == kFmtFP8) sc = __ldg(M.scale32 + row);
+    const float val = ldexp_exact(__fmul_rn(v[i], sc), xexp[i & 1] - 14);
+    if (EPI == kEpiSwiGLU) {
+      const float up = ldexp_exact(__fmul_rn(vu[i], su), xexp[i & 1] - 14);
+      reinterpret_cast<__nv_bfloat16*>(p.out)[(size_t)tok * p.out_ld + row] =
+          __float2bfloat16_rn(silu_mul_t(val, up));
+    } else {
+      const size_t o = (size_t)tok * p.out_ld + M.out_row_off + row;
+      if (EPI == kEpiStoreBF16)
+        reinterpret_cast<__nv_bfloat16*>(p.out)[o] = __float2bfloat16_rn(val);
+      else if (EPI == kEpiStoreF32)
+        reinterpret_cast<float*>(p.out)[o] = val;
+      else
+        reinterpret_cast<float*>(p.out)[o] = __fadd_rn(reinterpret_cast<float*>(p.out)[o], val);
+    }
+  }
+}
+
+// Products of one 16-row sub-tile with one unit's activations: w0 / w1 are
+// the lane's chunk words of rows g / g+8, sc0 / sc1 their two block scales
+// (NVFP4), xh the hi-band pieces, xl the lo band (when lo).
+template <int FMT, bool LO>
+BWS_DEV void sub_mma(float (&acc)[2][4], float (&accl)[4], const uint32_t (&w0)[4], const uint32_t (&w1)[4],
+                     uint32_t sc0, uint32_t sc1, const uint4 (&xh)[FMT == kFmtFP8 ? 2 : 4],
+                     const uint4 (&xl)[FMT == kFmtFP8 ? 2 : 4]) {
+  if constexpr (FMT == kFmtFP8) {
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      uint32_t a0, a2, a1, a3;
+      e4m3x4_to_f16x2x2(w0[j], a0, a2);
+      e4m3x4_to_f16x2x2(w1[j], a1, a3);
+      const uint4& xq = xh[j >> 1];
+      mma_f16_16816(acc[j & 1], a0, a1, a2, a3, (j & 1) ? xq.z : xq.x, (j & 1) ? xq.w : xq.y);
+      if (LO) {
+        const uint4& lq = xl[j >> 1];
+        mma_f16_16816(accl, a0, a1, a2, a3, (j & 1) ? lq.z : lq.x, (j & 1) ? lq.w : lq.y);
+      }
+    }
+  } else {
+    const uint32_t f0 = e4m3x2_to_f16x2(sc0), f1 = e4m3x2_to_f16x2(sc1);
+    const uint32_t m0[2] = {bcast_lo(f0), bcast_hi(f0)};
+    const uint32_t m1[2] = {bcast_lo(f1), bcast_hi(f1)};
+#pragma unroll
+    for (int w = 0; w < 4; ++w) {
+      uint32_t p0, p1, p2, p3, q0, q1, q2, q3;
+      e2m1x8_to_f16x2x4(w0[w], p0, p1, p2, p3);
+      e2m1x8_to_f16x2x4(w1[w], q0, q1, q2, q3);
+      const uint32_t sa = m0[w >> 1], sb = m1[w >> 1];
+      p0 = hmul2_u32(p0, sa); p1 = hmul2_u32(p1, sa); p2 = hmul2_u32(p2, sa); p3 = hmul2_u32(p3, sa);
+      q0 = hmul2_u32(q0, sb); q1 = hmul2_u32(q1, sb); q2 = hmul2_u32(q2, sb); q3 = hmul2_u32(q3, sb);
+      mma_f16_16816(acc[0], p0, q0, p1, q1, xh[w].x, xh[w].y);
+      mma_f16_16816(acc[1], p2, q2, p3, q3, xh[w].z, xh[w].w);
+      if (LO) {
+        mma_f16_16816(accl, p0, q0, p1, q1, xl[w].x, xl[w].y);
+        mma_f16_16816(accl, p2, q2, p3, q3, xl[w].z, xl[w].w);
+      }
+    }
+  }
+}
+
+// The consumer warps' loop over units u0..u1 (LO: the two-band activation
+// path, taken when some token has elements below the hi band's range).
+template <int FMT, int EPI, bool LO>
+BWS_DEV void consume(const TmaParams& p, Tail& T, uint32_t stage0, long long u0, long long u1, int warp, int lane,
+                     const uint16_t* xrow_l) {
+  const long long U = p.n_units, G = p.n_ctas;
+  const int NS = p.n_stages;
+  constexpr int kUnitK = FMT == kFmtFP8 ? 128 : 256;
+  constexpr int kXv = FMT == kFmtFP8 ? 2 : 4;     // 16-byte activation pieces per unit
+  const int b = warp & 3, half = warp >> 2;
+  const int g = lane >> 2, t = lane & 3;
+  const int c = 2 * t + half;                     // this lane's 16-byte chunk
+  // rows g + 8j of box b (j = 0..3) share the swizzle phase g
+  const uint32_t coff = b * kBoxBytes + g * 128 + ((c ^ g) << 4);
+  const uint32_t soff = kCodeBytes + b * kScaleBoxBytes + g * 16 + 2 * c;
+  // activations of token g (absent tokens read token 0's: their MMA columns
+  // are never stored), pieces at q * 128
+  const int xg = g < p.N ? g : 0;
+  const uint32_t xoff = (uint32_t)(p.x_off + xg * p.x_blk + c * 16);
+  xrow_l += (size_t)xg * p.d_in_pad;
+  float acc[2][2][4] = {}, accl[2][4] = {};
+  uint4 xh[kXv], xl[kXv];
+  bool dead = false;   // a wait ran out: keep the control flow (barriers), skip the work
+  int tile = (int)(u0 / p.nks), ks = (int)(u0 % p.nks);
+  int s = 0;
+  uint32_t ph = 0u;
+  bool piece_whole = ks == 0;   // the piece starts at the tile's first unit
+  for (long long u = u0; u < u1; ++u) {
+    if (LO) {   // two-band path: the lo band comes from global memory
+#pragma unroll
+      for (int q = 0; q < kXv; ++q)
+        xl[q] = ld_act_v4(xrow_l + (size_t)ks * kUnitK + q * 64 + c * 8);
+    }
+    if (!dead && !mbar_wait_bounded(smem_u32(&T.full[s]), ph, kMaxPolls)) {
+      if (lane == 0) atomicOr(p.status, kStatusTimeout);
+      dead = true;
+    }
+    const uint32_t base = stage0 + (uint32_t)s * p.stage_bytes;
+    uint4 cw[4];
+    uint32_t sc[4];
+    if (!dead) {
+#pragma unroll
+      for (int j = 0; j < 4; ++j) cw[j] = lds_v4(base + coff + j * 1024);
+      if (FMT == kFmtNVFP4) {
+#pragma unroll
+        for (int j = 0; j < 4; ++j) sc[j] = lds_u16(base + soff + j * 128);
+      }
+#pragma unroll
+      for (int q = 0; q < kXv; ++q) xh[q] = lds_v4(base + xoff + q * 128);
+    } else {
+#pragma unroll
+      for (int j = 0; j < 4; ++j) { cw[j] = make_uint4(0, 0, 0, 0); sc[j] = 0u; }
+#pragma unroll
+      for (int q = 0; q < kXv; ++q) xh[q] = make_uint4(0, 0, 0, 0);
+    }
+    // the stage's shared memory has been read: hand it back to the producer
+    __syncwarp();
+    if (lane == 0 && !dead) mbar_arrive(smem_u32(&T.empty[s]));
+    if (++s == NS) { s = 0; ph ^= 1u; }
+#pragma unroll
+    for (int st = 0; st < 2; ++st) {
+      const uint32_t w0[4] = {cw[2 * st].x, cw[2 * st].y, cw[2 * st].z, cw[2 * st].w};
+      const uint32_t w1[4] = {cw[2 * st + 1].x, cw[2 * st + 1].y, cw[2 * st + 1].z, cw[2 * st + 1].w};
+      sub_mma<FMT, LO>(acc[st], accl[st], w0, w1, sc[2 * st], sc[2 * st + 1], xh, xl);
+    }
+    // ---- end of a tile piece ----
+    const bool last_of_tile = ks == p.nks - 1;
+    const int cur_tile = tile;
+    if (++ks == p.nks) { ks = 0; ++tile; }
+    if (!last_of_tile && u + 1 < u1) continue;
+    float v[2][4];
+#pragma unroll
+    for (int st = 0; st < 2; ++st) {
+#pragma unroll
+      for (int r = 0; r < 4; ++r) {
+        const float a = __fadd_rn(acc[st][0][r], acc[st][1][r]);
+        v[st][r] = LO ? __fmaf_rn(accl[st][r], 0x1p-29f, a) : a;
+        acc[st][0][r] = acc[st][1][r] = accl[st][r] = 0.f;
+      }
+    }
+    // add the two halves: warps 4..7 hand their sums to warps 0..3
+    if (half == 1) {
+#pragma unroll
+      for (int st = 0; st < 2; ++st) T.red[b][st][lane] = make_float4(v[st][0], v[st][1], v[st][2], v[st][3]);
+    }
+    named_bar_sync(1, kConsumerWarps * 32);
+    if (half == 0) {
+#pragma unroll
+      for (int st = 0; st < 2; ++st) {
+        const float4 o = T.red[b][st][lane];
+        v[st][0] += o.x; v[st][1] += o.y; v[st][2] += o.z; v[st][3] += o.w;
+      }
+    }
+    named_bar_sync(1, kConsumerWarps * 32);
+    const bool whole = piece_whole && last_of_tile;
+    piece_whole = true;   // later pieces start at a tile's first unit
+    if (half == 1) continue;
+    // warps 0..3: finish or deposit
+    if (!whole) {
+      float4* slot = reinterpret_cast<float4*>(p.partials) + ((size_t)(cur_tile + blockIdx.x) * kBoxes + b) * 64;
+#pragma unroll
+      for (int st = 0; st < 2; ++st) slot[st * 32 + lane] = make_float4(v[st][0], v[st][1], v[st][2], v[st][3]);
+      __threadfence();
+      named_bar_sync(2, 4 * 32);
+      const long long c0 = owner((long long)cur_tile * p.nks, U, G);
+      const long long c1 = owner((long long)(cur_tile + 1) * p.nks - 1, U, G);
+      if (threadIdx.x == 0) T.flag = atomicAdd(p.counters + cur_tile, 1u);
+      named_bar_sync(2, 4 * 32);
+      const uint32_t prev = T.flag;
+      named_bar_sync(2, 4 * 32);
+      if (prev != (uint32_t)(c1 - c0)) continue;
+      __threadfence();
+      float a8[2][4] = {};
+      for (long long cc = c0; cc <= c1; ++cc) {
+#pragma unroll
+        for (int st = 0; st < 2; ++st) {
+          float4 o;
+          if (cc == blockIdx.x)
+            o = make_float4(v[st][0], v[st][1], v[st][2], v[st][3]);
+          else
+            o = ld_cg_f4(reinterpret_cast<const float4*>(p.partials) +
+                         ((size_t)(cur_tile + cc) * kBoxes + b) * 64 + st * 32 + lane);
+          a8[st][0] += o.x; a8[st][1] += o.y; a8[st][2] += o.z; a8[st][3] += o.w;
+        }
+      }
+#pragma unroll
+      for (int st = 0; st < 2; ++st)
+#pragma unroll
+        for (int r = 0; r < 4; ++r) v[st][r] = a8[st][r];
+      if (threadIdx.x == 0) p.counters[cur_tile] = 0u;
+    }
+    if (EPI == kEpiSwiGLU) {
+      // boxes 2, 3 (up rows) meet boxes 0, 1 (gate rows) of the same rows
+      if (b >= 2) {
+#pragma unroll
+        for (int st = 0; st < 2; ++st) T.swi[b - 2][st][lane] = make_float4(v[st][0], v[st][1], v[st][2], v[st][3]);
+      }
+      named_bar_sync(3, 4 * 32);
+      if (b < 2) {
+#pragma unroll
+        for (int st = 0; st < 2; ++st) {
+          const float4 o = T.swi[b][st][lane];
+          const float vu[4] = {o.x, o.y, o.z, o.w};
+          store_sub<FMT, EPI>(p, cur_tile, b, st, g, t, v[st], vu);
+        }
+      }
+      named_bar_sync(3, 4 * 32);
+    } else {
+      const float none[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+      for (int st = 0; st < 2; ++st) store_sub<FMT, EPI>(p, cur_tile, b, st, g, t, v[st], none);
+    }
+  }
+}
+
+// The rare two-band loop, out of line so that its registers do not weigh on
+// the main loop.
+template <int FMT, int EPI>
+__device__ __noinline__ void consume_lo(const TmaParams& p, Tail& T, uint32_t stage0, long long u0, long long u1,
+                                        int warp, int lane, const uint16_t* xrow_l) {
+  consume<FMT, EPI, true>(p, T, stage0, u0, u1, warp, lane, xrow_l);
+}
+
+template <int FMT, int EPI>
+__global__ void __launch_bounds__(kThreadsTma, 2) gemv_tma_kernel(const __grid_constant__ TmaParams p) {
+  extern __shared__ __align__(16) uint8_t smem_raw[];
+  // 128-byte swizzled TMA boxes need 1024-byte aligned destinations
+  const uint32_t mis = smem_u32(smem_raw) & 1023u;
+  uint8_t* sbase = smem_raw + ((1024u - mis) & 1023u);
+  Tail& T = *reinterpret_cast<Tail*>(sbase + (size_t)p.n_stages * p.stage_bytes);
+  const uint32_t stage0 = smem_u32(sbase);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const long long U = p.n_units, G = p.n_ctas;
+  const long long u0 = begin_of(blockIdx.x, U, G), u1 = begin_of(blockIdx.x + 1, U, G);
+  const int NS = p.n_stages;
+  pdl_launch_dependents();
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < NS; ++i) {
+      mbar_init(smem_u32(&T.full[i]), 1);
+      mbar_init(smem_u32(&T.empty[i]), kConsumerWarps);
+    }
+    T.flag = 0u;
+    mbar_fence_init();
+  }
+  __syncthreads();
+  constexpr int kUnitK = FMT == kFmtFP8 ? 128 : 256;
+
+  if (warp == kConsumerWarps) {
+    // ---- producer: weights before the inputs are ready, activations after ----
+    if (lane == 0) {
+      for (int i = 0; i < p.n_mats; ++i) {
+        tma_prefetch_desc(&p.mats[i].codes);
+        if (FMT == kFmtNVFP4) tma_prefetch_desc(&p.mats[i].scales);
+      }
+      const uint32_t w_tx = FMT == kFmtNVFP4 ? kCodeBytes + kBoxes * kScaleBoxBytes : kCodeBytes;
+      // weights of unit (tile, ks) into stage s (the stage's full barrier also
+      // expects the unit's activation bytes)
+      auto issue_weights = [&](int tile, int ks, int s) {
+        const uint32_t full = smem_u32(&T.full[s]);
+        const uint32_t dst = stage0 + (uint32_t)s * p.stage_bytes;
+        mbar_arrive_expect_tx(full, w_tx + (uint32_t)p.x_bytes);
+#pragma unroll
+        for (int b = 0; b < kBoxes; ++b) {
+          int m, row;
+          box_of<EPI>(p, tile, b, m, row);
+          tma_load_2d(dst + b * kBoxBytes, &p.mats[m].codes, ks * 128, row, full);
+          if (FMT == kFmtNVFP4)
+            tma_load_2d(dst + kCodeBytes + b * kScaleBoxBytes, &p.mats[m].scales, ks * 16, row, full);
+        }
+      };
+      auto issue_x = [&](int ks, int s) {
+        const uint32_t full = smem_u32(&T.full[s]);
+        const uint32_t dst = stage0 + (uint32_t)s * p.stage_bytes + p.x_off;
+        const uint16_t* src = p.x.hi + (size_t)ks * kUnitK;
+        for (int tok = 0; tok < p.N; ++tok)
+          bulk_load(dst + tok * p.x_blk, src + (size_t)tok * p.d_in_pad, kUnitK * 2, full);
+      };
+      // Prime the ring with weights before waiting for the activations: the
+      // weights never depend on the kernels before this one.
+      const int n_pre = (u1 - u0) < NS ? (int)(u1 - u0) : NS;
+      {
+        int tile = (int)(u0 / p.nks), ks = (int)(u0 % p.nks);
+        for (int k = 0; k < n_pre; ++k) {
+          issue_weights(tile, ks, k);
+          if (++ks == p.nks) { ks = 0; ++tile; }
+        }
+        pdl_wait();
+        ks = (int)(u0 % p.nks);
+        for (int k = 0; k < n_pre; ++k) {
+          issue_x(ks, k);
+          if (++ks == p.nks) ks = 0;
+        }
+      }
+      // The loop runs only when the ring was primed in full (n_pre == NS):
+      // unit n_pre + j reuses stage j % NS after its (j / NS)-th release.
+      int s = 0;
+      uint32_t ph = 0u;   // parity of the release to wait for
+      long long issued = n_pre;
+      int tile = (int)((u0 + n_pre) / p.nks), ks = (int)((u0 + n_pre) % p.nks);
+      for (long long u = u0 + n_pre; u < u1; ++u, ++issued) {
+        if (!mbar_wait_bounded(smem_u32(&T.empty[s]), ph, kMaxPolls)) {
+          atomicOr(p.status, kStatusTimeout);
+          // let copies already issued land before the CTA's shared memory goes away
+          for (long long k = (issued > NS ? issued - NS : 0); k < issued; ++k)
+            mbar_wait_bounded(smem_u32(&T.full[k % NS]), (uint32_t)(k / NS) & 1u, kMaxPolls);
+          break;
+        }
+        issue_weights(tile, ks, s);
+        issue_x(ks, s);
+        if (++s == NS) { s = 0; ph ^= 1u; }
+        if (++ks == p.nks) { ks = 0; ++tile; }
+      }
+    }
+    return;
+  }
+
+  // ---- consumers ----
+  pdl_wait();
+  uint32_t fl = 0u;
+  for (int tok = 0; tok < p.N; ++tok) fl |= __ldg(p.x.flags + tok);
+  if (fl & 1u)
+    consume_lo<FMT, EPI>(p, T, stage0, u0, u1, warp, lane, p.x.lo);
+  else
+    consume<FMT, EPI, false>(p, T, stage0, u0, u1, warp, lane, p.x.lo);
+}
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  if (fn == nullptr) {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  }
+  return fn;
+}
+
+bool encode_2d(CUtensorMap* m, const void* base, uint64_t inner_bytes, uint64_t rows, uint32_t box_inner,
+               uint32_t box_rows, bool swizzle) {
+  EncodeTiledFn fn = encode_fn();
+  if (fn == nullptr) return false;
+  const cuuint64_t dims[2] = {inner_bytes, rows};
+  const cuuint64_t strides[1] = {inner_bytes};
+  const cuuint32_t box[2] = {box_inner, box_rows};
+  const cuuint32_t estr[2] = {1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <int FMT, int EPI>
+cudaError_t launch_tma_one(const TmaParams& p, cudaStream_t st, bool pdl) {
+  const int smem = p.n_stages * p.stage_bytes + (int)sizeof(Tail) + 1024;
+  static bool attr = false;
+  if (!attr) {
+    cudaError_t e = cudaFuncSetAttribute(gemv_tma_kernel<FMT, EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         kSmemBudget + (int)sizeof(Tail) + 1024);
+    if (e != cudaSuccess) return e;
+    attr = true;
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)p.n_ctas);
+  cfg.blockDim = dim3(kThreadsTma);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute a[1];
+  a[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  a[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = a;
+  cfg.numAttrs = pdl ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, gemv_tma_kernel<FMT, EPI>, p);
+}
+
+}  // namespace
+
+bool gemv_tma_eligible(int fmt, const GemvParams& p) {
+  if (p.slots.n_slots != nullptr || encode_fn() == nullptr) return false;
+  if (fmt == kFmtNVFP4) {
+    if (p.d_in % 256 != 0) return false;
+  } else if (fmt == kFmtFP8) {
+    if (p.d_in % 128 != 0) return false;
+  } else {
+    return false;
+  }
+  for (int i = 0; i < p.n_mats; ++i) {
+    if (((uintptr_t)p.mats[i].codes & 15) != 0) return false;
+    if (fmt == kFmtNVFP4 && ((uintptr_t)p.mats[i].scales & 15) != 0) return false;
+  }
+  return true;
+}
+
+int gemv_tma_tiles(int epi, const GemvMat* mats, int n_mats) {
+  if (epi == kEpiSwiGLU) return (mats[0].d_out + 63) / 64;
+  int t = 0;
+  for (int i = 0; i < n_mats; ++i) t += (mats[i].d_out + 127) / 128;
+  return t;
+}
+
+// Runs the product described by g (plain mode, activations already prepared)
+// with the TMA kernel, in the scratch a product workspace provides: g.counters
+// (g.n_tiles words, zero) and g.partials ((g.n_tiles + gemv_max_warps()) KiB).
+cudaError_t launch_gemv_tma(int fmt, int epi, const GemvParams& g, uint32_t* status, cudaStream_t st, bool pdl) {
+  TmaParams p;
+  memset(&p, 0, sizeof(p));
+  p.n_mats = g.n_mats;
+  int tile = 0, row = 0;
+  for (int i = 0; i < g.n_mats; ++i) {
+    const GemvMat& M = g.mats[i];
+    const uint64_t row_bytes = fmt == kFmtFP8 ? (uint64_t)g.d_in : (uint64_t)g.d_in / 2;
+    if (!encode_2d(&p.mats[i].codes, M.codes, row_bytes, (uint64_t)M.d_out, 128, kBoxRows, true))
+      return cudaErrorInvalidValue;
+    if (fmt == kFmtNVFP4 &&
+        !encode_2d(&p.mats[i].scales, M.scales, (uint64_t)g.d_in / 16, (uint64_t)M.d_out, 16, kBoxRows, false))
+      return cudaErrorInvalidValue;
+    p.mats[i].scale32 = M.scale32;
+    p.mats[i].d_out = M.d_out;
+    p.mats[i].out_row_off = epi == kEpiSwiGLU ? 0 : row;
+    p.mats[i].tile_begin = tile;
+    row += M.d_out;
+    tile += (M.d_out + 127) / 128;
+  }
+  p.N = g.N;
+  p.d_in = g.d_in;
+  p.d_in_pad = g.d_in_pad;
+  p.nks = fmt == kFmtFP8 ? g.d_in / 128 : g.d_in / 256;
+  p.n_tiles = gemv_tma_tiles(epi, g.mats, g.n_mats);
+  p.n_units = (long long)p.n_tiles * p.nks;
+  const long long ctas = 2LL * num_sms();   // two CTAs per SM
+  p.n_ctas = (int)(p.n_units < ctas ? p.n_units : ctas);
+  p.x = g.x;
+  p.out = g.out;
+  p.out_ld = g.out_ld;
+  p.partials = g.partials;
+  p.counters = g.counters;
+  p.status = status;
+  // the scratch of the product workspace must cover this kernel's counters and partial sums
+  if (p.n_tiles > g.n_tiles ||
+      ((long long)p.n_tiles + p.n_ctas) * kPartialBytes >
+          ((long long)g.n_tiles + gemv_max_warps()) * kSlotFloats * (long long)sizeof(float))
+    return cudaErrorInvalidValue;
+  const int unit_k = fmt == kFmtFP8 ? 128 : 256;
+  p.x_off = fmt == kFmtNVFP4 ? kCodeBytes + kBoxes * kScaleBoxBytes : kCodeBytes;
+  p.x_blk = unit_k * 2 + 16;                    // one token's slice, skewed by 16 bytes
+  p.x_bytes = g.N * unit_k * 2;
+  p.stage_bytes = ((p.x_off + g.N * p.x_blk) + 1023) / 1024 * 1024;
+  p.n_stages = kSmemBudget / p.stage_bytes;
+  if (p.n_stages > kMaxStages) p.n_stages = kMaxStages;
+  if (p.n_stages < 2) return cudaErrorInvalidValue;
+  if (p.n_ctas <= 0) return cudaSuccess;
+#define BWS_CASE(F, E) \
+  if (fmt == F && epi == E) return launch_tma_one<F, E>(p, st, pdl);
+  BWS_CASE(kFmtNVFP4, kEpiStoreBF16)
+  BWS_CASE(kFmtNVFP4, kEpiResidF32)
+  BWS_CASE(kFmtNVFP4, kEpiSwiGLU)
+  BWS_CASE(kFmtNVFP4, kEpiStoreF32)
+  BWS_CASE(kFmtFP8, kEpiStoreF32)
+  BWS_CASE(kFmtFP8, kEpiStoreBF16)
+  BWS_CASE(kFmtFP8, kEpiResidF32)
+  BWS_CASE(kFmtFP8, kEpiSwiGLU)
+#undef BWS_CASE
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace bws

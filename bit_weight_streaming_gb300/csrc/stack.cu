@@ -19,7 +19,7 @@ struct bws_stack_plan {
   std::vector<bws_layer> layers;
   bws_matrix head;
   // workspace layout
-  size_t off_r, off_xp, off_u, off_vp, off_h, off_hp, off_moe, off_counters, off_partials, total;
+  size_t off_status, off_r, off_xp, off_u, off_vp, off_h, off_hp, off_moe, off_counters, off_partials, total;
   GemvWorkspace xw, vw, hw;    // prep-block offsets (relative to their block)
   int max_u, max_dv, max_inter, max_tiles;
   int kernels;
@@ -79,7 +79,7 @@ XPrep xprep_of(const Ctx& c, size_t block, const GemvWorkspace& L) {
 
 // prep into a block; zeroes `zero_words` counters at zero_ptr
 cudaError_t prep(const Ctx& c, int mode, const uint16_t* x, int ld, const uint16_t* x0, int d_in, size_t block,
-                 const GemvWorkspace& L, uint32_t* zero_ptr, int zero_words) {
+                 const GemvWorkspace& L, uint32_t* zero_ptr, int zero_words, int interleave = 0) {
   PrepParams q = {};
   q.mode = mode;
   q.x = x;
@@ -96,8 +96,10 @@ cudaError_t prep(const Ctx& c, int mode, const uint16_t* x, int ld, const uint16
   q.exp = const_cast<int*>(xp.exp);
   q.flags = const_cast<uint32_t*>(xp.flags);
   q.hdr = nullptr;
+  q.status_clear = x0 != nullptr ? reinterpret_cast<uint32_t*>(c.w + c.P->off_status) : nullptr;
   q.zero_ptr = zero_ptr;
   q.zero_words = zero_words;
+  q.interleave = interleave;
   return launch_prep(q, c.st, true);
 }
 
@@ -108,8 +110,8 @@ int tiles_for(const bws_matrix* mats, int nm, int epi) {
   return t;
 }
 
-cudaError_t product(const Ctx& c, const bws_matrix* mats, int nm, int epi, int d_in, const XPrep& x, void* out,
-                    int out_ld) {
+GemvParams product_params(const Ctx& c, const bws_matrix* mats, int nm, int epi, int d_in, const XPrep& x,
+                          void* out, int out_ld) {
   GemvParams p = {};
   p.n_mats = nm;
   int tile = 0, row = 0;
@@ -132,7 +134,17 @@ cudaError_t product(const Ctx& c, const bws_matrix* mats, int nm, int epi, int d
   p.counters = reinterpret_cast<uint32_t*>(c.w + c.P->off_counters);
   p.partials = reinterpret_cast<float*>(c.w + c.P->off_partials);
   p.prefetch_units = fmt_of(mats[0]) == kFmtFP8 ? 4 : 8;
-  return launch_gemv(fmt_of(mats[0]), epi, p, c.st, true);
+  return p;
+}
+
+// The activation layout the product's kernel reads.
+int layout_for(const bws_matrix* mats, const GemvParams& p) {
+  const int fmt = fmt_of(mats[0]);
+  return gemv_tma_eligible(fmt, p) ? tma_interleave(fmt) : 0;
+}
+
+cudaError_t product(const Ctx& c, const bws_matrix* mats, int nm, int epi, const GemvParams& p) {
+  return launch_product(fmt_of(mats[0]), epi, p, reinterpret_cast<uint32_t*>(c.w + c.P->off_status), c.st, true);
 }
 
 int enqueue_step(const bws_stack_plan* P, const uint16_t* x0, float* logits, void* ws, cudaStream_t st) {
@@ -158,22 +170,29 @@ int enqueue_step(const bws_stack_plan* P, const uint16_t* x0, float* logits, voi
     if (L.kind == BWS_LAYER_MIXER_MLP) {
       int sum_out = 0;
       for (int i = 0; i < L.n_mixer_in; ++i) sum_out += L.mixer_in[i].d_out;
+      const GemvParams pin = product_params(c, L.mixer_in, L.n_mixer_in, kEpiStoreBF16, H, xa, u, sum_out);
       BWS_TRY(prep(c, kPrepRmsNorm, nullptr, 0, init, H, P->off_xp, P->xw, counters,
-                   tiles_for(L.mixer_in, L.n_mixer_in, kEpiStoreBF16)));
+                   tiles_for(L.mixer_in, L.n_mixer_in, kEpiStoreBF16), layout_for(L.mixer_in, pin)));
       init = nullptr;
-      BWS_TRY(product(c, L.mixer_in, L.n_mixer_in, kEpiStoreBF16, H, xa, u, sum_out));
+      BWS_TRY(product(c, L.mixer_in, L.n_mixer_in, kEpiStoreBF16, pin));
       const int dv = L.mixer_out.d_in;
-      BWS_TRY(prep(c, kPrepCopy, u, sum_out, nullptr, dv, P->off_vp, P->vw, counters, tiles_for(&L.mixer_out, 1, kEpiResidF32)));
-      BWS_TRY(product(c, &L.mixer_out, 1, kEpiResidF32, dv, xv, r, H));
+      const GemvParams pout = product_params(c, &L.mixer_out, 1, kEpiResidF32, dv, xv, r, H);
+      BWS_TRY(prep(c, kPrepCopy, u, sum_out, nullptr, dv, P->off_vp, P->vw, counters,
+                   tiles_for(&L.mixer_out, 1, kEpiResidF32), layout_for(&L.mixer_out, pout)));
+      BWS_TRY(product(c, &L.mixer_out, 1, kEpiResidF32, pout));
     }
     if (L.kind == BWS_LAYER_MIXER_MLP || L.kind == BWS_LAYER_MLP) {
       const bws_matrix gu[2] = {L.gate, L.up};
-      BWS_TRY(prep(c, kPrepRmsNorm, nullptr, 0, init, H, P->off_xp, P->xw, counters, tiles_for(gu, 2, kEpiSwiGLU)));
+      const GemvParams pgu = product_params(c, gu, 2, kEpiSwiGLU, H, xa, h, L.gate.d_out);
+      BWS_TRY(prep(c, kPrepRmsNorm, nullptr, 0, init, H, P->off_xp, P->xw, counters, tiles_for(gu, 2, kEpiSwiGLU),
+                   layout_for(gu, pgu)));
       init = nullptr;
-      BWS_TRY(product(c, gu, 2, kEpiSwiGLU, H, xa, h, L.gate.d_out));
+      BWS_TRY(product(c, gu, 2, kEpiSwiGLU, pgu));
       const int I = L.down.d_in;
-      BWS_TRY(prep(c, kPrepCopy, h, I, nullptr, I, P->off_hp, P->hw, counters, tiles_for(&L.down, 1, kEpiResidF32)));
-      BWS_TRY(product(c, &L.down, 1, kEpiResidF32, I, xh, r, H));
+      const GemvParams pdn = product_params(c, &L.down, 1, kEpiResidF32, I, xh, r, H);
+      BWS_TRY(prep(c, kPrepCopy, h, I, nullptr, I, P->off_hp, P->hw, counters, tiles_for(&L.down, 1, kEpiResidF32),
+                   layout_for(&L.down, pdn)));
+      BWS_TRY(product(c, &L.down, 1, kEpiResidF32, pdn));
     }
     if (L.kind == BWS_LAYER_MOE) {
       size_t coff;
@@ -187,8 +206,10 @@ int enqueue_step(const bws_stack_plan* P, const uint16_t* x0, float* logits, voi
       if (rc != BWS_OK) return rc;
     }
   }
-  BWS_TRY(prep(c, kPrepRmsNorm, nullptr, 0, init, H, P->off_xp, P->xw, counters, tiles_for(&P->head, 1, kEpiStoreF32)));
-  BWS_TRY(product(c, &P->head, 1, kEpiStoreF32, H, xa, logits, P->head.d_out));
+  const GemvParams ph = product_params(c, &P->head, 1, kEpiStoreF32, H, xa, logits, P->head.d_out);
+  BWS_TRY(prep(c, kPrepRmsNorm, nullptr, 0, init, H, P->off_xp, P->xw, counters, tiles_for(&P->head, 1, kEpiStoreF32),
+               layout_for(&P->head, ph)));
+  BWS_TRY(product(c, &P->head, 1, kEpiStoreF32, ph));
 #undef BWS_TRY
   return BWS_OK;
 }
@@ -273,6 +294,7 @@ int bws_decode_step_plan_create(const bws_stack* S, int N, bws_stack_plan** plan
   P->max_tiles = th > P->max_tiles ? th : P->max_tiles;
   // workspace layout
   size_t o = 0;
+  P->off_status = o; o += 256;
   P->off_r = o; o += align256(sizeof(float) * (size_t)N * H);
   P->xw = gemv_workspace_layout(N, H, 0, 0, 1);
   P->off_xp = o; o += P->xw.off_counters;
