@@ -23,7 +23,8 @@ Page references in docstrings use these short names:
   [LingMoE]   magicnetworld.com, reading of "3 Ways to Boost MoE Inference on
               NVIDIA DGX Spark" (Ling-3.0-flash, sections numbered 一 to 十八)
 
-Parity status of each function is listed in DESIGN.md; none is "unpinned"
-except where its header says so.
+Every function here is pinned by the ``-m "not gpu"`` tests to values that
+do not come from this code (closed forms, brute force, page figures,
+library routines); none is unpinned.
 """
 from . import formats, quant, products, model, accounting, tolerance  # noqa: F401

@@ -47,8 +47,7 @@ def layer_kind_27b(i):
 def mixer_shapes_27b(kind, hidden=HIDDEN_27B):
     """Token-mixer projections (d_out, d_in). The pages give only the
     largest (12288 x 5120) and the stack total (17.83 GB); these shapes are
-    the reading stated in the design doc, chosen so the all-NVFP4 stack totals
-    17.824 GB."""
+    this project's reading, chosen so the all-NVFP4 stack totals 17.824 GB."""
     if kind == "attn":
         return {"in": [(12288, hidden), (1024, hidden), (1024, hidden)],
                 "out": (hidden, 6144)}

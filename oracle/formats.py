@@ -3,7 +3,7 @@
 [Spark27B] § "Fewer bytes per weight: NVFP4": an E2M1 element (1 sign,
 2 exponent, 1 mantissa bit) holds only 0, ±0.5, ±1, ±1.5, ±2, ±3, ±4, ±6;
 block scales are 8-bit E4M3. The exact bit layouts are not printed on the
-pages; the readings used here (stated in the design doc) are the OCP FP8 / MX
+pages; the readings used here are the OCP FP8 / MX
 definitions: E2M1 bias 1 with the e=0 code meaning 0.5*m, E4M3 bias 7 with
 no infinities (S.1111.111 is NaN, max 448), E8M0 = 2^(e-127) with 0xFF NaN.
 

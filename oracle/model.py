@@ -12,7 +12,7 @@ mixer arithmetic, shared-expert width or combine weights; the readings used
 for those (weightless RMSNorm, eps 1e-6; the mixer replaced by taking the
 first d_in(W_o) entries of its input projection; combine weights normalised
 to sum to 1; a shared expert of the routed experts' shape with weight 1) are
-listed in DESIGN.md.
+this project's readings, not the pages'.
 """
 import numpy as np
 

@@ -47,7 +47,8 @@ def nvfp4_quantize(W, s_t=None):
     d_in, one FP32 tensor scale ([Spark27B] § "Fewer bytes per weight:
     NVFP4"; the block scale makes the block's largest magnitude map to 6).
 
-    FP32 sequence per block b (reading stated in the design doc):
+    FP32 sequence per block b (this project's reading; the pages give only
+    the two scale levels and that amax maps to 6):
       sb   = fl32(fl32(amax_b / 6) / s_t)
       code = E4M3_rne_satfinite(sb)
       d_b  = fl32(dec(code) * s_t)
@@ -83,8 +84,8 @@ def floor_log2(a):
 def mxfp4_quantize(W):
     """MXFP4: E2M1 codes with one E8M0 (power-of-two) scale per 32 weights
     along d_in. [LingMoE] §十七 only says small blocks share a scale; the
-    block size, the scale rule and clipping are the OCP MX readings stated in
-    DESIGN.md:
+    block size, the scale rule and clipping are read from the OCP MX
+    specification:
       e    = clamp(floor(log2 amax_b) - 2, -127, 127)   (2 = E2M1's emax)
       code = e + 127
       q_j  = E2M1_rne_satfinite(w_j * 2^-e)             (exact scaling)

@@ -2,10 +2,12 @@
 
 Checked: the slot table (bit-exact: shared expert first, then the distinct
 routed experts in ascending order), the SwiGLU activations of every slot, and
-y. The y bound adds to the product bound the effect of the observed h
-differences (a legitimate one-ulp BF16 rounding difference in h moves y by
-|W_down| * |dh|): |dy| <= sum_s cw_s (1e-4 sum|D h| + sum_j |D_ij| |dh_j|)
-+ 1e-6 sum_s cw_s |ys| + 1/2 ulp(y).
+y. Every expected value and every bound comes from the oracle alone. The y
+bound adds to the product bound the largest legitimate difference in h: h is
+BF16-rounded on both sides from values that may differ by the h bound e_h,
+so |dh| <= e_h + ulp_bf16(|h| + e_h), which moves y by |W_down| |dh|:
+|dy| <= sum_s cw_s (1e-4 sum|D h| + sum_j |D_ij| dh_j) + 1e-6 sum_s cw_s |ys|
++ 1/2 ulp(y).
 """
 import numpy as np
 import pytest
@@ -16,39 +18,46 @@ from tests.gpu_util import device, bws, np_, f64
 import synth
 
 
-def _build(E, hidden, inter, seed, with_shared, oracle_quant=True, layer=0):
-    """Expert weights quantized (oracle on the CPU, or the GPU quantizer for
-    the full-size shape) and the oracle's dequantized view of each expert."""
+def _build(E, hidden, inter, seed, with_shared, gpu_quant=False, used=None, layer=0):
+    """Expert weights for the GPU and the oracle's dequantized view of each
+    expert. The oracle's view always comes from the oracle's own quantizer
+    run on the CPU. The device tensors hold the same oracle codes, or, with
+    gpu_quant (the full-size shape), the GPU quantizer's codes of the same
+    FP32 weights, checked bit-exact against the oracle's for every expert in
+    `used` (only those are read); the other experts stay zero."""
     dev = device()
     n = E + (1 if with_shared else 0)
-    gu_c = torch.empty((n, 2 * inter, hidden // 2), dtype=torch.uint8, device=dev)
-    gu_s = torch.empty((n, 2 * inter, hidden // 32), dtype=torch.uint8, device=dev)
-    dn_c = torch.empty((n, hidden, inter // 2), dtype=torch.uint8, device=dev)
-    dn_s = torch.empty((n, hidden, inter // 32), dtype=torch.uint8, device=dev)
-    for e in range(n):
-        Wgu = synth.weight_fp32((2 * inter, hidden), seed=seed, index=1000 * layer + 2 * e,
-                                device="cpu" if oracle_quant else dev)
-        Wd = synth.weight_fp32((hidden, inter), seed=seed, index=1000 * layer + 2 * e + 1,
-                               device="cpu" if oracle_quant else dev)
-        if oracle_quant:
-            c, s = Q.mxfp4_quantize(Wgu.numpy())
-            gu_c[e].copy_(torch.from_numpy(c)); gu_s[e].copy_(torch.from_numpy(s))
-            c, s = Q.mxfp4_quantize(Wd.numpy())
-            dn_c[e].copy_(torch.from_numpy(c)); dn_s[e].copy_(torch.from_numpy(s))
+    gu_c = torch.zeros((n, 2 * inter, hidden // 2), dtype=torch.uint8, device=dev)
+    gu_s = torch.zeros((n, 2 * inter, hidden // 32), dtype=torch.uint8, device=dev)
+    dn_c = torch.zeros((n, hidden, inter // 2), dtype=torch.uint8, device=dev)
+    dn_s = torch.zeros((n, hidden, inter // 32), dtype=torch.uint8, device=dev)
+    want = range(n) if used is None else sorted(set(E if e < 0 else e for e in used))
+    oracle_codes = {}
+    for e in want:
+        Wgu = synth.weight_fp32((2 * inter, hidden), seed=seed, index=1000 * layer + 2 * e)
+        Wd = synth.weight_fp32((hidden, inter), seed=seed, index=1000 * layer + 2 * e + 1)
+        cg, sg = Q.mxfp4_quantize(Wgu.numpy())
+        cd, sd = Q.mxfp4_quantize(Wd.numpy())
+        oracle_codes[e] = (cg, sg, cd, sd)
+        if gpu_quant:
+            c, s_ = bws().mxfp4_quantize(Wgu.to(dev))
+            assert np.array_equal(np_(c), cg) and np.array_equal(np_(s_), sg)
+            gu_c[e].copy_(c); gu_s[e].copy_(s_)
+            c, s_ = bws().mxfp4_quantize(Wd.to(dev))
+            assert np.array_equal(np_(c), cd) and np.array_equal(np_(s_), sd)
+            dn_c[e].copy_(c); dn_s[e].copy_(s_)
         else:
-            c, s = bws().mxfp4_quantize(Wgu)
-            gu_c[e].copy_(c); gu_s[e].copy_(s)
-            c, s = bws().mxfp4_quantize(Wd)
-            dn_c[e].copy_(c); dn_s[e].copy_(s)
+            gu_c[e].copy_(torch.from_numpy(cg)); gu_s[e].copy_(torch.from_numpy(sg))
+            dn_c[e].copy_(torch.from_numpy(cd)); dn_s[e].copy_(torch.from_numpy(sd))
     shared = (gu_c[E], gu_s[E], dn_c[E], dn_s[E]) if with_shared else None
     layer_w = bws().MoeWeights(gu_c[:E], gu_s[:E], dn_c[:E], dn_s[:E], shared)
     cache = {}
 
     def expert(e):
         if e not in cache:
-            i = E if e < 0 else e
-            gu = P.mxfp4_dequantize(np_(gu_c[i]), np_(gu_s[i]))
-            dn = P.mxfp4_dequantize(np_(dn_c[i]), np_(dn_s[i]))
+            cg, sg, cd, sd = oracle_codes[E if e < 0 else e]
+            gu = P.mxfp4_dequantize(cg, sg)
+            dn = P.mxfp4_dequantize(cd, sd)
             cache[e] = (gu[:inter], gu[inter:], dn)
         return cache[e]
     return layer_w, expert
@@ -85,7 +94,8 @@ def _check_moe(layer_w, expert, ids, rw, x, with_shared, rows=None):
         assert ok, ("h", e, worst, at)
         h_ref = F.round_bf16(h_exact)
         ys, A = P.matvec(wd, h_ref)
-        dh = np.abs(h_gpu - h_ref)
+        e_h = extra + 0.5 * F.bf16_ulp(np.abs(h_exact) + extra)   # the h bound checked above
+        dh = e_h + F.bf16_ulp(np.abs(h_exact) + e_h)
         cw = np.ones(N) if e < 0 else np.array([rwn[t][ids_np[t] == e].sum() for t in range(N)])
         Y += cw[:, None] * ys
         bound += np.abs(cw)[:, None] * (1e-4 * A + dh @ np.abs(wd).T)
@@ -137,21 +147,13 @@ def test_moe_single_expert_reduces_to_mlp():
 @pytest.mark.parametrize("N", [1])
 def test_moe_full_size_ling_shape(N):
     """512 experts, hidden 2560, intermediate 768, top-8 plus a shared expert;
-    codes from the GPU quantizer, checked bit-exact against the oracle for
-    every expert the tokens use; y compared on sampled rows."""
+    device codes from the GPU quantizer (bit-exact against the oracle's for
+    every expert the tokens use); y compared on sampled rows."""
     E, hidden, inter, topk = 512, 2560, 768, 8
-    layer_w, expert = _build(E, hidden, inter, seed=0, with_shared=True, oracle_quant=False)
     ids = synth.expert_ids(N, topk, E, seed=0, layer=2)
     rw = synth.route_weights(N, topk, seed=0, layer=2)
-    used = sorted(set(ids.numpy().reshape(-1).tolist())) + [E]
-    for e in used:   # GPU codes of used experts == oracle codes of the same FP32 weights
-        for k, shape in enumerate([(2 * inter, hidden), (hidden, inter)]):
-            W = synth.weight_fp32(shape, seed=0, index=2 * e + k, device=device())
-            c, s = Q.mxfp4_quantize(np_(W))
-            i = e if e < E else None
-            gc = (layer_w.gu_c, layer_w.dn_c)[k][i] if i is not None else layer_w.shared[2 * k]
-            gs = (layer_w.gu_s, layer_w.dn_s)[k][i] if i is not None else layer_w.shared[2 * k + 1]
-            assert np.array_equal(np_(gc), c) and np.array_equal(np_(gs), s)
+    used = sorted(set(ids.numpy().reshape(-1).tolist())) + [-1]
+    layer_w, expert = _build(E, hidden, inter, seed=0, with_shared=True, gpu_quant=True, used=used)
     x = synth.activation_bf16(N, hidden, seed=0, device=device())
     rows = np.random.default_rng(N).choice(hidden, 48, replace=False)
     _check_moe(layer_w, expert, ids, rw, x, with_shared=True, rows=rows)
