@@ -101,7 +101,7 @@ struct PrepParams {
   int* exp;
   uint32_t* flags;
   uint32_t* hdr;           // [0] = N (status reads), may be null
-  uint32_t* status_clear;  // zeroed by the prep (the status word of the call), may be null
+  uint32_t* status_clear;  // two words zeroed by the prep (the call's status words), may be null
   uint32_t* zero_ptr;      // counters of the next product, zeroed
   int zero_words;
   int interleave;          // 0: linear rows; else the unit size in k (256 NVFP4, 128 FP8) of

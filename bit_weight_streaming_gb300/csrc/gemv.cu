@@ -538,7 +538,7 @@ __global__ void __launch_bounds__(kPrepThreads) prep_kernel(const __grid_constan
   if (slot >= n_slots) return;
   if (blockIdx.x == 0 && threadIdx.x == 0) {
     if (q.hdr != nullptr) q.hdr[0] = (uint32_t)q.N;
-    if (q.status_clear != nullptr) q.status_clear[0] = 0u;
+    if (q.status_clear != nullptr) q.status_clear[0] = q.status_clear[1] = 0u;
   }
   __shared__ float sm[kPrepThreads / 32];
   __shared__ uint32_t sf[kPrepThreads / 32];

@@ -28,6 +28,7 @@
 
 #include "bws_common.cuh"
 #include "bws_internal.h"
+#include "stream_tile.cuh"
 
 namespace bws {
 
@@ -36,11 +37,6 @@ namespace {
 constexpr int kConsumerWarps = 8;
 constexpr int kThreadsTma = (kConsumerWarps + 1) * 32;
 constexpr int kMaxStages = 16;
-constexpr int kBoxRows = 32;
-constexpr int kBoxes = 4;                          // boxes per unit
-constexpr int kBoxBytes = kBoxRows * 128;          // one code box
-constexpr int kCodeBytes = kBoxes * kBoxBytes;     // code bytes of a unit
-constexpr int kScaleBoxBytes = kBoxRows * 16;      // one NVFP4 scale box
 constexpr int kSmemBudget = 100 * 1024;            // stages per CTA: two CTAs share an SM
 constexpr uint32_t kMaxPolls = 1u << 24;           // bounded waits (seconds)
 constexpr uint32_t kStatusTimeout = 0x100u;
@@ -100,11 +96,6 @@ BWS_DEV void box_of(const TmaParams& p, int tile, int b, int& m, int& row) {
 BWS_DEV long long owner(long long u, long long U, long long G) { return ((u + 1) * G - 1) / U; }
 BWS_DEV long long begin_of(long long c, long long U, long long G) { return c * U / G; }
 
-BWS_DEV float silu_mul_t(float g, float u) {
-  const float sg = __fdiv_rn(g, __fadd_rn(1.0f, expf(-g)));
-  return __fmul_rn(sg, u);
-}
-
 // Store v (raw sums of sub-tile s of box b; register i = row g + 8*(i>>1),
 // token 2t + (i&1)). SwiGLU: b is a gate box and vu the matching up sums.
 template <int FMT, int EPI>
@@ -143,48 +134,6 @@ BWS_DEV void store_sub(const TmaParams& p, int tile, int b, int s, int g, int t,
         reinterpret_cast<float*>(p.out)[o] = val;
       else
         reinterpret_cast<float*>(p.out)[o] = __fadd_rn(reinterpret_cast<float*>(p.out)[o], val);
-    }
-  }
-}
-
-// Products of one 16-row sub-tile with one unit's activations: w0 / w1 are
-// the lane's chunk words of rows g / g+8, sc0 / sc1 their two block scales
-// (NVFP4), xh the hi-band pieces, xl the lo band (when lo).
-template <int FMT, bool LO>
-BWS_DEV void sub_mma(float (&acc)[2][4], float (&accl)[4], const uint32_t (&w0)[4], const uint32_t (&w1)[4],
-                     uint32_t sc0, uint32_t sc1, const uint4 (&xh)[FMT == kFmtFP8 ? 2 : 4],
-                     const uint4 (&xl)[FMT == kFmtFP8 ? 2 : 4]) {
-  if constexpr (FMT == kFmtFP8) {
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      uint32_t a0, a2, a1, a3;
-      e4m3x4_to_f16x2x2(w0[j], a0, a2);
-      e4m3x4_to_f16x2x2(w1[j], a1, a3);
-      const uint4& xq = xh[j >> 1];
-      mma_f16_16816(acc[j & 1], a0, a1, a2, a3, (j & 1) ? xq.z : xq.x, (j & 1) ? xq.w : xq.y);
-      if (LO) {
-        const uint4& lq = xl[j >> 1];
-        mma_f16_16816(accl, a0, a1, a2, a3, (j & 1) ? lq.z : lq.x, (j & 1) ? lq.w : lq.y);
-      }
-    }
-  } else {
-    const uint32_t f0 = e4m3x2_to_f16x2(sc0), f1 = e4m3x2_to_f16x2(sc1);
-    const uint32_t m0[2] = {bcast_lo(f0), bcast_hi(f0)};
-    const uint32_t m1[2] = {bcast_lo(f1), bcast_hi(f1)};
-#pragma unroll
-    for (int w = 0; w < 4; ++w) {
-      uint32_t p0, p1, p2, p3, q0, q1, q2, q3;
-      e2m1x8_to_f16x2x4(w0[w], p0, p1, p2, p3);
-      e2m1x8_to_f16x2x4(w1[w], q0, q1, q2, q3);
-      const uint32_t sa = m0[w >> 1], sb = m1[w >> 1];
-      p0 = hmul2_u32(p0, sa); p1 = hmul2_u32(p1, sa); p2 = hmul2_u32(p2, sa); p3 = hmul2_u32(p3, sa);
-      q0 = hmul2_u32(q0, sb); q1 = hmul2_u32(q1, sb); q2 = hmul2_u32(q2, sb); q3 = hmul2_u32(q3, sb);
-      mma_f16_16816(acc[0], p0, q0, p1, q1, xh[w].x, xh[w].y);
-      mma_f16_16816(acc[1], p2, q2, p3, q3, xh[w].z, xh[w].w);
-      if (LO) {
-        mma_f16_16816(accl, p0, q0, p1, q1, xl[w].x, xl[w].y);
-        mma_f16_16816(accl, p2, q2, p3, q3, xl[w].z, xl[w].w);
-      }
     }
   }
 }
@@ -455,36 +404,6 @@ __global__ void __launch_bounds__(kThreadsTma, 2) gemv_tma_kernel(const __grid_c
     consume<FMT, EPI, false>(p, T, stage0, u0, u1, warp, lane, p.x.lo);
 }
 
-typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
-                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
-                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-EncodeTiledFn encode_fn() {
-  static EncodeTiledFn fn = nullptr;
-  if (fn == nullptr) {
-    void* p = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
-            cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<EncodeTiledFn>(p);
-  }
-  return fn;
-}
-
-bool encode_2d(CUtensorMap* m, const void* base, uint64_t inner_bytes, uint64_t rows, uint32_t box_inner,
-               uint32_t box_rows, bool swizzle) {
-  EncodeTiledFn fn = encode_fn();
-  if (fn == nullptr) return false;
-  const cuuint64_t dims[2] = {inner_bytes, rows};
-  const cuuint64_t strides[1] = {inner_bytes};
-  const cuuint32_t box[2] = {box_inner, box_rows};
-  const cuuint32_t estr[2] = {1, 1};
-  return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, estr,
-            CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
-            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
 template <int FMT, int EPI>
 cudaError_t launch_tma_one(const TmaParams& p, cudaStream_t st, bool pdl) {
   const int smem = p.n_stages * p.stage_bytes + (int)sizeof(Tail) + 1024;
@@ -511,7 +430,7 @@ cudaError_t launch_tma_one(const TmaParams& p, cudaStream_t st, bool pdl) {
 }  // namespace
 
 bool gemv_tma_eligible(int fmt, const GemvParams& p) {
-  if (p.slots.n_slots != nullptr || encode_fn() == nullptr) return false;
+  if (p.slots.n_slots != nullptr || !tensor_maps_available()) return false;
   if (fmt == kFmtNVFP4) {
     if (p.d_in % 256 != 0) return false;
   } else if (fmt == kFmtFP8) {

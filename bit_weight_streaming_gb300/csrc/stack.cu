@@ -4,12 +4,14 @@
 // before it finishes), and recorded once as a CUDA graph.
 #include <cuda_runtime.h>
 
+#include <cstdlib>
 #include <new>
 #include <vector>
 
 #include "../../include/bws.h"
 #include "bws_abi_util.h"
 #include "bws_internal.h"
+#include "step.h"
 
 using namespace bws;
 
@@ -23,6 +25,8 @@ struct bws_stack_plan {
   GemvWorkspace xw, vw, hw;    // prep-block offsets (relative to their block)
   int max_u, max_dv, max_inter, max_tiles;
   int kernels;
+  // dense stacks: the persistent step kernel's program (nullptr: the kernel chain)
+  StepProgram* step;
   // recorded graph
   cudaGraphExec_t exec;
   const void* key[4];
@@ -96,7 +100,7 @@ cudaError_t prep(const Ctx& c, int mode, const uint16_t* x, int ld, const uint16
   q.exp = const_cast<int*>(xp.exp);
   q.flags = const_cast<uint32_t*>(xp.flags);
   q.hdr = nullptr;
-  q.status_clear = x0 != nullptr ? reinterpret_cast<uint32_t*>(c.w + c.P->off_status) : nullptr;
+  q.status_clear = x0 != nullptr ? reinterpret_cast<uint32_t*>(c.w + c.P->off_status) : nullptr;   // words 0, 1
   q.zero_ptr = zero_ptr;
   q.zero_words = zero_words;
   q.interleave = interleave;
@@ -144,11 +148,13 @@ int layout_for(const bws_matrix* mats, const GemvParams& p) {
 }
 
 cudaError_t product(const Ctx& c, const bws_matrix* mats, int nm, int epi, const GemvParams& p) {
-  return launch_product(fmt_of(mats[0]), epi, p, reinterpret_cast<uint32_t*>(c.w + c.P->off_status), c.st, true);
+  return launch_product(fmt_of(mats[0]), epi, p, reinterpret_cast<uint32_t*>(c.w + c.P->off_status) + 1, c.st,
+                        true);
 }
 
 int enqueue_step(const bws_stack_plan* P, const uint16_t* x0, float* logits, void* ws, cudaStream_t st) {
   const char* name = "bws_decode_step_stream";
+  if (P->step) return cuda_status(step_program_enqueue(P->step, x0, logits, ws, st), name);
   Ctx c{P, static_cast<char*>(ws), st};
   float* r = reinterpret_cast<float*>(c.w + P->off_r);
   uint32_t* counters = reinterpret_cast<uint32_t*>(c.w + P->off_counters);
@@ -308,6 +314,17 @@ int bws_decode_step_plan_create(const bws_stack* S, int N, bws_stack_plan** plan
   P->off_counters = o; o += align256(sizeof(uint32_t) * (size_t)P->max_tiles);
   P->off_partials = o; o += align256(sizeof(float) * kSlotFloats * ((size_t)P->max_tiles + gemv_max_warps()));
   P->total = o;
+  // A dense stack can run as one persistent kernel. It is opt-in
+  // (BWS_STEP_KERNEL=1 at plan creation) until it outruns the kernel chain.
+  const char* opt = getenv("BWS_STEP_KERNEL");
+  P->step = (opt && opt[0] == '1')
+                ? step_program_create(N, H, P->eps, P->layers.data(), (int)P->layers.size(), P->head)
+                : nullptr;
+  if (P->step) {
+    const size_t sb = step_program_workspace(P->step);
+    P->total = sb > P->total ? sb : P->total;
+    P->kernels = 2;
+  }
   P->exec = nullptr;
   for (auto& k : P->key) k = nullptr;
   *plan = P;
@@ -318,6 +335,7 @@ int bws_decode_step_plan_create(const bws_stack* S, int N, bws_stack_plan** plan
 void bws_decode_step_plan_destroy(bws_stack_plan* plan) {
   if (!plan) return;
   if (plan->exec) cudaGraphExecDestroy(plan->exec);
+  step_program_destroy(plan->step);
   delete plan;
 }
 

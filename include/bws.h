@@ -62,8 +62,10 @@ enum bws_format {
 /* Bits of the device status word (bws_status_word). */
 enum bws_status_bits {
   BWS_STATUS_X_TWO_BANDS = 1u,  /* an activation needed the second f16 band  */
-  BWS_STATUS_X_FLUSHED = 2u     /* an activation below 2^-57 of its token's
+  BWS_STATUS_X_FLUSHED = 2u,    /* an activation below 2^-57 of its token's
                                    largest magnitude was treated as zero     */
+  BWS_STATUS_WAIT_TIMEOUT = 0x100u /* a bounded device wait ran out: the
+                                   results of that call are not valid        */
 };
 
 /* Library version (major*10000 + minor*100 + patch). */
@@ -263,7 +265,17 @@ typedef struct bws_stack {
 } bws_stack;
 
 /* A validated stack with its launch sequence. Create once, run many times;
- * the plan copies the descriptors and owns no device memory. */
+ * the plan copies the descriptors. A dense stack (layers MIXER_MLP or MLP,
+ * every layer matrix NVFP4 with d_in % 256 == 0, an NVFP4 or FP8 output layer
+ * with hidden % 128 == 0, 16-byte aligned tensors) can run as one persistent
+ * cooperative kernel after a small init kernel (opt-in for now: set the
+ * environment variable BWS_STEP_KERNEL=1 before creating the plan); for it
+ * the plan builds, on
+ * the device current at creation, a table of TMA descriptors in a small
+ * device allocation it owns (about 600 B per matrix) and frees on destroy.
+ * Any other stack runs as a chain of per-product kernels and the plan owns no
+ * device memory. Create, run and destroy the plan with the same device
+ * current. */
 typedef struct bws_stack_plan bws_stack_plan;
 
 int bws_decode_step_plan_create(const bws_stack* S, int N, bws_stack_plan** plan);
@@ -285,7 +297,7 @@ size_t bws_decode_step_workspace_size(const bws_stack_plan* plan);
 int bws_decode_step_stream(bws_stack_plan* plan, const uint16_t* x0, float* logits,
                            void* workspace, size_t workspace_bytes, void* stream);
 
-/* Number of kernels one decode step launches. */
+/* Number of kernels one decode step launches (2 for the persistent kernel). */
 int bws_decode_step_kernel_count(const bws_stack_plan* plan);
 
 /* ------------------------------------------------------------------------ */

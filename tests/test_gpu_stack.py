@@ -22,6 +22,26 @@ def _dense_small(N, n_layers=4):
                        gdn=(640, 192), quant=oracle_quantizers(device()), device=device())
 
 
+def _dense_persistent(N, n_layers=4, inter=1024):
+    """Shapes the persistent step kernel takes (every NVFP4 d_in % 256 == 0),
+    with that kernel enabled: one launch runs the whole step after the init
+    kernel."""
+    import os
+    from bit_weight_streaming_gb300 import workloads as W
+    bws()
+    os.environ["BWS_STEP_KERNEL"] = "1"
+    try:
+        return _dense_persistent_build(N, n_layers, inter, W)
+    finally:
+        del os.environ["BWS_STEP_KERNEL"]
+
+
+def _dense_persistent_build(N, n_layers, inter, W):
+    return W.dense_27b(N, seed=6, n_layers=n_layers, hidden=512, inter=inter, vocab=1000,
+                       attn=(768, 256, 256, 512), gdn=(1280, 512), quant=oracle_quantizers(device()),
+                       device=device())
+
+
 def _check(stack, N, seed):
     x0 = synth.activation_bf16(N, stack.hidden, seed=seed, device=device())
     logits = stack.step(x0)
@@ -70,3 +90,32 @@ def test_moe_stack_parity():
         stack = bws().stack.DecodeStack(256, layers, head, N, device=device())
         assert stack.kernel_count == 4 + 2 * 6 + 2
         _check(stack, N, seed=10 + N)
+
+
+@pytest.mark.parametrize("N", [1, 3, 8])
+def test_dense_stack_persistent_kernel(N):
+    stack = _dense_persistent(N)
+    assert stack.kernel_count == 2
+    _check(stack, N, seed=20 + N)
+
+
+def test_dense_stack_persistent_kernel_many_slabs():
+    """N = 8 with a 3072-wide MLP: the down projection's activations do not
+    fit one shared-memory slab, so its k range is cut into three slabs whose
+    partial sums meet in the tile fix-up."""
+    stack = _dense_persistent(8, n_layers=2, inter=3072)
+    assert stack.kernel_count == 2
+    _check(stack, 8, seed=31)
+
+
+def test_dense_stack_persistent_kernel_replay_is_deterministic():
+    stack = _dense_persistent(2, n_layers=2)
+    x0 = synth.activation_bf16(2, 512, seed=4, device=device())
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        a = stack.step(x0).clone()
+        b = stack.step(x0).clone()
+    s.synchronize()
+    d = stack.step(x0)
+    torch.cuda.synchronize()
+    assert torch.equal(a, b) and torch.equal(a, d)
