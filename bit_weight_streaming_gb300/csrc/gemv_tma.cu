@@ -24,6 +24,7 @@
 // sub-tile are added through shared memory at the end of each tile piece.
 #include <cuda.h>
 
+#include <cstddef>
 #include <cstring>
 
 #include "bws_common.cuh"
@@ -69,14 +70,17 @@ struct TmaParams {
   int n_stages, stage_bytes, x_off, x_blk, x_bytes;
 };
 
-// Shared memory after the stages.
+// Shared memory after the stages (which end on a 1024-byte boundary).
 struct Tail {
   float4 red[kBoxes][2][32];   // half-pair reduction (box, sub-tile, lane)
   float4 swi[2][2][32];        // SwiGLU: up sums handed to the gate warps
+  uint4 zero_x[33];             // zero activation pieces (one-token block-diagonal operand),
+                                // used from element 1 on (see consume)
   uint64_t full[kMaxStages];
   uint64_t empty[kMaxStages];
   uint32_t flag;
 };
+static_assert(offsetof(Tail, zero_x) % 128 == 0, "zero pieces must start on a 128-byte boundary");
 
 // Matrix and first row of box b of a tile.
 template <int EPI>
@@ -140,7 +144,7 @@ BWS_DEV void store_sub(const TmaParams& p, int tile, int b, int s, int g, int t,
 
 // The consumer warps' loop over units u0..u1 (LO: the two-band activation
 // path, taken when some token has elements below the hi band's range).
-template <int FMT, int EPI, bool LO>
+template <int FMT, int EPI, bool LO, bool N1>
 BWS_DEV void consume(const TmaParams& p, Tail& T, uint32_t stage0, long long u0, long long u1, int warp, int lane,
                      const uint16_t* xrow_l) {
   const long long U = p.n_units, G = p.n_ctas;
@@ -158,7 +162,14 @@ BWS_DEV void consume(const TmaParams& p, Tail& T, uint32_t stage0, long long u0,
   const int xg = g < p.N ? g : 0;
   const uint32_t xoff = (uint32_t)(p.x_off + xg * p.x_blk + c * 16);
   xrow_l += (size_t)xg * p.d_in_pad;
-  float acc[2][2][4] = {}, accl[2][4] = {};
+  // one token: lanes g == 2t feed their chunk's first block, g == 2t + 1 its
+  // second, the rest read zeros (see sub_mma_n1)
+  const bool m01 = g == 2 * t, m23 = g == 2 * t + 1;
+  // the zero pieces sit 16 bytes past a 128-byte boundary while the stages'
+  // activation blocks sit on one, so a phase's zero reads and real reads fall
+  // in different banks
+  const uint32_t zaddr = smem_u32(&T.zero_x[1]) + c * 16;
+  float acc[2][2][4] = {}, accl[2][4] = {};   // N1: acc[st][0] holds y, accl[st] the lo band's
   uint4 xh[kXv], xl[kXv];
   bool dead = false;   // a wait ran out: keep the control flow (barriers), skip the work
   int tile = (int)(u0 / p.nks), ks = (int)(u0 % p.nks);
@@ -168,8 +179,10 @@ BWS_DEV void consume(const TmaParams& p, Tail& T, uint32_t stage0, long long u0,
   for (long long u = u0; u < u1; ++u) {
     if (LO) {   // two-band path: the lo band comes from global memory
 #pragma unroll
-      for (int q = 0; q < kXv; ++q)
+      for (int q = 0; q < kXv; ++q) {
         xl[q] = ld_act_v4(xrow_l + (size_t)ks * kUnitK + q * 64 + c * 8);
+        if (N1 && !(q < 2 ? m01 : m23)) xl[q] = make_uint4(0, 0, 0, 0);
+      }
     }
     if (!dead && !mbar_wait_bounded(smem_u32(&T.full[s]), ph, kMaxPolls)) {
       if (lane == 0) atomicOr(p.status, kStatusTimeout);
@@ -185,8 +198,17 @@ BWS_DEV void consume(const TmaParams& p, Tail& T, uint32_t stage0, long long u0,
 #pragma unroll
         for (int j = 0; j < 4; ++j) sc[j] = lds_u16(base + soff + j * 128);
       }
+      if constexpr (N1) {
+        const uint32_t xb = base + xoff;
+        const uint32_t a01 = m01 ? xb : zaddr, a23 = m23 ? xb : zaddr;
+        xh[0] = lds_v4(a01);
+        xh[1] = lds_v4(a01 + 128);
+        xh[2] = lds_v4(a23 + 256);
+        xh[3] = lds_v4(a23 + 384);
+      } else {
 #pragma unroll
-      for (int q = 0; q < kXv; ++q) xh[q] = lds_v4(base + xoff + q * 128);
+        for (int q = 0; q < kXv; ++q) xh[q] = lds_v4(base + xoff + q * 128);
+      }
     } else {
 #pragma unroll
       for (int j = 0; j < 4; ++j) { cw[j] = make_uint4(0, 0, 0, 0); sc[j] = 0u; }
@@ -201,7 +223,10 @@ BWS_DEV void consume(const TmaParams& p, Tail& T, uint32_t stage0, long long u0,
     for (int st = 0; st < 2; ++st) {
       const uint32_t w0[4] = {cw[2 * st].x, cw[2 * st].y, cw[2 * st].z, cw[2 * st].w};
       const uint32_t w1[4] = {cw[2 * st + 1].x, cw[2 * st + 1].y, cw[2 * st + 1].z, cw[2 * st + 1].w};
-      sub_mma<FMT, LO>(acc[st], accl[st], w0, w1, sc[2 * st], sc[2 * st + 1], xh, xl);
+      if constexpr (N1)
+        sub_mma_n1<LO>(acc[st][0], accl[st], w0, w1, sc[2 * st], sc[2 * st + 1], xh, xl);
+      else
+        sub_mma<FMT, LO>(acc[st], accl[st], w0, w1, sc[2 * st], sc[2 * st + 1], xh, xl);
     }
     // ---- end of a tile piece ----
     const bool last_of_tile = ks == p.nks - 1;
@@ -209,13 +234,32 @@ BWS_DEV void consume(const TmaParams& p, Tail& T, uint32_t stage0, long long u0,
     if (++ks == p.nks) { ks = 0; ++tile; }
     if (!last_of_tile && u + 1 < u1) continue;
     float v[2][4];
+    if constexpr (N1) {
+      // rows g and g + 8: this lane's two blocks, then the four chunks of the half
 #pragma unroll
-    for (int st = 0; st < 2; ++st) {
+      for (int st = 0; st < 2; ++st) {
+        float yg = __fadd_rn(acc[st][0][0], acc[st][0][1]), y8 = __fadd_rn(acc[st][0][2], acc[st][0][3]);
+        if (LO) {
+          yg = __fmaf_rn(__fadd_rn(accl[st][0], accl[st][1]), 0x1p-29f, yg);
+          y8 = __fmaf_rn(__fadd_rn(accl[st][2], accl[st][3]), 0x1p-29f, y8);
+        }
+        yg += __shfl_xor_sync(0xffffffffu, yg, 1);
+        y8 += __shfl_xor_sync(0xffffffffu, y8, 1);
+        yg += __shfl_xor_sync(0xffffffffu, yg, 2);
+        y8 += __shfl_xor_sync(0xffffffffu, y8, 2);
+        v[st][0] = yg; v[st][1] = 0.f; v[st][2] = y8; v[st][3] = 0.f;
 #pragma unroll
-      for (int r = 0; r < 4; ++r) {
-        const float a = __fadd_rn(acc[st][0][r], acc[st][1][r]);
-        v[st][r] = LO ? __fmaf_rn(accl[st][r], 0x1p-29f, a) : a;
-        acc[st][0][r] = acc[st][1][r] = accl[st][r] = 0.f;
+        for (int r = 0; r < 4; ++r) acc[st][0][r] = accl[st][r] = 0.f;
+      }
+    } else {
+#pragma unroll
+      for (int st = 0; st < 2; ++st) {
+#pragma unroll
+        for (int r = 0; r < 4; ++r) {
+          const float a = __fadd_rn(acc[st][0][r], acc[st][1][r]);
+          v[st][r] = LO ? __fmaf_rn(accl[st][r], 0x1p-29f, a) : a;
+          acc[st][0][r] = acc[st][1][r] = accl[st][r] = 0.f;
+        }
       }
     }
     // add the two halves: warps 4..7 hand their sums to warps 0..3
@@ -295,13 +339,13 @@ BWS_DEV void consume(const TmaParams& p, Tail& T, uint32_t stage0, long long u0,
 
 // The rare two-band loop, out of line so that its registers do not weigh on
 // the main loop.
-template <int FMT, int EPI>
+template <int FMT, int EPI, bool N1>
 __device__ __noinline__ void consume_lo(const TmaParams& p, Tail& T, uint32_t stage0, long long u0, long long u1,
                                         int warp, int lane, const uint16_t* xrow_l) {
-  consume<FMT, EPI, true>(p, T, stage0, u0, u1, warp, lane, xrow_l);
+  consume<FMT, EPI, true, N1>(p, T, stage0, u0, u1, warp, lane, xrow_l);
 }
 
-template <int FMT, int EPI>
+template <int FMT, int EPI, bool N1>
 __global__ void __launch_bounds__(kThreadsTma, 2) gemv_tma_kernel(const __grid_constant__ TmaParams p) {
   extern __shared__ __align__(16) uint8_t smem_raw[];
   // 128-byte swizzled TMA boxes need 1024-byte aligned destinations
@@ -322,6 +366,7 @@ __global__ void __launch_bounds__(kThreadsTma, 2) gemv_tma_kernel(const __grid_c
     T.flag = 0u;
     mbar_fence_init();
   }
+  for (int i = threadIdx.x; i < 33; i += blockDim.x) T.zero_x[i] = make_uint4(0, 0, 0, 0);
   __syncthreads();
   constexpr int kUnitK = FMT == kFmtFP8 ? 128 : 256;
 
@@ -399,17 +444,17 @@ __global__ void __launch_bounds__(kThreadsTma, 2) gemv_tma_kernel(const __grid_c
   uint32_t fl = 0u;
   for (int tok = 0; tok < p.N; ++tok) fl |= __ldg(p.x.flags + tok);
   if (fl & 1u)
-    consume_lo<FMT, EPI>(p, T, stage0, u0, u1, warp, lane, p.x.lo);
+    consume_lo<FMT, EPI, N1>(p, T, stage0, u0, u1, warp, lane, p.x.lo);
   else
-    consume<FMT, EPI, false>(p, T, stage0, u0, u1, warp, lane, p.x.lo);
+    consume<FMT, EPI, false, N1>(p, T, stage0, u0, u1, warp, lane, p.x.lo);
 }
 
-template <int FMT, int EPI>
+template <int FMT, int EPI, bool N1>
 cudaError_t launch_tma_one(const TmaParams& p, cudaStream_t st, bool pdl) {
   const int smem = p.n_stages * p.stage_bytes + (int)sizeof(Tail) + 1024;
   static bool attr = false;
   if (!attr) {
-    cudaError_t e = cudaFuncSetAttribute(gemv_tma_kernel<FMT, EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    cudaError_t e = cudaFuncSetAttribute(gemv_tma_kernel<FMT, EPI, N1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          kSmemBudget + (int)sizeof(Tail) + 1024);
     if (e != cudaSuccess) return e;
     attr = true;
@@ -424,7 +469,7 @@ cudaError_t launch_tma_one(const TmaParams& p, cudaStream_t st, bool pdl) {
   a[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = a;
   cfg.numAttrs = pdl ? 1 : 0;
-  return cudaLaunchKernelEx(&cfg, gemv_tma_kernel<FMT, EPI>, p);
+  return cudaLaunchKernelEx(&cfg, gemv_tma_kernel<FMT, EPI, N1>, p);
 }
 
 }  // namespace
@@ -503,8 +548,11 @@ cudaError_t launch_gemv_tma(int fmt, int epi, const GemvParams& g, uint32_t* sta
   if (p.n_stages > kMaxStages) p.n_stages = kMaxStages;
   if (p.n_stages < 2) return cudaErrorInvalidValue;
   if (p.n_ctas <= 0) return cudaSuccess;
-#define BWS_CASE(F, E) \
-  if (fmt == F && epi == E) return launch_tma_one<F, E>(p, st, pdl);
+  // one NVFP4 token: the block-diagonal operand (block scales on the accumulators)
+  const bool n1 = fmt == kFmtNVFP4 && p.N == 1;
+#define BWS_CASE(F, E)                                                              \
+  if (fmt == F && epi == E)                                                         \
+    return n1 ? launch_tma_one<F, E, (F == kFmtNVFP4)>(p, st, pdl) : launch_tma_one<F, E, false>(p, st, pdl);
   BWS_CASE(kFmtNVFP4, kEpiStoreBF16)
   BWS_CASE(kFmtNVFP4, kEpiResidF32)
   BWS_CASE(kFmtNVFP4, kEpiSwiGLU)

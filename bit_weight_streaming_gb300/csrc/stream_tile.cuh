@@ -69,6 +69,50 @@ BWS_DEV void sub_mma(float (&acc)[2][4], float (&accl)[4], const uint32_t (&w0)[
 
 // True if the driver's tensor-map encoder can be reached.
 bool tensor_maps_available();
+// One token, NVFP4: the products of one 16-row sub-tile with one unit, block
+// scales applied to the accumulators. The activation operand is block
+// diagonal: lanes with g == 2t hold their chunk's first-block activations
+// (words 0, 1) and lanes with g == 2t + 1 its second-block ones (words 2, 3),
+// every other lane zeros, so MMA column 2t' + e collects exactly block e of
+// lane t''s chunk. Lane (g, t) then holds, for rows g and g + 8, the raw sums
+// of its own chunk's two blocks and adds them, times their E4M3 scales, to y
+// (y[0], y[1]: row g blocks 0, 1; y[2], y[3]: row g + 8).
+template <bool LO>
+BWS_DEV void sub_mma_n1(float (&y)[4], float (&yl)[4], const uint32_t (&w0)[4], const uint32_t (&w1)[4],
+                        uint32_t sc0, uint32_t sc1, const uint4 (&xh)[4], const uint4 (&xl)[4]) {
+  float da[4] = {0.f, 0.f, 0.f, 0.f}, db[4] = {0.f, 0.f, 0.f, 0.f};
+  float la[4] = {0.f, 0.f, 0.f, 0.f}, lb[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+  for (int w = 0; w < 4; ++w) {
+    uint32_t p0, p1, p2, p3, q0, q1, q2, q3;
+    e2m1x8_to_f16x2x4(w0[w], p0, p1, p2, p3);
+    e2m1x8_to_f16x2x4(w1[w], q0, q1, q2, q3);
+    float (&d)[4] = w < 2 ? da : db;
+    mma_f16_16816(d, p0, q0, p1, q1, xh[w].x, xh[w].y);
+    mma_f16_16816(d, p2, q2, p3, q3, xh[w].z, xh[w].w);
+    if (LO) {
+      float (&l)[4] = w < 2 ? la : lb;
+      mma_f16_16816(l, p0, q0, p1, q1, xl[w].x, xl[w].y);
+      mma_f16_16816(l, p2, q2, p3, q3, xl[w].z, xl[w].w);
+    }
+  }
+  const uint32_t f0 = e4m3x2_to_f16x2(sc0), f1 = e4m3x2_to_f16x2(sc1);
+  const float s[4] = {__half2float(__ushort_as_half((unsigned short)(f0 & 0xFFFF))),
+                      __half2float(__ushort_as_half((unsigned short)(f0 >> 16))),
+                      __half2float(__ushort_as_half((unsigned short)(f1 & 0xFFFF))),
+                      __half2float(__ushort_as_half((unsigned short)(f1 >> 16)))};
+  y[0] = __fmaf_rn(s[0], da[0], y[0]);
+  y[1] = __fmaf_rn(s[1], db[1], y[1]);
+  y[2] = __fmaf_rn(s[2], da[2], y[2]);
+  y[3] = __fmaf_rn(s[3], db[3], y[3]);
+  if (LO) {
+    yl[0] = __fmaf_rn(s[0], la[0], yl[0]);
+    yl[1] = __fmaf_rn(s[1], lb[1], yl[1]);
+    yl[2] = __fmaf_rn(s[2], la[2], yl[2]);
+    yl[3] = __fmaf_rn(s[3], lb[3], yl[3]);
+  }
+}
+
 // Encodes a 2D u8 tensor map [rows][inner_bytes] with the given box (128-byte
 // swizzle or none). False if the driver entry point is missing or refuses.
 bool encode_2d(CUtensorMap* m, const void* base, uint64_t inner_bytes, uint64_t rows, uint32_t box_inner,
