@@ -100,6 +100,7 @@ struct StepTail {
   uint64_t empty[kStages];
   float inv_rms[kMaxTokens];
   int E[kMaxTokens];
+  float hs[kMaxTokens];        // 2^(14 - E) when a normal float, else 0
   uint32_t maxbits[kMaxTokens];
   float2 stat[4][kMaxTokens];
   uint32_t xflags;
@@ -158,6 +159,11 @@ BWS_DEV uint32_t ld_cg_u32(const uint32_t* p) {
   return v;
 }
 BWS_DEV float ld_cg_f32(const float* p) { return __uint_as_float(ld_cg_u32(reinterpret_cast<const uint32_t*>(p))); }
+BWS_DEV uint2 ld_cg_u2(const void* p) {
+  uint2 v;
+  asm volatile("ld.global.cg.v2.u32 {%0,%1}, [%2];" : "=r"(v.x), "=r"(v.y) : "l"(p));
+  return v;
+}
 BWS_DEV uint4 ld_cg_u4(const void* p) {
   uint4 v;
   asm volatile("ld.global.cg.v4.u32 {%0,%1,%2,%3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "l"(p));
@@ -224,6 +230,28 @@ BWS_DEV uint4 piece_hi(const uint32_t (&w)[4], int E, uint32_t& flags) {
   }
   return make_uint4(h[0], h[1], h[2], h[3]);
 }
+// The same with the scale 2^(14 - E) given as a float (14 - E in the normal
+// range): one multiply per element, exact (a power of two; results below
+// 2^-14 leave the hi band whatever their rounding).
+BWS_DEV uint4 piece_hi_fast(const uint32_t (&w)[4], float hs, int E, uint32_t& flags) {
+  uint32_t h[4];
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const float f0 = __uint_as_float(w[j] << 16), f1 = __uint_as_float(w[j] & 0xFFFF0000u);
+    float a0 = __fmul_rn(f0, hs), a1 = __fmul_rn(f1, hs);
+    if (fabsf(a0) < 0x1p-14f) {
+      if (f0 != 0.0f) flags |= fabsf(ldexp_exact(f0, 43 - E)) >= 0x1p-14f ? 1u : 2u;
+      a0 = 0.0f;
+    }
+    if (fabsf(a1) < 0x1p-14f) {
+      if (f1 != 0.0f) flags |= fabsf(ldexp_exact(f1, 43 - E)) >= 0x1p-14f ? 1u : 2u;
+      a1 = 0.0f;
+    }
+    const __half2 v = __floats2half2_rn(a0, a1);
+    h[j] = *reinterpret_cast<const uint32_t*>(&v);
+  }
+  return make_uint4(h[0], h[1], h[2], h[3]);
+}
 BWS_DEV uint4 piece_lo(const uint32_t (&w)[4], int E) {
   uint32_t l[4];
 #pragma unroll
@@ -274,12 +302,22 @@ __device__ __noinline__ uint32_t build_slab(const StepParams& p, const StepProdu
     }
   }
   if (warp < N) {
-    const float2* st = reinterpret_cast<const float2*>(p.ws + P.stats_off);
+    // the tiles' statistics of this token, eight per lane in flight at once
+    const float2* st = reinterpret_cast<const float2*>(p.ws + P.stats_off) + warp;
+    const int tiles = P.stats_tiles;
     float sq = 0.0f, mx = 0.0f;
-    for (int t = lane; t < P.stats_tiles; t += 32) {
-      const float* f = reinterpret_cast<const float*>(st + (size_t)t * N + warp);
-      sq = __fadd_rn(sq, ld_cg_f32(f));
-      mx = fmaxf(mx, ld_cg_f32(f + 1));
+    for (int t0 = lane; t0 < tiles; t0 += 8 * 32) {
+      uint2 v[8];
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        const int t = t0 + k * 32;
+        v[k] = t < tiles ? ld_cg_u2(st + (size_t)t * N) : make_uint2(0u, 0u);
+      }
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        sq = __fadd_rn(sq, __uint_as_float(v[k].x));
+        mx = fmaxf(mx, __uint_as_float(v[k].y));
+      }
     }
     sq = warp_sum(sq);
     mx = warp_max(mx);
@@ -290,7 +328,9 @@ __device__ __noinline__ uint32_t build_slab(const StepParams& p, const StepProdu
         amax = __bfloat162float(__float2bfloat16_rn(__fmul_rn(mx, inv)));
       }
       T.inv_rms[warp] = inv;
-      T.E[warp] = amax > 0.0f ? floor_log2_abs(amax) : 0;
+      const int E = amax > 0.0f ? floor_log2_abs(amax) : 0;
+      T.E[warp] = E;
+      T.hs[warp] = (14 - E >= -126 && 14 - E <= 127) ? exp2i(14 - E) : 0.0f;   // 0: exact slow path
     }
   }
   if (tid == 0) T.xflags = 0u;
@@ -316,7 +356,8 @@ __device__ __noinline__ uint32_t build_slab(const StepParams& p, const StepProdu
       piece_bf16(P, raw[k], T.inv_rms[n], w);
       const int j = i8 / u8, kl8 = i8 - j * u8;
       const int off = (j * N + n) * xblk + (kl8 / lk) * 16 + (kl8 % lk) * 128;
-      *reinterpret_cast<uint4*>(xs + off) = piece_hi(w, T.E[n], flags);
+      const float hs = T.hs[n];
+      *reinterpret_cast<uint4*>(xs + off) = hs != 0.0f ? piece_hi_fast(w, hs, T.E[n], flags) : piece_hi(w, T.E[n], flags);
     }
   }
   if (flags) atomicOr(&T.xflags, flags);
@@ -339,11 +380,17 @@ __device__ __noinline__ uint32_t build_slab(const StepParams& p, const StepProdu
   return fl;
 }
 
-// Pieces of tile t over all slabs, and the partial-sum slot of piece (s, l).
-BWS_DEV int tile_pieces(const StepProduct& P, int t, int G) {
+// Where CTA c works in product Pp.
+BWS_DEV SlabPos pos_of(const StepProduct* Pp, int c, int G) {
+  return slab_pos(__ldg(&Pp->n_tiles), __ldg(&Pp->nks), __ldg(&Pp->n_slabs), c, G);
+}
+
+// Pieces of tile t over all slabs.
+BWS_DEV int tile_pieces(const StepProduct* Pp, int t, int G) {
+  const int S = __ldg(&Pp->n_slabs), T = __ldg(&Pp->n_tiles), K = __ldg(&Pp->nks);
   int n = 0;
-  for (int s = 0; s < P.n_slabs; ++s) {
-    const SlabPos q = slab_pos(P.n_tiles, P.nks, P.n_slabs, (int)((long long)s * G / P.n_slabs), G);
+  for (int s = 0; s < S; ++s) {
+    const SlabPos q = slab_pos(T, K, S, (int)((long long)s * G / S), G);
     n += (int)(owner_of((long long)t * q.nk + q.nk - 1, q.units, q.gs) - owner_of((long long)t * q.nk, q.units, q.gs)) + 1;
   }
   return n;
@@ -394,54 +441,55 @@ BWS_DEV void step_store(const StepParams& p, const StepProduct& P, int tile, int
   }
 }
 
-// End of a tile piece for warps 0..3 (v: the piece's sums in true units):
-// deposit it, and if it is the tile's last piece add all pieces, store the
-// outputs and statistics, and count the tile done.
-BWS_DEV void piece_end(const StepParams& p, const StepProduct& P, int pidx, const SlabPos& pos,
-                                       StepTail& T, int cur, bool whole, float (&v)[2][4], int b, int g, int t,
-                                       int lane) {
+// End of a tile piece of product pi for warps 0..3 (v0 / v1: sub-tiles 0 and
+// 1 of box b, sums in true units): deposit it, and if it is the tile's last
+// piece add all pieces, store the outputs and statistics and count the tile
+// done. Out of line, with scalar arguments: it runs once per piece, and the
+// unit loop keeps its registers.
+__device__ __noinline__ void piece_end(const StepParams& p, int pi, StepTail& T, int cur, bool whole, float4 v0,
+                                       float4 v1) {
+  const StepProduct P = p.prods[pi];
   const int N = p.N;
+  const int lane = threadIdx.x & 31, b = threadIdx.x >> 5, g = lane >> 2, t = lane & 3;
+  float v[2][4] = {{v0.x, v0.y, v0.z, v0.w}, {v1.x, v1.y, v1.z, v1.w}};
   float* partials = reinterpret_cast<float*>(p.ws + p.partials_off);
   uint32_t* counters = reinterpret_cast<uint32_t*>(p.ws + p.counters_off);
   uint32_t* done = reinterpret_cast<uint32_t*>(p.ws + p.done_off);
   if (!whole) {
-    float4* slot = reinterpret_cast<float4*>(partials) +
-                   ((size_t)pos.s * p.slab_stride + cur + pos.l) * kSlotF4 + b * 64;
-#pragma unroll
-    for (int st = 0; st < 2; ++st) slot[st * 32 + lane] = make_float4(v[st][0], v[st][1], v[st][2], v[st][3]);
+    const SlabPos pos = slab_pos(P.n_tiles, P.nks, P.n_slabs, blockIdx.x, p.G);
+    float4* slot = reinterpret_cast<float4*>(partials) + ((size_t)pos.s * p.slab_stride + cur + pos.l) * kSlotF4 + b * 64;
+    slot[lane] = v0;
+    slot[32 + lane] = v1;
     __threadfence();
     named_bar_sync(2, 4 * 32);
     if (threadIdx.x == 0) T.prev = atomicAdd(counters + cur, 1u);
     named_bar_sync(2, 4 * 32);
     const uint32_t prev = T.prev;
     named_bar_sync(2, 4 * 32);
-    if (prev + 1 != (uint32_t)tile_pieces(P, cur, p.G)) return;
+    if (prev + 1 != (uint32_t)tile_pieces(p.prods + pi, cur, p.G)) return;
     __threadfence();
-    // all pieces of the tile, added in (slab, CTA) order; loads issued a few slots at a time
+    // all pieces of the tile, added in (slab, CTA) order, two slots' loads in flight
     float a8[2][4] = {};
-    constexpr int kFix = 4;
     for (int s2 = 0; s2 < P.n_slabs; ++s2) {
       const SlabPos q = slab_pos(P.n_tiles, P.nks, P.n_slabs, (int)((long long)s2 * p.G / P.n_slabs), p.G);
       const int l0 = (int)owner_of((long long)cur * q.nk, q.units, q.gs);
       const int l1 = (int)owner_of((long long)cur * q.nk + q.nk - 1, q.units, q.gs);
-      const float4* src0 = reinterpret_cast<const float4*>(partials) +
-                           ((size_t)s2 * p.slab_stride + cur) * kSlotF4 + b * 64 + lane;
-      for (int l = l0; l <= l1; l += kFix) {
-        float4 o[kFix][2];
-#pragma unroll
-        for (int k = 0; k < kFix; ++k)
-          if (l + k <= l1) {
-            o[k][0] = ld_cg_f4(src0 + (size_t)(l + k) * kSlotF4);
-            o[k][1] = ld_cg_f4(src0 + (size_t)(l + k) * kSlotF4 + 32);
-          }
-#pragma unroll
-        for (int k = 0; k < kFix; ++k)
-          if (l + k <= l1) {
-#pragma unroll
-            for (int st = 0; st < 2; ++st) {
-              a8[st][0] += o[k][st].x; a8[st][1] += o[k][st].y; a8[st][2] += o[k][st].z; a8[st][3] += o[k][st].w;
-            }
-          }
+      const float4* src0 =
+          reinterpret_cast<const float4*>(partials) + ((size_t)s2 * p.slab_stride + cur) * kSlotF4 + b * 64 + lane;
+      for (int l = l0; l <= l1; l += 2) {
+        const bool two = l + 1 <= l1;
+        const float4 o0 = ld_cg_f4(src0 + (size_t)l * kSlotF4), o1 = ld_cg_f4(src0 + (size_t)l * kSlotF4 + 32);
+        float4 o2 = make_float4(0.f, 0.f, 0.f, 0.f), o3 = o2;
+        if (two) {
+          o2 = ld_cg_f4(src0 + (size_t)(l + 1) * kSlotF4);
+          o3 = ld_cg_f4(src0 + (size_t)(l + 1) * kSlotF4 + 32);
+        }
+        a8[0][0] += o0.x; a8[0][1] += o0.y; a8[0][2] += o0.z; a8[0][3] += o0.w;
+        a8[1][0] += o1.x; a8[1][1] += o1.y; a8[1][2] += o1.z; a8[1][3] += o1.w;
+        if (two) {
+          a8[0][0] += o2.x; a8[0][1] += o2.y; a8[0][2] += o2.z; a8[0][3] += o2.w;
+          a8[1][0] += o3.x; a8[1][1] += o3.y; a8[1][2] += o3.z; a8[1][3] += o3.w;
+        }
       }
     }
 #pragma unroll
@@ -495,17 +543,19 @@ BWS_DEV void piece_end(const StepParams& p, const StepProduct& P, int pidx, cons
   }
   __threadfence();
   named_bar_sync(2, 4 * 32);
-  if (threadIdx.x == 0) atomicAdd(done + pidx, 1u);
+  if (threadIdx.x == 0) atomicAdd(done + pi, 1u);
 }
 
-// The consumer warps' units of product P (LO: the two-band path).
+// The consumer warps' units [u0, u1) of product pi (slab k-units nk; tiles
+// whole if the product has one slab); LO: the two-band path. Keeps little
+// state in registers: everything else is reread at the piece ends.
 template <int FMT, bool LO>
-BWS_DEV void step_units(const StepParams& p, const StepProduct& P, int pidx, const SlabPos& pos, StepTail& T,
-                        uint32_t stage0, uint32_t xs0, const uint8_t* lo_glob, int& s, uint32_t& ph, int warp,
-                        int lane) {
+BWS_DEV void step_units(const StepParams& p, int pi, long long u0, long long u1, int nk, bool one_slab, StepTail& T,
+                        uint32_t stage0, uint32_t xs0, const uint8_t* lo_glob, int& s, uint32_t& ph) {
   constexpr int kUnitK = FMT == kFmtFP8 ? 128 : 256;
   constexpr int kXv = FMT == kFmtFP8 ? 2 : 4;
   const int N = p.N;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int xblk = kUnitK * 2 + 16;
   const int b = warp & 3, half = warp >> 2;
   const int g = lane >> 2, t = lane & 3;
@@ -513,25 +563,25 @@ BWS_DEV void step_units(const StepParams& p, const StepProduct& P, int pidx, con
   const uint32_t coff = b * kBoxBytes + g * 128 + ((c ^ g) << 4);
   const uint32_t soff = kCodeBytes + b * kScaleBoxBytes + g * 16 + 2 * c;
   const int xg = g < N ? g : 0;
-  const uint32_t xlane = (uint32_t)(xg * xblk + c * 16);
-  uint32_t* status = reinterpret_cast<uint32_t*>(p.ws) + 1;
+  const uint32_t xlane = xs0 + (uint32_t)(xg * xblk + c * 16);
+  const uint32_t xstep = (uint32_t)(N * xblk);
 
   float acc[2][2][4] = {}, accl[2][4] = {};
   uint4 xh[kXv], xl[kXv];
-  int tile = (int)(pos.u0 / pos.nk), kl = (int)(pos.u0 % pos.nk);
+  int tile = (int)(u0 / nk), kl = (int)(u0 % nk);
   bool piece_whole = kl == 0;
-  for (long long u = pos.u0; u < pos.u1; ++u) {
-    const uint32_t xu = xlane + (uint32_t)(kl * N * xblk);
+  for (long long u = u0; u < u1; ++u) {
+    const uint32_t xu = xlane + (uint32_t)kl * xstep;
     if (LO) {
 #pragma unroll
-      for (int q = 0; q < kXv; ++q) xl[q] = ld_cg_u4(lo_glob + xu + q * 128);
+      for (int q = 0; q < kXv; ++q) xl[q] = ld_cg_u4(lo_glob + (xu - xs0) + q * 128);
     }
     // once a wait has run out nothing is waited for or released any more, so
     // the producer runs out of released stages and stops (no copy is ever
     // issued into a stage that a copy may still be filling)
     bool have = !T.dead;
     if (have && !mbar_wait_bounded(smem_u32(&T.full[s]), ph, kPolls)) {
-      if (lane == 0) atomicOr(status, kStatusTimeout);
+      if (lane == 0) atomicOr(reinterpret_cast<uint32_t*>(p.ws) + 1, kStatusTimeout);
       T.dead = 1u;
       have = false;
     }
@@ -545,7 +595,7 @@ BWS_DEV void step_units(const StepParams& p, const StepProduct& P, int pidx, con
       for (int j = 0; j < 4; ++j) sc[j] = lds_u16(base + soff + j * 128);
     }
 #pragma unroll
-    for (int q = 0; q < kXv; ++q) xh[q] = lds_v4(xs0 + xu + q * 128);
+    for (int q = 0; q < kXv; ++q) xh[q] = lds_v4(xu + q * 128);
     __syncwarp();
     if (lane == 0 && have) mbar_arrive(smem_u32(&T.empty[s]));
     if (++s == kStages) { s = 0; ph ^= 1u; }
@@ -555,14 +605,11 @@ BWS_DEV void step_units(const StepParams& p, const StepProduct& P, int pidx, con
       const uint32_t w1[4] = {cw[2 * st + 1].x, cw[2 * st + 1].y, cw[2 * st + 1].z, cw[2 * st + 1].w};
       sub_mma<FMT, LO>(acc[st], accl[st], w0, w1, sc[2 * st], sc[2 * st + 1], xh, xl);
     }
-    const bool last_of_tile = kl == pos.nk - 1;
+    const bool last_of_tile = kl == nk - 1;
     const int cur = tile;
-    if (++kl == pos.nk) { kl = 0; ++tile; }
-    if (!last_of_tile && u + 1 < pos.u1) continue;
-    // ---- end of a tile piece: sums in true units ----
-    int e[2];
-#pragma unroll
-    for (int i = 0; i < 2; ++i) e[i] = (2 * t + i < N ? T.E[2 * t + i] : 0) - 14;
+    if (++kl == nk) { kl = 0; ++tile; }
+    if (!last_of_tile && u + 1 < u1) continue;
+    // ---- end of a tile piece: the two halves added, sums in true units ----
     float v[2][4];
 #pragma unroll
     for (int st = 0; st < 2; ++st) {
@@ -578,32 +625,79 @@ BWS_DEV void step_units(const StepParams& p, const StepProduct& P, int pidx, con
       for (int st = 0; st < 2; ++st) T.red[b][st][lane] = make_float4(v[st][0], v[st][1], v[st][2], v[st][3]);
     }
     named_bar_sync(1, kConsumerThreads);
+    const bool whole = piece_whole && last_of_tile && one_slab;
+    piece_whole = true;
     if (half == 0) {
+      const int e0 = (2 * t < N ? T.E[2 * t] : 0) - 14, e1 = (2 * t + 1 < N ? T.E[2 * t + 1] : 0) - 14;
+      float4 w[2];
 #pragma unroll
       for (int st = 0; st < 2; ++st) {
         const float4 o = T.red[b][st][lane];
-        v[st][0] = ldexp_exact(v[st][0] + o.x, e[0]);
-        v[st][1] = ldexp_exact(v[st][1] + o.y, e[1]);
-        v[st][2] = ldexp_exact(v[st][2] + o.z, e[0]);
-        v[st][3] = ldexp_exact(v[st][3] + o.w, e[1]);
+        w[st] = make_float4(ldexp_exact(v[st][0] + o.x, e0), ldexp_exact(v[st][1] + o.y, e1),
+                            ldexp_exact(v[st][2] + o.z, e0), ldexp_exact(v[st][3] + o.w, e1));
       }
+      named_bar_sync(1, kConsumerThreads);   // T.red read: warps 4..7 may go on
+      piece_end(p, pi, T, cur, whole, w[0], w[1]);
+    } else {
+      named_bar_sync(1, kConsumerThreads);
     }
-    named_bar_sync(1, kConsumerThreads);
-    const bool whole = piece_whole && last_of_tile && P.n_slabs == 1;
-    piece_whole = true;
-    if (half == 1) continue;
-    // warps 0..3: finish the tile, or deposit the piece
-    piece_end(p, P, pidx, pos, T, cur, whole, v, b, g, t, lane);
   }
 }
 
 // The two-band unit loops, out of line (rare; their registers stay out of the
 // main loops).
-template <int FMT, bool LO>
-__device__ __noinline__ void step_units_call(const StepParams& p, const StepProduct& P, int pidx, const SlabPos& pos,
-                                             StepTail& T, uint32_t stage0, uint32_t xs0, const uint8_t* lo_glob,
-                                             int& s, uint32_t& ph, int warp, int lane) {
-  step_units<FMT, LO>(p, P, pidx, pos, T, stage0, xs0, lo_glob, s, ph, warp, lane);
+template <int FMT>
+__device__ __noinline__ void step_units_lo(const StepParams& p, int pi, long long u0, long long u1, int nk,
+                                           bool one_slab, StepTail& T, uint32_t stage0, uint32_t xs0,
+                                           const uint8_t* lo_glob, int& s, uint32_t& ph) {
+  step_units<FMT, true>(p, pi, u0, u1, nk, one_slab, T, stage0, xs0, lo_glob, s, ph);
+}
+
+// A position in this CTA's sequence of weight units (products in order, each
+// product's units tile-major within its slab). pi == n_prods: past the end.
+struct UnitCursor {
+  int pi, tile, kl, nk, k0;
+  long long u, u1;
+};
+
+BWS_DEV void cursor_product(const StepParams& p, UnitCursor& c) {
+  for (; c.pi < p.n_prods; ++c.pi) {
+    const SlabPos q = pos_of(p.prods + c.pi, blockIdx.x, p.G);
+    if (q.u1 > q.u0) {
+      c.u = q.u0;
+      c.u1 = q.u1;
+      c.nk = q.nk;
+      c.k0 = q.k0;
+      c.tile = (int)(q.u0 / q.nk);
+      c.kl = (int)(q.u0 % q.nk);
+      return;
+    }
+  }
+}
+BWS_DEV void cursor_start(const StepParams& p, UnitCursor& c) {
+  c.pi = 0;
+  cursor_product(p, c);
+}
+BWS_DEV void cursor_next(const StepParams& p, UnitCursor& c) {
+  if (++c.kl == c.nk) { c.kl = 0; ++c.tile; }
+  if (++c.u == c.u1) {
+    ++c.pi;
+    cursor_product(p, c);
+  }
+}
+
+// The unit at the cursor into the stage at dst, completing on bar.
+BWS_DEV void issue_unit(const StepParams& p, const UnitCursor& c, uint32_t dst, uint32_t bar) {
+  const StepProduct P = p.prods[c.pi];
+  const int ks = c.k0 + c.kl;
+  mbar_arrive_expect_tx(bar, P.fmt == kFmtNVFP4 ? kStageBytes : kCodeBytes);
+#pragma unroll
+  for (int b = 0; b < kBoxes; ++b) {
+    int m, row;
+    step_box(P, p.mats, c.tile, b, m, row);
+    tma_load_2d(dst + b * kBoxBytes, &p.mats[m].codes, ks * 128, row, bar);
+    if (P.fmt == kFmtNVFP4) tma_load_2d(dst + kCodeBytes + b * kScaleBoxBytes, &p.mats[m].scales, ks * 16, row, bar);
+  }
 }
 
 __global__ void __launch_bounds__(kStepThreads, 2) step_kernel(const __grid_constant__ StepParams p) {
@@ -627,36 +721,19 @@ __global__ void __launch_bounds__(kStepThreads, 2) step_kernel(const __grid_cons
   if (warp == kSW) {
     // ---- producer: the weight units of every product, in order ----
     if (lane == 0) {
+      UnitCursor ld;
+      cursor_start(p, ld);
       int s = 0;
       uint32_t ph = 0u;
       long long issued = 0;
-      bool ok = true;
-      for (int pi = 0; pi < p.n_prods && ok; ++pi) {
-        const StepProduct P = p.prods[pi];
-        const SlabPos pos = slab_pos(P.n_tiles, P.nks, P.n_slabs, blockIdx.x, p.G);
-        const uint32_t w_tx = P.fmt == kFmtNVFP4 ? kStageBytes : kCodeBytes;
-        int tile = (int)(pos.u0 / pos.nk), kl = (int)(pos.u0 % pos.nk);
-        for (long long u = pos.u0; u < pos.u1; ++u, ++issued) {
-          if (issued >= kStages && !mbar_wait_bounded(smem_u32(&T.empty[s]), ph ^ 1u, kPolls)) {
-            atomicOr(reinterpret_cast<uint32_t*>(p.ws) + 1, kStatusTimeout);
-            ok = false;
-            break;
-          }
-          const uint32_t full = smem_u32(&T.full[s]);
-          const uint32_t dst = stage0 + (uint32_t)s * kStageBytes;
-          mbar_arrive_expect_tx(full, w_tx);
-          const int ks = pos.k0 + kl;
-#pragma unroll
-          for (int b = 0; b < kBoxes; ++b) {
-            int m, row;
-            step_box(P, p.mats, tile, b, m, row);
-            tma_load_2d(dst + b * kBoxBytes, &p.mats[m].codes, ks * 128, row, full);
-            if (P.fmt == kFmtNVFP4)
-              tma_load_2d(dst + kCodeBytes + b * kScaleBoxBytes, &p.mats[m].scales, ks * 16, row, full);
-          }
-          if (++s == kStages) { s = 0; ph ^= 1u; }
-          if (++kl == pos.nk) { kl = 0; ++tile; }
+      for (; ld.pi < p.n_prods; ++issued) {
+        if (issued >= kStages && !mbar_wait_bounded(smem_u32(&T.empty[s]), ph ^ 1u, kPolls)) {
+          atomicOr(reinterpret_cast<uint32_t*>(p.ws) + 1, kStatusTimeout);
+          break;
         }
+        issue_unit(p, ld, stage0 + (uint32_t)s * kStageBytes, smem_u32(&T.full[s]));
+        cursor_next(p, ld);
+        if (++s == kStages) { s = 0; ph ^= 1u; }
       }
       // let copies in flight land before the CTA's shared memory goes away
       for (long long k = (issued > kStages ? issued - kStages : 0); k < issued; ++k)
@@ -675,13 +752,13 @@ __global__ void __launch_bounds__(kStepThreads, 2) step_kernel(const __grid_cons
   int s = 0;
   uint32_t ph = 0u;
   for (int pi = 0; pi < p.n_prods; ++pi) {
-    const StepProduct P = p.prods[pi];
-    const SlabPos pos = slab_pos(P.n_tiles, P.nks, P.n_slabs, blockIdx.x, p.G);
+    const StepProduct* Pp = p.prods + pi;
+    const SlabPos pos = pos_of(Pp, blockIdx.x, p.G);
     if (pos.u1 <= pos.u0) continue;
     if (pi > 0) {
       // the previous product's outputs (this product's input) are complete
       if (tid == 0 && !T.dead) {
-        const uint32_t want = (uint32_t)p.prods[pi - 1].n_tiles;
+        const uint32_t want = (uint32_t)__ldg(&p.prods[pi - 1].n_tiles);
         uint32_t k = 0;
         while (ld_acquire_u32(done + pi - 1) < want) {
           if (++k == kPolls) {
@@ -689,27 +766,26 @@ __global__ void __launch_bounds__(kStepThreads, 2) step_kernel(const __grid_cons
             T.dead = 1u;
             break;
           }
-          __nanosleep(64);
+          __nanosleep(32);
         }
-        __threadfence();
       }
       named_bar_sync(4, kConsumerThreads);
     }
-    const uint32_t fl = build_slab(p, P, pos, T, xs, lo_glob, tid);
+    const uint32_t fl = build_slab(p, *Pp, pos, T, xs, lo_glob, tid);
     if (tid == 0 && fl) atomicOr(status, fl);
+    const bool fp8 = __ldg(&Pp->fmt) == kFmtFP8;
+    const bool one_slab = __ldg(&Pp->n_slabs) == 1;
     if (fl & 1u) {
-      if (P.fmt == kFmtFP8)
-        step_units_call<kFmtFP8, true>(p, P, pi, pos, T, stage0, xs0, lo_glob, s, ph, warp, lane);
+      if (fp8)
+        step_units_lo<kFmtFP8>(p, pi, pos.u0, pos.u1, pos.nk, one_slab, T, stage0, xs0, lo_glob, s, ph);
       else
-        step_units_call<kFmtNVFP4, true>(p, P, pi, pos, T, stage0, xs0, lo_glob, s, ph, warp, lane);
+        step_units_lo<kFmtNVFP4>(p, pi, pos.u0, pos.u1, pos.nk, one_slab, T, stage0, xs0, lo_glob, s, ph);
     } else {
-      if (P.fmt == kFmtFP8)
-        step_units<kFmtFP8, false>(p, P, pi, pos, T, stage0, xs0, lo_glob, s, ph, warp, lane);
+      if (fp8)
+        step_units<kFmtFP8, false>(p, pi, pos.u0, pos.u1, pos.nk, one_slab, T, stage0, xs0, lo_glob, s, ph);
       else
-        step_units<kFmtNVFP4, false>(p, P, pi, pos, T, stage0, xs0, lo_glob, s, ph, warp, lane);
+        step_units<kFmtNVFP4, false>(p, pi, pos.u0, pos.u1, pos.nk, one_slab, T, stage0, xs0, lo_glob, s, ph);
     }
-    // the slab is rebuilt for the next product only after every consumer warp is done with it
-    named_bar_sync(4, kConsumerThreads);
   }
 }
 
