@@ -476,179 +476,7 @@ __global__ void __launch_bounds__(kWarpsPerCta * 32, BWS_GEMV_MIN_BLOCKS) gemv_k
   }
 }
 
-// ---- activation prep ----------------------------------------------------------
-
-// One CTA per (slot, token) row: optionally RMSNorm, then E = floor(log2
-// max|x|) and the two f16 bands. Each thread handles 8-element chunks
-// (d_in % 32 == 0, so a chunk never straddles d_in). Also zeroes the counters
-// of the product that follows.
-constexpr int kPrepThreads = 1024;
-
-BWS_DEV float block_reduce_max(float v, float* sm) {
-  v = warp_max(v);
-  __syncthreads();
-  if ((threadIdx.x & 31) == 0) sm[threadIdx.x >> 5] = v;
-  __syncthreads();
-  float r = 0.0f;
-#pragma unroll 8
-  for (int i = 0; i < kPrepThreads / 32; ++i) r = fmaxf(r, sm[i]);
-  return r;
-}
-BWS_DEV float block_reduce_sum(float v, float* sm) {
-  v = warp_sum(v);
-  __syncthreads();
-  if ((threadIdx.x & 31) == 0) sm[threadIdx.x >> 5] = v;
-  __syncthreads();
-  float r = 0.0f;
-  for (int i = 0; i < kPrepThreads / 32; ++i) r += sm[i];   // fixed order
-  return r;
-}
-
-BWS_DEV float bf16_bits_to_f32(uint32_t b) { return __uint_as_float(b << 16); }
-
-// The row's values as BF16 bit patterns, chunk c (8 values).
-BWS_DEV void prep_chunk(const PrepParams& q, int c, int nchunk, const float* rr, const uint4* xr, float inv_rms,
-                        uint32_t (&w)[4]) {
-  if (c >= nchunk) {
-    w[0] = w[1] = w[2] = w[3] = 0u;
-  } else if (q.mode == kPrepRmsNorm) {
-    const float4 a = reinterpret_cast<const float4*>(rr)[2 * c];
-    const float4 b = reinterpret_cast<const float4*>(rr)[2 * c + 1];
-    const float v[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const uint32_t lo = __bfloat16_as_ushort(__float2bfloat16_rn(__fmul_rn(v[2 * i], inv_rms)));
-      const uint32_t hi = __bfloat16_as_ushort(__float2bfloat16_rn(__fmul_rn(v[2 * i + 1], inv_rms)));
-      w[i] = lo | (hi << 16);
-    }
-  } else {
-    const uint4 b = __ldg(xr + c);
-    w[0] = b.x; w[1] = b.y; w[2] = b.z; w[3] = b.w;
-  }
-}
-
-__global__ void __launch_bounds__(kPrepThreads) prep_kernel(const __grid_constant__ PrepParams q) {
-  pdl_launch_dependents();
-  pdl_wait();
-  for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < q.zero_words; i += gridDim.x * blockDim.x)
-    q.zero_ptr[i] = 0u;
-  const int slot = blockIdx.x / q.N;
-  const int tok = blockIdx.x - slot * q.N;
-  const int n_slots = q.n_slots != nullptr ? __ldg(q.n_slots) : 1;
-  if (slot >= n_slots) return;
-  if (blockIdx.x == 0 && threadIdx.x == 0) {
-    if (q.hdr != nullptr) q.hdr[0] = (uint32_t)q.N;
-    if (q.status_clear != nullptr) q.status_clear[0] = q.status_clear[1] = 0u;
-  }
-  __shared__ float sm[kPrepThreads / 32];
-  __shared__ uint32_t sf[kPrepThreads / 32];
-  const size_t rowbase = ((size_t)slot * (q.N + 1)) * q.d_in_pad;
-  if (tok == 0) {   // this slot's all-zero row
-    uint4* zh = reinterpret_cast<uint4*>(q.hi + rowbase + (size_t)q.N * q.d_in_pad);
-    uint4* zl = reinterpret_cast<uint4*>(q.lo + rowbase + (size_t)q.N * q.d_in_pad);
-    for (int c = threadIdx.x; c < (q.d_in_pad >> 3); c += blockDim.x) {
-      zh[c] = make_uint4(0, 0, 0, 0);
-      zl[c] = make_uint4(0, 0, 0, 0);
-    }
-  }
-  const int nchunk = q.d_in >> 3, nchunk_pad = q.d_in_pad >> 3;
-  float inv_rms = 1.0f;
-  const uint4* xr = nullptr;
-  float* rr = nullptr;
-  if (q.mode == kPrepRmsNorm) {
-    rr = q.r + (size_t)tok * q.d_in;
-    const uint4* x0 = q.x0 != nullptr ? reinterpret_cast<const uint4*>(q.x0 + (size_t)tok * q.d_in) : nullptr;
-    float ss = 0.0f;
-    for (int c = threadIdx.x; c < nchunk; c += blockDim.x) {
-      float v[8];
-      if (x0 != nullptr) {
-        const uint4 b = __ldg(x0 + c);
-        const uint32_t w[4] = {b.x, b.y, b.z, b.w};
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          v[2 * i] = bf16_bits_to_f32(w[i] & 0xFFFF);
-          v[2 * i + 1] = bf16_bits_to_f32(w[i] >> 16);
-        }
-        reinterpret_cast<float4*>(rr)[2 * c] = make_float4(v[0], v[1], v[2], v[3]);
-        reinterpret_cast<float4*>(rr)[2 * c + 1] = make_float4(v[4], v[5], v[6], v[7]);
-      } else {
-        const float4 a = reinterpret_cast<const float4*>(rr)[2 * c];
-        const float4 b = reinterpret_cast<const float4*>(rr)[2 * c + 1];
-        v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w; v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
-      }
-#pragma unroll
-      for (int i = 0; i < 8; ++i) ss = __fmaf_rn(v[i], v[i], ss);
-    }
-    const float ms = __fdiv_rn(block_reduce_sum(ss, sm), (float)q.d_in);
-    inv_rms = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(ms, q.eps)));
-  } else {
-    xr = reinterpret_cast<const uint4*>(q.x + (size_t)slot * q.x_slot_stride + (size_t)tok * q.ld);
-  }
-  float m = 0.0f;
-  for (int c = threadIdx.x; c < nchunk; c += blockDim.x) {
-    uint32_t w[4];
-    prep_chunk(q, c, nchunk, rr, xr, inv_rms, w);
-#pragma unroll
-    for (int i = 0; i < 4; ++i)
-      m = fmaxf(m, fmaxf(fabsf(bf16_bits_to_f32(w[i] & 0xFFFF)), fabsf(bf16_bits_to_f32(w[i] >> 16))));
-  }
-  const float mx = block_reduce_max(m, sm);
-  const int E = mx > 0.0f ? floor_log2_abs(mx) : 0;
-  uint32_t flags = 0u;
-  uint4* hi4 = reinterpret_cast<uint4*>(q.hi + rowbase + (size_t)tok * q.d_in_pad);
-  uint4* lo4 = reinterpret_cast<uint4*>(q.lo + rowbase + (size_t)tok * q.d_in_pad);
-  // TMA-kernel layout: within each unit of K_u values, the 8-value chunk j of
-  // lane chunk cl (cl = 0..7, lane chunks of K_u/8 values) moves to chunk
-  // position j * 8 + cl, so that the 8 lanes of a shared-memory phase read 8
-  // different banks.
-  const int ku8 = q.interleave / 8, lk8 = q.interleave / 64;
-  for (int c = threadIdx.x; c < nchunk_pad; c += blockDim.x) {
-    int dst = c;
-    if (q.interleave) {
-      const int u = c / ku8, r8 = c - u * ku8;
-      dst = u * ku8 + (r8 % lk8) * 8 + r8 / lk8;
-    }
-    uint32_t w[4];
-    prep_chunk(q, c, nchunk, rr, xr, inv_rms, w);
-    uint32_t h[4], l[4];
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      uint32_t hh[2], ll[2];
-#pragma unroll
-      for (int j = 0; j < 2; ++j) {
-        const float f = bf16_bits_to_f32(j == 0 ? (w[i] & 0xFFFF) : (w[i] >> 16));
-        const float a = ldexp_exact(f, 14 - E);
-        hh[j] = 0u;
-        ll[j] = 0u;
-        if (fabsf(a) >= 0x1p-14f) {
-          hh[j] = __half_as_ushort(__float2half_rn(a));
-        } else if (f != 0.0f) {
-          const float b = ldexp_exact(f, 43 - E);
-          if (fabsf(b) >= 0x1p-14f) {
-            ll[j] = __half_as_ushort(__float2half_rn(b));
-            flags |= 1u;
-          } else {
-            flags |= 2u;
-          }
-        }
-      }
-      h[i] = hh[0] | (hh[1] << 16);
-      l[i] = ll[0] | (ll[1] << 16);
-    }
-    hi4[dst] = make_uint4(h[0], h[1], h[2], h[3]);
-    lo4[dst] = make_uint4(l[0], l[1], l[2], l[3]);
-  }
-  flags = __reduce_or_sync(0xffffffffu, flags);
-  __syncthreads();
-  if ((threadIdx.x & 31) == 0) sf[threadIdx.x >> 5] = flags;
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    uint32_t f = 0u;
-    for (int i = 0; i < kPrepThreads / 32; ++i) f |= sf[i];
-    q.exp[slot * q.N + tok] = E;
-    q.flags[slot * q.N + tok] = f;
-  }
-}
+// ---- launches ------------------------------------------------------------------
 
 cudaLaunchConfig_t make_cfg(dim3 grid, dim3 block, size_t smem, cudaStream_t st, bool pdl,
                             cudaLaunchAttribute* attr) {
@@ -773,13 +601,6 @@ GemvWorkspace gemv_workspace_layout(int N, int d_in, int n_tiles, long long max_
   w.off_partials = o; o += align256(sizeof(float) * kSlotFloats * ((size_t)n_tiles + max_warps));
   w.total = o;
   return w;
-}
-
-cudaError_t launch_prep(const PrepParams& q, cudaStream_t st, bool pdl) {
-  cudaLaunchAttribute attr[1];
-  const int slots = q.n_slots != nullptr ? q.max_slots : 1;
-  cudaLaunchConfig_t cfg = make_cfg(dim3((unsigned)(slots * q.N)), dim3(kPrepThreads), 0, st, pdl, attr);
-  return cudaLaunchKernelEx(&cfg, prep_kernel, q);
 }
 
 cudaError_t launch_gemv(int fmt, int epi, const GemvParams& p, cudaStream_t st, bool pdl) {

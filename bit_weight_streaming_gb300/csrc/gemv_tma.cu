@@ -294,17 +294,34 @@ BWS_DEV void consume(const TmaParams& p, Tail& T, uint32_t stage0, long long u0,
       named_bar_sync(2, 4 * 32);
       if (prev != (uint32_t)(c1 - c0)) continue;
       __threadfence();
+      // the tile's pieces in CTA order; their loads are issued kFix pieces at a
+      // time, so the tail of a product waits for a few L2 round trips, not one
+      // per piece
+      constexpr int kFix = 4;
       float a8[2][4] = {};
-      for (long long cc = c0; cc <= c1; ++cc) {
+      const float4* slots = reinterpret_cast<const float4*>(p.partials) + (size_t)cur_tile * kBoxes * 64 + b * 64 + lane;
+      for (long long cc0 = c0; cc0 <= c1; cc0 += kFix) {
+        float4 o[kFix][2];
 #pragma unroll
-        for (int st = 0; st < 2; ++st) {
-          float4 o;
-          if (cc == blockIdx.x)
-            o = make_float4(v[st][0], v[st][1], v[st][2], v[st][3]);
-          else
-            o = ld_cg_f4(reinterpret_cast<const float4*>(p.partials) +
-                         ((size_t)(cur_tile + cc) * kBoxes + b) * 64 + st * 32 + lane);
-          a8[st][0] += o.x; a8[st][1] += o.y; a8[st][2] += o.z; a8[st][3] += o.w;
+        for (int k = 0; k < kFix; ++k) {
+          const long long cc = cc0 + k;
+#pragma unroll
+          for (int st = 0; st < 2; ++st) {
+            if (cc > c1)
+              o[k][st] = make_float4(0.f, 0.f, 0.f, 0.f);
+            else if (cc == blockIdx.x)
+              o[k][st] = make_float4(v[st][0], v[st][1], v[st][2], v[st][3]);
+            else
+              o[k][st] = ld_cg_f4(slots + (size_t)cc * kBoxes * 64 + st * 32);
+          }
+        }
+#pragma unroll
+        for (int k = 0; k < kFix; ++k) {
+          if (cc0 + k > c1) break;
+#pragma unroll
+          for (int st = 0; st < 2; ++st) {
+            a8[st][0] += o[k][st].x; a8[st][1] += o[k][st].y; a8[st][2] += o[k][st].z; a8[st][3] += o[k][st].w;
+          }
         }
       }
 #pragma unroll

@@ -1,0 +1,238 @@
+// Activation prep: for each (slot, token) row, optionally r = x0, then
+// BF16(RMSNorm(r)) or the BF16 input itself, its exponent E = floor(log2
+// max|x|) and the two f16 bands x * 2^(14 - E) / x * 2^(43 - E) the product
+// kernels read. Also zeroes the tile counters of the product that follows.
+//
+// A long row (d > 8192) gets a thread-block cluster of 8 CTAs of 256 threads:
+// each CTA takes a contiguous share of the row's 8-element chunks, and the
+// row's sum of squares, largest magnitude and band flags are exchanged through
+// distributed shared memory, combined in CTA-rank order (deterministic), so
+// the row costs one pass of loads spread over 8 SMs. A shorter row gets one
+// CTA of 1024 threads (a cluster of one): it starts sooner while the previous
+// product's CTAs still hold most SMs.
+#include <cooperative_groups.h>
+
+#include "bws_common.cuh"
+#include "bws_internal.h"
+
+namespace cg = cooperative_groups;
+
+namespace bws {
+
+namespace {
+
+constexpr int kLongRow = 8192;    // longer rows get a cluster
+
+BWS_DEV float bf16_bits_to_f32(uint32_t b) { return __uint_as_float(b << 16); }
+
+// The row's values as BF16 bit patterns, chunk c (8 values); for RMSNorm, the
+// FP32 residual times inv_rms rounded to BF16.
+BWS_DEV void chunk_bf16(const PrepParams& q, int c, const float* rr, const uint4* xr, float inv_rms,
+                        uint32_t (&w)[4]) {
+  if (q.mode == kPrepRmsNorm) {
+    const float4 a = reinterpret_cast<const float4*>(rr)[2 * c];
+    const float4 b = reinterpret_cast<const float4*>(rr)[2 * c + 1];
+    const float v[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const uint32_t lo = __bfloat16_as_ushort(__float2bfloat16_rn(__fmul_rn(v[2 * i], inv_rms)));
+      const uint32_t hi = __bfloat16_as_ushort(__float2bfloat16_rn(__fmul_rn(v[2 * i + 1], inv_rms)));
+      w[i] = lo | (hi << 16);
+    }
+  } else {
+    const uint4 b = __ldg(xr + c);
+    w[0] = b.x; w[1] = b.y; w[2] = b.z; w[3] = b.w;
+  }
+}
+
+// Sum (or max, or OR) of one value per CTA of the cluster, in rank order,
+// through each CTA's `slot`; every CTA gets the same result.
+template <int OP, int CL, int THREADS>   // OP 0: sum, 1: max, 2: bitwise or
+BWS_DEV float cluster_combine(float* slot, float v, float* warp_part) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (OP == 0) v = warp_sum(v);
+  if (OP == 1) v = warp_max(v);
+  if (OP == 2) v = __uint_as_float(__reduce_or_sync(0xffffffffu, __float_as_uint(v)));
+  if (lane == 0) warp_part[warp] = v;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    float r = warp_part[0];
+    for (int i = 1; i < THREADS / 32; ++i) {
+      if (OP == 0) r += warp_part[i];
+      if (OP == 1) r = fmaxf(r, warp_part[i]);
+      if (OP == 2) r = __uint_as_float(__float_as_uint(r) | __float_as_uint(warp_part[i]));
+    }
+    *slot = r;
+  }
+  if (CL == 1) {
+    __syncthreads();
+    return *slot;
+  }
+  cg::cluster_group cl = cg::this_cluster();
+  cl.sync();
+  float r = *cl.map_shared_rank(slot, 0);
+  for (int k = 1; k < CL; ++k) {
+    const float o = *cl.map_shared_rank(slot, k);
+    if (OP == 0) r += o;
+    if (OP == 1) r = fmaxf(r, o);
+    if (OP == 2) r = __uint_as_float(__float_as_uint(r) | __float_as_uint(o));
+  }
+  return r;
+}
+
+template <int CL, int THREADS>
+__global__ void __launch_bounds__(THREADS) prep_kernel(const __grid_constant__ PrepParams q) {
+  pdl_launch_dependents();
+  pdl_wait();
+  const int rank = CL == 1 ? 0 : (int)cg::this_cluster().block_rank();
+  for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < q.zero_words; i += gridDim.x * blockDim.x)
+    q.zero_ptr[i] = 0u;
+  const int row = blockIdx.x / CL;
+  const int slot = row / q.N;
+  const int tok = row - slot * q.N;
+  const int n_slots = q.n_slots != nullptr ? __ldg(q.n_slots) : 1;
+  if (slot >= n_slots) return;   // the whole cluster returns together
+  if (blockIdx.x == 0 && threadIdx.x == 0) {
+    if (q.hdr != nullptr) q.hdr[0] = (uint32_t)q.N;
+    if (q.status_clear != nullptr) q.status_clear[0] = q.status_clear[1] = 0u;
+  }
+  __shared__ float warp_part[THREADS / 32];
+  __shared__ float xch[3];   // this CTA's values in the cluster exchanges
+  const int nchunk = q.d_in >> 3, nchunk_pad = q.d_in_pad >> 3;
+  // this CTA's chunks [c0, c1)
+  const int per = (nchunk_pad + CL - 1) / CL;
+  const int c0 = rank * per < nchunk_pad ? rank * per : nchunk_pad;
+  const int c1 = c0 + per < nchunk_pad ? c0 + per : nchunk_pad;
+  const size_t rowbase = ((size_t)slot * (q.N + 1)) * q.d_in_pad;
+  if (tok == 0) {   // this slot's all-zero row
+    uint4* zh = reinterpret_cast<uint4*>(q.hi + rowbase + (size_t)q.N * q.d_in_pad);
+    uint4* zl = reinterpret_cast<uint4*>(q.lo + rowbase + (size_t)q.N * q.d_in_pad);
+    for (int c = c0 + threadIdx.x; c < c1; c += blockDim.x) {
+      zh[c] = make_uint4(0, 0, 0, 0);
+      zl[c] = make_uint4(0, 0, 0, 0);
+    }
+  }
+  float inv_rms = 1.0f;
+  const uint4* xr = nullptr;
+  float* rr = nullptr;
+  if (q.mode == kPrepRmsNorm) {
+    rr = q.r + (size_t)tok * q.d_in;
+    const uint4* x0 = q.x0 != nullptr ? reinterpret_cast<const uint4*>(q.x0 + (size_t)tok * q.d_in) : nullptr;
+    float ss = 0.0f;
+    for (int c = c0 + threadIdx.x; c < c1 && c < nchunk; c += blockDim.x) {
+      float v[8];
+      if (x0 != nullptr) {
+        const uint4 b = __ldg(x0 + c);
+        const uint32_t w[4] = {b.x, b.y, b.z, b.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          v[2 * i] = bf16_bits_to_f32(w[i] & 0xFFFF);
+          v[2 * i + 1] = bf16_bits_to_f32(w[i] >> 16);
+        }
+        reinterpret_cast<float4*>(rr)[2 * c] = make_float4(v[0], v[1], v[2], v[3]);
+        reinterpret_cast<float4*>(rr)[2 * c + 1] = make_float4(v[4], v[5], v[6], v[7]);
+      } else {
+        const float4 a = reinterpret_cast<const float4*>(rr)[2 * c];
+        const float4 b = reinterpret_cast<const float4*>(rr)[2 * c + 1];
+        v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w; v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
+      }
+#pragma unroll
+      for (int i = 0; i < 8; ++i) ss = __fmaf_rn(v[i], v[i], ss);
+    }
+    const float ms = __fdiv_rn(cluster_combine<0, CL, THREADS>(&xch[0], ss, warp_part), (float)q.d_in);
+    inv_rms = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(ms, q.eps)));
+  } else {
+    xr = reinterpret_cast<const uint4*>(q.x + (size_t)slot * q.x_slot_stride + (size_t)tok * q.ld);
+  }
+  float m = 0.0f;
+  for (int c = c0 + threadIdx.x; c < c1 && c < nchunk; c += blockDim.x) {
+    uint32_t w[4];
+    chunk_bf16(q, c, rr, xr, inv_rms, w);
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+      m = fmaxf(m, fmaxf(fabsf(bf16_bits_to_f32(w[i] & 0xFFFF)), fabsf(bf16_bits_to_f32(w[i] >> 16))));
+  }
+  const float mx = cluster_combine<1, CL, THREADS>(&xch[1], m, warp_part);
+  const int E = mx > 0.0f ? floor_log2_abs(mx) : 0;
+  uint32_t flags = 0u;
+  uint4* hi4 = reinterpret_cast<uint4*>(q.hi + rowbase + (size_t)tok * q.d_in_pad);
+  uint4* lo4 = reinterpret_cast<uint4*>(q.lo + rowbase + (size_t)tok * q.d_in_pad);
+  // TMA-kernel layout: within each unit of K_u values, the 8-value chunk j of
+  // lane chunk cl (cl = 0..7, lane chunks of K_u/8 values) moves to chunk
+  // position j * 8 + cl, so that the 8 lanes of a shared-memory phase read 8
+  // different banks.
+  const int ku8 = q.interleave / 8, lk8 = q.interleave / 64;
+  for (int c = c0 + threadIdx.x; c < c1; c += blockDim.x) {
+    int dst = c;
+    if (q.interleave) {
+      const int u = c / ku8, r8 = c - u * ku8;
+      dst = u * ku8 + (r8 % lk8) * 8 + r8 / lk8;
+    }
+    uint32_t w[4] = {0u, 0u, 0u, 0u};
+    if (c < nchunk) chunk_bf16(q, c, rr, xr, inv_rms, w);
+    uint32_t h[4], l[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      uint32_t hh[2], ll[2];
+#pragma unroll
+      for (int j = 0; j < 2; ++j) {
+        const float f = bf16_bits_to_f32(j == 0 ? (w[i] & 0xFFFF) : (w[i] >> 16));
+        const float a = ldexp_exact(f, 14 - E);
+        hh[j] = 0u;
+        ll[j] = 0u;
+        if (fabsf(a) >= 0x1p-14f) {
+          hh[j] = __half_as_ushort(__float2half_rn(a));
+        } else if (f != 0.0f) {
+          const float b = ldexp_exact(f, 43 - E);
+          if (fabsf(b) >= 0x1p-14f) {
+            ll[j] = __half_as_ushort(__float2half_rn(b));
+            flags |= 1u;
+          } else {
+            flags |= 2u;
+          }
+        }
+      }
+      h[i] = hh[0] | (hh[1] << 16);
+      l[i] = ll[0] | (ll[1] << 16);
+    }
+    hi4[dst] = make_uint4(h[0], h[1], h[2], h[3]);
+    lo4[dst] = make_uint4(l[0], l[1], l[2], l[3]);
+  }
+  const uint32_t f = __float_as_uint(cluster_combine<2, CL, THREADS>(&xch[2], __uint_as_float(flags), warp_part));
+  if (rank == 0 && threadIdx.x == 0) {
+    q.exp[slot * q.N + tok] = E;
+    q.flags[slot * q.N + tok] = f;
+  }
+  if (CL > 1) cg::this_cluster().sync();   // no CTA leaves while another may still read its exchange slots
+}
+
+}  // namespace
+
+cudaError_t launch_prep(const PrepParams& q, cudaStream_t st, bool pdl) {
+  const int slots = q.n_slots != nullptr ? q.max_slots : 1;
+  const bool long_row = q.d_in_pad > kLongRow;
+  const int cl = long_row ? 8 : 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)(slots * q.N * cl));
+  cfg.blockDim = dim3(long_row ? 256 : 1024);
+  cfg.stream = st;
+  cudaLaunchAttribute a[2];
+  int na = 0;
+  if (pdl) {
+    a[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    a[na].val.programmaticStreamSerializationAllowed = 1;
+    ++na;
+  }
+  if (long_row) {
+    a[na].id = cudaLaunchAttributeClusterDimension;
+    a[na].val.clusterDim.x = cl;
+    a[na].val.clusterDim.y = 1;
+    a[na].val.clusterDim.z = 1;
+    ++na;
+  }
+  cfg.attrs = a;
+  cfg.numAttrs = na;
+  return long_row ? cudaLaunchKernelEx(&cfg, prep_kernel<8, 256>, q) : cudaLaunchKernelEx(&cfg, prep_kernel<1, 1024>, q);
+}
+
+}  // namespace bws
