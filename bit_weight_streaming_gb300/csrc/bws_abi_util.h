@@ -5,10 +5,9 @@
 #include <stdint.h>
 
 #include "../../include/bws.h"
+#include "bws_internal.h"
 
 namespace bws {
-
-struct XPrep;
 
 // MoE layer pieces used by the decode stream (moe.cu).
 size_t moe_workspace_bytes(const bws_moe_layer* L, int N, int topk);
@@ -17,6 +16,20 @@ int check_moe_layer(const bws_moe_layer* L, int N, int topk, const char* name);
 int enqueue_moe(const bws_moe_layer* L, const int32_t* ids, const float* route_w, int N, int topk,
                 const uint16_t* x, void* y, int out_mode, void* ws, cudaStream_t st, const XPrep* x_prepped,
                 const char* name);
+// The decode stream's view of an MoE workspace: route buffer `buffer` (0 or
+// 1) with the routing parameters of a layer, the slot outputs ys and the tile
+// counters the prep before the experts zeroes.
+struct MoeStackView {
+  MoeRoute route;
+  float* ys;
+  uint32_t* counters;
+  int n_counters;
+};
+MoeStackView moe_stack_view(const bws_moe_layer* L, const int32_t* ids, const float* route_w, int N, int topk,
+                            void* ws, int buffer);
+// gate/up, prep h and down for the slots of a slot table (activations xp).
+int enqueue_moe_experts(const bws_moe_layer* L, int N, int topk, const int* n_slots, const int* slot_expert,
+                        const XPrep& xp, char* w, cudaStream_t st, const char* name);
 
 // Records a message for bws_last_error() and returns code.
 int fail(int code, const char* fmt, ...);

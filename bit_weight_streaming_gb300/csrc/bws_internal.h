@@ -82,6 +82,18 @@ struct GemvParams {
   int prefetch_units;      // units pulled into L2 before waiting on the inputs
 };
 
+// MoE helpers.
+struct MoeRoute {
+  const int32_t* ids;      // [N][topk]
+  const float* route_w;    // [N][topk]
+  int N, topk, n_experts;
+  int has_shared;
+  int max_slots;
+  int* n_slots;            // out [1]
+  int* slot_expert;        // out [max_slots]
+  float* cw;               // out [max_slots][N] combine weights
+  uint32_t* status;        // out [1]: bit 4 set if an id was out of range
+};
 // Input of the activation prep kernel.
 constexpr int kPrepCopy = 0;      // x bf16 -> bands
 constexpr int kPrepRmsNorm = 1;   // r fp32 -> BF16(RMSNorm(r)) -> bands
@@ -106,6 +118,15 @@ struct PrepParams {
   int zero_words;
   int interleave;          // 0: linear rows; else the unit size in k (256 NVFP4, 128 FP8) of
                            // the TMA kernel's layout (see gemv_tma.cu)
+  // kPrepRmsNorm, optional (comb_ys != nullptr): the previous MoE layer's
+  // combine first, r[tok] += sum over live slots s, in slot order, of
+  // comb_cw[s][tok] * comb_ys[s][tok][:]
+  const float* comb_ys;
+  const float* comb_cw;
+  const int* comb_n_slots;
+  // optional: one extra CTA computes an MoE layer's slot table (one-CTA rows only)
+  int has_route;
+  MoeRoute route;
 };
 
 // Workspace of one product call (all offsets 256-byte aligned).
@@ -131,18 +152,6 @@ inline cudaError_t launch_product(int fmt, int epi, const GemvParams& p, uint32_
   return gemv_tma_eligible(fmt, p) ? launch_gemv_tma(fmt, epi, p, status, st, pdl) : launch_gemv(fmt, epi, p, st, pdl);
 }
 
-// MoE helpers.
-struct MoeRoute {
-  const int32_t* ids;      // [N][topk]
-  const float* route_w;    // [N][topk]
-  int N, topk, n_experts;
-  int has_shared;
-  int max_slots;
-  int* n_slots;            // out [1]
-  int* slot_expert;        // out [max_slots]
-  float* cw;               // out [max_slots][N] combine weights
-  uint32_t* status;        // out [1]: bit 4 set if an id was out of range
-};
 cudaError_t launch_moe_route(const MoeRoute& m, cudaStream_t st, bool pdl);
 // y[tok][i] (+)= sum over live slots s of cw[s][tok] * ys[s][tok][i]
 cudaError_t launch_moe_combine(const float* ys, const float* cw, const int* n_slots, int N, int d,

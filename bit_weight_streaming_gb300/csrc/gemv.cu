@@ -22,6 +22,7 @@
 // unit partial sum rescaled by 2^e_ref in FP32.
 #include "bws_common.cuh"
 #include "bws_internal.h"
+#include "moe_route.cuh"
 
 namespace bws {
 
@@ -458,7 +459,12 @@ __global__ void __launch_bounds__(kWarpsPerCta * 32, BWS_GEMV_MIN_BLOCKS) gemv_k
     pdl_wait();
     const long long n_slots = __ldg(p.slots.n_slots);
     U = n_slots * p.slots.tiles_per_slot * p.nseg;
-    W = p.n_warps < U ? p.n_warps : U;
+    // A short k range (at most 8 units, like an expert's down projection):
+    // each warp takes whole tiles rather than slicing every tile between
+    // warps, whose partial sums would then all go through the fix-up.
+    const long long per = p.nseg <= 8 ? p.nseg : 1;
+    const long long want = (U + per - 1) / per;
+    W = p.n_warps < want ? p.n_warps : want;
     if (warp_id >= W) return;
   }
   long long u = range_begin(warp_id, U, W);
@@ -509,47 +515,9 @@ cudaError_t launch_one(const GemvParams& p, cudaStream_t st, bool pdl) {
 __global__ void __launch_bounds__(128) moe_route_kernel(const MoeRoute m) {
   pdl_launch_dependents();
   pdl_wait();
-  __shared__ int ids[kMaxTokens * kMaxTopk];
-  __shared__ int first[kMaxTokens * kMaxTopk];
-  const int n = m.N * m.topk;
-  const int i = threadIdx.x;
-  int bad = 0;
-  if (i < n) {
-    int e = m.ids[i];
-    if (e < 0 || e >= m.n_experts) {
-      bad = 1;
-      e = -1;
-    }
-    ids[i] = e;
-  }
-  bad = __syncthreads_or(bad);
-  if (i == 0) m.status[0] = bad ? 4u : 0u;
-  for (int s = i; s < m.max_slots * m.N; s += blockDim.x) m.cw[s] = 0.0f;
-  __syncthreads();
-  if (i < n) {
-    int is_first = ids[i] >= 0 ? 1 : 0;
-    for (int j = 0; j < i; ++j) is_first &= ids[j] != ids[i];
-    first[i] = is_first;
-  }
-  __syncthreads();
-  int rank = 0;
-  if (i < n && ids[i] >= 0)
-    for (int j = 0; j < n; ++j) rank += (first[j] && ids[j] < ids[i]) ? 1 : 0;
-  const int slot = m.has_shared + rank;
-  if (i < n && first[i]) m.slot_expert[slot] = ids[i];
-  if (i == 0) {
-    int c = 0;
-    for (int j = 0; j < n; ++j) c += first[j];
-    if (m.has_shared) m.slot_expert[0] = -1;
-    m.n_slots[0] = c + m.has_shared;
-  }
-  __syncthreads();   // cw zeroing above is complete
-  // ids are distinct per token, so each (slot, token) cell gets one weight
-  if (i < n && ids[i] >= 0) m.cw[slot * m.N + i / m.topk] = m.route_w[i];
-  if (m.has_shared && i < m.N) m.cw[i] = 1.0f;
+  moe_route_body(m);
 }
 
-// y[tok][i] (+)= sum over slots, in slot order, of cw[s][tok] * ys[s][tok][i]
 __global__ void __launch_bounds__(256) moe_combine_kernel(const float* __restrict__ ys, const float* __restrict__ cw,
                                                           const int* __restrict__ n_slots_p, int N, int d,
                                                           void* __restrict__ out, int out_mode) {

@@ -11,6 +11,9 @@
 //   down    -> ys[slot] = W_down h[slot] (FP32)
 //   combine -> y = sum over slots, in slot order, of cw * ys
 // Every expert that any token uses is read exactly once per call.
+// In the decode stream the routing runs as one extra CTA of the RMSNorm prep
+// before the experts, and the combine is folded into the next RMSNorm prep,
+// so an MoE layer there costs four kernels.
 #include <cuda_runtime.h>
 
 #include "../../include/bws.h"
@@ -21,7 +24,11 @@ namespace bws {
 
 struct MoeLayout {
   int max_slots, tiles_gu, tiles_dn, n_tiles, d_pad_x, d_pad_h;
+  // two route buffers (n_slots, slot table, combine weights): the decode
+  // stream alternates them by layer, so that a layer's routing never
+  // overwrites the weights the previous layer's combine still reads
   size_t off_route, off_slot_expert, off_cw, off_status;
+  size_t off_route_b, off_slot_expert_b, off_cw_b;
   GemvWorkspace xw;   // offsets relative to off_x
   size_t off_x;
   size_t off_h;
@@ -42,6 +49,9 @@ static MoeLayout moe_layout(const bws_moe_layer* L, int N, int topk) {
   m.off_status = m.off_route + 16;
   m.off_slot_expert = o; o += align256(sizeof(int) * m.max_slots);
   m.off_cw = o; o += align256(sizeof(float) * (size_t)m.max_slots * N);
+  m.off_route_b = o; o += 256;
+  m.off_slot_expert_b = o; o += align256(sizeof(int) * m.max_slots);
+  m.off_cw_b = o; o += align256(sizeof(float) * (size_t)m.max_slots * N);
   m.off_x = o;
   m.xw = gemv_workspace_layout(N, L->hidden, 0, 0, 1);
   o += m.xw.off_counters;   // header, exps, flags, hi, lo
@@ -79,65 +89,15 @@ static int check_moe(const bws_moe_layer* L, int N, int topk, const char* name) 
   return BWS_OK;
 }
 
-// Enqueues the six kernels. out_mode: kEpiStoreBF16 (y bf16) or kEpiResidF32
-// (y fp32 accumulated into). x_prepped: activations already prepared in the
-// workspace's x block by the caller (the decode stream), so prep x is skipped.
-int enqueue_moe(const bws_moe_layer* L, const int32_t* ids, const float* route_w, int N, int topk,
-                const uint16_t* x, void* y, int out_mode, void* ws, cudaStream_t st, const XPrep* x_prepped,
-                const char* name) {
+// gate/up, prep h and down of one MoE layer for the slots of the given slot
+// table: ys[slot][tok] = W_down h (FP32) in the workspace.
+int enqueue_moe_experts(const bws_moe_layer* L, int N, int topk, const int* n_slots, const int* slot_expert,
+                        const XPrep& xp, char* w, cudaStream_t st, const char* name) {
   const MoeLayout m = moe_layout(L, N, topk);
-  char* w = static_cast<char*>(ws);
-  int* n_slots = reinterpret_cast<int*>(w + m.off_route);
-  int* slot_expert = reinterpret_cast<int*>(w + m.off_slot_expert);
-  float* cw = reinterpret_cast<float*>(w + m.off_cw);
   uint32_t* counters = reinterpret_cast<uint32_t*>(w + m.off_counters);
   float* partials = reinterpret_cast<float*>(w + m.off_partials);
-  const int has_shared = L->shared_gate_up_codes != nullptr ? 1 : 0;
-
-  MoeRoute r = {};
-  r.ids = ids;
-  r.route_w = route_w;
-  r.N = N;
-  r.topk = topk;
-  r.n_experts = L->n_experts;
-  r.has_shared = has_shared;
-  r.max_slots = m.max_slots;
-  r.n_slots = n_slots;
-  r.slot_expert = slot_expert;
-  r.cw = cw;
-  r.status = reinterpret_cast<uint32_t*>(w + m.off_status);
-  cudaError_t e = launch_moe_route(r, st, true);
-  if (e != cudaSuccess) return cuda_status(e, name);
-
-  XPrep xp;
   const int dpx = nseg_of(L->hidden) * 128;
-  if (x_prepped != nullptr) {
-    xp = *x_prepped;
-  } else {
-    char* xb = w + m.off_x;
-    PrepParams q = {};
-    q.mode = kPrepCopy;
-    q.x = x;
-    q.ld = L->hidden;
-    q.N = N;
-    q.d_in = L->hidden;
-    q.d_in_pad = dpx;
-    q.hi = reinterpret_cast<uint16_t*>(xb + m.xw.off_hi);
-    q.lo = reinterpret_cast<uint16_t*>(xb + m.xw.off_lo);
-    q.exp = reinterpret_cast<int*>(xb + m.xw.off_exp);
-    q.flags = reinterpret_cast<uint32_t*>(xb + m.xw.off_flags);
-    q.hdr = reinterpret_cast<uint32_t*>(xb + m.xw.off_hdr);
-    q.zero_ptr = counters;
-    q.zero_words = m.n_tiles;
-    e = launch_prep(q, st, true);
-    if (e != cudaSuccess) return cuda_status(e, name);
-    xp.hi = q.hi;
-    xp.lo = q.lo;
-    xp.exp = q.exp;
-    xp.flags = q.flags;
-    xp.shared = 1;
-  }
-
+  cudaError_t e;
   uint16_t* h = reinterpret_cast<uint16_t*>(w + m.off_h);
   GemvParams p = {};
   p.slots.n_slots = n_slots;
@@ -212,13 +172,98 @@ int enqueue_moe(const bws_moe_layer* L, const int32_t* ids, const float* route_w
   d.out_ld = L->hidden;
   d.out_slot_stride = (size_t)N * L->hidden;
   e = launch_gemv(kFmtMXFP4, kEpiStoreF32, d, st, true);
+  return cuda_status(e, name);
+
+}
+
+// Enqueues the six kernels. out_mode: kEpiStoreBF16 (y bf16) or kEpiResidF32
+// (y fp32 accumulated into). x_prepped: activations already prepared in the
+// workspace's x block by the caller (the decode stream), so prep x is skipped.
+int enqueue_moe(const bws_moe_layer* L, const int32_t* ids, const float* route_w, int N, int topk,
+                const uint16_t* x, void* y, int out_mode, void* ws, cudaStream_t st, const XPrep* x_prepped,
+                const char* name) {
+  const MoeLayout m = moe_layout(L, N, topk);
+  char* w = static_cast<char*>(ws);
+  int* n_slots = reinterpret_cast<int*>(w + m.off_route);
+  int* slot_expert = reinterpret_cast<int*>(w + m.off_slot_expert);
+  float* cw = reinterpret_cast<float*>(w + m.off_cw);
+  uint32_t* counters = reinterpret_cast<uint32_t*>(w + m.off_counters);
+  const int has_shared = L->shared_gate_up_codes != nullptr ? 1 : 0;
+
+  MoeRoute r = {};
+  r.ids = ids;
+  r.route_w = route_w;
+  r.N = N;
+  r.topk = topk;
+  r.n_experts = L->n_experts;
+  r.has_shared = has_shared;
+  r.max_slots = m.max_slots;
+  r.n_slots = n_slots;
+  r.slot_expert = slot_expert;
+  r.cw = cw;
+  r.status = reinterpret_cast<uint32_t*>(w + m.off_status);
+  cudaError_t e = launch_moe_route(r, st, true);
   if (e != cudaSuccess) return cuda_status(e, name);
 
+  XPrep xp;
+  const int dpx = nseg_of(L->hidden) * 128;
+  if (x_prepped != nullptr) {
+    xp = *x_prepped;
+  } else {
+    char* xb = w + m.off_x;
+    PrepParams q = {};
+    q.mode = kPrepCopy;
+    q.x = x;
+    q.ld = L->hidden;
+    q.N = N;
+    q.d_in = L->hidden;
+    q.d_in_pad = dpx;
+    q.hi = reinterpret_cast<uint16_t*>(xb + m.xw.off_hi);
+    q.lo = reinterpret_cast<uint16_t*>(xb + m.xw.off_lo);
+    q.exp = reinterpret_cast<int*>(xb + m.xw.off_exp);
+    q.flags = reinterpret_cast<uint32_t*>(xb + m.xw.off_flags);
+    q.hdr = reinterpret_cast<uint32_t*>(xb + m.xw.off_hdr);
+    q.zero_ptr = counters;
+    q.zero_words = m.n_tiles;
+    e = launch_prep(q, st, true);
+    if (e != cudaSuccess) return cuda_status(e, name);
+    xp.hi = q.hi;
+    xp.lo = q.lo;
+    xp.exp = q.exp;
+    xp.flags = q.flags;
+    xp.shared = 1;
+  }
+
+  const int rc = enqueue_moe_experts(L, N, topk, n_slots, slot_expert, xp, w, st, name);
+  if (rc != BWS_OK) return rc;
+  float* ys = reinterpret_cast<float*>(w + m.off_ys);
   e = launch_moe_combine(ys, cw, n_slots, N, L->hidden, y, out_mode, st, true);
   return cuda_status(e, name);
 }
 
 size_t moe_workspace_bytes(const bws_moe_layer* L, int N, int topk) { return moe_layout(L, N, topk).total; }
+
+MoeStackView moe_stack_view(const bws_moe_layer* L, const int32_t* ids, const float* route_w, int N, int topk,
+                            void* ws, int buffer) {
+  const MoeLayout m = moe_layout(L, N, topk);
+  char* w = static_cast<char*>(ws);
+  MoeStackView v;
+  v.route.ids = ids;
+  v.route.route_w = route_w;
+  v.route.N = N;
+  v.route.topk = topk;
+  v.route.n_experts = L->n_experts;
+  v.route.has_shared = L->shared_gate_up_codes != nullptr ? 1 : 0;
+  v.route.max_slots = m.max_slots;
+  v.route.n_slots = reinterpret_cast<int*>(w + (buffer ? m.off_route_b : m.off_route));
+  v.route.slot_expert = reinterpret_cast<int*>(w + (buffer ? m.off_slot_expert_b : m.off_slot_expert));
+  v.route.cw = reinterpret_cast<float*>(w + (buffer ? m.off_cw_b : m.off_cw));
+  v.route.status = reinterpret_cast<uint32_t*>(w + m.off_status);
+  v.ys = reinterpret_cast<float*>(w + m.off_ys);
+  v.counters = reinterpret_cast<uint32_t*>(w + m.off_counters);
+  v.n_counters = m.n_tiles;
+  return v;
+}
 
 void moe_counter_span(const bws_moe_layer* L, int N, int topk, size_t* offset, int* words) {
   const MoeLayout m = moe_layout(L, N, topk);

@@ -14,6 +14,7 @@
 
 #include "bws_common.cuh"
 #include "bws_internal.h"
+#include "moe_route.cuh"
 
 namespace cg = cooperative_groups;
 
@@ -44,6 +45,41 @@ BWS_DEV void chunk_bf16(const PrepParams& q, int c, const float* rr, const uint4
     w[0] = b.x; w[1] = b.y; w[2] = b.z; w[3] = b.w;
   }
 }
+
+// The previous MoE layer's combine for chunk c of token tok, in slot order,
+// added to r (v: the chunk's residual values, updated). Out of line: its
+// registers stay out of the prep's main path.
+__device__ __noinline__ void combine_chunk(const PrepParams& q, int tok, int c, float (&v)[8], float* rr) {
+  const int ns = __ldg(q.comb_n_slots);
+  float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+  // four slots' loads in flight at a time; slots still added in order
+  for (int s0 = 0; s0 < ns; s0 += 4) {
+    float wt[4];
+    float4 ya[4], yb[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const int sl = s0 + k;
+      wt[k] = sl < ns ? __ldg(q.comb_cw + sl * q.N + tok) : 0.0f;
+      const float4* yp = reinterpret_cast<const float4*>(q.comb_ys + ((size_t)sl * q.N + tok) * q.d_in) + 2 * c;
+      ya[k] = sl < ns ? __ldg(yp) : make_float4(0.f, 0.f, 0.f, 0.f);
+      yb[k] = sl < ns ? __ldg(yp + 1) : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      if (wt[k] == 0.0f) continue;
+      const float y8[8] = {ya[k].x, ya[k].y, ya[k].z, ya[k].w, yb[k].x, yb[k].y, yb[k].z, yb[k].w};
+#pragma unroll
+      for (int i = 0; i < 8; ++i) acc[i] = __fmaf_rn(wt[k], y8[i], acc[i]);
+    }
+  }
+#pragma unroll
+  for (int i = 0; i < 8; ++i) v[i] = __fadd_rn(v[i], acc[i]);
+  reinterpret_cast<float4*>(rr)[2 * c] = make_float4(v[0], v[1], v[2], v[3]);
+  reinterpret_cast<float4*>(rr)[2 * c + 1] = make_float4(v[4], v[5], v[6], v[7]);
+}
+
+// The routing CTA, out of line for the same reason.
+__device__ __noinline__ void route_cta(const MoeRoute& m) { moe_route_body(m); }
 
 // Sum (or max, or OR) of one value per CTA of the cluster, in rank order,
 // through each CTA's `slot`; every CTA gets the same result.
@@ -80,13 +116,19 @@ BWS_DEV float cluster_combine(float* slot, float v, float* warp_part) {
   return r;
 }
 
-template <int CL, int THREADS>
+// MOE: the instantiation with the routing CTA and the folded combine (the
+// plain one keeps fewer registers, so it fits beside running product CTAs).
+template <int CL, int THREADS, bool MOE>
 __global__ void __launch_bounds__(THREADS) prep_kernel(const __grid_constant__ PrepParams q) {
   pdl_launch_dependents();
   pdl_wait();
   const int rank = CL == 1 ? 0 : (int)cg::this_cluster().block_rank();
   for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < q.zero_words; i += gridDim.x * blockDim.x)
     q.zero_ptr[i] = 0u;
+  if (MOE && CL == 1 && q.has_route && blockIdx.x == gridDim.x - 1) {   // the routing CTA
+    route_cta(q.route);
+    return;
+  }
   const int row = blockIdx.x / CL;
   const int slot = row / q.N;
   const int tok = row - slot * q.N;
@@ -135,6 +177,7 @@ __global__ void __launch_bounds__(THREADS) prep_kernel(const __grid_constant__ P
         const float4 a = reinterpret_cast<const float4*>(rr)[2 * c];
         const float4 b = reinterpret_cast<const float4*>(rr)[2 * c + 1];
         v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w; v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
+        if (MOE && q.comb_ys != nullptr) combine_chunk(q, tok, c, v, rr);
       }
 #pragma unroll
       for (int i = 0; i < 8; ++i) ss = __fmaf_rn(v[i], v[i], ss);
@@ -211,9 +254,10 @@ __global__ void __launch_bounds__(THREADS) prep_kernel(const __grid_constant__ P
 cudaError_t launch_prep(const PrepParams& q, cudaStream_t st, bool pdl) {
   const int slots = q.n_slots != nullptr ? q.max_slots : 1;
   const bool long_row = q.d_in_pad > kLongRow;
+  if (q.has_route && long_row) return cudaErrorInvalidValue;   // the routing CTA needs one-CTA rows
   const int cl = long_row ? 8 : 1;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((unsigned)(slots * q.N * cl));
+  cfg.gridDim = dim3((unsigned)(slots * q.N * cl + (q.has_route ? 1 : 0)));
   cfg.blockDim = dim3(long_row ? 256 : 1024);
   cfg.stream = st;
   cudaLaunchAttribute a[2];
@@ -232,7 +276,14 @@ cudaError_t launch_prep(const PrepParams& q, cudaStream_t st, bool pdl) {
   }
   cfg.attrs = a;
   cfg.numAttrs = na;
-  return long_row ? cudaLaunchKernelEx(&cfg, prep_kernel<8, 256>, q) : cudaLaunchKernelEx(&cfg, prep_kernel<1, 1024>, q);
+  const bool moe = q.has_route || q.comb_ys != nullptr;
+  if (long_row)
+    return moe ? cudaLaunchKernelEx(&cfg, prep_kernel<8, 256, true>, q) : cudaLaunchKernelEx(&cfg, prep_kernel<8, 256, false>, q);
+  if (moe) {
+    cfg.blockDim = dim3(512);   // fits beside a running product CTA despite its registers
+    return cudaLaunchKernelEx(&cfg, prep_kernel<1, 512, true>, q);
+  }
+  return cudaLaunchKernelEx(&cfg, prep_kernel<1, 1024, false>, q);
 }
 
 }  // namespace bws

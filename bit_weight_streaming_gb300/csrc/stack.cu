@@ -82,8 +82,11 @@ XPrep xprep_of(const Ctx& c, size_t block, const GemvWorkspace& L) {
 }
 
 // prep into a block; zeroes `zero_words` counters at zero_ptr
+// comb: the previous MoE layer's combine, folded into this RMSNorm prep;
+// route: this MoE layer's routing, done by one extra CTA of this prep.
 cudaError_t prep(const Ctx& c, int mode, const uint16_t* x, int ld, const uint16_t* x0, int d_in, size_t block,
-                 const GemvWorkspace& L, uint32_t* zero_ptr, int zero_words, int interleave = 0) {
+                 const GemvWorkspace& L, uint32_t* zero_ptr, int zero_words, int interleave = 0,
+                 const MoeStackView* comb = nullptr, const MoeRoute* route = nullptr) {
   PrepParams q = {};
   q.mode = mode;
   q.x = x;
@@ -104,6 +107,15 @@ cudaError_t prep(const Ctx& c, int mode, const uint16_t* x, int ld, const uint16
   q.zero_ptr = zero_ptr;
   q.zero_words = zero_words;
   q.interleave = interleave;
+  if (comb != nullptr) {
+    q.comb_ys = comb->ys;
+    q.comb_cw = comb->route.cw;
+    q.comb_n_slots = comb->route.n_slots;
+  }
+  if (route != nullptr) {
+    q.has_route = 1;
+    q.route = *route;
+  }
   return launch_prep(q, c.st, true);
 }
 
@@ -165,6 +177,11 @@ int enqueue_step(const bws_stack_plan* P, const uint16_t* x0, float* logits, voi
   const XPrep xh = xprep_of(c, P->off_hp, P->hw);
   const int H = P->hidden;
   const uint16_t* init = x0;   // the first RMSNorm also sets r = x0
+  // an MoE layer's combine is folded into the next RMSNorm prep; its route
+  // buffers alternate between consecutive MoE layers
+  MoeStackView pend_v;
+  const MoeStackView* pending = nullptr;
+  int moe_buf = 0;
   cudaError_t e = cudaSuccess;
 #define BWS_TRY(call)                          \
   do {                                         \
@@ -178,8 +195,9 @@ int enqueue_step(const bws_stack_plan* P, const uint16_t* x0, float* logits, voi
       for (int i = 0; i < L.n_mixer_in; ++i) sum_out += L.mixer_in[i].d_out;
       const GemvParams pin = product_params(c, L.mixer_in, L.n_mixer_in, kEpiStoreBF16, H, xa, u, sum_out);
       BWS_TRY(prep(c, kPrepRmsNorm, nullptr, 0, init, H, P->off_xp, P->xw, counters,
-                   tiles_for(L.mixer_in, L.n_mixer_in, kEpiStoreBF16), layout_for(L.mixer_in, pin)));
+                   tiles_for(L.mixer_in, L.n_mixer_in, kEpiStoreBF16), layout_for(L.mixer_in, pin), pending));
       init = nullptr;
+      pending = nullptr;
       BWS_TRY(product(c, L.mixer_in, L.n_mixer_in, kEpiStoreBF16, pin));
       const int dv = L.mixer_out.d_in;
       const GemvParams pout = product_params(c, &L.mixer_out, 1, kEpiResidF32, dv, xv, r, H);
@@ -191,8 +209,9 @@ int enqueue_step(const bws_stack_plan* P, const uint16_t* x0, float* logits, voi
       const bws_matrix gu[2] = {L.gate, L.up};
       const GemvParams pgu = product_params(c, gu, 2, kEpiSwiGLU, H, xa, h, L.gate.d_out);
       BWS_TRY(prep(c, kPrepRmsNorm, nullptr, 0, init, H, P->off_xp, P->xw, counters, tiles_for(gu, 2, kEpiSwiGLU),
-                   layout_for(gu, pgu)));
+                   layout_for(gu, pgu), pending));
       init = nullptr;
+      pending = nullptr;
       BWS_TRY(product(c, gu, 2, kEpiSwiGLU, pgu));
       const int I = L.down.d_in;
       const GemvParams pdn = product_params(c, &L.down, 1, kEpiResidF32, I, xh, r, H);
@@ -201,20 +220,21 @@ int enqueue_step(const bws_stack_plan* P, const uint16_t* x0, float* logits, voi
       BWS_TRY(product(c, &L.down, 1, kEpiResidF32, pdn));
     }
     if (L.kind == BWS_LAYER_MOE) {
-      size_t coff;
-      int cwords;
-      moe_counter_span(&L.moe, P->N, L.topk, &coff, &cwords);
-      BWS_TRY(prep(c, kPrepRmsNorm, nullptr, 0, init, H, P->off_xp, P->xw,
-                   reinterpret_cast<uint32_t*>(c.w + P->off_moe + coff), cwords));
+      const MoeStackView v = moe_stack_view(&L.moe, L.ids, L.route_w, P->N, L.topk, c.w + P->off_moe, moe_buf);
+      BWS_TRY(prep(c, kPrepRmsNorm, nullptr, 0, init, H, P->off_xp, P->xw, v.counters, v.n_counters, 0, pending,
+                   &v.route));
       init = nullptr;
-      const int rc = enqueue_moe(&L.moe, L.ids, L.route_w, P->N, L.topk, nullptr, r, kEpiResidF32,
-                                 c.w + P->off_moe, st, &xa, name);
+      const int rc = enqueue_moe_experts(&L.moe, P->N, L.topk, v.route.n_slots, v.route.slot_expert, xa,
+                                         c.w + P->off_moe, st, name);
       if (rc != BWS_OK) return rc;
+      pend_v = v;
+      pending = &pend_v;
+      moe_buf ^= 1;
     }
   }
   const GemvParams ph = product_params(c, &P->head, 1, kEpiStoreF32, H, xa, logits, P->head.d_out);
   BWS_TRY(prep(c, kPrepRmsNorm, nullptr, 0, init, H, P->off_xp, P->xw, counters, tiles_for(&P->head, 1, kEpiStoreF32),
-               layout_for(&P->head, ph)));
+               layout_for(&P->head, ph), pending));
   BWS_TRY(product(c, &P->head, 1, kEpiStoreF32, ph));
 #undef BWS_TRY
   return BWS_OK;
@@ -289,7 +309,7 @@ int bws_decode_step_plan_create(const bws_stack* S, int N, bws_stack_plan** plan
       if (!L.ids || !L.route_w) return bad(fail(BWS_ERR_INVALID_ARG, "%s: layer %d: null routing", name, li));
       const size_t b = moe_workspace_bytes(&L.moe, N, L.topk);
       moe_bytes = b > moe_bytes ? b : moe_bytes;
-      P->kernels += 6;
+      P->kernels += 4;
     } else if (L.kind != BWS_LAYER_MIXER_MLP) {
       return bad(fail(BWS_ERR_INVALID_ARG, "%s: layer %d: unknown kind %d", name, li, L.kind));
     }

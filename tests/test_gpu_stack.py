@@ -88,7 +88,7 @@ def test_moe_stack_parity():
                                     dense_inter=384, quant=oracle_quantizers(device()), device=device())
         head = W.make_matrix(3, (900, 256), 4, 7, oracle_quantizers(device()), device())
         stack = bws().stack.DecodeStack(256, layers, head, N, device=device())
-        assert stack.kernel_count == 4 + 2 * 6 + 2
+        assert stack.kernel_count == 4 + 2 * 4 + 2
         _check(stack, N, seed=10 + N)
 
 
