@@ -346,12 +346,12 @@ def run_gpu(args):
         dist.destroy_process_group()
 
 
-def run_moe(args, dev, stream):
+def run_moe(args, dev, stream, tokens=(1, 4)):
     import torch
     from bit_weight_streaming_gb300 import workloads as W
     import synth
     out = {}
-    for N in (1, 4):
+    for N in tokens:
         t0 = time.time()
         with torch.cuda.stream(stream):
             st = W.moe_ling(N, seed=args.seed, device=dev)
@@ -444,6 +444,18 @@ def run_product_only(args):
                       "us_per_call": round(t * 1e6, 2), "GB/s": round(nb / t / 1e9, 1)}), flush=True)
 
 
+def run_moe_only(args):
+    """The MoE step alone at --tokens N (a short workload for profiler launch
+    lists): one JSON line with its timing."""
+    import torch
+    import __graft_entry__ as g
+    g.build()
+    dev = torch.device("cuda", 0)
+    stream = torch.cuda.Stream(dev)
+    out = run_moe(args, dev, stream, tokens=(args.tokens,))
+    print(json.dumps({"moe_only": out}), flush=True)
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
@@ -453,6 +465,7 @@ def main(argv=None):
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-moe", action="store_true")
     ap.add_argument("--product", default=None, help="ROWSxCOLS: time one NVFP4 product only (profiling)")
+    ap.add_argument("--moe-only", action="store_true", help="time the MoE step alone at --tokens N (profiling)")
     ap.add_argument("--tokens", type=int, default=1)
     ap.add_argument("--copies", type=int, default=4, help="--product: distinct weight copies to rotate")
     args = ap.parse_args(argv)
@@ -460,6 +473,8 @@ def main(argv=None):
         args.warmup = 3
     if args.product:
         run_product_only(args)
+    elif args.moe_only:
+        run_moe_only(args)
     elif args.impl == "reference":
         run_reference(args)
     else:
