@@ -27,6 +27,8 @@ struct MoeStackView {
 };
 MoeStackView moe_stack_view(const bws_moe_layer* L, const int32_t* ids, const float* route_w, int N, int topk,
                             void* ws, int buffer);
+// Activation layout the layer's gate/up kernel reads (PrepParams::interleave).
+int moe_x_layout(const bws_moe_layer* L, int N);
 // gate/up, prep h and down for the slots of a slot table (activations xp).
 int enqueue_moe_experts(const bws_moe_layer* L, int N, int topk, const int* n_slots, const int* slot_expert,
                         const XPrep& xp, char* w, cudaStream_t st, const char* name);

@@ -64,6 +64,15 @@ BWS_DEV float4 ld_cg_f4(const float4* p) {
 BWS_DEV void cp_async16(uint32_t smem_addr, const void* g) {
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" :: "r"(smem_addr), "l"(g) : "memory");
 }
+// 8 bytes global -> shared, asynchronously; src_bytes 0 writes zeros and reads nothing.
+BWS_DEV void cp_async8_zfill(uint32_t smem_addr, const void* g, uint32_t src_bytes) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 8, %2;" :: "r"(smem_addr), "l"(g), "r"(src_bytes) : "memory");
+}
+// One arrival on the mbarrier once every earlier cp.async of this thread has
+// landed (counted in the barrier's expected arrivals: no pending increment).
+BWS_DEV void cp_async_mbar_arrive(uint32_t bar) {
+  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" :: "r"(bar) : "memory");
+}
 BWS_DEV void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 template <int N>
 BWS_DEV void cp_async_wait() { asm volatile("cp.async.wait_group %0;" :: "n"(N) : "memory"); }
@@ -107,6 +116,12 @@ BWS_DEV void tma_load_2d(uint32_t dst, const void* tmap, int x, int y, uint32_t 
       "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];"
       :: "r"(dst), "l"(tmap), "r"(x), "r"(y), "r"(bar) : "memory");
 }
+// 3D tiled TMA load of box (x, y, z) into shared memory, completing on bar.
+BWS_DEV void tma_load_3d(uint32_t dst, const void* tmap, int x, int y, int z, uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], [%5];"
+      :: "r"(dst), "l"(tmap), "r"(x), "r"(y), "r"(z), "r"(bar) : "memory");
+}
 // 1D bulk copy global -> shared (16-byte aligned, size % 16 == 0).
 BWS_DEV void bulk_load(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
   asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
@@ -122,6 +137,11 @@ BWS_DEV void tma_prefetch_desc(const void* tmap) {
 }
 BWS_DEV void named_bar_sync(int id, int threads) {
   asm volatile("bar.sync %0, %1;" :: "r"(id), "r"(threads) : "memory");
+}
+BWS_DEV uint32_t lds_u8(uint32_t addr) {
+  unsigned short v;
+  asm volatile("ld.shared.u8 %0, [%1];" : "=h"(v) : "r"(addr));
+  return v;
 }
 BWS_DEV uint32_t lds_u16(uint32_t addr) {
   unsigned short v;

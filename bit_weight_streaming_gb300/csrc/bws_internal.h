@@ -80,6 +80,7 @@ struct GemvParams {
   float* partials;         // [(n_tiles + warps) * kSlotFloats]
   uint32_t* counters;      // [n_tiles], zero on entry, left zero on exit
   int prefetch_units;      // units pulled into L2 before waiting on the inputs
+  size_t partials_bytes;   // slot mode: size of the partials scratch (0: the plain-mode size)
 };
 
 // MoE helpers.
@@ -146,6 +147,16 @@ bool gemv_tma_eligible(int fmt, const GemvParams& p);
 // Activation layout the TMA kernel reads for this format (PrepParams::interleave).
 inline int tma_interleave(int fmt) { return fmt == kFmtFP8 ? 128 : 256; }
 cudaError_t launch_gemv_tma(int fmt, int epi, const GemvParams& p, uint32_t* status, cudaStream_t st, bool pdl);
+// The TMA-fed MXFP4 expert kernel (gemv_tma_moe.cu) for slot-mode products
+// with d_in % 256 == 0 and 16-byte aligned expert tensors and strides; its
+// activations are prepared with the 256-weight TMA layout.
+bool moe_tma_shape_ok(const uint8_t* codes, size_t codes_stride, const uint8_t* shared_codes, const uint8_t* scales,
+                      size_t scales_stride, const uint8_t* shared_scales, int d_in, int N);
+bool moe_tma_eligible(int epi, const GemvParams& p);
+// Partial-sum scratch (bytes) the TMA expert kernel needs for max_slots slots of rows rows.
+size_t moe_tma_partials_bytes(int epi, int rows, int max_slots);
+int moe_tma_tiles_per_slot(int epi, int rows);
+cudaError_t launch_gemv_tma_moe(int epi, const GemvParams& p, uint32_t* status, cudaStream_t st, bool pdl);
 // Product with the best kernel for its shape.
 inline cudaError_t launch_product(int fmt, int epi, const GemvParams& p, uint32_t* status, cudaStream_t st,
                                   bool pdl) {

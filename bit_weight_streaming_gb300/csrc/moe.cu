@@ -34,7 +34,7 @@ struct MoeLayout {
   size_t off_h;
   GemvWorkspace hw;   // offsets relative to off_hp (prep part only)
   size_t off_hp;
-  size_t off_ys, off_counters, off_partials, total;
+  size_t off_ys, off_counters, off_partials, partials_bytes, total;
 };
 
 static MoeLayout moe_layout(const bws_moe_layer* L, int N, int topk) {
@@ -61,7 +61,14 @@ static MoeLayout moe_layout(const bws_moe_layer* L, int N, int topk) {
   o += m.hw.off_counters;
   m.off_ys = o; o += align256(sizeof(float) * (size_t)m.max_slots * N * L->hidden);
   m.off_counters = o; o += align256(sizeof(uint32_t) * (size_t)m.n_tiles);
-  m.off_partials = o; o += align256(sizeof(float) * kSlotFloats * ((size_t)m.n_tiles + gemv_max_warps()));
+  // partial sums of either expert kernel
+  m.partials_bytes = sizeof(float) * kSlotFloats * ((size_t)m.n_tiles + gemv_max_warps());
+  const size_t pt = moe_tma_partials_bytes(kEpiSwiGLU, L->inter, m.max_slots) >
+                            moe_tma_partials_bytes(kEpiStoreF32, L->hidden, m.max_slots)
+                        ? moe_tma_partials_bytes(kEpiSwiGLU, L->inter, m.max_slots)
+                        : moe_tma_partials_bytes(kEpiStoreF32, L->hidden, m.max_slots);
+  if (pt > m.partials_bytes) m.partials_bytes = pt;
+  m.off_partials = o; o += align256(m.partials_bytes);
   m.total = o;
   return m;
 }
@@ -125,7 +132,13 @@ int enqueue_moe_experts(const bws_moe_layer* L, int N, int topk, const int* n_sl
   p.out_slot_stride = (size_t)N * L->inter;
   p.counters = counters;
   p.partials = partials;
-  e = launch_gemv(kFmtMXFP4, kEpiSwiGLU, p, st, true);
+  p.partials_bytes = m.partials_bytes;
+  uint32_t* status = reinterpret_cast<uint32_t*>(w + m.off_status);
+  // the TMA expert kernel when the shapes allow (the caller prepared x in its
+  // layout, moe_x_layout), else the first kernel
+  const bool tma_gu = moe_x_layout(L, N) != 0;
+  if (tma_gu && !moe_tma_eligible(kEpiSwiGLU, p)) return fail(BWS_ERR_WORKSPACE, "%s: expert kernel scratch too small", name);
+  e = tma_gu ? launch_gemv_tma_moe(kEpiSwiGLU, p, status, st, true) : launch_gemv(kFmtMXFP4, kEpiSwiGLU, p, st, true);
   if (e != cudaSuccess) return cuda_status(e, name);
 
   char* hb = w + m.off_hp;
@@ -145,10 +158,6 @@ int enqueue_moe_experts(const bws_moe_layer* L, int N, int topk, const int* n_sl
   q.flags = reinterpret_cast<uint32_t*>(hb + m.hw.off_flags);
   q.zero_ptr = counters;
   q.zero_words = m.n_tiles;
-  e = launch_prep(q, st, true);
-  if (e != cudaSuccess) return cuda_status(e, name);
-
-  float* ys = reinterpret_cast<float*>(w + m.off_ys);
   GemvParams d = p;
   d.slots.codes = L->down_codes;
   d.slots.codes_stride = L->down_codes_stride;
@@ -168,10 +177,14 @@ int enqueue_moe_experts(const bws_moe_layer* L, int N, int topk, const int* n_sl
   d.x.exp = q.exp;
   d.x.flags = q.flags;
   d.x.shared = 0;
-  d.out = ys;
+  d.out = reinterpret_cast<float*>(w + m.off_ys);
   d.out_ld = L->hidden;
   d.out_slot_stride = (size_t)N * L->hidden;
-  e = launch_gemv(kFmtMXFP4, kEpiStoreF32, d, st, true);
+  const bool tma_dn = moe_tma_eligible(kEpiStoreF32, d);
+  q.interleave = tma_dn ? 256 : 0;
+  e = launch_prep(q, st, true);
+  if (e != cudaSuccess) return cuda_status(e, name);
+  e = tma_dn ? launch_gemv_tma_moe(kEpiStoreF32, d, status, st, true) : launch_gemv(kFmtMXFP4, kEpiStoreF32, d, st, true);
   return cuda_status(e, name);
 
 }
@@ -225,6 +238,7 @@ int enqueue_moe(const bws_moe_layer* L, const int32_t* ids, const float* route_w
     q.hdr = reinterpret_cast<uint32_t*>(xb + m.xw.off_hdr);
     q.zero_ptr = counters;
     q.zero_words = m.n_tiles;
+    q.interleave = moe_x_layout(L, N);
     e = launch_prep(q, st, true);
     if (e != cudaSuccess) return cuda_status(e, name);
     xp.hi = q.hi;
@@ -242,6 +256,13 @@ int enqueue_moe(const bws_moe_layer* L, const int32_t* ids, const float* route_w
 }
 
 size_t moe_workspace_bytes(const bws_moe_layer* L, int N, int topk) { return moe_layout(L, N, topk).total; }
+
+int moe_x_layout(const bws_moe_layer* L, int N) {
+  return moe_tma_shape_ok(L->gate_up_codes, L->gate_up_codes_stride, L->shared_gate_up_codes, L->gate_up_scales,
+                          L->gate_up_scales_stride, L->shared_gate_up_scales, L->hidden, N)
+             ? 256
+             : 0;
+}
 
 MoeStackView moe_stack_view(const bws_moe_layer* L, const int32_t* ids, const float* route_w, int N, int topk,
                             void* ws, int buffer) {

@@ -52,20 +52,22 @@ BWS_DEV void chunk_bf16(const PrepParams& q, int c, const float* rr, const uint4
 __device__ __noinline__ void combine_chunk(const PrepParams& q, int tok, int c, float (&v)[8], float* rr) {
   const int ns = __ldg(q.comb_n_slots);
   float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-  // four slots' loads in flight at a time; slots still added in order
-  for (int s0 = 0; s0 < ns; s0 += 4) {
-    float wt[4];
-    float4 ya[4], yb[4];
+  // eight slots' loads in flight at a time, none for a slot the token does
+  // not use (weight 0); slots still added in order
+  constexpr int kB = 8;
+  for (int s0 = 0; s0 < ns; s0 += kB) {
+    float wt[kB];
 #pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      const int sl = s0 + k;
-      wt[k] = sl < ns ? __ldg(q.comb_cw + sl * q.N + tok) : 0.0f;
-      const float4* yp = reinterpret_cast<const float4*>(q.comb_ys + ((size_t)sl * q.N + tok) * q.d_in) + 2 * c;
-      ya[k] = sl < ns ? __ldg(yp) : make_float4(0.f, 0.f, 0.f, 0.f);
-      yb[k] = sl < ns ? __ldg(yp + 1) : make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int k = 0; k < kB; ++k) wt[k] = s0 + k < ns ? __ldg(q.comb_cw + (s0 + k) * q.N + tok) : 0.0f;
+    float4 ya[kB], yb[kB];
+#pragma unroll
+    for (int k = 0; k < kB; ++k) {
+      const float4* yp = reinterpret_cast<const float4*>(q.comb_ys + ((size_t)(s0 + k) * q.N + tok) * q.d_in) + 2 * c;
+      ya[k] = wt[k] != 0.0f ? __ldg(yp) : make_float4(0.f, 0.f, 0.f, 0.f);
+      yb[k] = wt[k] != 0.0f ? __ldg(yp + 1) : make_float4(0.f, 0.f, 0.f, 0.f);
     }
 #pragma unroll
-    for (int k = 0; k < 4; ++k) {
+    for (int k = 0; k < kB; ++k) {
       if (wt[k] == 0.0f) continue;
       const float y8[8] = {ya[k].x, ya[k].y, ya[k].z, ya[k].w, yb[k].x, yb[k].y, yb[k].z, yb[k].w};
 #pragma unroll

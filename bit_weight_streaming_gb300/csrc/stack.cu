@@ -221,8 +221,8 @@ int enqueue_step(const bws_stack_plan* P, const uint16_t* x0, float* logits, voi
     }
     if (L.kind == BWS_LAYER_MOE) {
       const MoeStackView v = moe_stack_view(&L.moe, L.ids, L.route_w, P->N, L.topk, c.w + P->off_moe, moe_buf);
-      BWS_TRY(prep(c, kPrepRmsNorm, nullptr, 0, init, H, P->off_xp, P->xw, v.counters, v.n_counters, 0, pending,
-                   &v.route));
+      BWS_TRY(prep(c, kPrepRmsNorm, nullptr, 0, init, H, P->off_xp, P->xw, v.counters, v.n_counters,
+                   moe_x_layout(&L.moe, P->N), pending, &v.route));
       init = nullptr;
       const int rc = enqueue_moe_experts(&L.moe, P->N, L.topk, v.route.n_slots, v.route.slot_expert, xa,
                                          c.w + P->off_moe, st, name);

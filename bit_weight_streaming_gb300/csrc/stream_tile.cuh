@@ -117,5 +117,9 @@ BWS_DEV void sub_mma_n1(float (&y)[4], float (&yl)[4], const uint32_t (&w0)[4], 
 // swizzle or none). False if the driver entry point is missing or refuses.
 bool encode_2d(CUtensorMap* m, const void* base, uint64_t inner_bytes, uint64_t rows, uint32_t box_inner,
                uint32_t box_rows, bool swizzle);
+// A 3D u8 tensor map [n][rows][inner_bytes] (byte stride stride2 between the
+// n planes) with box {box_inner, box_rows, 1} and 128-byte swizzle.
+bool encode_3d(CUtensorMap* m, const void* base, uint64_t inner_bytes, uint64_t rows, uint64_t n,
+               uint64_t stride2, uint32_t box_inner, uint32_t box_rows);
 
 }  // namespace bws

@@ -123,6 +123,21 @@ def test_moe_small(N):
 
 
 @pytest.mark.gpu
+@pytest.mark.parametrize("N,hidden,inter", [(1, 512, 256), (3, 512, 256), (8, 512, 256), (2, 256, 96),
+                                            (1, 768, 512), (5, 1024, 768)])
+def test_moe_stream_shapes(N, hidden, inter):
+    """Shapes that take the TMA expert kernels (hidden and, for down, the
+    intermediate size a multiple of 256), with several tiles per slot, a
+    ragged last gate/up tile, and fewer units than CTAs."""
+    E, topk = 24, 4
+    layer_w, expert = _build(E, hidden, inter, seed=hidden + inter, with_shared=True)
+    ids = synth.expert_ids(N, topk, E, seed=40 + N)
+    rw = synth.route_weights(N, topk, seed=40 + N)
+    x = synth.activation_bf16(N, hidden, seed=40 + N, device=device())
+    _check_moe(layer_w, expert, ids, rw, x, with_shared=True)
+
+
+@pytest.mark.gpu
 def test_moe_no_shared_and_bad_id():
     E, hidden, inter, topk = 12, 320, 96, 3
     layer_w, expert = _build(E, hidden, inter, seed=5, with_shared=False)
