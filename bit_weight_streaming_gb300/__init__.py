@@ -29,3 +29,4 @@ from . import stack, workloads  # noqa: F401,E402
 
 BWS_STATUS_X_TWO_BANDS = 1
 BWS_STATUS_X_FLUSHED = 2
+BWS_STATUS_X_ROUNDED = 8

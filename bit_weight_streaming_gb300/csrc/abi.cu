@@ -86,7 +86,7 @@ int run_product(int fmt, int epi, GemvParams& p, const uint16_t* x, int N, int d
   p.out_ld = out_ld;
   p.out_slot_stride = 0;
   p.prefetch_units = fmt == kFmtFP8 ? 4 : 8;
-  q.interleave = gemv_tma_eligible(fmt, p) ? tma_interleave(fmt) : 0;   // the layout its product reads
+  q.interleave = product_layout(fmt, p);   // the layout its product reads
   cudaError_t e = launch_prep(q, st, true);
   if (e != cudaSuccess) return cuda_status(e, name);
   e = launch_product(fmt, epi, p, q.hdr + 1, st, true);

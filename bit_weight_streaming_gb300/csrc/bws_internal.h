@@ -117,8 +117,9 @@ struct PrepParams {
   uint32_t* status_clear;  // two words zeroed by the prep (the call's status words), may be null
   uint32_t* zero_ptr;      // counters of the next product, zeroed
   int zero_words;
-  int interleave;          // 0: linear rows; else the unit size in k (256 NVFP4, 128 FP8) of
-                           // the TMA kernel's layout (see gemv_tma.cu)
+  int interleave;          // 0: linear rows; kLayoutImage: the tensor-core kernel's E4M3 band
+                           // image (one token); else the unit size in k (256 NVFP4, 128 FP8)
+                           // of the TMA kernel's layout (see gemv_tma.cu)
   // kPrepRmsNorm, optional (comb_ys != nullptr): the previous MoE layer's
   // combine first, r[tok] += sum over live slots s, in slot order, of
   // comb_cw[s][tok] * comb_ys[s][tok][:]
@@ -144,8 +145,24 @@ cudaError_t launch_gemv(int fmt, int epi, const GemvParams& p, cudaStream_t st, 
 // The TMA-fed product kernel (gemv_tma.cu) for plain-mode NVFP4 (d_in % 256
 // == 0) and FP8 (d_in % 128 == 0) products with 16-byte aligned tensors.
 bool gemv_tma_eligible(int fmt, const GemvParams& p);
+// Tiles of 128 rows (SwiGLU: 64 gate + 64 up rows) of the TMA kernels.
+int gemv_tma_tiles(int epi, const GemvMat* mats, int n_mats);
 // Activation layout the TMA kernel reads for this format (PrepParams::interleave).
 inline int tma_interleave(int fmt) { return fmt == kFmtFP8 ? 128 : 256; }
+// PrepParams::interleave for the tensor-core kernel: one token's E4M3 band
+// image (gemv_umma.cu), written over the token's two f16 band rows.
+constexpr int kLayoutImage = -1;
+// The tensor-core product (gemv_umma.cu): one-token NVFP4, d_in % 256 == 0,
+// codes 32-byte and scales 16-byte aligned, taken when the environment sets
+// BWS_PRODUCT_KERNEL=tcgen05 (opt-in: it streams slower than the mma.sync
+// kernel, see gemv_umma.cu).
+bool gemv_umma_eligible(int fmt, const GemvParams& p);
+cudaError_t launch_gemv_umma(int epi, const GemvParams& p, uint32_t* status, cudaStream_t st, bool pdl);
+// The activation layout the product of p reads (PrepParams::interleave).
+inline int product_layout(int fmt, const GemvParams& p) {
+  if (gemv_umma_eligible(fmt, p)) return kLayoutImage;
+  return gemv_tma_eligible(fmt, p) ? tma_interleave(fmt) : 0;
+}
 cudaError_t launch_gemv_tma(int fmt, int epi, const GemvParams& p, uint32_t* status, cudaStream_t st, bool pdl);
 // The TMA-fed MXFP4 expert kernel (gemv_tma_moe.cu) for slot-mode products
 // with d_in % 256 == 0 and 16-byte aligned expert tensors and strides; its
@@ -160,6 +177,7 @@ cudaError_t launch_gemv_tma_moe(int epi, const GemvParams& p, uint32_t* status, 
 // Product with the best kernel for its shape.
 inline cudaError_t launch_product(int fmt, int epi, const GemvParams& p, uint32_t* status, cudaStream_t st,
                                   bool pdl) {
+  if (gemv_umma_eligible(fmt, p)) return launch_gemv_umma(epi, p, status, st, pdl);
   return gemv_tma_eligible(fmt, p) ? launch_gemv_tma(fmt, epi, p, status, st, pdl) : launch_gemv(fmt, epi, p, st, pdl);
 }
 

@@ -118,6 +118,57 @@ BWS_DEV float cluster_combine(float* slot, float v, float* warp_part) {
   return r;
 }
 
+// E4M3 code of a (RN) and its value.
+BWS_DEV uint32_t e4m3_code(float a, float& dec) {
+  const uint32_t c = f32x2_to_e4m3x2(0.0f, a) & 0xFFu;
+  dec = e4m3_to_f32(c);
+  return c;
+}
+
+// The tensor-core kernel's activation image of one token (gemv_umma.cu):
+// a = x * 2^(7-E) splits into E4M3 bands, a = hi0 + lo0 for |a| >= 2^-2,
+// a = 2^-10 (hi1 + lo1) below (exact down to |a| = 2^-12, rounded under
+// that, flag 8). Per 256-value unit 2 KB: MMA kk (blocks 2kk, 2kk+1) owns
+// bytes [256kk, 256kk + 256), two 8-row x 16-byte core matrices (K chunk 0
+// then 1); rows 0-3 of the first hold block 2kk's bands (hi0, lo0, hi1, lo1),
+// rows 4-7 of the second block 2kk+1's, the other rows are zero. Out of
+// line: its registers stay out of the prep's main path. Returns the flags.
+__device__ __noinline__ uint32_t image_chunks(const PrepParams& q, int c0, int c1, const float* rr, const uint4* xr,
+                                              float inv_rms, int E) {
+  uint8_t* img = reinterpret_cast<uint8_t*>(q.hi);
+  uint32_t flags = 0u;
+  for (int c = c0 + threadIdx.x; c < c1; c += blockDim.x) {
+    uint32_t w[4];
+    chunk_bf16(q, c, rr, xr, inv_rms, w);
+    uint32_t band[4][2] = {{0u, 0u}, {0u, 0u}, {0u, 0u}, {0u, 0u}};
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const float f = bf16_bits_to_f32(i & 1 ? (w[i >> 1] >> 16) : (w[i >> 1] & 0xFFFFu));
+      const float a = ldexp_exact(f, 7 - E);
+      const int pair = fabsf(a) >= 0.25f ? 0 : 1;
+      const float b = pair == 0 ? a : ldexp_exact(a, 10);
+      float dh, dl;
+      const uint32_t h = e4m3_code(b, dh);
+      const float rest = __fsub_rn(b, dh);
+      const uint32_t l = e4m3_code(rest, dl);
+      if (dl != rest) flags |= 8u;
+      band[2 * pair][i >> 2] |= h << (8 * (i & 3));
+      band[2 * pair + 1][i >> 2] |= l << (8 * (i & 3));
+    }
+    const int u = c >> 5, j = (c >> 1) & 15, half = c & 1;
+    uint8_t* unit = img + (size_t)u * 2048;
+    uint8_t* piece = unit + 256 * (j >> 1) + (j & 1) * 192 + half * 8;
+#pragma unroll
+    for (int k = 0; k < 4; ++k) *reinterpret_cast<uint2*>(piece + 16 * k) = make_uint2(band[k][0], band[k][1]);
+    if ((j & 1) == 0) {
+      uint4* z = reinterpret_cast<uint4*>(unit + 256 * (j >> 1) + 64 + 64 * half);
+#pragma unroll
+      for (int k = 0; k < 4; ++k) z[k] = make_uint4(0, 0, 0, 0);
+    }
+  }
+  return flags;
+}
+
 // MOE: the instantiation with the routing CTA and the folded combine (the
 // plain one keeps fewer registers, so it fits beside running product CTAs).
 template <int CL, int THREADS, bool MOE>
@@ -148,7 +199,7 @@ __global__ void __launch_bounds__(THREADS) prep_kernel(const __grid_constant__ P
   const int c0 = rank * per < nchunk_pad ? rank * per : nchunk_pad;
   const int c1 = c0 + per < nchunk_pad ? c0 + per : nchunk_pad;
   const size_t rowbase = ((size_t)slot * (q.N + 1)) * q.d_in_pad;
-  if (tok == 0) {   // this slot's all-zero row
+  if (tok == 0 && q.interleave != kLayoutImage) {   // this slot's all-zero row
     uint4* zh = reinterpret_cast<uint4*>(q.hi + rowbase + (size_t)q.N * q.d_in_pad);
     uint4* zl = reinterpret_cast<uint4*>(q.lo + rowbase + (size_t)q.N * q.d_in_pad);
     for (int c = c0 + threadIdx.x; c < c1; c += blockDim.x) {
@@ -200,6 +251,9 @@ __global__ void __launch_bounds__(THREADS) prep_kernel(const __grid_constant__ P
   const float mx = cluster_combine<1, CL, THREADS>(&xch[1], m, warp_part);
   const int E = mx > 0.0f ? floor_log2_abs(mx) : 0;
   uint32_t flags = 0u;
+  if (q.interleave == kLayoutImage) {
+    flags = image_chunks(q, c0, c1, rr, xr, inv_rms, E);
+  } else {
   uint4* hi4 = reinterpret_cast<uint4*>(q.hi + rowbase + (size_t)tok * q.d_in_pad);
   uint4* lo4 = reinterpret_cast<uint4*>(q.lo + rowbase + (size_t)tok * q.d_in_pad);
   // TMA-kernel layout: within each unit of K_u values, the 8-value chunk j of
@@ -242,6 +296,7 @@ __global__ void __launch_bounds__(THREADS) prep_kernel(const __grid_constant__ P
     }
     hi4[dst] = make_uint4(h[0], h[1], h[2], h[3]);
     lo4[dst] = make_uint4(l[0], l[1], l[2], l[3]);
+  }
   }
   const uint32_t f = __float_as_uint(cluster_combine<2, CL, THREADS>(&xch[2], __uint_as_float(flags), warp_part));
   if (rank == 0 && threadIdx.x == 0) {

@@ -156,7 +156,7 @@ GemvParams product_params(const Ctx& c, const bws_matrix* mats, int nm, int epi,
 // The activation layout the product's kernel reads.
 int layout_for(const bws_matrix* mats, const GemvParams& p) {
   const int fmt = fmt_of(mats[0]);
-  return gemv_tma_eligible(fmt, p) ? tma_interleave(fmt) : 0;
+  return product_layout(fmt, p);
 }
 
 cudaError_t product(const Ctx& c, const bws_matrix* mats, int nm, int epi, const GemvParams& p) {

@@ -117,6 +117,12 @@ BWS_DEV void sub_mma_n1(float (&y)[4], float (&yl)[4], const uint32_t (&w0)[4], 
 // swizzle or none). False if the driver entry point is missing or refuses.
 bool encode_2d(CUtensorMap* m, const void* base, uint64_t inner_bytes, uint64_t rows, uint32_t box_inner,
                uint32_t box_rows, bool swizzle);
+// A 2D tensor map of packed E2M1 codes [rows][d_in / 2 bytes] that TMA
+// unpacks on the way into shared memory: each 16 codes (8 bytes) land in a
+// 16-byte slot, the layout the tensor cores read 4-bit operands from. Box
+// {128 codes, box_rows}, 128-byte swizzle; d_in % 128 == 0, base 32-byte
+// aligned, d_in / 2 a multiple of 32.
+bool encode_fp4_2d(CUtensorMap* m, const void* base, uint64_t d_in, uint64_t rows, uint32_t box_rows);
 // A 3D u8 tensor map [n][rows][inner_bytes] (byte stride stride2 between the
 // n planes) with box {box_inner, box_rows, 1} and 128-byte swizzle.
 bool encode_3d(CUtensorMap* m, const void* base, uint64_t inner_bytes, uint64_t rows, uint64_t n,

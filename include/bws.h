@@ -64,6 +64,10 @@ enum bws_status_bits {
   BWS_STATUS_X_TWO_BANDS = 1u,  /* an activation needed the second f16 band  */
   BWS_STATUS_X_FLUSHED = 2u,    /* an activation below 2^-57 of its token's
                                    largest magnitude was treated as zero     */
+  BWS_STATUS_X_ROUNDED = 8u,    /* one-token NVFP4 products on the tensor
+                                   cores: an activation below 2^-19 of its
+                                   token's largest magnitude was rounded to a
+                                   multiple of 2^-26 of that magnitude       */
   BWS_STATUS_WAIT_TIMEOUT = 0x100u /* a bounded device wait ran out: the
                                    results of that call are not valid        */
 };
