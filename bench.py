@@ -192,12 +192,19 @@ def time_steps(fn, steps, warmup, stream):
     return s.elapsed_time(e) / 1e3 / steps
 
 
+# DRAM bytes (read + write) per algorithmic byte of the one-token NVFP4
+# product kernel, from ncu counters on four of the step's matrix shapes
+# (profiles/gemv_tma_nvfp4_traffic_n1.md).
+TRAFFIC_RATIO = 1.036
+
+
 def time_dominant_kernel(stack, stream, reps=3):
-    """Average duration of the NVFP4 weight-stream product on the stack's own
-    matrices (one call per matrix, rotating through all MLP and mixer
-    matrices, so every launch reads cold weights), timed with CUDA events on
-    the launching stream. Each call is the activation prep (one small kernel)
-    plus the product kernel, so the rate is a lower bound for the product."""
+    """Average duration of the NVFP4 product kernel alone, on the stack's own
+    matrices: the activations of each input width are prepared once
+    (bws_nvfp4_prepare, outside the timed launches), then every MLP and
+    mixer matrix runs bws_nvfp4_gemv_prepared once per rep, rotating through
+    all of them (15 GB) so that every launch reads cold weights. CUDA events
+    on the launching stream around each product launch."""
     import torch
     import bit_weight_streaming_gb300 as bws
     mats = []
@@ -205,17 +212,22 @@ def time_dominant_kernel(stack, stream, reps=3):
         for m in [L.get("gate"), L.get("up"), L.get("down")] + list(L.get("mixer_in", [])):
             if m is not None and m.fmt == 1:
                 mats.append(m)
-    xs = {}
-    ws = bws.Workspace(stack.device)
-    ys = {}
+    d_out_max = {}
     for m in mats:
-        if m.d_in not in xs:
-            xs[m.d_in] = torch.randn((1, m.d_in), device=stack.device).to(torch.bfloat16)
-        if m.d_out not in ys:
-            ys[m.d_out] = torch.empty((1, m.d_out), dtype=torch.bfloat16, device=stack.device)
+        d_out_max[m.d_in] = max(d_out_max.get(m.d_in, 0), m.d_out)
+    ys = {m.d_out: torch.empty((1, m.d_out), dtype=torch.bfloat16, device=stack.device) for m in mats}
+    wss = {}
     with torch.cuda.stream(stream):
+        for d_in, dmax in d_out_max.items():
+            wss[d_in] = bws.Workspace(stack.device)
+            x = torch.randn((1, d_in), device=stack.device).to(torch.bfloat16)
+            bws.nvfp4_prepare(x, dmax, wss[d_in])
+
+        def run(m):
+            bws.nvfp4_gemv_prepared(m.codes, m.scales, m.scale32, 1, m.d_in, wss[m.d_in], y=ys[m.d_out])
+
         for m in mats[:8]:   # warm-up
-            bws.nvfp4_gemv(m.codes, m.scales, m.scale32, xs[m.d_in], y=ys[m.d_out], ws=ws)
+            run(m)
         stream.synchronize()
         events = []
         for _ in range(reps):
@@ -223,7 +235,7 @@ def time_dominant_kernel(stack, stream, reps=3):
                 a = torch.cuda.Event(enable_timing=True)
                 b = torch.cuda.Event(enable_timing=True)
                 a.record(stream)
-                bws.nvfp4_gemv(m.codes, m.scales, m.scale32, xs[m.d_in], y=ys[m.d_out], ws=ws)
+                run(m)
                 b.record(stream)
                 events.append((m.nbytes(), a, b))
         stream.synchronize()
@@ -334,8 +346,11 @@ def run_gpu(args):
                     "d2h_bytes_per_step": out_host.numel() * 4},
             "gpu_launches": stack1.kernel_count * args.steps,
             "roofline": {"bound": "hbm", "achieved": round(dk_bytes / dk_secs / 1e9, 1), "peak": peak,
-                         "unit": "GB/s", "frac": round(dk_bytes / dk_secs / 1e9 / peak, 4), "traffic": None,
-                         "kernel": "NVFP4 weight-stream product (activation prep + product per call), N=1",
+                         "unit": "GB/s", "frac": round(dk_bytes / dk_secs / 1e9 / peak, 4),
+                         "traffic": round(TRAFFIC_RATIO * dk_bytes),
+                         "traffic_basis": "ncu dram__bytes_read.sum + dram__bytes_write.sum per launch on four of "
+                                          "the step's shapes, x algorithmic bytes (profiles/gemv_tma_nvfp4_traffic_n1.md)",
+                         "kernel": "NVFP4 weight-stream product kernel (gemv_tma_kernel, one token), activations prepared beforehand",
                          "launches_timed": dk_n, "bytes_per_launch": round(dk_bytes), "peak_kind": peak_kind},
             "clocks": clk,
             "cpu_baseline": cpu,

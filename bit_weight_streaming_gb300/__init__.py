@@ -12,6 +12,8 @@ from .api import (  # noqa: F401
     fp8_rowwise_quantize,
     gemv_workspace_size,
     nvfp4_gemv,
+    nvfp4_prepare,
+    nvfp4_gemv_prepared,
     nvfp4_gate_up_silu,
     fp8_lmhead_gemv,
     status_word,

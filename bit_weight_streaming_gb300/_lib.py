@@ -20,6 +20,8 @@ SIGNATURES = {
     "bws_fp8_rowwise_quantize": (I, [P, I, I, P, P, P]),
     "bws_gemv_workspace_size": (Z, [I, I, I]),
     "bws_nvfp4_gemv": (I, [P, P, P, P, I, I, I, P, P, Z, P]),
+    "bws_nvfp4_prepare": (I, [P, I, I, I, P, Z, P]),
+    "bws_nvfp4_gemv_prepared": (I, [P, P, P, I, I, I, P, P, Z, P]),
     "bws_nvfp4_gemv_noalloc": (I, [P, P, P, P, I, I, I, P, P]),
     "bws_nvfp4_gate_up_silu": (I, [P, P, P, P, P, P, P, I, I, I, P, P, Z, P]),
     "bws_fp8_lmhead_gemv": (I, [P, P, P, I, I, I, P, P, Z, P]),

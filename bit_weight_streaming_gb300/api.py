@@ -98,6 +98,30 @@ def nvfp4_gemv(codes, scales, ts, x, y=None, ws=None):
     return y
 
 
+def nvfp4_prepare(x, d_out_max, ws):
+    """Prepares x bf16 [N, d_in] in ws for nvfp4_gemv_prepared calls with
+    d_out <= d_out_max (the activation prep of nvfp4_gemv, run once)."""
+    _need_cuda(x)
+    N, d_in = x.shape
+    buf = _ws(ws, gemv_workspace_size(N, d_out_max, d_in), x.device)
+    check(lib().bws_nvfp4_prepare(_ptr(x), N, d_in, d_out_max, _ptr(buf), buf.numel(), _stream(x.device)),
+          "bws_nvfp4_prepare")
+    return ws
+
+
+def nvfp4_gemv_prepared(codes, scales, ts, N, d_in, ws, y=None):
+    """y bf16 [N, d_out] = the activations last prepared in ws times the NVFP4
+    matrix, transposed (the product kernel of nvfp4_gemv alone)."""
+    _need_cuda(codes, scales, ts, y)
+    d_out = codes.shape[0]
+    if y is None:
+        y = torch.empty((N, d_out), dtype=torch.bfloat16, device=codes.device)
+    buf = _ws(ws, gemv_workspace_size(N, d_out, d_in), codes.device)
+    check(lib().bws_nvfp4_gemv_prepared(_ptr(codes), _ptr(scales), _ptr(ts), N, d_out, d_in, _ptr(y), _ptr(buf),
+                                        buf.numel(), _stream(codes.device)), "bws_nvfp4_gemv_prepared")
+    return y
+
+
 def nvfp4_gate_up_silu(gate, up, x, h=None, ws=None):
     """gate, up: (codes, scales, ts) NVFP4 [d_inter, d_in]; h bf16 [N, d_inter]."""
     _need_cuda(*gate, *up, x, h)

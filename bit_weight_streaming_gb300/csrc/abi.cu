@@ -45,9 +45,24 @@ int check_tokens(int N) {
 }
 
 
-// Shared body of every product call: prep the activations, then the product.
+// The activation layout a prepare-only call writes: the one the product of an
+// aligned matrix of this shape reads (the pointers below are never
+// dereferenced, only tested for alignment).
+int generic_layout(int fmt, const GemvParams& shape) {
+  GemvParams g = shape;
+  g.n_mats = 1;
+  g.mats[0].codes = reinterpret_cast<const uint8_t*>(256);
+  g.mats[0].scales = reinterpret_cast<const uint8_t*>(256);
+  return product_layout(fmt, g);
+}
+
+constexpr int kPhaseBoth = 0, kPhasePrepare = 1, kPhaseProduct = 2;
+
+// Shared body of every product call: prep the activations, then the product
+// (phase: both, the prep alone, or the product on activations an earlier
+// prepare-only call left in the workspace).
 int run_product(int fmt, int epi, GemvParams& p, const uint16_t* x, int N, int d_in, void* ws,
-                size_t ws_bytes, void* out, int out_ld, cudaStream_t st, const char* name) {
+                size_t ws_bytes, void* out, int out_ld, cudaStream_t st, const char* name, int phase = kPhaseBoth) {
   p.N = N;
   p.d_in = d_in;
   p.nseg = nseg_of(d_in);
@@ -86,7 +101,19 @@ int run_product(int fmt, int epi, GemvParams& p, const uint16_t* x, int N, int d
   p.out_ld = out_ld;
   p.out_slot_stride = 0;
   p.prefetch_units = fmt == kFmtFP8 ? 4 : 8;
+  if (phase == kPhasePrepare) {
+    q.interleave = generic_layout(fmt, p);
+    return cuda_status(launch_prep(q, st, true), name);
+  }
   q.interleave = product_layout(fmt, p);   // the layout its product reads
+  if (phase == kPhaseProduct) {
+    if (q.interleave != generic_layout(fmt, p))
+      return fail(BWS_ERR_MISALIGNED,
+                  "%s: the prepared activations are laid out for 16-byte aligned codes and scales "
+                  "(32-byte codes for the tensor-core kernel); this matrix is not",
+                  name);
+    return cuda_status(launch_product(fmt, epi, p, q.hdr + 1, st, true), name);
+  }
   cudaError_t e = launch_prep(q, st, true);
   if (e != cudaSuccess) return cuda_status(e, name);
   e = launch_product(fmt, epi, p, q.hdr + 1, st, true);
@@ -185,6 +212,37 @@ int bws_nvfp4_gemv(const uint8_t* codes, const uint8_t* scales, const float* ten
   p.n_tiles = tiles_rows32(d_out);
   return run_product(kFmtNVFP4, kEpiStoreBF16, p, x, N, d_in, workspace, workspace_bytes, y, d_out,
                      as_stream(stream), name);
+}
+
+int bws_nvfp4_prepare(const uint16_t* x, int N, int d_in, int d_out_max, void* workspace, size_t workspace_bytes,
+                      void* stream) {
+  const char* name = "bws_nvfp4_prepare";
+  bool noop;
+  const uint8_t* dummy = reinterpret_cast<const uint8_t*>(x);   // only the shape checks read it
+  int rc = check_product_common(name, dummy, x, x, N, d_out_max, d_in, &noop);
+  if (rc || noop) return rc;
+  GemvParams p = {};
+  p.n_tiles = tiles_rows32(d_out_max);
+  return run_product(kFmtNVFP4, kEpiStoreBF16, p, x, N, d_in, workspace, workspace_bytes, nullptr, 0,
+                     as_stream(stream), name, kPhasePrepare);
+}
+
+int bws_nvfp4_gemv_prepared(const uint8_t* codes, const uint8_t* scales, const float* tensor_scale, int N,
+                            int d_out, int d_in, uint16_t* y, void* workspace, size_t workspace_bytes,
+                            void* stream) {
+  const char* name = "bws_nvfp4_gemv_prepared";
+  bool noop;
+  int rc = check_product_common(name, codes, codes, y, N, d_out, d_in, &noop);
+  if (rc || noop) return rc;
+  if (!scales || !tensor_scale) return fail(BWS_ERR_INVALID_ARG, "%s: null scales", name);
+  if (!aligned(scales, 2) || !aligned(tensor_scale, 4) || !aligned(y, 2))
+    return fail(BWS_ERR_MISALIGNED, "%s: scales 2-byte, tensor_scale 4-byte, y 2-byte alignment needed", name);
+  GemvParams p = {};
+  p.n_mats = 1;
+  p.mats[0] = {codes, scales, tensor_scale, d_out, 0, 0};
+  p.n_tiles = tiles_rows32(d_out);
+  return run_product(kFmtNVFP4, kEpiStoreBF16, p, nullptr, N, d_in, workspace, workspace_bytes, y, d_out,
+                     as_stream(stream), name, kPhaseProduct);
 }
 
 int bws_nvfp4_gate_up_silu(const uint8_t* gate_codes, const uint8_t* gate_scales, const float* gate_ts,

@@ -138,6 +138,26 @@ int bws_nvfp4_gemv(const uint8_t* codes, const uint8_t* scales,
                    int d_out, int d_in, uint16_t* y, void* workspace,
                    size_t workspace_bytes, void* stream);
 
+/* bws_nvfp4_gemv in two phases, for several products of one input (the
+ * query, key and value projections of a token, or the gate and up halves
+ * called separately): bws_nvfp4_prepare writes the activations x bf16
+ * [N][d_in] into the workspace, sized with bws_gemv_workspace_size(N,
+ * d_out_max, d_in), in the layout the product kernel of a matrix with
+ * 16-byte aligned codes and scales reads; every bws_nvfp4_gemv_prepared
+ * call with the same N and d_in and d_out <= d_out_max then runs only the
+ * product on them (same results as bws_nvfp4_gemv). The workspace holds the
+ * prepared activations until the next prepare or bws_nvfp4_gemv call on it;
+ * its status word (bws_status_word) is cleared by the prepare and collects
+ * the products'. A matrix whose codes or scales are not 16-byte aligned
+ * (d_in % 256 == 0) is rejected with BWS_ERR_MISALIGNED: its kernel reads
+ * another layout. Same shape constraints as bws_nvfp4_gemv. */
+int bws_nvfp4_prepare(const uint16_t* x, int N, int d_in, int d_out_max,
+                      void* workspace, size_t workspace_bytes, void* stream);
+int bws_nvfp4_gemv_prepared(const uint8_t* codes, const uint8_t* scales,
+                            const float* tensor_scale, int N, int d_out,
+                            int d_in, uint16_t* y, void* workspace,
+                            size_t workspace_bytes, void* stream);
+
 /* bws_nvfp4_gemv for callers that cannot allocate device memory (a caller
  * whose framework owns the whole device pool, a plugin called from a runtime
  * that forbids allocation during a step, a latency-critical path that must

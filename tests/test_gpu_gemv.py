@@ -156,3 +156,34 @@ def test_empty_calls_are_noops():
     x = rand_x(1, 128, seed=1)
     y = torch.full((0, 64), 7.0, dtype=torch.bfloat16, device=device())
     bws().nvfp4_gemv(c, s, t, x[:0], y=y)
+
+
+@pytest.mark.parametrize("N", [1, 3])
+def test_prepared_products_match_one_call_products(N):
+    """One prepare, several products of the same input (different d_out, up
+    to d_out_max): bit-equal to bws_nvfp4_gemv of each matrix."""
+    d_in = 1024
+    x = rand_x(N, d_in, seed=31 + N)
+    mats = [_quant_nvfp4(rand_W((d_out, d_in), seed=40 + d_out)) for d_out in (384, 100, 1000)]
+    ws = bws().Workspace(device())
+    bws().nvfp4_prepare(x, 1000, ws)
+    ys = [bws().nvfp4_gemv_prepared(c, s, t, N, d_in, ws) for c, s, t, _ in mats]
+    for (c, s, t, host), y in zip(mats, ys):
+        assert torch.equal(y, bws().nvfp4_gemv(c, s, t, x))
+        y_ref, A = P.nvfp4_gemv(*host, f64(x))
+        ok, worst, at = T.check(y_ref, f64(y), A)
+        assert ok, (worst, at)
+
+
+def test_prepared_product_rejects_a_matrix_of_another_layout():
+    """Activations prepared for 16-byte aligned matrices (d_in % 256 == 0);
+    scales at an 8-byte offset need the other kernel's layout."""
+    d_in = 512
+    c, s, t, _ = _quant_nvfp4(rand_W((64, d_in), seed=50))
+    s_off = torch.empty(s.numel() + 8, dtype=torch.uint8, device=device())[8:].view(s.shape)
+    s_off.copy_(s)
+    x = rand_x(1, d_in, seed=50)
+    ws = bws().Workspace(device())
+    bws().nvfp4_prepare(x, 64, ws)
+    with pytest.raises(Exception, match="status 3"):
+        bws().nvfp4_gemv_prepared(c, s_off, t, 1, d_in, ws)
