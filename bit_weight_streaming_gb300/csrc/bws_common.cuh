@@ -53,6 +53,12 @@ BWS_DEV void prefetch_l2_bulk(const void* p, uint32_t bytes) {
   asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" :: "l"(p), "r"(bytes) : "memory");
 }
 // Coherent (L1-bypassing) load of data another SM wrote in this grid.
+// Atomic add with acquire-release semantics at GPU scope; returns the old value.
+BWS_DEV uint32_t atom_add_acq_rel_gpu(uint32_t* p, uint32_t v) {
+  uint32_t old;
+  asm volatile("atom.add.acq_rel.gpu.global.u32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
+  return old;
+}
 BWS_DEV float4 ld_cg_f4(const float4* p) {
   float4 v;
   asm volatile("ld.global.cg.v4.f32 {%0,%1,%2,%3}, [%4];"

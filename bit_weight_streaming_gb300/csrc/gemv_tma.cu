@@ -104,17 +104,11 @@ BWS_DEV long long begin_of(long long c, long long U, long long G) { return c * U
 // token 2t + (i&1)). SwiGLU: b is a gate box and vu the matching up sums.
 template <int FMT, int EPI>
 BWS_DEV void store_sub(const TmaParams& p, int tile, int b, int s, int g, int t, const float (&v)[4],
-                       const float (&vu)[4]) {
+                       const float (&vu)[4], const int (&xexp)[2]) {
   int mi, row_b;
   box_of<EPI>(p, tile, b, mi, row_b);
   const TmaMat& M = p.mats[mi];
   const int row0 = row_b + 16 * s;
-  int xexp[2];
-#pragma unroll
-  for (int i = 0; i < 2; ++i) {
-    const int tok = 2 * t + i;
-    xexp[i] = tok < p.N ? __ldg(p.x.exp + tok) : 0;
-  }
   float su = 1.0f;
   if (EPI == kEpiSwiGLU) su = __ldg(p.mats[1].scale32);
 #pragma unroll
@@ -154,6 +148,10 @@ BWS_DEV void consume(const TmaParams& p, Tail& T, uint32_t stage0, long long u0,
   const int b = warp & 3, half = warp >> 2;
   const int g = lane >> 2, t = lane & 3;
   const int c = 2 * t + half;                     // this lane's 16-byte chunk
+  // exponents of this lane's two output tokens (inputs are ready: loaded once)
+  int xexp[2];
+#pragma unroll
+  for (int i = 0; i < 2; ++i) xexp[i] = 2 * t + i < p.N ? __ldg(p.x.exp + 2 * t + i) : 0;
   // rows g + 8j of box b (j = 0..3) share the swizzle phase g
   const uint32_t coff = b * kBoxBytes + g * 128 + ((c ^ g) << 4);
   const uint32_t soff = kCodeBytes + b * kScaleBoxBytes + g * 16 + 2 * c;
@@ -284,16 +282,17 @@ BWS_DEV void consume(const TmaParams& p, Tail& T, uint32_t stage0, long long u0,
       float4* slot = reinterpret_cast<float4*>(p.partials) + ((size_t)(cur_tile + blockIdx.x) * kBoxes + b) * 64;
 #pragma unroll
       for (int st = 0; st < 2; ++st) slot[st * 32 + lane] = make_float4(v[st][0], v[st][1], v[st][2], v[st][3]);
-      __threadfence();
+      // the four warps' deposits, then one acquire-release count: it publishes
+      // them (release, cumulative over the barrier) and, for the last arriver,
+      // makes the other CTAs' deposits visible (acquire)
       named_bar_sync(2, 4 * 32);
       const long long c0 = owner((long long)cur_tile * p.nks, U, G);
       const long long c1 = owner((long long)(cur_tile + 1) * p.nks - 1, U, G);
-      if (threadIdx.x == 0) T.flag = atomicAdd(p.counters + cur_tile, 1u);
+      if (threadIdx.x == 0) T.flag = atom_add_acq_rel_gpu(p.counters + cur_tile, 1u);
       named_bar_sync(2, 4 * 32);
       const uint32_t prev = T.flag;
       named_bar_sync(2, 4 * 32);
       if (prev != (uint32_t)(c1 - c0)) continue;
-      __threadfence();
       // the tile's pieces in CTA order; their loads are issued kFix pieces at a
       // time, so the tail of a product waits for a few L2 round trips, not one
       // per piece
@@ -342,14 +341,14 @@ BWS_DEV void consume(const TmaParams& p, Tail& T, uint32_t stage0, long long u0,
         for (int st = 0; st < 2; ++st) {
           const float4 o = T.swi[b][st][lane];
           const float vu[4] = {o.x, o.y, o.z, o.w};
-          store_sub<FMT, EPI>(p, cur_tile, b, st, g, t, v[st], vu);
+          store_sub<FMT, EPI>(p, cur_tile, b, st, g, t, v[st], vu, xexp);
         }
       }
       named_bar_sync(3, 4 * 32);
     } else {
       const float none[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-      for (int st = 0; st < 2; ++st) store_sub<FMT, EPI>(p, cur_tile, b, st, g, t, v[st], none);
+      for (int st = 0; st < 2; ++st) store_sub<FMT, EPI>(p, cur_tile, b, st, g, t, v[st], none, xexp);
     }
   }
 }

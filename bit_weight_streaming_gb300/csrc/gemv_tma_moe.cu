@@ -325,16 +325,14 @@ BWS_DEV void consume_moe(const MoeTmaParams& p, MoeTail& T, uint32_t stage0, lon
       float4* slot4 = reinterpret_cast<float4*>(p.partials) + ((size_t)(cur_tile + blockIdx.x) * kBoxes + b) * 64;
 #pragma unroll
       for (int st = 0; st < 2; ++st) slot4[st * 32 + lane] = make_float4(v[st][0], v[st][1], v[st][2], v[st][3]);
-      __threadfence();
-      named_bar_sync(2, 4 * 32);
+      named_bar_sync(2, 4 * 32);   // deposits, then an acquire-release count (see gemv_tma.cu)
       const long long c0 = owner_m((long long)cur_tile * p.nks, U, G);
       const long long c1 = owner_m((long long)(cur_tile + 1) * p.nks - 1, U, G);
-      if (threadIdx.x == 0) T.flag = atomicAdd(p.counters + cur_tile, 1u);
+      if (threadIdx.x == 0) T.flag = atom_add_acq_rel_gpu(p.counters + cur_tile, 1u);
       named_bar_sync(2, 4 * 32);
       const uint32_t prev = T.flag;
       named_bar_sync(2, 4 * 32);
       if (prev != (uint32_t)(c1 - c0)) continue;
-      __threadfence();
       float a8[2][4] = {};
       const float4* slots = reinterpret_cast<const float4*>(p.partials) + (size_t)cur_tile * kBoxes * 64 + b * 64 + lane;
       for (long long cc = c0; cc <= c1; ++cc) {

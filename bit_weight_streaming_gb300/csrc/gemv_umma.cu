@@ -407,15 +407,13 @@ __global__ void __launch_bounds__(kUThreads, 1) gemv_umma_kernel(const __grid_co
     if (kh == 1) continue;
     if (!whole) {
       p.partials[(size_t)(cur_tile + blockIdx.x) * kURows + R] = v;
-      __threadfence();
-      named_bar_sync(1, 128);
+      named_bar_sync(1, 128);   // deposits, then an acquire-release count
       const long long c0 = u_owner((long long)cur_tile * nks, U, G);
       const long long c1 = u_owner((long long)(cur_tile + 1) * nks - 1, U, G);
-      if (warp == 2 && lane == 0) T.flag = atomicAdd(p.counters + cur_tile, 1u);
+      if (warp == 2 && lane == 0) T.flag = atom_add_acq_rel_gpu(p.counters + cur_tile, 1u);
       named_bar_sync(1, 128);
       const uint32_t prev = T.flag;
       if (prev != (uint32_t)(c1 - c0)) continue;
-      __threadfence();
       float a = 0.0f;
       for (long long cc = c0; cc <= c1; ++cc)
         a += cc == blockIdx.x ? v : __ldcg(p.partials + (size_t)(cur_tile + cc) * kURows + R);
