@@ -100,28 +100,57 @@ BWS_DEV void box_of(const TmaParams& p, int tile, int b, int& m, int& row) {
 BWS_DEV long long owner(long long u, long long U, long long G) { return ((u + 1) * G - 1) / U; }
 BWS_DEV long long begin_of(long long c, long long U, long long G) { return c * U / G; }
 
+// Inputs of a tile's stores that live in global memory, read when the tile
+// piece ends, before its reductions and the fix-up handshake, so that they
+// arrive meanwhile: per sub-tile s and register i (row g + 8*(i>>1), token
+// 2t + (i&1)) the residual a ResidF32 store adds to and, for FP8, the row's
+// scale; the tensor scales of the matrices (loaded once per CTA).
+struct EpiIn {
+  float r[2][4];
+  float rs[2][2];
+  float ts[kMaxMats];
+};
+
+template <int FMT, int EPI>
+BWS_DEV void epi_read(const TmaParams& p, int tile, int b, int g, int t, EpiIn& in) {
+  int mi, row_b;
+  box_of<EPI>(p, tile, b, mi, row_b);
+  const TmaMat& M = p.mats[mi];
+#pragma unroll
+  for (int s = 0; s < 2; ++s) {
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int row = row_b + 16 * s + g + 8 * (i >> 1);
+      const int tok = 2 * t + (i & 1);
+      const bool ok = row < M.d_out && tok < p.N;
+      if (EPI == kEpiResidF32)
+        in.r[s][i] = ok ? reinterpret_cast<const float*>(p.out)[(size_t)tok * p.out_ld + M.out_row_off + row] : 0.0f;
+      if (FMT == kFmtFP8 && (i & 1) == 0) in.rs[s][i >> 1] = row < M.d_out ? __ldg(M.scale32 + row) : 0.0f;
+    }
+  }
+}
+
 // Store v (raw sums of sub-tile s of box b; register i = row g + 8*(i>>1),
 // token 2t + (i&1)). SwiGLU: b is a gate box and vu the matching up sums.
 template <int FMT, int EPI>
 BWS_DEV void store_sub(const TmaParams& p, int tile, int b, int s, int g, int t, const float (&v)[4],
-                       const float (&vu)[4], const int (&xexp)[2]) {
+                       const float (&vu)[4], const int (&xexp)[2], const EpiIn& in) {
   int mi, row_b;
   box_of<EPI>(p, tile, b, mi, row_b);
   const TmaMat& M = p.mats[mi];
   const int row0 = row_b + 16 * s;
-  float su = 1.0f;
-  if (EPI == kEpiSwiGLU) su = __ldg(p.mats[1].scale32);
+  const float tsm = mi == 0 ? in.ts[0] : mi == 1 ? in.ts[1] : mi == 2 ? in.ts[2] : in.ts[kMaxMats - 1];
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
     const int row = row0 + g + 8 * (i >> 1);
     const int tok = 2 * t + (i & 1);
     if (row >= M.d_out || tok >= p.N) continue;
     float sc = 1.0f;
-    if (FMT == kFmtNVFP4) sc = __ldg(M.scale32);
-    if (FMT == kFmtFP8) sc = __ldg(M.scale32 + row);
+    if (FMT == kFmtNVFP4) sc = tsm;
+    if (FMT == kFmtFP8) sc = in.rs[s][i >> 1];
     const float val = ldexp_exact(__fmul_rn(v[i], sc), xexp[i & 1] - 14);
     if (EPI == kEpiSwiGLU) {
-      const float up = ldexp_exact(__fmul_rn(vu[i], su), xexp[i & 1] - 14);
+      const float up = ldexp_exact(__fmul_rn(vu[i], in.ts[1]), xexp[i & 1] - 14);
       reinterpret_cast<__nv_bfloat16*>(p.out)[(size_t)tok * p.out_ld + row] =
           __float2bfloat16_rn(silu_mul_t(val, up));
     } else {
@@ -131,7 +160,7 @@ BWS_DEV void store_sub(const TmaParams& p, int tile, int b, int s, int g, int t,
       else if (EPI == kEpiStoreF32)
         reinterpret_cast<float*>(p.out)[o] = val;
       else
-        reinterpret_cast<float*>(p.out)[o] = __fadd_rn(reinterpret_cast<float*>(p.out)[o], val);
+        reinterpret_cast<float*>(p.out)[o] = __fadd_rn(in.r[s][i], val);
     }
   }
 }
@@ -152,6 +181,9 @@ BWS_DEV void consume(const TmaParams& p, Tail& T, uint32_t stage0, long long u0,
   int xexp[2];
 #pragma unroll
   for (int i = 0; i < 2; ++i) xexp[i] = 2 * t + i < p.N ? __ldg(p.x.exp + 2 * t + i) : 0;
+  EpiIn ein;
+#pragma unroll
+  for (int i = 0; i < kMaxMats; ++i) ein.ts[i] = (FMT != kFmtFP8 && i < p.n_mats) ? __ldg(p.mats[i].scale32) : 1.0f;
   // rows g + 8j of box b (j = 0..3) share the swizzle phase g
   const uint32_t coff = b * kBoxBytes + g * 128 + ((c ^ g) << 4);
   const uint32_t soff = kCodeBytes + b * kScaleBoxBytes + g * 16 + 2 * c;
@@ -260,6 +292,8 @@ BWS_DEV void consume(const TmaParams& p, Tail& T, uint32_t stage0, long long u0,
         }
       }
     }
+    // the stores' global inputs of the storing warps, in flight during the reductions
+    if (half == 0 && (EPI == kEpiResidF32 || FMT == kFmtFP8)) epi_read<FMT, EPI>(p, cur_tile, b, g, t, ein);
     // add the two halves: warps 4..7 hand their sums to warps 0..3
     if (half == 1) {
 #pragma unroll
@@ -341,14 +375,14 @@ BWS_DEV void consume(const TmaParams& p, Tail& T, uint32_t stage0, long long u0,
         for (int st = 0; st < 2; ++st) {
           const float4 o = T.swi[b][st][lane];
           const float vu[4] = {o.x, o.y, o.z, o.w};
-          store_sub<FMT, EPI>(p, cur_tile, b, st, g, t, v[st], vu, xexp);
+          store_sub<FMT, EPI>(p, cur_tile, b, st, g, t, v[st], vu, xexp, ein);
         }
       }
       named_bar_sync(3, 4 * 32);
     } else {
       const float none[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-      for (int st = 0; st < 2; ++st) store_sub<FMT, EPI>(p, cur_tile, b, st, g, t, v[st], none, xexp);
+      for (int st = 0; st < 2; ++st) store_sub<FMT, EPI>(p, cur_tile, b, st, g, t, v[st], none, xexp, ein);
     }
   }
 }
