@@ -68,6 +68,7 @@ struct TmaParams {
   // shared-memory stage layout: code boxes at 0, scale boxes at kCodeBytes
   // (NVFP4), one activation block per token at x_off + tok * x_blk
   int n_stages, stage_bytes, x_off, x_blk, x_bytes;
+  int n_prime;   // stages given their weights before the inputs are ready
 };
 
 // Shared memory after the stages (which end on a 1024-byte boundary).
@@ -450,9 +451,11 @@ __global__ void __launch_bounds__(kThreadsTma, 2) gemv_tma_kernel(const __grid_c
         for (int tok = 0; tok < p.N; ++tok)
           bulk_load(dst + tok * p.x_blk, src + (size_t)tok * p.d_in_pad, kUnitK * 2, full);
       };
-      // Prime the ring with weights before waiting for the activations: the
-      // weights never depend on the kernels before this one.
-      const int n_pre = (u1 - u0) < NS ? (int)(u1 - u0) : NS;
+      // Prime the first n_prime stages with weights before waiting for the
+      // activations (the weights never depend on the kernels before this
+      // one), then fill the rest of the ring.
+      const int n_ring = (u1 - u0) < NS ? (int)(u1 - u0) : NS;
+      const int n_pre = n_ring < p.n_prime ? n_ring : p.n_prime;
       {
         int tile = (int)(u0 / p.nks), ks = (int)(u0 % p.nks);
         for (int k = 0; k < n_pre; ++k) {
@@ -460,19 +463,21 @@ __global__ void __launch_bounds__(kThreadsTma, 2) gemv_tma_kernel(const __grid_c
           if (++ks == p.nks) { ks = 0; ++tile; }
         }
         pdl_wait();
+        tile = (int)(u0 / p.nks);
         ks = (int)(u0 % p.nks);
-        for (int k = 0; k < n_pre; ++k) {
+        for (int k = 0; k < n_ring; ++k) {
+          if (k >= n_pre) issue_weights(tile, ks, k);
           issue_x(ks, k);
-          if (++ks == p.nks) ks = 0;
+          if (++ks == p.nks) { ks = 0; ++tile; }
         }
       }
-      // The loop runs only when the ring was primed in full (n_pre == NS):
-      // unit n_pre + j reuses stage j % NS after its (j / NS)-th release.
+      // The loop runs only when the ring was filled (n_ring == NS): unit
+      // n_ring + j reuses stage j % NS after its (j / NS)-th release.
       int s = 0;
       uint32_t ph = 0u;   // parity of the release to wait for
-      long long issued = n_pre;
-      int tile = (int)((u0 + n_pre) / p.nks), ks = (int)((u0 + n_pre) % p.nks);
-      for (long long u = u0 + n_pre; u < u1; ++u, ++issued) {
+      long long issued = n_ring;
+      int tile = (int)((u0 + n_ring) / p.nks), ks = (int)((u0 + n_ring) % p.nks);
+      for (long long u = u0 + n_ring; u < u1; ++u, ++issued) {
         if (!mbar_wait_bounded(smem_u32(&T.empty[s]), ph, kMaxPolls)) {
           atomicOr(p.status, kStatusTimeout);
           // let copies already issued land before the CTA's shared memory goes away
@@ -597,6 +602,13 @@ cudaError_t launch_gemv_tma(int fmt, int epi, const GemvParams& g, uint32_t* sta
   p.n_stages = kSmemBudget / p.stage_bytes;
   if (p.n_stages > kMaxStages) p.n_stages = kMaxStages;
   if (p.n_stages < 2) return cudaErrorInvalidValue;
+  // Weights primed before the inputs are ready: every CTA of the product
+  // starts while the previous kernels finish, and a full ring of weight
+  // copies from all of them (about 30 MB) queues ahead of those kernels'
+  // last loads and stores, which decide when the inputs are ready. A stage
+  // or two keeps the overlap without the queue (measured: 1 token best with
+  // 2, 2-4 tokens with 1, 8 tokens with none).
+  p.n_prime = p.N == 1 ? 2 : (p.N <= 4 ? 1 : 0);
   if (p.n_ctas <= 0) return cudaSuccess;
   // one NVFP4 token: the block-diagonal operand (block scales on the accumulators)
   const bool n1 = fmt == kFmtNVFP4 && p.N == 1;
