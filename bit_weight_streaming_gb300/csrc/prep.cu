@@ -83,24 +83,22 @@ __device__ __noinline__ void combine_chunk(const PrepParams& q, int tok, int c, 
 // The routing CTA, out of line for the same reason.
 __device__ __noinline__ void route_cta(const MoeRoute& m) { moe_route_body(m); }
 
-// Sum (or max, or OR) of one value per CTA of the cluster, in rank order,
-// through each CTA's `slot`; every CTA gets the same result.
-template <int OP, int CL, int THREADS>   // OP 0: sum, 1: max, 2: bitwise or
-BWS_DEV float cluster_combine(float* slot, float v, float* warp_part) {
+// The row's sum (of squares) and largest magnitude over the cluster: each
+// warp reduces its lanes, warp 0 the CTA's warps, then every CTA adds the
+// CTAs' values in rank order through their `slot`s. The shuffle trees are
+// fixed, so the result is the same on every run and in every thread.
+template <int CL, int THREADS>
+BWS_DEV float2 cluster_sum_max(float2* slot, float s, float m, float2* warp_part) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  if (OP == 0) v = warp_sum(v);
-  if (OP == 1) v = warp_max(v);
-  if (OP == 2) v = __uint_as_float(__reduce_or_sync(0xffffffffu, __float_as_uint(v)));
-  if (lane == 0) warp_part[warp] = v;
+  s = warp_sum(s);
+  m = warp_max(m);
+  if (lane == 0) warp_part[warp] = make_float2(s, m);
   __syncthreads();
-  if (threadIdx.x == 0) {
-    float r = warp_part[0];
-    for (int i = 1; i < THREADS / 32; ++i) {
-      if (OP == 0) r += warp_part[i];
-      if (OP == 1) r = fmaxf(r, warp_part[i]);
-      if (OP == 2) r = __uint_as_float(__float_as_uint(r) | __float_as_uint(warp_part[i]));
-    }
-    *slot = r;
+  if (warp == 0) {
+    const float2 v = lane < THREADS / 32 ? warp_part[lane] : make_float2(0.0f, 0.0f);
+    s = warp_sum(v.x);
+    m = warp_max(v.y);
+    if (lane == 0) *slot = make_float2(s, m);
   }
   if (CL == 1) {
     __syncthreads();
@@ -108,13 +106,15 @@ BWS_DEV float cluster_combine(float* slot, float v, float* warp_part) {
   }
   cg::cluster_group cl = cg::this_cluster();
   cl.sync();
-  float r = *cl.map_shared_rank(slot, 0);
+  float2 r = *cl.map_shared_rank(slot, 0);
   for (int k = 1; k < CL; ++k) {
-    const float o = *cl.map_shared_rank(slot, k);
-    if (OP == 0) r += o;
-    if (OP == 1) r = fmaxf(r, o);
-    if (OP == 2) r = __uint_as_float(__float_as_uint(r) | __float_as_uint(o));
+    const float2 o = *cl.map_shared_rank(slot, k);
+    r.x += o.x;
+    r.y = fmaxf(r.y, o.y);
   }
+  // this CTA is done with the others' slots; the matching wait at the end of
+  // the kernel keeps every CTA alive until all have read
+  asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
   return r;
 }
 
@@ -191,8 +191,11 @@ __global__ void __launch_bounds__(THREADS) prep_kernel(const __grid_constant__ P
     if (q.hdr != nullptr) q.hdr[0] = (uint32_t)q.N;
     if (q.status_clear != nullptr) q.status_clear[0] = q.status_clear[1] = 0u;
   }
-  __shared__ float warp_part[THREADS / 32];
-  __shared__ float xch[3];   // this CTA's values in the cluster exchanges
+  __shared__ float2 warp_part[THREADS / 32];
+  __shared__ float2 xch;     // this CTA's values in the cluster exchange
+  // the row's band flags are OR-ed into global memory by the warps that find
+  // any; the cluster barrier below orders this clearing store before them
+  if (rank == 0 && threadIdx.x == 0) q.flags[slot * q.N + tok] = 0u;
   const int nchunk = q.d_in >> 3, nchunk_pad = q.d_in_pad >> 3;
   // this CTA's chunks [c0, c1)
   const int per = (nchunk_pad + CL - 1) / CL;
@@ -207,13 +210,18 @@ __global__ void __launch_bounds__(THREADS) prep_kernel(const __grid_constant__ P
       zl[c] = make_uint4(0, 0, 0, 0);
     }
   }
+  // One pass of statistics: the sum of squares (RMSNorm) and the largest
+  // magnitude of the values the bands are cut from. Rounding to BF16 after a
+  // multiplication by inv_rms > 0 is monotone and odd, so the largest
+  // normalised magnitude is the normalisation of the largest raw one, and
+  // the exponent E needs no second pass.
   float inv_rms = 1.0f;
   const uint4* xr = nullptr;
   float* rr = nullptr;
+  float ss = 0.0f, ma = 0.0f;
   if (q.mode == kPrepRmsNorm) {
     rr = q.r + (size_t)tok * q.d_in;
     const uint4* x0 = q.x0 != nullptr ? reinterpret_cast<const uint4*>(q.x0 + (size_t)tok * q.d_in) : nullptr;
-    float ss = 0.0f;
     for (int c = c0 + threadIdx.x; c < c1 && c < nchunk; c += blockDim.x) {
       float v[8];
       if (x0 != nullptr) {
@@ -233,22 +241,28 @@ __global__ void __launch_bounds__(THREADS) prep_kernel(const __grid_constant__ P
         if (MOE && q.comb_ys != nullptr) combine_chunk(q, tok, c, v, rr);
       }
 #pragma unroll
-      for (int i = 0; i < 8; ++i) ss = __fmaf_rn(v[i], v[i], ss);
+      for (int i = 0; i < 8; ++i) {
+        ss = __fmaf_rn(v[i], v[i], ss);
+        ma = fmaxf(ma, fabsf(v[i]));
+      }
     }
-    const float ms = __fdiv_rn(cluster_combine<0, CL, THREADS>(&xch[0], ss, warp_part), (float)q.d_in);
-    inv_rms = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(ms, q.eps)));
   } else {
     xr = reinterpret_cast<const uint4*>(q.x + (size_t)slot * q.x_slot_stride + (size_t)tok * q.ld);
-  }
-  float m = 0.0f;
-  for (int c = c0 + threadIdx.x; c < c1 && c < nchunk; c += blockDim.x) {
-    uint32_t w[4];
-    chunk_bf16(q, c, rr, xr, inv_rms, w);
+    for (int c = c0 + threadIdx.x; c < c1 && c < nchunk; c += blockDim.x) {
+      const uint4 b = __ldg(xr + c);
+      const uint32_t w[4] = {b.x, b.y, b.z, b.w};
 #pragma unroll
-    for (int i = 0; i < 4; ++i)
-      m = fmaxf(m, fmaxf(fabsf(bf16_bits_to_f32(w[i] & 0xFFFF)), fabsf(bf16_bits_to_f32(w[i] >> 16))));
+      for (int i = 0; i < 4; ++i)
+        ma = fmaxf(ma, fmaxf(fabsf(bf16_bits_to_f32(w[i] & 0xFFFF)), fabsf(bf16_bits_to_f32(w[i] >> 16))));
+    }
   }
-  const float mx = cluster_combine<1, CL, THREADS>(&xch[1], m, warp_part);
+  const float2 st = cluster_sum_max<CL, THREADS>(&xch, ss, ma, warp_part);
+  float mx = st.y;
+  if (q.mode == kPrepRmsNorm) {
+    const float ms = __fdiv_rn(st.x, (float)q.d_in);
+    inv_rms = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(ms, q.eps)));
+    mx = __bfloat162float(__float2bfloat16_rn(__fmul_rn(mx, inv_rms)));
+  }
   const int E = mx > 0.0f ? floor_log2_abs(mx) : 0;
   uint32_t flags = 0u;
   if (q.interleave == kLayoutImage) {
@@ -298,12 +312,10 @@ __global__ void __launch_bounds__(THREADS) prep_kernel(const __grid_constant__ P
     lo4[dst] = make_uint4(l[0], l[1], l[2], l[3]);
   }
   }
-  const uint32_t f = __float_as_uint(cluster_combine<2, CL, THREADS>(&xch[2], __uint_as_float(flags), warp_part));
-  if (rank == 0 && threadIdx.x == 0) {
-    q.exp[slot * q.N + tok] = E;
-    q.flags[slot * q.N + tok] = f;
-  }
-  if (CL > 1) cg::this_cluster().sync();   // no CTA leaves while another may still read its exchange slots
+  const uint32_t wf = __reduce_or_sync(0xffffffffu, flags);
+  if (wf != 0u && (threadIdx.x & 31) == 0) atomicOr(q.flags + slot * q.N + tok, wf);
+  if (rank == 0 && threadIdx.x == 0) q.exp[slot * q.N + tok] = E;
+  if (CL > 1) asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 
 }  // namespace
