@@ -122,6 +122,21 @@ BWS_DEV void tma_load_2d(uint32_t dst, const void* tmap, int x, int y, uint32_t 
       "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];"
       :: "r"(dst), "l"(tmap), "r"(x), "r"(y), "r"(bar) : "memory");
 }
+// An L2 policy for data read once per step (streamed weights): its lines are
+// the first to be replaced, so the stream does not push out the small data
+// that every kernel reads back soon (activations, partial sums, code).
+BWS_DEV uint64_t l2_evict_first() {
+  uint64_t pol;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+  return pol;
+}
+// tma_load_2d with an L2 policy.
+BWS_DEV void tma_load_2d_hint(uint32_t dst, const void* tmap, int x, int y, uint32_t bar, uint64_t pol) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
+      " [%0], [%1, {%2, %3}], [%4], %5;"
+      :: "r"(dst), "l"(tmap), "r"(x), "r"(y), "r"(bar), "l"(pol) : "memory");
+}
 // 3D tiled TMA load of box (x, y, z) into shared memory, completing on bar.
 BWS_DEV void tma_load_3d(uint32_t dst, const void* tmap, int x, int y, int z, uint32_t bar) {
   asm volatile(

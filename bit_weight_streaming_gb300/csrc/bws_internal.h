@@ -81,6 +81,8 @@ struct GemvParams {
   uint32_t* counters;      // [n_tiles], zero on entry, left zero on exit
   int prefetch_units;      // units pulled into L2 before waiting on the inputs
   size_t partials_bytes;   // slot mode: size of the partials scratch (0: the plain-mode size)
+  int deposit;             // TMA kernel: tile pieces leave their raw sums in partials for the
+                           // next prep to finish (PrepParams::fin_*), nothing else is stored
 };
 
 // MoE helpers.
@@ -129,6 +131,19 @@ struct PrepParams {
   // optional: one extra CTA computes an MoE layer's slot table (one-CTA rows only)
   int has_route;
   MoeRoute route;
+  // optional (fin_partials != nullptr): the input rows are the previous
+  // product's outputs, finished here from the raw sums its CTAs deposited
+  // (GemvParams::deposit): for each row, its tile's deposits added in CTA
+  // order, scaled, then the product's store (kEpiResidF32: r += y, in
+  // kPrepRmsNorm; kEpiStoreBF16: bf16(y), kEpiSwiGLU: bf16(SiLU(g) * u), in
+  // kPrepCopy, also written back to x)
+  const float* fin_partials;
+  long long fin_units;     // the product's stream-K geometry (TmaGeom)
+  int fin_ctas, fin_nks;
+  int fin_epi, fin_fmt, fin_n_mats;
+  int fin_d_out[kMaxMats], fin_row_off[kMaxMats], fin_tile_begin[kMaxMats];
+  const float* fin_scale[kMaxMats];
+  const int* fin_xexp;     // exponents of the product's input rows [N]
 };
 
 // Workspace of one product call (all offsets 256-byte aligned).
@@ -147,6 +162,16 @@ cudaError_t launch_gemv(int fmt, int epi, const GemvParams& p, cudaStream_t st, 
 bool gemv_tma_eligible(int fmt, const GemvParams& p);
 // Tiles of 128 rows (SwiGLU: 64 gate + 64 up rows) of the TMA kernels.
 int gemv_tma_tiles(int epi, const GemvMat* mats, int n_mats);
+// The TMA kernel's stream-K split of a product: n_tiles tiles of nks units,
+// units [c * n_units / n_ctas, (c + 1) * n_units / n_ctas) to CTA c.
+struct TmaGeom {
+  int n_tiles, nks, n_ctas;
+  long long n_units;
+};
+TmaGeom gemv_tma_geometry(int fmt, int epi, const GemvParams& g);
+// Whether g's partials scratch holds the deposits (GemvParams::deposit) of
+// the TMA kernel's split: one [N][128] float slot per (tile, CTA) piece.
+bool gemv_tma_deposit_fits(const TmaGeom& t, const GemvParams& g);
 // Activation layout the TMA kernel reads for this format (PrepParams::interleave).
 inline int tma_interleave(int fmt) { return fmt == kFmtFP8 ? 128 : 256; }
 // PrepParams::interleave for the tensor-core kernel: one token's E4M3 band

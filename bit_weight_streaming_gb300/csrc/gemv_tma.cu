@@ -69,6 +69,7 @@ struct TmaParams {
   // (NVFP4), one activation block per token at x_off + tok * x_blk
   int n_stages, stage_bytes, x_off, x_blk, x_bytes;
   int n_prime;   // stages given their weights before the inputs are ready
+  int deposit;   // 1: each tile piece writes its raw sums to its partial slot, nothing else
 };
 
 // Shared memory after the stages (which end on a 1024-byte boundary).
@@ -294,7 +295,8 @@ BWS_DEV void consume(const TmaParams& p, Tail& T, uint32_t stage0, long long u0,
       }
     }
     // the stores' global inputs of the storing warps, in flight during the reductions
-    if (half == 0 && (EPI == kEpiResidF32 || FMT == kFmtFP8)) epi_read<FMT, EPI>(p, cur_tile, b, g, t, ein);
+    if (half == 0 && (EPI == kEpiResidF32 || FMT == kFmtFP8) && !p.deposit)
+      epi_read<FMT, EPI>(p, cur_tile, b, g, t, ein);
     // add the two halves: warps 4..7 hand their sums to warps 0..3
     if (half == 1) {
 #pragma unroll
@@ -312,6 +314,21 @@ BWS_DEV void consume(const TmaParams& p, Tail& T, uint32_t stage0, long long u0,
     const bool whole = piece_whole && last_of_tile;
     piece_whole = true;   // later pieces start at a tile's first unit
     if (half == 1) continue;
+    if (p.deposit) {
+      // the piece's raw sums, row-major per token in the slot of (tile, CTA):
+      // the next prep adds a tile's slots in CTA order and finishes the rows
+      float* slot = p.partials + (size_t)(cur_tile + blockIdx.x) * p.N * 128;
+#pragma unroll
+      for (int st = 0; st < 2; ++st) {
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const int row = 32 * b + 16 * st + g + 8 * (i >> 1);
+          const int tok = N1 ? 0 : 2 * t + (i & 1);
+          if (N1 ? (t == 0 && (i & 1) == 0) : tok < p.N) slot[tok * 128 + row] = v[st][i];
+        }
+      }
+      continue;
+    }
     // warps 0..3: finish or deposit
     if (!whole) {
       float4* slot = reinterpret_cast<float4*>(p.partials) + ((size_t)(cur_tile + blockIdx.x) * kBoxes + b) * 64;
@@ -429,6 +446,7 @@ __global__ void __launch_bounds__(kThreadsTma, 2) gemv_tma_kernel(const __grid_c
         if (FMT == kFmtNVFP4) tma_prefetch_desc(&p.mats[i].scales);
       }
       const uint32_t w_tx = FMT == kFmtNVFP4 ? kCodeBytes + kBoxes * kScaleBoxBytes : kCodeBytes;
+      const uint64_t pol = l2_evict_first();   // weights are read once per step
       // weights of unit (tile, ks) into stage s (the stage's full barrier also
       // expects the unit's activation bytes)
       auto issue_weights = [&](int tile, int ks, int s) {
@@ -439,9 +457,9 @@ __global__ void __launch_bounds__(kThreadsTma, 2) gemv_tma_kernel(const __grid_c
         for (int b = 0; b < kBoxes; ++b) {
           int m, row;
           box_of<EPI>(p, tile, b, m, row);
-          tma_load_2d(dst + b * kBoxBytes, &p.mats[m].codes, ks * 128, row, full);
+          tma_load_2d_hint(dst + b * kBoxBytes, &p.mats[m].codes, ks * 128, row, full, pol);
           if (FMT == kFmtNVFP4)
-            tma_load_2d(dst + kCodeBytes + b * kScaleBoxBytes, &p.mats[m].scales, ks * 16, row, full);
+            tma_load_2d_hint(dst + kCodeBytes + b * kScaleBoxBytes, &p.mats[m].scales, ks * 16, row, full, pol);
         }
       };
       auto issue_x = [&](int ks, int s) {
@@ -545,6 +563,21 @@ bool gemv_tma_eligible(int fmt, const GemvParams& p) {
   return true;
 }
 
+TmaGeom gemv_tma_geometry(int fmt, int epi, const GemvParams& g) {
+  TmaGeom t;
+  t.nks = fmt == kFmtFP8 ? g.d_in / 128 : g.d_in / 256;
+  t.n_tiles = gemv_tma_tiles(epi, g.mats, g.n_mats);
+  t.n_units = (long long)t.n_tiles * t.nks;
+  const long long ctas = 2LL * num_sms();   // two CTAs per SM
+  t.n_ctas = (int)(t.n_units < ctas ? t.n_units : ctas);
+  return t;
+}
+
+bool gemv_tma_deposit_fits(const TmaGeom& t, const GemvParams& g) {
+  return ((long long)t.n_tiles + t.n_ctas) * g.N * 128 * (long long)sizeof(float) <=
+         ((long long)g.n_tiles + gemv_max_warps()) * kSlotFloats * (long long)sizeof(float);
+}
+
 int gemv_tma_tiles(int epi, const GemvMat* mats, int n_mats) {
   if (epi == kEpiSwiGLU) return (mats[0].d_out + 63) / 64;
   int t = 0;
@@ -578,11 +611,13 @@ cudaError_t launch_gemv_tma(int fmt, int epi, const GemvParams& g, uint32_t* sta
   p.N = g.N;
   p.d_in = g.d_in;
   p.d_in_pad = g.d_in_pad;
-  p.nks = fmt == kFmtFP8 ? g.d_in / 128 : g.d_in / 256;
-  p.n_tiles = gemv_tma_tiles(epi, g.mats, g.n_mats);
-  p.n_units = (long long)p.n_tiles * p.nks;
-  const long long ctas = 2LL * num_sms();   // two CTAs per SM
-  p.n_ctas = (int)(p.n_units < ctas ? p.n_units : ctas);
+  const TmaGeom geo = gemv_tma_geometry(fmt, epi, g);
+  p.nks = geo.nks;
+  p.n_tiles = geo.n_tiles;
+  p.n_units = geo.n_units;
+  p.n_ctas = geo.n_ctas;
+  p.deposit = g.deposit;
+  if (p.deposit && (epi == kEpiStoreF32 || !gemv_tma_deposit_fits(geo, g))) return cudaErrorInvalidValue;
   p.x = g.x;
   p.out = g.out;
   p.out_ld = g.out_ld;

@@ -15,6 +15,7 @@
 #include "bws_common.cuh"
 #include "bws_internal.h"
 #include "moe_route.cuh"
+#include "stream_tile.cuh"
 
 namespace cg = cooperative_groups;
 
@@ -28,8 +29,11 @@ BWS_DEV float bf16_bits_to_f32(uint32_t b) { return __uint_as_float(b << 16); }
 
 // The row's values as BF16 bit patterns, chunk c (8 values); for RMSNorm, the
 // FP32 residual times inv_rms rounded to BF16.
+template <bool FIN>
 BWS_DEV void chunk_bf16(const PrepParams& q, int c, const float* rr, const uint4* xr, float inv_rms,
                         uint32_t (&w)[4]) {
+  // a copied row that this kernel finished and wrote (fin_partials) is read
+  // back through L2, not the read-only path
   if (q.mode == kPrepRmsNorm) {
     const float4 a = reinterpret_cast<const float4*>(rr)[2 * c];
     const float4 b = reinterpret_cast<const float4*>(rr)[2 * c + 1];
@@ -41,9 +45,78 @@ BWS_DEV void chunk_bf16(const PrepParams& q, int c, const float* rr, const uint4
       w[i] = lo | (hi << 16);
     }
   } else {
-    const uint4 b = __ldg(xr + c);
+    const uint4 b = FIN ? __ldcg(xr + c) : __ldg(xr + c);
     w[0] = b.x; w[1] = b.y; w[2] = b.z; w[3] = b.w;
   }
+}
+
+// Elements e..e+7 of token tok of the previous product's output (one 8-element
+// chunk: never across a tile), finished from its CTAs' deposits the way the
+// product kernel's last arriving CTA finishes a tile: the tile's slots added
+// in CTA order from zero, times the matrix's scale, times 2^(E - 14) of the
+// product's input; SwiGLU (SWI): SiLU(gate) * up. Only the finishing
+// instantiations of the prep use it.
+template <bool SWI>
+__device__ __forceinline__ void finish_chunk(const PrepParams& q, int tok, int e, float (&out)[8]) {
+  int m = 0;
+  for (int i = 1; i < q.fin_n_mats; ++i)
+    if (e >= q.fin_row_off[i]) m = i;
+  const int lrow = e - q.fin_row_off[m];
+  constexpr int kRows = SWI ? 64 : 128;
+  const int tile = (SWI ? 0 : q.fin_tile_begin[m]) + lrow / kRows, rit = lrow % kRows;
+  // the CTAs that hold the tile's first and last units
+  const long long U = q.fin_units, G = q.fin_ctas;
+  const int cc0 = (int)((((long long)tile * q.fin_nks + 1) * G - 1) / U);
+  const int cc1 = (int)(((long long)(tile + 1) * q.fin_nks * G - 1) / U);
+  float a[8], au[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) a[i] = au[i] = 0.0f;
+  // 32 values in flight per batch of slots
+  constexpr int kB = SWI ? 2 : 4, kV = SWI ? 4 : 2;
+  for (int cb = cc0; cb <= cc1; cb += kB) {
+    float4 o[kB][kV];
+#pragma unroll
+    for (int k = 0; k < kB; ++k) {
+      const float4* base =
+          reinterpret_cast<const float4*>(q.fin_partials + ((size_t)(tile + cb + k) * q.N + tok) * 128 + rit);
+#pragma unroll
+      for (int j = 0; j < kV; ++j)   // gate pieces at 0, 1; up pieces at 16, 17 (64 rows on)
+        o[k][j] = cb + k <= cc1 ? __ldcg(base + (j & 1) + 16 * (j >> 1)) : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+#pragma unroll
+    for (int k = 0; k < kB; ++k) {
+      if (cb + k > cc1) break;
+#pragma unroll
+      for (int j = 0; j < kV; ++j) {
+        float* d = (j >> 1) ? au : a;
+        const int h = 4 * (j & 1);
+        d[h] += o[k][j].x;
+        d[h + 1] += o[k][j].y;
+        d[h + 2] += o[k][j].z;
+        d[h + 3] += o[k][j].w;
+      }
+    }
+  }
+  const int xe = __ldg(q.fin_xexp + tok) - 14;
+  if (SWI) {
+    const float tg = __ldg(q.fin_scale[0]), tu = __ldg(q.fin_scale[1]);
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+      out[i] = silu_mul_t(ldexp_exact(__fmul_rn(a[i], tg), xe), ldexp_exact(__fmul_rn(au[i], tu), xe));
+  } else {
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const float sc = q.fin_fmt == kFmtFP8 ? __ldg(q.fin_scale[m] + lrow + i) : __ldg(q.fin_scale[m]);
+      out[i] = ldexp_exact(__fmul_rn(a[i], sc), xe);
+    }
+  }
+}
+
+BWS_DEV void finish(const PrepParams& q, int tok, int e, float (&out)[8]) {
+  if (q.fin_epi == kEpiSwiGLU)
+    finish_chunk<true>(q, tok, e, out);
+  else
+    finish_chunk<false>(q, tok, e, out);
 }
 
 // The previous MoE layer's combine for chunk c of token tok, in slot order,
@@ -133,13 +206,14 @@ BWS_DEV uint32_t e4m3_code(float a, float& dec) {
 // then 1); rows 0-3 of the first hold block 2kk's bands (hi0, lo0, hi1, lo1),
 // rows 4-7 of the second block 2kk+1's, the other rows are zero. Out of
 // line: its registers stay out of the prep's main path. Returns the flags.
+template <bool FIN>
 __device__ __noinline__ uint32_t image_chunks(const PrepParams& q, int c0, int c1, const float* rr, const uint4* xr,
                                               float inv_rms, int E) {
   uint8_t* img = reinterpret_cast<uint8_t*>(q.hi);
   uint32_t flags = 0u;
   for (int c = c0 + threadIdx.x; c < c1; c += blockDim.x) {
     uint32_t w[4];
-    chunk_bf16(q, c, rr, xr, inv_rms, w);
+    chunk_bf16<FIN>(q, c, rr, xr, inv_rms, w);
     uint32_t band[4][2] = {{0u, 0u}, {0u, 0u}, {0u, 0u}, {0u, 0u}};
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
@@ -169,10 +243,10 @@ __device__ __noinline__ uint32_t image_chunks(const PrepParams& q, int c0, int c
   return flags;
 }
 
-// MOE: the instantiation with the routing CTA and the folded combine (the
-// plain one keeps fewer registers, so it fits beside running product CTAs).
-template <int CL, int THREADS, bool MOE>
-__global__ void __launch_bounds__(THREADS) prep_kernel(const __grid_constant__ PrepParams q) {
+// MOE: the body with the routing CTA and the folded combine; FIN: the one
+// that finishes the previous product's rows from its deposits.
+template <int CL, int THREADS, bool MOE, bool FIN>
+__device__ __forceinline__ void prep_body(const PrepParams& q) {
   pdl_launch_dependents();
   pdl_wait();
   const int rank = CL == 1 ? 0 : (int)cg::this_cluster().block_rank();
@@ -238,6 +312,14 @@ __global__ void __launch_bounds__(THREADS) prep_kernel(const __grid_constant__ P
         const float4 a = reinterpret_cast<const float4*>(rr)[2 * c];
         const float4 b = reinterpret_cast<const float4*>(rr)[2 * c + 1];
         v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w; v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
+        if constexpr (FIN) {   // r += the previous product's rows
+          float f[8];
+          finish(q, tok, 8 * c, f);
+#pragma unroll
+          for (int i = 0; i < 8; ++i) v[i] = __fadd_rn(v[i], f[i]);
+          reinterpret_cast<float4*>(rr)[2 * c] = make_float4(v[0], v[1], v[2], v[3]);
+          reinterpret_cast<float4*>(rr)[2 * c + 1] = make_float4(v[4], v[5], v[6], v[7]);
+        }
         if (MOE && q.comb_ys != nullptr) combine_chunk(q, tok, c, v, rr);
       }
 #pragma unroll
@@ -249,7 +331,20 @@ __global__ void __launch_bounds__(THREADS) prep_kernel(const __grid_constant__ P
   } else {
     xr = reinterpret_cast<const uint4*>(q.x + (size_t)slot * q.x_slot_stride + (size_t)tok * q.ld);
     for (int c = c0 + threadIdx.x; c < c1 && c < nchunk; c += blockDim.x) {
-      const uint4 b = __ldg(xr + c);
+      uint4 b;
+      if constexpr (FIN) {   // the previous product's rows, stored as it would have
+        float f[8];
+        finish(q, tok, 8 * c, f);
+        uint32_t wb[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+          wb[i] = (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(f[2 * i])) |
+                  ((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(f[2 * i + 1])) << 16);
+        b = make_uint4(wb[0], wb[1], wb[2], wb[3]);
+        const_cast<uint4*>(xr)[c] = b;
+      } else {
+        b = __ldg(xr + c);
+      }
       const uint32_t w[4] = {b.x, b.y, b.z, b.w};
 #pragma unroll
       for (int i = 0; i < 4; ++i)
@@ -266,7 +361,7 @@ __global__ void __launch_bounds__(THREADS) prep_kernel(const __grid_constant__ P
   const int E = mx > 0.0f ? floor_log2_abs(mx) : 0;
   uint32_t flags = 0u;
   if (q.interleave == kLayoutImage) {
-    flags = image_chunks(q, c0, c1, rr, xr, inv_rms, E);
+    flags = image_chunks<FIN>(q, c0, c1, rr, xr, inv_rms, E);
   } else {
   uint4* hi4 = reinterpret_cast<uint4*>(q.hi + rowbase + (size_t)tok * q.d_in_pad);
   uint4* lo4 = reinterpret_cast<uint4*>(q.lo + rowbase + (size_t)tok * q.d_in_pad);
@@ -282,7 +377,7 @@ __global__ void __launch_bounds__(THREADS) prep_kernel(const __grid_constant__ P
       dst = u * ku8 + (r8 % lk8) * 8 + r8 / lk8;
     }
     uint32_t w[4] = {0u, 0u, 0u, 0u};
-    if (c < nchunk) chunk_bf16(q, c, rr, xr, inv_rms, w);
+    if (c < nchunk) chunk_bf16<FIN>(q, c, rr, xr, inv_rms, w);
     uint32_t h[4], l[4];
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
@@ -318,16 +413,35 @@ __global__ void __launch_bounds__(THREADS) prep_kernel(const __grid_constant__ P
   if (CL > 1) asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 
+// The plain instantiations keep few registers, so that they fit beside
+// running product CTAs; the finishing one is capped to fit beside one.
+template <int CL, int THREADS, bool MOE>
+__global__ void __launch_bounds__(THREADS) prep_kernel(const __grid_constant__ PrepParams q) {
+  prep_body<CL, THREADS, MOE, false>(q);
+}
+
+template <int CL, int THREADS>
+__global__ void __launch_bounds__(THREADS, 2) prep_fin_kernel(const __grid_constant__ PrepParams q) {
+  prep_body<CL, THREADS, false, true>(q);
+}
+
 }  // namespace
 
 cudaError_t launch_prep(const PrepParams& q, cudaStream_t st, bool pdl) {
   const int slots = q.n_slots != nullptr ? q.max_slots : 1;
   const bool long_row = q.d_in_pad > kLongRow;
+  const bool moe = q.has_route || q.comb_ys != nullptr;
+  const bool fin = q.fin_partials != nullptr;
   if (q.has_route && long_row) return cudaErrorInvalidValue;   // the routing CTA needs one-CTA rows
-  const int cl = long_row ? 8 : 1;
+  // a finished row is the previous product's output: r += y for RMSNorm,
+  // y itself (or SiLU(g) * u) for a copy
+  if (fin && (moe || (q.mode == kPrepRmsNorm) != (q.fin_epi == kEpiResidF32))) return cudaErrorInvalidValue;
+  // rows: one CTA of 1024 threads; 8192 on, a cluster of 8 x 256; finishing
+  // a product, a cluster of 2 x 512 (or 8 x 256) with room for its loads
+  const int cl = long_row ? 8 : (fin ? 2 : 1);
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)(slots * q.N * cl + (q.has_route ? 1 : 0)));
-  cfg.blockDim = dim3(long_row ? 256 : 1024);
+  cfg.blockDim = dim3(long_row ? 256 : (fin || moe ? 512 : 1024));
   cfg.stream = st;
   cudaLaunchAttribute a[2];
   int na = 0;
@@ -336,7 +450,7 @@ cudaError_t launch_prep(const PrepParams& q, cudaStream_t st, bool pdl) {
     a[na].val.programmaticStreamSerializationAllowed = 1;
     ++na;
   }
-  if (long_row) {
+  if (cl > 1) {
     a[na].id = cudaLaunchAttributeClusterDimension;
     a[na].val.clusterDim.x = cl;
     a[na].val.clusterDim.y = 1;
@@ -345,13 +459,13 @@ cudaError_t launch_prep(const PrepParams& q, cudaStream_t st, bool pdl) {
   }
   cfg.attrs = a;
   cfg.numAttrs = na;
-  const bool moe = q.has_route || q.comb_ys != nullptr;
-  if (long_row)
-    return moe ? cudaLaunchKernelEx(&cfg, prep_kernel<8, 256, true>, q) : cudaLaunchKernelEx(&cfg, prep_kernel<8, 256, false>, q);
-  if (moe) {
-    cfg.blockDim = dim3(512);   // fits beside a running product CTA despite its registers
-    return cudaLaunchKernelEx(&cfg, prep_kernel<1, 512, true>, q);
+  if (long_row) {
+    if (fin) return cudaLaunchKernelEx(&cfg, prep_fin_kernel<8, 256>, q);
+    return moe ? cudaLaunchKernelEx(&cfg, prep_kernel<8, 256, true>, q)
+               : cudaLaunchKernelEx(&cfg, prep_kernel<8, 256, false>, q);
   }
+  if (fin) return cudaLaunchKernelEx(&cfg, prep_fin_kernel<2, 512>, q);
+  if (moe) return cudaLaunchKernelEx(&cfg, prep_kernel<1, 512, true>, q);
   return cudaLaunchKernelEx(&cfg, prep_kernel<1, 1024, false>, q);
 }
 

@@ -84,10 +84,45 @@ XPrep xprep_of(const Ctx& c, size_t block, const GemvWorkspace& L) {
 // prep into a block; zeroes `zero_words` counters at zero_ptr
 // comb: the previous MoE layer's combine, folded into this RMSNorm prep;
 // route: this MoE layer's routing, done by one extra CTA of this prep.
+// A product whose outputs only the next prep reads: run by the TMA kernel,
+// its CTAs deposit raw sums and that prep finishes the rows, so no CTA of
+// the product waits on a fix-up. Needs tiles that never share an 8-row chunk
+// with another matrix. Returns whether p now deposits; f: the prep's fields.
+bool deposit_setup(const bws_matrix* mats, int nm, int epi, GemvParams& p, PrepParams& f) {
+  const int fmt = fmt_of(mats[0]);
+  if (fmt == kFmtMXFP4 || epi == kEpiStoreF32 || gemv_umma_eligible(fmt, p) || !gemv_tma_eligible(fmt, p))
+    return false;
+  const int rows = epi == kEpiSwiGLU ? 64 : 128;
+  for (int i = 0; i < nm; ++i)
+    if (mats[i].d_out % rows) return false;
+  const TmaGeom geo = gemv_tma_geometry(fmt, epi, p);
+  if (!gemv_tma_deposit_fits(geo, p)) return false;
+  p.deposit = 1;
+  f.fin_partials = p.partials;
+  f.fin_units = geo.n_units;
+  f.fin_ctas = geo.n_ctas;
+  f.fin_nks = geo.nks;
+  f.fin_epi = epi;
+  f.fin_fmt = fmt;
+  f.fin_n_mats = nm;
+  int tile = 0;
+  for (int i = 0; i < nm; ++i) {
+    f.fin_d_out[i] = mats[i].d_out;
+    f.fin_row_off[i] = p.mats[i].out_row_off;
+    f.fin_tile_begin[i] = tile;
+    f.fin_scale[i] = mats[i].scale32;
+    tile += mats[i].d_out / rows;
+  }
+  f.fin_xexp = p.x.exp;
+  return true;
+}
+
 cudaError_t prep(const Ctx& c, int mode, const uint16_t* x, int ld, const uint16_t* x0, int d_in, size_t block,
                  const GemvWorkspace& L, uint32_t* zero_ptr, int zero_words, int interleave = 0,
-                 const MoeStackView* comb = nullptr, const MoeRoute* route = nullptr) {
+                 const MoeStackView* comb = nullptr, const MoeRoute* route = nullptr,
+                 const PrepParams* fin = nullptr) {
   PrepParams q = {};
+  if (fin != nullptr) q = *fin;   // the finishing fields
   q.mode = mode;
   q.x = x;
   q.ld = ld;
@@ -182,6 +217,13 @@ int enqueue_step(const bws_stack_plan* P, const uint16_t* x0, float* logits, voi
   MoeStackView pend_v;
   const MoeStackView* pending = nullptr;
   int moe_buf = 0;
+  // the last product's rows, when it deposited them for the next prep
+  PrepParams fin_v = {};
+  const PrepParams* fin = nullptr;
+  auto deposit = [&](const bws_matrix* mats, int nm, int epi, GemvParams& p) {
+    fin_v = PrepParams{};
+    fin = deposit_setup(mats, nm, epi, p, fin_v) ? &fin_v : nullptr;
+  };
   cudaError_t e = cudaSuccess;
 #define BWS_TRY(call)                          \
   do {                                         \
@@ -193,30 +235,41 @@ int enqueue_step(const bws_stack_plan* P, const uint16_t* x0, float* logits, voi
     if (L.kind == BWS_LAYER_MIXER_MLP) {
       int sum_out = 0;
       for (int i = 0; i < L.n_mixer_in; ++i) sum_out += L.mixer_in[i].d_out;
-      const GemvParams pin = product_params(c, L.mixer_in, L.n_mixer_in, kEpiStoreBF16, H, xa, u, sum_out);
+      GemvParams pin = product_params(c, L.mixer_in, L.n_mixer_in, kEpiStoreBF16, H, xa, u, sum_out);
       BWS_TRY(prep(c, kPrepRmsNorm, nullptr, 0, init, H, P->off_xp, P->xw, counters,
-                   tiles_for(L.mixer_in, L.n_mixer_in, kEpiStoreBF16), layout_for(L.mixer_in, pin), pending));
+                   tiles_for(L.mixer_in, L.n_mixer_in, kEpiStoreBF16), layout_for(L.mixer_in, pin), pending,
+                   nullptr, fin));
       init = nullptr;
       pending = nullptr;
+      deposit(L.mixer_in, L.n_mixer_in, kEpiStoreBF16, pin);
       BWS_TRY(product(c, L.mixer_in, L.n_mixer_in, kEpiStoreBF16, pin));
       const int dv = L.mixer_out.d_in;
-      const GemvParams pout = product_params(c, &L.mixer_out, 1, kEpiResidF32, dv, xv, r, H);
+      GemvParams pout = product_params(c, &L.mixer_out, 1, kEpiResidF32, dv, xv, r, H);
       BWS_TRY(prep(c, kPrepCopy, u, sum_out, nullptr, dv, P->off_vp, P->vw, counters,
-                   tiles_for(&L.mixer_out, 1, kEpiResidF32), layout_for(&L.mixer_out, pout)));
+                   tiles_for(&L.mixer_out, 1, kEpiResidF32), layout_for(&L.mixer_out, pout), nullptr, nullptr, fin));
+      deposit(&L.mixer_out, 1, kEpiResidF32, pout);
       BWS_TRY(product(c, &L.mixer_out, 1, kEpiResidF32, pout));
     }
     if (L.kind == BWS_LAYER_MIXER_MLP || L.kind == BWS_LAYER_MLP) {
       const bws_matrix gu[2] = {L.gate, L.up};
-      const GemvParams pgu = product_params(c, gu, 2, kEpiSwiGLU, H, xa, h, L.gate.d_out);
+      GemvParams pgu = product_params(c, gu, 2, kEpiSwiGLU, H, xa, h, L.gate.d_out);
       BWS_TRY(prep(c, kPrepRmsNorm, nullptr, 0, init, H, P->off_xp, P->xw, counters, tiles_for(gu, 2, kEpiSwiGLU),
-                   layout_for(gu, pgu), pending));
+                   layout_for(gu, pgu), pending, nullptr, fin));
       init = nullptr;
       pending = nullptr;
+      deposit(gu, 2, kEpiSwiGLU, pgu);
       BWS_TRY(product(c, gu, 2, kEpiSwiGLU, pgu));
       const int I = L.down.d_in;
-      const GemvParams pdn = product_params(c, &L.down, 1, kEpiResidF32, I, xh, r, H);
+      GemvParams pdn = product_params(c, &L.down, 1, kEpiResidF32, I, xh, r, H);
       BWS_TRY(prep(c, kPrepCopy, h, I, nullptr, I, P->off_hp, P->hw, counters, tiles_for(&L.down, 1, kEpiResidF32),
-                   layout_for(&L.down, pdn)));
+                   layout_for(&L.down, pdn), nullptr, nullptr, fin));
+      // the next prep finishes the down rows unless it is an MoE layer's
+      // (routing and combine), which reads r as the product leaves it
+      const bool next_moe = li + 1 < P->layers.size() && P->layers[li + 1].kind == BWS_LAYER_MOE;
+      if (next_moe)
+        fin = nullptr;
+      else
+        deposit(&L.down, 1, kEpiResidF32, pdn);
       BWS_TRY(product(c, &L.down, 1, kEpiResidF32, pdn));
     }
     if (L.kind == BWS_LAYER_MOE) {
@@ -234,7 +287,7 @@ int enqueue_step(const bws_stack_plan* P, const uint16_t* x0, float* logits, voi
   }
   const GemvParams ph = product_params(c, &P->head, 1, kEpiStoreF32, H, xa, logits, P->head.d_out);
   BWS_TRY(prep(c, kPrepRmsNorm, nullptr, 0, init, H, P->off_xp, P->xw, counters, tiles_for(&P->head, 1, kEpiStoreF32),
-               layout_for(&P->head, ph), pending));
+               layout_for(&P->head, ph), pending, nullptr, fin));
   BWS_TRY(product(c, &P->head, 1, kEpiStoreF32, ph));
 #undef BWS_TRY
   return BWS_OK;
