@@ -74,6 +74,11 @@ BWS_DEV void cp_async16(uint32_t smem_addr, const void* g) {
 BWS_DEV void cp_async8_zfill(uint32_t smem_addr, const void* g, uint32_t src_bytes) {
   asm volatile("cp.async.ca.shared.global [%0], [%1], 8, %2;" :: "r"(smem_addr), "l"(g), "r"(src_bytes) : "memory");
 }
+// cp_async8_zfill with an L2 policy (see l2_evict_first).
+BWS_DEV void cp_async8_zfill_hint(uint32_t smem_addr, const void* g, uint32_t src_bytes, uint64_t pol) {
+  asm volatile("cp.async.ca.shared.global.L2::cache_hint [%0], [%1], 8, %2, %3;"
+               :: "r"(smem_addr), "l"(g), "r"(src_bytes), "l"(pol) : "memory");
+}
 // One arrival on the mbarrier once every earlier cp.async of this thread has
 // landed (counted in the barrier's expected arrivals: no pending increment).
 BWS_DEV void cp_async_mbar_arrive(uint32_t bar) {
@@ -136,6 +141,13 @@ BWS_DEV void tma_load_2d_hint(uint32_t dst, const void* tmap, int x, int y, uint
       "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
       " [%0], [%1, {%2, %3}], [%4], %5;"
       :: "r"(dst), "l"(tmap), "r"(x), "r"(y), "r"(bar), "l"(pol) : "memory");
+}
+// tma_load_3d (below) with an L2 policy.
+BWS_DEV void tma_load_3d_hint(uint32_t dst, const void* tmap, int x, int y, int z, uint32_t bar, uint64_t pol) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
+      " [%0], [%1, {%2, %3, %4}], [%5], %6;"
+      :: "r"(dst), "l"(tmap), "r"(x), "r"(y), "r"(z), "r"(bar), "l"(pol) : "memory");
 }
 // 3D tiled TMA load of box (x, y, z) into shared memory, completing on bar.
 BWS_DEV void tma_load_3d(uint32_t dst, const void* tmap, int x, int y, int z, uint32_t bar) {

@@ -417,6 +417,7 @@ __global__ void __launch_bounds__(kThreadsMoe, 2) gemv_tma_moe_kernel(const __gr
     // ---- producer warp: lane 0 the TMA code boxes and activations of each
     // unit, every lane one scale row of each box ----
     const int rb = p.d_in >> 5;
+    const uint64_t pol = l2_evict_first();   // expert weights are read once per step
     auto issue = [&](int tile, int ks, int s) {
       const int slot = tile / p.tiles_per_slot, lt = tile - slot * p.tiles_per_slot;
       const int e = T.slot_expert[slot];
@@ -428,9 +429,9 @@ __global__ void __launch_bounds__(kThreadsMoe, 2) gemv_tma_moe_kernel(const __gr
         for (int b = 0; b < kBoxes; ++b) {
           const int row = box_row<EPI>(p, lt, b);
           if (e < 0)
-            tma_load_2d(dst + b * kBoxBytes, &p.shared, ks * 128, row, full);
+            tma_load_2d_hint(dst + b * kBoxBytes, &p.shared, ks * 128, row, full, pol);
           else
-            tma_load_3d(dst + b * kBoxBytes, &p.experts, ks * 128, row, e, full);
+            tma_load_3d_hint(dst + b * kBoxBytes, &p.experts, ks * 128, row, e, full, pol);
         }
         const uint16_t* src = p.x.hi + (size_t)(p.x.shared ? 0 : slot) * (p.N + 1) * p.d_in_pad + (size_t)ks * 256;
         for (int tok = 0; tok < p.N; ++tok)
@@ -441,7 +442,8 @@ __global__ void __launch_bounds__(kThreadsMoe, 2) gemv_tma_moe_kernel(const __gr
       for (int b = 0; b < kBoxes; ++b) {
         const int row = box_row<EPI>(p, lt, b) + lane;
         const bool in = row < box_limit<EPI>(p, b);
-        cp_async8_zfill(dst + kCodeBytes + b * 256 + lane * 8, sb + (size_t)(in ? row : 0) * rb, in ? 8u : 0u);
+        cp_async8_zfill_hint(dst + kCodeBytes + b * 256 + lane * 8, sb + (size_t)(in ? row : 0) * rb, in ? 8u : 0u,
+                             pol);
       }
       cp_async_mbar_arrive(full);
     };
