@@ -437,11 +437,12 @@ cudaError_t launch_prep(const PrepParams& q, cudaStream_t st, bool pdl) {
   // y itself (or SiLU(g) * u) for a copy
   if (fin && (moe || (q.mode == kPrepRmsNorm) != (q.fin_epi == kEpiResidF32))) return cudaErrorInvalidValue;
   // rows: one CTA of 1024 threads; 8192 on, a cluster of 8 x 256; finishing
-  // a product, a cluster of 2 x 512 (or 8 x 256) with room for its loads
+  // a product, a cluster of 2 x 512 (8 x 512 from 8192 on: a chunk per
+  // thread up to 32768) with room for its loads
   const int cl = long_row ? 8 : (fin ? 2 : 1);
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)(slots * q.N * cl + (q.has_route ? 1 : 0)));
-  cfg.blockDim = dim3(long_row ? 256 : (fin || moe ? 512 : 1024));
+  cfg.blockDim = dim3(long_row ? (fin ? 512 : 256) : (fin || moe ? 512 : 1024));
   cfg.stream = st;
   cudaLaunchAttribute a[2];
   int na = 0;
@@ -460,7 +461,7 @@ cudaError_t launch_prep(const PrepParams& q, cudaStream_t st, bool pdl) {
   cfg.attrs = a;
   cfg.numAttrs = na;
   if (long_row) {
-    if (fin) return cudaLaunchKernelEx(&cfg, prep_fin_kernel<8, 256>, q);
+    if (fin) return cudaLaunchKernelEx(&cfg, prep_fin_kernel<8, 512>, q);
     return moe ? cudaLaunchKernelEx(&cfg, prep_kernel<8, 256, true>, q)
                : cudaLaunchKernelEx(&cfg, prep_kernel<8, 256, false>, q);
   }
