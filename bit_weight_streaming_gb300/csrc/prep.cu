@@ -56,7 +56,7 @@ BWS_DEV void chunk_bf16(const PrepParams& q, int c, const float* rr, const uint4
 // in CTA order from zero, times the matrix's scale, times 2^(E - 14) of the
 // product's input; SwiGLU (SWI): SiLU(gate) * up. Only the finishing
 // instantiations of the prep use it.
-template <bool SWI>
+template <bool SWI, int KB>
 __device__ __forceinline__ void finish_chunk(const PrepParams& q, int tok, int e, float (&out)[8]) {
   int m = 0;
   for (int i = 1; i < q.fin_n_mats; ++i)
@@ -71,8 +71,8 @@ __device__ __forceinline__ void finish_chunk(const PrepParams& q, int tok, int e
   float a[8], au[8];
 #pragma unroll
   for (int i = 0; i < 8; ++i) a[i] = au[i] = 0.0f;
-  // 32 values in flight per batch of slots
-  constexpr int kB = SWI ? 2 : 4, kV = SWI ? 4 : 2;
+  // KB slots' loads in flight per batch
+  constexpr int kB = KB, kV = SWI ? 4 : 2;
   for (int cb = cc0; cb <= cc1; cb += kB) {
     float4 o[kB][kV];
 #pragma unroll
@@ -112,11 +112,14 @@ __device__ __forceinline__ void finish_chunk(const PrepParams& q, int tok, int e
   }
 }
 
+// KBN / KBS: slots per batch of loads for plain / SwiGLU rows (a tile of the
+// product's split has about nks * CTAs / units + 1 slots).
+template <int KBN, int KBS>
 BWS_DEV void finish(const PrepParams& q, int tok, int e, float (&out)[8]) {
   if (q.fin_epi == kEpiSwiGLU)
-    finish_chunk<true>(q, tok, e, out);
+    finish_chunk<true, KBS>(q, tok, e, out);
   else
-    finish_chunk<false>(q, tok, e, out);
+    finish_chunk<false, KBN>(q, tok, e, out);
 }
 
 // The previous MoE layer's combine for chunk c of token tok, in slot order,
@@ -245,7 +248,7 @@ __device__ __noinline__ uint32_t image_chunks(const PrepParams& q, int c0, int c
 
 // MOE: the body with the routing CTA and the folded combine; FIN: the one
 // that finishes the previous product's rows from its deposits.
-template <int CL, int THREADS, bool MOE, bool FIN>
+template <int CL, int THREADS, bool MOE, bool FIN, int KBN = 1, int KBS = 1>
 __device__ __forceinline__ void prep_body(const PrepParams& q) {
   pdl_launch_dependents();
   pdl_wait();
@@ -314,7 +317,7 @@ __device__ __forceinline__ void prep_body(const PrepParams& q) {
         v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w; v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
         if constexpr (FIN) {   // r += the previous product's rows
           float f[8];
-          finish(q, tok, 8 * c, f);
+          finish<KBN, KBS>(q, tok, 8 * c, f);
 #pragma unroll
           for (int i = 0; i < 8; ++i) v[i] = __fadd_rn(v[i], f[i]);
           reinterpret_cast<float4*>(rr)[2 * c] = make_float4(v[0], v[1], v[2], v[3]);
@@ -334,7 +337,7 @@ __device__ __forceinline__ void prep_body(const PrepParams& q) {
       uint4 b;
       if constexpr (FIN) {   // the previous product's rows, stored as it would have
         float f[8];
-        finish(q, tok, 8 * c, f);
+        finish<KBN, KBS>(q, tok, 8 * c, f);
         uint32_t wb[4];
 #pragma unroll
         for (int i = 0; i < 4; ++i)
@@ -420,9 +423,9 @@ __global__ void __launch_bounds__(THREADS) prep_kernel(const __grid_constant__ P
   prep_body<CL, THREADS, MOE, false>(q);
 }
 
-template <int CL, int THREADS>
+template <int CL, int THREADS, int KBN, int KBS>
 __global__ void __launch_bounds__(THREADS, 2) prep_fin_kernel(const __grid_constant__ PrepParams q) {
-  prep_body<CL, THREADS, false, true>(q);
+  prep_body<CL, THREADS, false, true, KBN, KBS>(q);
 }
 
 }  // namespace
@@ -436,13 +439,13 @@ cudaError_t launch_prep(const PrepParams& q, cudaStream_t st, bool pdl) {
   // a finished row is the previous product's output: r += y for RMSNorm,
   // y itself (or SiLU(g) * u) for a copy
   if (fin && (moe || (q.mode == kPrepRmsNorm) != (q.fin_epi == kEpiResidF32))) return cudaErrorInvalidValue;
-  // rows: one CTA of 1024 threads; 8192 on, a cluster of 8 x 256; finishing
-  // a product, a cluster of 2 x 512 (8 x 512 from 8192 on: a chunk per
-  // thread up to 32768) with room for its loads
-  const int cl = long_row ? 8 : (fin ? 2 : 1);
+  // rows: one CTA of 1024 threads; 8192 on, a cluster of 8 x 256. Finishing
+  // a product: a chunk per thread, and registers for a tile's slots in one
+  // batch of loads: a cluster of 4 x 256 (8 x 384 from 8192 on, to 24576)
+  const int cl = long_row ? 8 : (fin ? 4 : 1);
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)(slots * q.N * cl + (q.has_route ? 1 : 0)));
-  cfg.blockDim = dim3(long_row ? (fin ? 512 : 256) : (fin || moe ? 512 : 1024));
+  cfg.blockDim = dim3(long_row ? (fin ? 384 : 256) : (fin ? 256 : (moe ? 512 : 1024)));
   cfg.stream = st;
   cudaLaunchAttribute a[2];
   int na = 0;
@@ -461,11 +464,11 @@ cudaError_t launch_prep(const PrepParams& q, cudaStream_t st, bool pdl) {
   cfg.attrs = a;
   cfg.numAttrs = na;
   if (long_row) {
-    if (fin) return cudaLaunchKernelEx(&cfg, prep_fin_kernel<8, 512>, q);
+    if (fin) return cudaLaunchKernelEx(&cfg, prep_fin_kernel<8, 384, 4, 3>, q);
     return moe ? cudaLaunchKernelEx(&cfg, prep_kernel<8, 256, true>, q)
                : cudaLaunchKernelEx(&cfg, prep_kernel<8, 256, false>, q);
   }
-  if (fin) return cudaLaunchKernelEx(&cfg, prep_fin_kernel<2, 512>, q);
+  if (fin) return cudaLaunchKernelEx(&cfg, prep_fin_kernel<4, 256, 10, 4>, q);
   if (moe) return cudaLaunchKernelEx(&cfg, prep_kernel<1, 512, true>, q);
   return cudaLaunchKernelEx(&cfg, prep_kernel<1, 1024, false>, q);
 }
