@@ -156,6 +156,8 @@ int num_sms();
 long long gemv_max_warps();
 
 cudaError_t launch_prep(const PrepParams& q, cudaStream_t st, bool pdl);
+// Whether a prep can finish the deposits of a product into rows of d values.
+bool prep_can_finish(int d);
 cudaError_t launch_gemv(int fmt, int epi, const GemvParams& p, cudaStream_t st, bool pdl);
 // The TMA-fed product kernel (gemv_tma.cu) for plain-mode NVFP4 (d_in % 256
 // == 0) and FP8 (d_in % 128 == 0) products with 16-byte aligned tensors.

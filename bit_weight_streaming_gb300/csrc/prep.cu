@@ -112,15 +112,6 @@ __device__ __forceinline__ void finish_chunk(const PrepParams& q, int tok, int e
   }
 }
 
-// KBN / KBS: slots per batch of loads for plain / SwiGLU rows (a tile of the
-// product's split has about nks * CTAs / units + 1 slots).
-template <int KBN, int KBS>
-BWS_DEV void finish(const PrepParams& q, int tok, int e, float (&out)[8]) {
-  if (q.fin_epi == kEpiSwiGLU)
-    finish_chunk<true, KBS>(q, tok, e, out);
-  else
-    finish_chunk<false, KBN>(q, tok, e, out);
-}
 
 // The previous MoE layer's combine for chunk c of token tok, in slot order,
 // added to r (v: the chunk's residual values, updated). Out of line: its
@@ -246,10 +237,54 @@ __device__ __noinline__ uint32_t image_chunks(const PrepParams& q, int c0, int c
   return flags;
 }
 
-// MOE: the body with the routing CTA and the folded combine; FIN: the one
-// that finishes the previous product's rows from its deposits.
-template <int CL, int THREADS, bool MOE, bool FIN, int KBN = 1, int KBS = 1>
+// The f16 bands of one 8-value chunk (BF16 bit patterns w) at exponent E,
+// stored at chunk position dst of the row's band arrays; flags: bit 0 an
+// element needs the lo band, bit 1 an element is below both.
+BWS_DEV void store_bands(const uint32_t (&w)[4], int E, uint4* hi4, uint4* lo4, int dst, uint32_t& flags) {
+  uint32_t h[4], l[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    uint32_t hh[2], ll[2];
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+      const float f = bf16_bits_to_f32(j == 0 ? (w[i] & 0xFFFF) : (w[i] >> 16));
+      const float a = ldexp_exact(f, 14 - E);
+      hh[j] = 0u;
+      ll[j] = 0u;
+      if (fabsf(a) >= 0x1p-14f) {
+        hh[j] = __half_as_ushort(__float2half_rn(a));
+      } else if (f != 0.0f) {
+        const float b = ldexp_exact(f, 43 - E);
+        if (fabsf(b) >= 0x1p-14f) {
+          ll[j] = __half_as_ushort(__float2half_rn(b));
+          flags |= 1u;
+        } else {
+          flags |= 2u;
+        }
+      }
+    }
+    h[i] = hh[0] | (hh[1] << 16);
+    l[i] = ll[0] | (ll[1] << 16);
+  }
+  hi4[dst] = make_uint4(h[0], h[1], h[2], h[3]);
+  lo4[dst] = make_uint4(l[0], l[1], l[2], l[3]);
+}
+
+// Chunk position of chunk c in the TMA kernel's layout: within each unit of
+// K_u values, the 8-value chunk j of lane chunk cl (cl = 0..7, lane chunks of
+// K_u/8 values) moves to j * 8 + cl, so that the 8 lanes of a shared-memory
+// phase read 8 different banks.
+BWS_DEV int band_pos(int c, int interleave) {
+  if (!interleave) return c;
+  const int ku8 = interleave / 8, lk8 = interleave / 64;
+  const int u = c / ku8, r8 = c - u * ku8;
+  return u * ku8 + (r8 % lk8) * 8 + r8 / lk8;
+}
+
+// MOE: the body with the routing CTA and the folded combine.
+template <int CL, int THREADS, bool MOE>
 __device__ __forceinline__ void prep_body(const PrepParams& q) {
+  constexpr bool FIN = false;
   pdl_launch_dependents();
   pdl_wait();
   const int rank = CL == 1 ? 0 : (int)cg::this_cluster().block_rank();
@@ -315,14 +350,6 @@ __device__ __forceinline__ void prep_body(const PrepParams& q) {
         const float4 a = reinterpret_cast<const float4*>(rr)[2 * c];
         const float4 b = reinterpret_cast<const float4*>(rr)[2 * c + 1];
         v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w; v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
-        if constexpr (FIN) {   // r += the previous product's rows
-          float f[8];
-          finish<KBN, KBS>(q, tok, 8 * c, f);
-#pragma unroll
-          for (int i = 0; i < 8; ++i) v[i] = __fadd_rn(v[i], f[i]);
-          reinterpret_cast<float4*>(rr)[2 * c] = make_float4(v[0], v[1], v[2], v[3]);
-          reinterpret_cast<float4*>(rr)[2 * c + 1] = make_float4(v[4], v[5], v[6], v[7]);
-        }
         if (MOE && q.comb_ys != nullptr) combine_chunk(q, tok, c, v, rr);
       }
 #pragma unroll
@@ -334,20 +361,7 @@ __device__ __forceinline__ void prep_body(const PrepParams& q) {
   } else {
     xr = reinterpret_cast<const uint4*>(q.x + (size_t)slot * q.x_slot_stride + (size_t)tok * q.ld);
     for (int c = c0 + threadIdx.x; c < c1 && c < nchunk; c += blockDim.x) {
-      uint4 b;
-      if constexpr (FIN) {   // the previous product's rows, stored as it would have
-        float f[8];
-        finish<KBN, KBS>(q, tok, 8 * c, f);
-        uint32_t wb[4];
-#pragma unroll
-        for (int i = 0; i < 4; ++i)
-          wb[i] = (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(f[2 * i])) |
-                  ((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(f[2 * i + 1])) << 16);
-        b = make_uint4(wb[0], wb[1], wb[2], wb[3]);
-        const_cast<uint4*>(xr)[c] = b;
-      } else {
-        b = __ldg(xr + c);
-      }
+      const uint4 b = __ldg(xr + c);
       const uint32_t w[4] = {b.x, b.y, b.z, b.w};
 #pragma unroll
       for (int i = 0; i < 4; ++i)
@@ -368,46 +382,10 @@ __device__ __forceinline__ void prep_body(const PrepParams& q) {
   } else {
   uint4* hi4 = reinterpret_cast<uint4*>(q.hi + rowbase + (size_t)tok * q.d_in_pad);
   uint4* lo4 = reinterpret_cast<uint4*>(q.lo + rowbase + (size_t)tok * q.d_in_pad);
-  // TMA-kernel layout: within each unit of K_u values, the 8-value chunk j of
-  // lane chunk cl (cl = 0..7, lane chunks of K_u/8 values) moves to chunk
-  // position j * 8 + cl, so that the 8 lanes of a shared-memory phase read 8
-  // different banks.
-  const int ku8 = q.interleave / 8, lk8 = q.interleave / 64;
   for (int c = c0 + threadIdx.x; c < c1; c += blockDim.x) {
-    int dst = c;
-    if (q.interleave) {
-      const int u = c / ku8, r8 = c - u * ku8;
-      dst = u * ku8 + (r8 % lk8) * 8 + r8 / lk8;
-    }
     uint32_t w[4] = {0u, 0u, 0u, 0u};
     if (c < nchunk) chunk_bf16<FIN>(q, c, rr, xr, inv_rms, w);
-    uint32_t h[4], l[4];
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      uint32_t hh[2], ll[2];
-#pragma unroll
-      for (int j = 0; j < 2; ++j) {
-        const float f = bf16_bits_to_f32(j == 0 ? (w[i] & 0xFFFF) : (w[i] >> 16));
-        const float a = ldexp_exact(f, 14 - E);
-        hh[j] = 0u;
-        ll[j] = 0u;
-        if (fabsf(a) >= 0x1p-14f) {
-          hh[j] = __half_as_ushort(__float2half_rn(a));
-        } else if (f != 0.0f) {
-          const float b = ldexp_exact(f, 43 - E);
-          if (fabsf(b) >= 0x1p-14f) {
-            ll[j] = __half_as_ushort(__float2half_rn(b));
-            flags |= 1u;
-          } else {
-            flags |= 2u;
-          }
-        }
-      }
-      h[i] = hh[0] | (hh[1] << 16);
-      l[i] = ll[0] | (ll[1] << 16);
-    }
-    hi4[dst] = make_uint4(h[0], h[1], h[2], h[3]);
-    lo4[dst] = make_uint4(l[0], l[1], l[2], l[3]);
+    store_bands(w, E, hi4, lo4, band_pos(c, q.interleave), flags);
   }
   }
   const uint32_t wf = __reduce_or_sync(0xffffffffu, flags);
@@ -416,19 +394,129 @@ __device__ __forceinline__ void prep_body(const PrepParams& q) {
   if (CL > 1) asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 
-// The plain instantiations keep few registers, so that they fit beside
-// running product CTAs; the finishing one is capped to fit beside one.
-template <int CL, int THREADS, bool MOE>
-__global__ void __launch_bounds__(THREADS) prep_kernel(const __grid_constant__ PrepParams q) {
-  prep_body<CL, THREADS, MOE, false>(q);
+// The prep that finishes the previous product's rows (one slot; a cluster of
+// CL CTAs, one 8-value chunk per thread): RMS, the RMSNorm of r += y (the
+// product a residual update), else a copy of y (SWI: SiLU(g) * u). Each
+// thread keeps its chunk in registers from the statistics to the bands, and
+// the cluster's statistics meet in rank 0's shared memory in one barrier.
+// KB: slots per batch of loads (a tile of the product's split has about
+// nks * CTAs / units + 1 slots).
+template <int CL, int THREADS, int KB, bool RMS, bool SWI>
+__device__ __forceinline__ void prep_fin_body(const PrepParams& q) {
+  constexpr int kW = THREADS / 32;
+  pdl_launch_dependents();
+  pdl_wait();
+  cg::cluster_group cl = cg::this_cluster();
+  const int rank = (int)cl.block_rank();
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < q.zero_words; i += gridDim.x * blockDim.x)
+    q.zero_ptr[i] = 0u;
+  const int tok = blockIdx.x / CL;
+  // the band flags are OR-ed in by the warps that find any; the cluster
+  // barrier below orders this clearing store before them
+  if (rank == 0 && threadIdx.x == 0) q.flags[tok] = 0u;
+  const int nchunk = q.d_in >> 3, nchunk_pad = q.d_in_pad >> 3;
+  const int per = (nchunk_pad + CL - 1) / CL;   // <= THREADS (launch_prep)
+  const int c0 = rank * per < nchunk_pad ? rank * per : nchunk_pad;
+  const int c1 = c0 + per < nchunk_pad ? c0 + per : nchunk_pad;
+  const int c = c0 + threadIdx.x;
+  const bool live = c < c1 && c < nchunk;
+  if (tok == 0 && q.interleave != kLayoutImage && c < c1) {   // the all-zero row
+    reinterpret_cast<uint4*>(q.hi + (size_t)q.N * q.d_in_pad)[c] = make_uint4(0, 0, 0, 0);
+    reinterpret_cast<uint4*>(q.lo + (size_t)q.N * q.d_in_pad)[c] = make_uint4(0, 0, 0, 0);
+  }
+  float* rr = RMS ? q.r + (size_t)tok * q.d_in : nullptr;
+  uint4* xr = RMS ? nullptr : const_cast<uint4*>(reinterpret_cast<const uint4*>(q.x + (size_t)tok * q.ld));
+  float v[8];
+  uint32_t w[4] = {0u, 0u, 0u, 0u};
+  float ss = 0.0f, ma = 0.0f;
+  if (live) {
+    if (RMS) {   // r += y
+      const float4 a = reinterpret_cast<const float4*>(rr)[2 * c];
+      const float4 b = reinterpret_cast<const float4*>(rr)[2 * c + 1];
+      float f[8];
+      finish_chunk<false, KB>(q, tok, 8 * c, f);
+      v[0] = __fadd_rn(a.x, f[0]); v[1] = __fadd_rn(a.y, f[1]); v[2] = __fadd_rn(a.z, f[2]);
+      v[3] = __fadd_rn(a.w, f[3]); v[4] = __fadd_rn(b.x, f[4]); v[5] = __fadd_rn(b.y, f[5]);
+      v[6] = __fadd_rn(b.z, f[6]); v[7] = __fadd_rn(b.w, f[7]);
+      reinterpret_cast<float4*>(rr)[2 * c] = make_float4(v[0], v[1], v[2], v[3]);
+      reinterpret_cast<float4*>(rr)[2 * c + 1] = make_float4(v[4], v[5], v[6], v[7]);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        ss = __fmaf_rn(v[i], v[i], ss);
+        ma = fmaxf(ma, fabsf(v[i]));
+      }
+    } else {     // y as the product would have stored it
+      finish_chunk<SWI, KB>(q, tok, 8 * c, v);
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+        w[i] = (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(v[2 * i])) |
+               ((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(v[2 * i + 1])) << 16);
+      xr[c] = make_uint4(w[0], w[1], w[2], w[3]);
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+        ma = fmaxf(ma, fmaxf(fabsf(bf16_bits_to_f32(w[i] & 0xFFFF)), fabsf(bf16_bits_to_f32(w[i] >> 16))));
+    }
+  }
+  // the statistics: each warp's into rank 0's table, one cluster barrier,
+  // then every warp adds the table in the same fixed order
+  __shared__ float2 parts[CL * kW];
+  ss = warp_sum(ss);
+  ma = warp_max(ma);
+  if (lane == 0) *cl.map_shared_rank(&parts[rank * kW + warp], 0) = make_float2(ss, ma);
+  cl.sync();
+  const float2* tab = cl.map_shared_rank(parts, 0);
+  float ts = 0.0f, tm = 0.0f;
+  for (int i = lane; i < CL * kW; i += 32) {
+    const float2 o = tab[i];
+    ts += o.x;
+    tm = fmaxf(tm, o.y);
+  }
+  ts = warp_sum(ts);
+  tm = warp_max(tm);
+  // done with rank 0's table; the wait at the end keeps rank 0 alive until all have read
+  asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+  float inv_rms = 1.0f, mx = tm;
+  if (RMS) {
+    inv_rms = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(__fdiv_rn(ts, (float)q.d_in), q.eps)));
+    mx = __bfloat162float(__float2bfloat16_rn(__fmul_rn(mx, inv_rms)));
+  }
+  const int E = mx > 0.0f ? floor_log2_abs(mx) : 0;
+  uint32_t flags = 0u;
+  if (q.interleave == kLayoutImage) {   // the tensor-core kernel's image reads the row back
+    flags = image_chunks<true>(q, c0, c1, rr, xr, inv_rms, E);
+  } else if (c < c1) {
+    if (live && RMS) {
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+        w[i] = (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(__fmul_rn(v[2 * i], inv_rms))) |
+               ((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(__fmul_rn(v[2 * i + 1], inv_rms))) << 16);
+    }
+    uint4* hi4 = reinterpret_cast<uint4*>(q.hi + (size_t)tok * q.d_in_pad);
+    uint4* lo4 = reinterpret_cast<uint4*>(q.lo + (size_t)tok * q.d_in_pad);
+    store_bands(w, E, hi4, lo4, band_pos(c, q.interleave), flags);
+  }
+  const uint32_t wf = __reduce_or_sync(0xffffffffu, flags);
+  if (wf != 0u && lane == 0) atomicOr(q.flags + tok, wf);
+  if (rank == 0 && threadIdx.x == 0) q.exp[tok] = E;
+  asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 
-template <int CL, int THREADS, int KBN, int KBS>
+// The plain instantiations keep few registers, so that they fit beside
+// running product CTAs; the finishing ones are capped to fit beside one.
+template <int CL, int THREADS, bool MOE>
+__global__ void __launch_bounds__(THREADS) prep_kernel(const __grid_constant__ PrepParams q) {
+  prep_body<CL, THREADS, MOE>(q);
+}
+
+template <int CL, int THREADS, int KB, bool RMS, bool SWI>
 __global__ void __launch_bounds__(THREADS, 2) prep_fin_kernel(const __grid_constant__ PrepParams q) {
-  prep_body<CL, THREADS, false, true, KBN, KBS>(q);
+  prep_fin_body<CL, THREADS, KB, RMS, SWI>(q);
 }
 
 }  // namespace
+
+bool prep_can_finish(int d) { return (d + 127) / 128 * 128 <= 3 * kLongRow; }
 
 cudaError_t launch_prep(const PrepParams& q, cudaStream_t st, bool pdl) {
   const int slots = q.n_slots != nullptr ? q.max_slots : 1;
@@ -436,12 +524,16 @@ cudaError_t launch_prep(const PrepParams& q, cudaStream_t st, bool pdl) {
   const bool moe = q.has_route || q.comb_ys != nullptr;
   const bool fin = q.fin_partials != nullptr;
   if (q.has_route && long_row) return cudaErrorInvalidValue;   // the routing CTA needs one-CTA rows
-  // a finished row is the previous product's output: r += y for RMSNorm,
-  // y itself (or SiLU(g) * u) for a copy
-  if (fin && (moe || (q.mode == kPrepRmsNorm) != (q.fin_epi == kEpiResidF32))) return cudaErrorInvalidValue;
   // rows: one CTA of 1024 threads; 8192 on, a cluster of 8 x 256. Finishing
-  // a product: a chunk per thread, and registers for a tile's slots in one
-  // batch of loads: a cluster of 4 x 256 (8 x 384 from 8192 on, to 24576)
+  // a product (one slot, no x0, status or combine): a chunk per thread, and
+  // registers for a tile's slots in one batch of loads: a cluster of 4 x 256
+  // (8 x 384 from 8192 on, to 24576)
+  if (fin) {
+    const bool rms = q.mode == kPrepRmsNorm;
+    if (moe || q.n_slots != nullptr || q.x0 != nullptr || q.hdr != nullptr || q.status_clear != nullptr ||
+        rms != (q.fin_epi == kEpiResidF32) || q.d_in_pad > 3 * kLongRow)
+      return cudaErrorInvalidValue;
+  }
   const int cl = long_row ? 8 : (fin ? 4 : 1);
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)(slots * q.N * cl + (q.has_route ? 1 : 0)));
@@ -463,12 +555,20 @@ cudaError_t launch_prep(const PrepParams& q, cudaStream_t st, bool pdl) {
   }
   cfg.attrs = a;
   cfg.numAttrs = na;
-  if (long_row) {
-    if (fin) return cudaLaunchKernelEx(&cfg, prep_fin_kernel<8, 384, 4, 3>, q);
+  if (fin) {
+    const bool swi = q.fin_epi == kEpiSwiGLU;
+    if (q.mode == kPrepRmsNorm)
+      return long_row ? cudaLaunchKernelEx(&cfg, prep_fin_kernel<8, 384, 4, true, false>, q)
+                      : cudaLaunchKernelEx(&cfg, prep_fin_kernel<4, 256, 10, true, false>, q);
+    if (swi)
+      return long_row ? cudaLaunchKernelEx(&cfg, prep_fin_kernel<8, 384, 3, false, true>, q)
+                      : cudaLaunchKernelEx(&cfg, prep_fin_kernel<4, 256, 4, false, true>, q);
+    return long_row ? cudaLaunchKernelEx(&cfg, prep_fin_kernel<8, 384, 4, false, false>, q)
+                    : cudaLaunchKernelEx(&cfg, prep_fin_kernel<4, 256, 10, false, false>, q);
+  }
+  if (long_row)
     return moe ? cudaLaunchKernelEx(&cfg, prep_kernel<8, 256, true>, q)
                : cudaLaunchKernelEx(&cfg, prep_kernel<8, 256, false>, q);
-  }
-  if (fin) return cudaLaunchKernelEx(&cfg, prep_fin_kernel<4, 256, 10, 4>, q);
   if (moe) return cudaLaunchKernelEx(&cfg, prep_kernel<1, 512, true>, q);
   return cudaLaunchKernelEx(&cfg, prep_kernel<1, 1024, false>, q);
 }

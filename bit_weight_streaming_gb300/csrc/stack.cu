@@ -87,10 +87,12 @@ XPrep xprep_of(const Ctx& c, size_t block, const GemvWorkspace& L) {
 // A product whose outputs only the next prep reads: run by the TMA kernel,
 // its CTAs deposit raw sums and that prep finishes the rows, so no CTA of
 // the product waits on a fix-up. Needs tiles that never share an 8-row chunk
-// with another matrix. Returns whether p now deposits; f: the prep's fields.
-bool deposit_setup(const bws_matrix* mats, int nm, int epi, GemvParams& p, PrepParams& f) {
+// with another matrix, and a finishing prep shape for the next_d rows the
+// prep reads. Returns whether p now deposits; f: the prep's fields.
+bool deposit_setup(const bws_matrix* mats, int nm, int epi, GemvParams& p, int next_d, PrepParams& f) {
   const int fmt = fmt_of(mats[0]);
-  if (fmt == kFmtMXFP4 || epi == kEpiStoreF32 || gemv_umma_eligible(fmt, p) || !gemv_tma_eligible(fmt, p))
+  if (fmt == kFmtMXFP4 || epi == kEpiStoreF32 || gemv_umma_eligible(fmt, p) || !gemv_tma_eligible(fmt, p) ||
+      !prep_can_finish(next_d))
     return false;
   const int rows = epi == kEpiSwiGLU ? 64 : 128;
   for (int i = 0; i < nm; ++i)
@@ -220,9 +222,9 @@ int enqueue_step(const bws_stack_plan* P, const uint16_t* x0, float* logits, voi
   // the last product's rows, when it deposited them for the next prep
   PrepParams fin_v = {};
   const PrepParams* fin = nullptr;
-  auto deposit = [&](const bws_matrix* mats, int nm, int epi, GemvParams& p) {
+  auto deposit = [&](const bws_matrix* mats, int nm, int epi, GemvParams& p, int next_d) {
     fin_v = PrepParams{};
-    fin = deposit_setup(mats, nm, epi, p, fin_v) ? &fin_v : nullptr;
+    fin = deposit_setup(mats, nm, epi, p, next_d, fin_v) ? &fin_v : nullptr;
   };
   cudaError_t e = cudaSuccess;
 #define BWS_TRY(call)                          \
@@ -241,13 +243,13 @@ int enqueue_step(const bws_stack_plan* P, const uint16_t* x0, float* logits, voi
                    nullptr, fin));
       init = nullptr;
       pending = nullptr;
-      deposit(L.mixer_in, L.n_mixer_in, kEpiStoreBF16, pin);
+      deposit(L.mixer_in, L.n_mixer_in, kEpiStoreBF16, pin, L.mixer_out.d_in);
       BWS_TRY(product(c, L.mixer_in, L.n_mixer_in, kEpiStoreBF16, pin));
       const int dv = L.mixer_out.d_in;
       GemvParams pout = product_params(c, &L.mixer_out, 1, kEpiResidF32, dv, xv, r, H);
       BWS_TRY(prep(c, kPrepCopy, u, sum_out, nullptr, dv, P->off_vp, P->vw, counters,
                    tiles_for(&L.mixer_out, 1, kEpiResidF32), layout_for(&L.mixer_out, pout), nullptr, nullptr, fin));
-      deposit(&L.mixer_out, 1, kEpiResidF32, pout);
+      deposit(&L.mixer_out, 1, kEpiResidF32, pout, H);
       BWS_TRY(product(c, &L.mixer_out, 1, kEpiResidF32, pout));
     }
     if (L.kind == BWS_LAYER_MIXER_MLP || L.kind == BWS_LAYER_MLP) {
@@ -257,7 +259,7 @@ int enqueue_step(const bws_stack_plan* P, const uint16_t* x0, float* logits, voi
                    layout_for(gu, pgu), pending, nullptr, fin));
       init = nullptr;
       pending = nullptr;
-      deposit(gu, 2, kEpiSwiGLU, pgu);
+      deposit(gu, 2, kEpiSwiGLU, pgu, L.gate.d_out);
       BWS_TRY(product(c, gu, 2, kEpiSwiGLU, pgu));
       const int I = L.down.d_in;
       GemvParams pdn = product_params(c, &L.down, 1, kEpiResidF32, I, xh, r, H);
@@ -269,7 +271,7 @@ int enqueue_step(const bws_stack_plan* P, const uint16_t* x0, float* logits, voi
       if (next_moe)
         fin = nullptr;
       else
-        deposit(&L.down, 1, kEpiResidF32, pdn);
+        deposit(&L.down, 1, kEpiResidF32, pdn, H);
       BWS_TRY(product(c, &L.down, 1, kEpiResidF32, pdn));
     }
     if (L.kind == BWS_LAYER_MOE) {
