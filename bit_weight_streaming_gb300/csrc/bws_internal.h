@@ -81,6 +81,8 @@ struct GemvParams {
   uint32_t* counters;      // [n_tiles], zero on entry, left zero on exit
   int prefetch_units;      // units pulled into L2 before waiting on the inputs
   size_t partials_bytes;   // slot mode: size of the partials scratch (0: the plain-mode size)
+  int split_light;         // TMA kernel: the last split_light CTAs start late (they wait for the
+                           // slots the prep before holds): give them a lighter share (SplitK)
   int deposit;             // TMA kernel: tile pieces leave their raw sums in partials for the
                            // next prep to finish (PrepParams::fin_*), nothing else is stored
 };
@@ -97,6 +99,28 @@ struct MoeRoute {
   float* cw;               // out [max_slots][N] combine weights
   uint32_t* status;        // out [1]: bit 4 set if an id was out of range
 };
+// A stream-K split of n_units units over n_ctas CTAs into contiguous ranges:
+// CTA c takes units [splitk_begin(c), splitk_begin(c + 1)). The CTAs from lf
+// on get num/den of the others' share (uniform: lf = n_ctas, num = den = 1).
+struct SplitK {
+  long long n_units;
+  int n_ctas, lf, num, den;
+};
+__host__ __device__ inline long long splitk_weight(const SplitK& s, long long c) {
+  return c <= s.lf ? c * s.den : (long long)s.lf * s.den + (c - s.lf) * s.num;
+}
+__host__ __device__ inline long long splitk_begin(const SplitK& s, long long c) {
+  return s.n_units * splitk_weight(s, c) / splitk_weight(s, s.n_ctas);
+}
+// The CTA whose range holds unit u: the last c with splitk_begin(c) <= u,
+// i.e. with weight W(c) <= ((u + 1) W(n_ctas) - 1) / n_units.
+__host__ __device__ inline int splitk_owner(const SplitK& s, long long u) {
+  const long long t = ((u + 1) * splitk_weight(s, s.n_ctas) - 1) / s.n_units;
+  const long long w_lf = (long long)s.lf * s.den;
+  const long long c = t < w_lf ? t / s.den : s.lf + (t - w_lf) / s.num;
+  return (int)(c < s.n_ctas - 1 ? c : s.n_ctas - 1);
+}
+
 // Input of the activation prep kernel.
 constexpr int kPrepCopy = 0;      // x bf16 -> bands
 constexpr int kPrepRmsNorm = 1;   // r fp32 -> BF16(RMSNorm(r)) -> bands
@@ -138,8 +162,8 @@ struct PrepParams {
   // kPrepRmsNorm; kEpiStoreBF16: bf16(y), kEpiSwiGLU: bf16(SiLU(g) * u), in
   // kPrepCopy, also written back to x)
   const float* fin_partials;
-  long long fin_units;     // the product's stream-K geometry (TmaGeom)
-  int fin_ctas, fin_nks;
+  SplitK fin_split;        // the product's stream-K split and units per tile (TmaGeom)
+  int fin_nks;
   int fin_epi, fin_fmt, fin_n_mats;
   int fin_d_out[kMaxMats], fin_row_off[kMaxMats], fin_tile_begin[kMaxMats];
   const float* fin_scale[kMaxMats];
@@ -158,17 +182,18 @@ long long gemv_max_warps();
 cudaError_t launch_prep(const PrepParams& q, cudaStream_t st, bool pdl);
 // Whether a prep can finish the deposits of a product into rows of d values.
 bool prep_can_finish(int d);
+// CTAs a prep of rows of d values runs per row (a cluster), finishing or not.
+int prep_ctas_per_row(int d, bool fin);
 cudaError_t launch_gemv(int fmt, int epi, const GemvParams& p, cudaStream_t st, bool pdl);
 // The TMA-fed product kernel (gemv_tma.cu) for plain-mode NVFP4 (d_in % 256
 // == 0) and FP8 (d_in % 128 == 0) products with 16-byte aligned tensors.
 bool gemv_tma_eligible(int fmt, const GemvParams& p);
 // Tiles of 128 rows (SwiGLU: 64 gate + 64 up rows) of the TMA kernels.
 int gemv_tma_tiles(int epi, const GemvMat* mats, int n_mats);
-// The TMA kernel's stream-K split of a product: n_tiles tiles of nks units,
-// units [c * n_units / n_ctas, (c + 1) * n_units / n_ctas) to CTA c.
+// The TMA kernel's stream-K split of a product: n_tiles tiles of nks units.
 struct TmaGeom {
-  int n_tiles, nks, n_ctas;
-  long long n_units;
+  int n_tiles, nks;
+  SplitK split;
 };
 TmaGeom gemv_tma_geometry(int fmt, int epi, const GemvParams& g);
 // Whether g's partials scratch holds the deposits (GemvParams::deposit) of

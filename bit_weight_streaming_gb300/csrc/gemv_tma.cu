@@ -59,6 +59,7 @@ struct TmaParams {
   int n_tiles;
   long long n_units;
   int n_ctas;
+  int lf, num, den;   // the split's lighter CTAs (SplitK)
   XPrep x;
   void* out;
   int out_ld;
@@ -99,8 +100,15 @@ BWS_DEV void box_of(const TmaParams& p, int tile, int b, int& m, int& row) {
   row = (tile - p.mats[m].tile_begin) * 128 + 32 * b;
 }
 
-BWS_DEV long long owner(long long u, long long U, long long G) { return ((u + 1) * G - 1) / U; }
-BWS_DEV long long begin_of(long long c, long long U, long long G) { return c * U / G; }
+BWS_DEV SplitK split_of(const TmaParams& p) {
+  SplitK s;
+  s.n_units = p.n_units;
+  s.n_ctas = p.n_ctas;
+  s.lf = p.lf;
+  s.num = p.num;
+  s.den = p.den;
+  return s;
+}
 
 // Inputs of a tile's stores that live in global memory, read when the tile
 // piece ends, before its reductions and the fix-up handshake, so that they
@@ -172,7 +180,6 @@ BWS_DEV void store_sub(const TmaParams& p, int tile, int b, int s, int g, int t,
 template <int FMT, int EPI, bool LO, bool N1>
 BWS_DEV void consume(const TmaParams& p, Tail& T, uint32_t stage0, long long u0, long long u1, int warp, int lane,
                      const uint16_t* xrow_l) {
-  const long long U = p.n_units, G = p.n_ctas;
   const int NS = p.n_stages;
   constexpr int kUnitK = FMT == kFmtFP8 ? 128 : 256;
   constexpr int kXv = FMT == kFmtFP8 ? 2 : 4;     // 16-byte activation pieces per unit
@@ -338,8 +345,8 @@ BWS_DEV void consume(const TmaParams& p, Tail& T, uint32_t stage0, long long u0,
       // them (release, cumulative over the barrier) and, for the last arriver,
       // makes the other CTAs' deposits visible (acquire)
       named_bar_sync(2, 4 * 32);
-      const long long c0 = owner((long long)cur_tile * p.nks, U, G);
-      const long long c1 = owner((long long)(cur_tile + 1) * p.nks - 1, U, G);
+      const long long c0 = splitk_owner(split_of(p), (long long)cur_tile * p.nks);
+      const long long c1 = splitk_owner(split_of(p), (long long)(cur_tile + 1) * p.nks - 1);
       if (threadIdx.x == 0) T.flag = atom_add_acq_rel_gpu(p.counters + cur_tile, 1u);
       named_bar_sync(2, 4 * 32);
       const uint32_t prev = T.flag;
@@ -422,8 +429,7 @@ __global__ void __launch_bounds__(kThreadsTma, 2) gemv_tma_kernel(const __grid_c
   Tail& T = *reinterpret_cast<Tail*>(sbase + (size_t)p.n_stages * p.stage_bytes);
   const uint32_t stage0 = smem_u32(sbase);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const long long U = p.n_units, G = p.n_ctas;
-  const long long u0 = begin_of(blockIdx.x, U, G), u1 = begin_of(blockIdx.x + 1, U, G);
+  const long long u0 = splitk_begin(split_of(p), blockIdx.x), u1 = splitk_begin(split_of(p), blockIdx.x + 1);
   const int NS = p.n_stages;
   pdl_launch_dependents();
   if (threadIdx.x == 0) {
@@ -567,14 +573,34 @@ TmaGeom gemv_tma_geometry(int fmt, int epi, const GemvParams& g) {
   TmaGeom t;
   t.nks = fmt == kFmtFP8 ? g.d_in / 128 : g.d_in / 256;
   t.n_tiles = gemv_tma_tiles(epi, g.mats, g.n_mats);
-  t.n_units = (long long)t.n_tiles * t.nks;
+  SplitK& s = t.split;
+  s.n_units = (long long)t.n_tiles * t.nks;
   const long long ctas = 2LL * num_sms();   // two CTAs per SM
-  t.n_ctas = (int)(t.n_units < ctas ? t.n_units : ctas);
+  s.n_ctas = (int)(s.n_units < ctas ? s.n_units : ctas);
+  s.lf = s.n_ctas;
+  s.num = s.den = 1;
+  // CTAs that start when the inputs are ready (behind the prep's slots) are
+  // about 1.5 us, two units of streaming, behind the others: their share is
+  // cut by that much, within [1/4, 1] of the others'
+  // (one token only: with more tokens fewer stages are primed, so the late
+  // CTAs lose less, and measured, lighter shares made those steps slower)
+  const int light = g.N == 1 ? g.split_light : 0;
+  if (light > 0 && light < s.n_ctas / 4 && s.n_ctas == ctas) {
+    const double per = (double)s.n_units / s.n_ctas;
+    int num = (int)(16.0 * (1.0 - 2.0 / per) + 0.5);
+    num = num < 4 ? 4 : num;
+    const long long w = 16LL * (s.n_ctas - light) + (long long)num * light;
+    if (num < 16 && (long long)num * s.n_units >= w) {   // every range keeps a unit
+      s.lf = s.n_ctas - light;
+      s.num = num;
+      s.den = 16;
+    }
+  }
   return t;
 }
 
 bool gemv_tma_deposit_fits(const TmaGeom& t, const GemvParams& g) {
-  return ((long long)t.n_tiles + t.n_ctas) * g.N * 128 * (long long)sizeof(float) <=
+  return ((long long)t.n_tiles + t.split.n_ctas) * g.N * 128 * (long long)sizeof(float) <=
          ((long long)g.n_tiles + gemv_max_warps()) * kSlotFloats * (long long)sizeof(float);
 }
 
@@ -614,8 +640,11 @@ cudaError_t launch_gemv_tma(int fmt, int epi, const GemvParams& g, uint32_t* sta
   const TmaGeom geo = gemv_tma_geometry(fmt, epi, g);
   p.nks = geo.nks;
   p.n_tiles = geo.n_tiles;
-  p.n_units = geo.n_units;
-  p.n_ctas = geo.n_ctas;
+  p.n_units = geo.split.n_units;
+  p.n_ctas = geo.split.n_ctas;
+  p.lf = geo.split.lf;
+  p.num = geo.split.num;
+  p.den = geo.split.den;
   p.deposit = g.deposit;
   if (p.deposit && (epi == kEpiStoreF32 || !gemv_tma_deposit_fits(geo, g))) return cudaErrorInvalidValue;
   p.x = g.x;

@@ -65,9 +65,8 @@ __device__ __forceinline__ void finish_chunk(const PrepParams& q, int tok, int e
   constexpr int kRows = SWI ? 64 : 128;
   const int tile = (SWI ? 0 : q.fin_tile_begin[m]) + lrow / kRows, rit = lrow % kRows;
   // the CTAs that hold the tile's first and last units
-  const long long U = q.fin_units, G = q.fin_ctas;
-  const int cc0 = (int)((((long long)tile * q.fin_nks + 1) * G - 1) / U);
-  const int cc1 = (int)(((long long)(tile + 1) * q.fin_nks * G - 1) / U);
+  const int cc0 = splitk_owner(q.fin_split, (long long)tile * q.fin_nks);
+  const int cc1 = splitk_owner(q.fin_split, (long long)(tile + 1) * q.fin_nks - 1);
   float a[8], au[8];
 #pragma unroll
   for (int i = 0; i < 8; ++i) a[i] = au[i] = 0.0f;
@@ -517,6 +516,8 @@ __global__ void __launch_bounds__(THREADS, 2) prep_fin_kernel(const __grid_const
 }  // namespace
 
 bool prep_can_finish(int d) { return (d + 127) / 128 * 128 <= 3 * kLongRow; }
+
+int prep_ctas_per_row(int d, bool fin) { return (d + 127) / 128 * 128 > kLongRow ? 8 : (fin ? 4 : 1); }
 
 cudaError_t launch_prep(const PrepParams& q, cudaStream_t st, bool pdl) {
   const int slots = q.n_slots != nullptr ? q.max_slots : 1;

@@ -101,8 +101,7 @@ bool deposit_setup(const bws_matrix* mats, int nm, int epi, GemvParams& p, int n
   if (!gemv_tma_deposit_fits(geo, p)) return false;
   p.deposit = 1;
   f.fin_partials = p.partials;
-  f.fin_units = geo.n_units;
-  f.fin_ctas = geo.n_ctas;
+  f.fin_split = geo.split;
   f.fin_nks = geo.nks;
   f.fin_epi = epi;
   f.fin_fmt = fmt;
@@ -222,6 +221,9 @@ int enqueue_step(const bws_stack_plan* P, const uint16_t* x0, float* logits, voi
   // the last product's rows, when it deposited them for the next prep
   PrepParams fin_v = {};
   const PrepParams* fin = nullptr;
+  // the product's CTAs that start late: the slots the prep before it (of rows
+  // of d values, finishing when fin is set) holds, on about twice as many
+  auto late_ctas = [&](int d) { return 2 * prep_ctas_per_row(d, fin != nullptr); };
   auto deposit = [&](const bws_matrix* mats, int nm, int epi, GemvParams& p, int next_d) {
     fin_v = PrepParams{};
     fin = deposit_setup(mats, nm, epi, p, next_d, fin_v) ? &fin_v : nullptr;
@@ -238,6 +240,7 @@ int enqueue_step(const bws_stack_plan* P, const uint16_t* x0, float* logits, voi
       int sum_out = 0;
       for (int i = 0; i < L.n_mixer_in; ++i) sum_out += L.mixer_in[i].d_out;
       GemvParams pin = product_params(c, L.mixer_in, L.n_mixer_in, kEpiStoreBF16, H, xa, u, sum_out);
+      pin.split_light = late_ctas(H);
       BWS_TRY(prep(c, kPrepRmsNorm, nullptr, 0, init, H, P->off_xp, P->xw, counters,
                    tiles_for(L.mixer_in, L.n_mixer_in, kEpiStoreBF16), layout_for(L.mixer_in, pin), pending,
                    nullptr, fin));
@@ -247,6 +250,7 @@ int enqueue_step(const bws_stack_plan* P, const uint16_t* x0, float* logits, voi
       BWS_TRY(product(c, L.mixer_in, L.n_mixer_in, kEpiStoreBF16, pin));
       const int dv = L.mixer_out.d_in;
       GemvParams pout = product_params(c, &L.mixer_out, 1, kEpiResidF32, dv, xv, r, H);
+      pout.split_light = late_ctas(dv);
       BWS_TRY(prep(c, kPrepCopy, u, sum_out, nullptr, dv, P->off_vp, P->vw, counters,
                    tiles_for(&L.mixer_out, 1, kEpiResidF32), layout_for(&L.mixer_out, pout), nullptr, nullptr, fin));
       deposit(&L.mixer_out, 1, kEpiResidF32, pout, H);
@@ -255,6 +259,7 @@ int enqueue_step(const bws_stack_plan* P, const uint16_t* x0, float* logits, voi
     if (L.kind == BWS_LAYER_MIXER_MLP || L.kind == BWS_LAYER_MLP) {
       const bws_matrix gu[2] = {L.gate, L.up};
       GemvParams pgu = product_params(c, gu, 2, kEpiSwiGLU, H, xa, h, L.gate.d_out);
+      pgu.split_light = late_ctas(H);
       BWS_TRY(prep(c, kPrepRmsNorm, nullptr, 0, init, H, P->off_xp, P->xw, counters, tiles_for(gu, 2, kEpiSwiGLU),
                    layout_for(gu, pgu), pending, nullptr, fin));
       init = nullptr;
@@ -263,6 +268,7 @@ int enqueue_step(const bws_stack_plan* P, const uint16_t* x0, float* logits, voi
       BWS_TRY(product(c, gu, 2, kEpiSwiGLU, pgu));
       const int I = L.down.d_in;
       GemvParams pdn = product_params(c, &L.down, 1, kEpiResidF32, I, xh, r, H);
+      pdn.split_light = late_ctas(I);
       BWS_TRY(prep(c, kPrepCopy, h, I, nullptr, I, P->off_hp, P->hw, counters, tiles_for(&L.down, 1, kEpiResidF32),
                    layout_for(&L.down, pdn), nullptr, nullptr, fin));
       // the next prep finishes the down rows unless it is an MoE layer's
@@ -287,7 +293,8 @@ int enqueue_step(const bws_stack_plan* P, const uint16_t* x0, float* logits, voi
       moe_buf ^= 1;
     }
   }
-  const GemvParams ph = product_params(c, &P->head, 1, kEpiStoreF32, H, xa, logits, P->head.d_out);
+  GemvParams ph = product_params(c, &P->head, 1, kEpiStoreF32, H, xa, logits, P->head.d_out);
+  ph.split_light = late_ctas(H);
   BWS_TRY(prep(c, kPrepRmsNorm, nullptr, 0, init, H, P->off_xp, P->xw, counters, tiles_for(&P->head, 1, kEpiStoreF32),
                layout_for(&P->head, ph), pending, nullptr, fin));
   BWS_TRY(product(c, &P->head, 1, kEpiStoreF32, ph));
