@@ -195,7 +195,7 @@ def time_steps(fn, steps, warmup, stream):
 # DRAM bytes (read + write) per algorithmic byte of the one-token NVFP4
 # product kernel, from ncu counters on four of the step's matrix shapes
 # (profiles/gemv_tma_nvfp4_traffic_n1.md).
-TRAFFIC_RATIO = 1.036
+TRAFFIC_RATIO = 1.033
 
 
 def time_dominant_kernel(stack, stream, reps=3):
