@@ -114,11 +114,14 @@ __host__ __device__ inline long long splitk_begin(const SplitK& s, long long c) 
 }
 // The CTA whose range holds unit u: the last c with splitk_begin(c) <= u,
 // i.e. with weight W(c) <= ((u + 1) W(n_ctas) - 1) / n_units.
+// (Divisions in 32 bits where the operands fit: a 64-bit division is a long
+// dependent chain on the GPU.)
 __host__ __device__ inline int splitk_owner(const SplitK& s, long long u) {
-  const long long t = ((u + 1) * splitk_weight(s, s.n_ctas) - 1) / s.n_units;
-  const long long w_lf = (long long)s.lf * s.den;
-  const long long c = t < w_lf ? t / s.den : s.lf + (t - w_lf) / s.num;
-  return (int)(c < s.n_ctas - 1 ? c : s.n_ctas - 1);
+  const long long x = (u + 1) * splitk_weight(s, s.n_ctas) - 1;
+  const uint32_t t = x <= 0xFFFFFFFFLL ? (uint32_t)x / (uint32_t)s.n_units : (uint32_t)(x / s.n_units);
+  const uint32_t w_lf = (uint32_t)s.lf * (uint32_t)s.den;
+  const uint32_t c = t < w_lf ? t / (uint32_t)s.den : (uint32_t)s.lf + (t - w_lf) / (uint32_t)s.num;
+  return (int)(c < (uint32_t)s.n_ctas - 1 ? c : (uint32_t)s.n_ctas - 1);
 }
 
 // Input of the activation prep kernel.

@@ -59,6 +59,19 @@ def test_dense_stack_parity(N):
     _check(stack, N, seed=N)
 
 
+def test_dense_stack_at_step_scale_one_token():
+    """Shapes large enough (hundreds of units per product, the h row over 8192
+    values) that at one token every path of the in-stack chain runs: products
+    depositing raw tile sums and the preps that finish them (residual, BF16
+    and SwiGLU stores, one- and long-row clusters), and the stream-K split
+    that gives the CTAs starting behind the prep a lighter share."""
+    from bit_weight_streaming_gb300 import workloads as W
+    bws()
+    stack = W.dense_27b(1, seed=11, n_layers=2, hidden=2048, inter=9216, vocab=1000, attn=(2048, 256, 256, 1536),
+                        gdn=(6144, 1536), quant=oracle_quantizers(device()), device=device())
+    _check(stack, 1, seed=12)
+
+
 def test_dense_stack_graph_replay_is_deterministic():
     stack = _dense_small(2)
     x0 = synth.activation_bf16(2, 256, seed=1, device=device())
