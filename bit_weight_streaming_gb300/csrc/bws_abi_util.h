@@ -30,8 +30,10 @@ MoeStackView moe_stack_view(const bws_moe_layer* L, const int32_t* ids, const fl
 // Activation layout the layer's gate/up kernel reads (PrepParams::interleave).
 int moe_x_layout(const bws_moe_layer* L, int N);
 // gate/up, prep h and down for the slots of a slot table (activations xp).
+// ready: optional flag of the slot table (SlotMode::ready).
 int enqueue_moe_experts(const bws_moe_layer* L, int N, int topk, const int* n_slots, const int* slot_expert,
-                        const XPrep& xp, char* w, cudaStream_t st, const char* name);
+                        const XPrep& xp, char* w, cudaStream_t st, const char* name,
+                        const uint32_t* ready = nullptr);
 
 // Records a message for bws_last_error() and returns code.
 int fail(int code, const char* fmt, ...);

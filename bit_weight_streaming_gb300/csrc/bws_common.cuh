@@ -269,6 +269,21 @@ BWS_DEV int floor_log2_abs(float x) {
   return (31 - __clz((int)b)) - 149;
 }
 
+// Polls a flag until it is non-zero (acquire, GPU scope); false after
+// max_polls reads.
+BWS_DEV bool poll_acquire(const uint32_t* f, uint32_t max_polls) {
+  for (uint32_t i = 0; i < max_polls; ++i) {
+    uint32_t v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(f) : "memory");
+    if (v != 0u) return true;
+    __nanosleep(32);
+  }
+  return false;
+}
+BWS_DEV void store_release(uint32_t* f, uint32_t v) {
+  asm volatile("st.release.gpu.global.u32 [%0], %1;" :: "l"(f), "r"(v) : "memory");
+}
+
 BWS_DEV float warp_max(float v) {
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));

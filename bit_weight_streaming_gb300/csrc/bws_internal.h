@@ -50,6 +50,9 @@ struct SlotMode {
   int tiles_per_slot;
   int max_slots;
   int n_experts;
+  const uint32_t* ready;       // optional: non-zero once the slot table is written (MoeRoute::ready):
+                               // the TMA expert kernel then reads it, and primes its first
+                               // weight stages, before waiting for the kernels before
 };
 
 // Activations as the product kernels read them. Row (slot, tok) holds, for
@@ -98,6 +101,9 @@ struct MoeRoute {
   int* slot_expert;        // out [max_slots]
   float* cw;               // out [max_slots][N] combine weights
   uint32_t* status;        // out [1]: bit 4 set if an id was out of range
+  uint32_t* ready;         // optional: set to 1 (release) once the table is written; the routing
+                           // then runs without waiting for the kernels before (it reads only
+                           // ids and weights), so the experts' kernels can read the table early
 };
 // A stream-K split of n_units units over n_ctas CTAs into contiguous ranges:
 // CTA c takes units [splitk_begin(c), splitk_begin(c + 1)). The CTAs from lf

@@ -49,6 +49,8 @@ struct MoeTmaParams {
   const uint8_t* shared_scales;
   const int* n_slots;
   const int* slot_expert;
+  const uint32_t* ready;  // optional: the slot table may be read once this is set (SlotMode::ready)
+  int n_prime;            // with ready: stages given their weights before the inputs are ready
   int max_slots;
   int rows;               // rows of one output matrix (inter for gate/up, hidden for down)
   int up_row_off;         // SwiGLU: first up row in the expert tensor
@@ -397,14 +399,24 @@ __global__ void __launch_bounds__(kThreadsMoe, 2) gemv_tma_moe_kernel(const __gr
     mbar_fence_init();
   }
   for (int i = threadIdx.x; i < 33; i += blockDim.x) T.zero_x[i] = make_uint4(0, 0, 0, 0);
-  // the slot table is the previous kernel's output
-  pdl_wait();
+  // the slot table: with a ready flag, written by a routing CTA that does not
+  // wait for the kernels before, so it is read (and the first weight stages
+  // issued) before this kernel waits for them; else the previous kernel's output
+  const bool early = p.ready != nullptr;
+  if (early) {
+    if (threadIdx.x == 0 && !poll_acquire(p.ready, kPollsMoe)) atomicOr(p.status, kStatusTimeoutMoe);
+    __syncthreads();   // the table reads below follow thread 0's acquire
+  } else {
+    pdl_wait();
+  }
   if (threadIdx.x == 0) {
-    int n = __ldg(p.n_slots);
+    // (read through L2: with a ready flag the table is written while this kernel runs)
+    int n = early ? __ldcg(p.n_slots) : __ldg(p.n_slots);
     n = n < 0 ? 0 : (n > p.max_slots ? p.max_slots : n);
     T.n_slots = n;
   }
-  for (int i = threadIdx.x; i < p.max_slots; i += blockDim.x) T.slot_expert[i] = __ldg(p.slot_expert + i);
+  for (int i = threadIdx.x; i < p.max_slots; i += blockDim.x)
+    T.slot_expert[i] = early ? __ldcg(p.slot_expert + i) : __ldg(p.slot_expert + i);
   __syncthreads();
   // units dealt over G = min(CTAs, units) CTAs, so that every CTA that
   // shares a tile holds at least one unit of it; the rest have none
@@ -418,7 +430,9 @@ __global__ void __launch_bounds__(kThreadsMoe, 2) gemv_tma_moe_kernel(const __gr
     // unit, every lane one scale row of each box ----
     const int rb = p.d_in >> 5;
     const uint64_t pol = l2_evict_first();   // expert weights are read once per step
-    auto issue = [&](int tile, int ks, int s) {
+    // the weights of unit (tile, ks) into stage s (the full barrier also
+    // expects the unit's activation bytes), and its activations
+    auto issue_w = [&](int tile, int ks, int s) {
       const int slot = tile / p.tiles_per_slot, lt = tile - slot * p.tiles_per_slot;
       const int e = T.slot_expert[slot];
       const uint32_t full = smem_u32(&T.full[s]);
@@ -433,9 +447,6 @@ __global__ void __launch_bounds__(kThreadsMoe, 2) gemv_tma_moe_kernel(const __gr
           else
             tma_load_3d_hint(dst + b * kBoxBytes, &p.experts, ks * 128, row, e, full, pol);
         }
-        const uint16_t* src = p.x.hi + (size_t)(p.x.shared ? 0 : slot) * (p.N + 1) * p.d_in_pad + (size_t)ks * 256;
-        for (int tok = 0; tok < p.N; ++tok)
-          bulk_load(dst + p.x_off + tok * p.x_blk, src + (size_t)tok * p.d_in_pad, 512, full);
       }
       const uint8_t* sb = scale_base(p, e) + ks * 8;
 #pragma unroll
@@ -447,11 +458,37 @@ __global__ void __launch_bounds__(kThreadsMoe, 2) gemv_tma_moe_kernel(const __gr
       }
       cp_async_mbar_arrive(full);
     };
+    auto issue_x = [&](int tile, int ks, int s) {
+      if (lane != 0) return;
+      const int slot = tile / p.tiles_per_slot;
+      const uint32_t full = smem_u32(&T.full[s]);
+      const uint32_t dst = stage0 + (uint32_t)s * p.stage_bytes;
+      const uint16_t* src = p.x.hi + (size_t)(p.x.shared ? 0 : slot) * (p.N + 1) * p.d_in_pad + (size_t)ks * 256;
+      for (int tok = 0; tok < p.N; ++tok)
+        bulk_load(dst + p.x_off + tok * p.x_blk, src + (size_t)tok * p.d_in_pad, 512, full);
+    };
     int tile = (int)(u0 / p.nks), ks = (int)(u0 % p.nks);
     int s = 0;
     uint32_t ph = 0u;
     long long issued = 0;
-    for (long long u = u0; u < u1; ++u, ++issued) {
+    if (early) {   // weights of the first stages, then the wait, then their activations
+      const long long n_pre = (u1 - u0) < p.n_prime ? (u1 - u0) : p.n_prime;
+      for (long long k = 0; k < n_pre; ++k) {
+        issue_w(tile, ks, s);
+        if (++ks == p.nks) { ks = 0; ++tile; }
+        ++s;
+      }
+      pdl_wait();
+      tile = (int)(u0 / p.nks);
+      ks = (int)(u0 % p.nks);
+      for (long long k = 0; k < n_pre; ++k) {
+        issue_x(tile, ks, (int)k);
+        if (++ks == p.nks) { ks = 0; ++tile; }
+      }
+      issued = n_pre;   // n_prime < NS: the stages after them are still free
+      if (s == NS) { s = 0; ph ^= 1u; }
+    }
+    for (long long u = u0 + issued; u < u1; ++u, ++issued) {
       if (issued >= NS) {
         bool ok = true;
         if (lane == 0) ok = mbar_wait_bounded(smem_u32(&T.empty[s]), ph ^ 1u, kPollsMoe);
@@ -460,7 +497,8 @@ __global__ void __launch_bounds__(kThreadsMoe, 2) gemv_tma_moe_kernel(const __gr
           break;
         }
       }
-      issue(tile, ks, s);
+      issue_w(tile, ks, s);
+      issue_x(tile, ks, s);
       if (++s == NS) { s = 0; ph ^= 1u; }
       if (++ks == p.nks) { ks = 0; ++tile; }
     }
@@ -473,6 +511,7 @@ __global__ void __launch_bounds__(kThreadsMoe, 2) gemv_tma_moe_kernel(const __gr
   }
 
   // ---- consumers ----
+  if (early) pdl_wait();   // the activations are the previous kernel's output
   // the lo band is needed if any activation row this CTA reads has one
   uint32_t fl = 0u;
   if (u0 < u1) {
@@ -560,6 +599,7 @@ cudaError_t launch_gemv_tma_moe(int epi, const GemvParams& g, uint32_t* status, 
   p.shared_scales = S.shared_scales;
   p.n_slots = S.n_slots;
   p.slot_expert = S.slot_expert;
+  p.ready = S.ready;
   p.max_slots = S.max_slots;
   p.rows = S.rows;
   p.up_row_off = S.up_row_off;
@@ -584,6 +624,11 @@ cudaError_t launch_gemv_tma_moe(int epi, const GemvParams& g, uint32_t* status, 
   p.n_stages = kSmemBudgetMoe / p.stage_bytes;
   if (p.n_stages > kMaxStagesMoe) p.n_stages = kMaxStagesMoe;
   if (p.n_stages < 2) return cudaErrorInvalidValue;
+  // weights ahead of the inputs: two stages at one token; with more tokens
+  // none (measured at 4 tokens: 0 / 1 / 2 / 3 stages 2.43 / 2.47 / 2.46 /
+  // 2.47 ms per step, the table still read early)
+  p.n_prime = g.N == 1 ? 2 : 0;
+  if (p.n_prime > p.n_stages) p.n_prime = p.n_stages;
   const bool n1 = g.N == 1;
   if (epi == kEpiSwiGLU) return n1 ? launch_moe_one<kEpiSwiGLU, true>(p, st, pdl) : launch_moe_one<kEpiSwiGLU, false>(p, st, pdl);
   if (epi == kEpiStoreF32)

@@ -99,7 +99,7 @@ static int check_moe(const bws_moe_layer* L, int N, int topk, const char* name) 
 // gate/up, prep h and down of one MoE layer for the slots of the given slot
 // table: ys[slot][tok] = W_down h (FP32) in the workspace.
 int enqueue_moe_experts(const bws_moe_layer* L, int N, int topk, const int* n_slots, const int* slot_expert,
-                        const XPrep& xp, char* w, cudaStream_t st, const char* name) {
+                        const XPrep& xp, char* w, cudaStream_t st, const char* name, const uint32_t* ready) {
   const MoeLayout m = moe_layout(L, N, topk);
   uint32_t* counters = reinterpret_cast<uint32_t*>(w + m.off_counters);
   float* partials = reinterpret_cast<float*>(w + m.off_partials);
@@ -109,6 +109,7 @@ int enqueue_moe_experts(const bws_moe_layer* L, int N, int topk, const int* n_sl
   GemvParams p = {};
   p.slots.n_slots = n_slots;
   p.slots.slot_expert = slot_expert;
+  p.slots.ready = ready;
   p.slots.codes = L->gate_up_codes;
   p.slots.codes_stride = L->gate_up_codes_stride;
   p.slots.scales = L->gate_up_scales;

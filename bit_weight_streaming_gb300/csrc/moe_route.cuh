@@ -49,6 +49,10 @@ static BWS_DEV void moe_route_body(const MoeRoute& m) {
   // ids are distinct per token, so each (slot, token) cell gets one weight
   if (i < n && ids[i] >= 0) m.cw[slot * m.N + i / m.topk] = m.route_w[i];
   if (m.has_shared && i < m.N) m.cw[i] = 1.0f;
+  if (m.ready != nullptr) {   // the table is complete: raise the flag (cumulative over the barrier)
+    __syncthreads();
+    if (i == 0) store_release(m.ready, 1u);
+  }
 }
 
 }  // namespace bws

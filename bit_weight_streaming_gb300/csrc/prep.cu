@@ -285,11 +285,20 @@ template <int CL, int THREADS, bool MOE>
 __device__ __forceinline__ void prep_body(const PrepParams& q) {
   constexpr bool FIN = false;
   pdl_launch_dependents();
+  // the routing CTA: with a ready flag it reads only ids and weights, so it
+  // need not wait for the kernels before
+  const bool route = MOE && CL == 1 && q.has_route && blockIdx.x == gridDim.x - 1;
+  const bool early = route && q.route.ready != nullptr;
+  if (early) {
+    route_cta(q.route);
+    return;
+  }
   pdl_wait();
   const int rank = CL == 1 ? 0 : (int)cg::this_cluster().block_rank();
-  for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < q.zero_words; i += gridDim.x * blockDim.x)
+  const int zctas = gridDim.x - (MOE && q.has_route && q.route.ready != nullptr ? 1 : 0);
+  for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < q.zero_words; i += zctas * blockDim.x)
     q.zero_ptr[i] = 0u;
-  if (MOE && CL == 1 && q.has_route && blockIdx.x == gridDim.x - 1) {   // the routing CTA
+  if (route) {
     route_cta(q.route);
     return;
   }

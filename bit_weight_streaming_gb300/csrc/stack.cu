@@ -22,6 +22,10 @@ struct bws_stack_plan {
   bws_matrix head;
   // workspace layout
   size_t off_status, off_r, off_xp, off_u, off_vp, off_h, off_hp, off_moe, off_counters, off_partials, total;
+  // MoE layers: one slot table per layer (n_slots, slot_expert, cw) and its
+  // ready flag, cleared at the start of every step
+  size_t off_routes, route_stride, off_ready;
+  int n_moe;
   GemvWorkspace xw, vw, hw;    // prep-block offsets (relative to their block)
   int max_u, max_dv, max_inter, max_tiles;
   int kernels;
@@ -217,7 +221,11 @@ int enqueue_step(const bws_stack_plan* P, const uint16_t* x0, float* logits, voi
   // buffers alternate between consecutive MoE layers
   MoeStackView pend_v;
   const MoeStackView* pending = nullptr;
-  int moe_buf = 0;
+  int moe_buf = 0, moe_i = 0;
+  if (P->n_moe > 0) {
+    const cudaError_t e0 = cudaMemsetAsync(c.w + P->off_ready, 0, sizeof(uint32_t) * (size_t)P->n_moe, st);
+    if (e0 != cudaSuccess) return cuda_status(e0, name);
+  }
   // the last product's rows, when it deposited them for the next prep
   PrepParams fin_v = {};
   const PrepParams* fin = nullptr;
@@ -281,12 +289,20 @@ int enqueue_step(const bws_stack_plan* P, const uint16_t* x0, float* logits, voi
       BWS_TRY(product(c, &L.down, 1, kEpiResidF32, pdn));
     }
     if (L.kind == BWS_LAYER_MOE) {
-      const MoeStackView v = moe_stack_view(&L.moe, L.ids, L.route_w, P->N, L.topk, c.w + P->off_moe, moe_buf);
+      MoeStackView v = moe_stack_view(&L.moe, L.ids, L.route_w, P->N, L.topk, c.w + P->off_moe, moe_buf);
+      {   // this layer's own table, routed ahead of the layer (MoeRoute::ready)
+        char* rt = c.w + P->off_routes + (size_t)moe_i * P->route_stride;
+        v.route.n_slots = reinterpret_cast<int*>(rt);
+        v.route.slot_expert = reinterpret_cast<int*>(rt + 256);
+        v.route.cw = reinterpret_cast<float*>(rt + 256 + align256(sizeof(int) * (size_t)v.route.max_slots));
+        v.route.ready = reinterpret_cast<uint32_t*>(c.w + P->off_ready) + moe_i;
+        ++moe_i;
+      }
       BWS_TRY(prep(c, kPrepRmsNorm, nullptr, 0, init, H, P->off_xp, P->xw, v.counters, v.n_counters,
                    moe_x_layout(&L.moe, P->N), pending, &v.route));
       init = nullptr;
       const int rc = enqueue_moe_experts(&L.moe, P->N, L.topk, v.route.n_slots, v.route.slot_expert, xa,
-                                         c.w + P->off_moe, st, name);
+                                         c.w + P->off_moe, st, name, v.route.ready);
       if (rc != BWS_OK) return rc;
       pend_v = v;
       pending = &pend_v;
@@ -325,7 +341,8 @@ int bws_decode_step_plan_create(const bws_stack* S, int N, bws_stack_plan** plan
   P->max_u = P->max_dv = P->max_inter = 32;
   P->max_tiles = 1;
   P->kernels = 2;
-  size_t moe_bytes = 0;
+  size_t moe_bytes = 0, route_bytes = 256;
+  P->n_moe = 0;
   auto bad = [&](int code) {
     delete P;
     return code;
@@ -371,6 +388,10 @@ int bws_decode_step_plan_create(const bws_stack* S, int N, bws_stack_plan** plan
       if (!L.ids || !L.route_w) return bad(fail(BWS_ERR_INVALID_ARG, "%s: layer %d: null routing", name, li));
       const size_t b = moe_workspace_bytes(&L.moe, N, L.topk);
       moe_bytes = b > moe_bytes ? b : moe_bytes;
+      const size_t slots = (size_t)N * L.topk + (L.moe.shared_gate_up_codes != nullptr ? 1 : 0);
+      const size_t rb = 256 + align256(sizeof(int) * slots) + align256(sizeof(float) * slots * N);
+      route_bytes = rb > route_bytes ? rb : route_bytes;
+      ++P->n_moe;
       P->kernels += 4;
     } else if (L.kind != BWS_LAYER_MIXER_MLP) {
       return bad(fail(BWS_ERR_INVALID_ARG, "%s: layer %d: unknown kind %d", name, li, L.kind));
@@ -393,6 +414,9 @@ int bws_decode_step_plan_create(const bws_stack* S, int N, bws_stack_plan** plan
   P->hw = gemv_workspace_layout(N, P->max_inter, 0, 0, 1);
   P->off_hp = o; o += P->hw.off_counters;
   P->off_moe = o; o += align256(moe_bytes);
+  P->route_stride = route_bytes;
+  P->off_routes = o; o += route_bytes * (size_t)P->n_moe;
+  P->off_ready = o; o += align256(sizeof(uint32_t) * (size_t)(P->n_moe > 0 ? P->n_moe : 1));
   P->off_counters = o; o += align256(sizeof(uint32_t) * (size_t)P->max_tiles);
   P->off_partials = o; o += align256(sizeof(float) * kSlotFloats * ((size_t)P->max_tiles + gemv_max_warps()));
   P->total = o;
