@@ -161,6 +161,7 @@ struct PrepParams {
   const float* comb_ys;
   const float* comb_cw;
   const int* comb_n_slots;
+  int comb_max_slots;      // the layer's most slots (the arrays' extent)
   // optional: one extra CTA computes an MoE layer's slot table (one-CTA rows only)
   int has_route;
   MoeRoute route;

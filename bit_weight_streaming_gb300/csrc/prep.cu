@@ -116,25 +116,29 @@ __device__ __forceinline__ void finish_chunk(const PrepParams& q, int tok, int e
 // added to r (v: the chunk's residual values, updated). Out of line: its
 // registers stay out of the prep's main path.
 __device__ __noinline__ void combine_chunk(const PrepParams& q, int tok, int c, float (&v)[8], float* rr) {
+  // the slot count, weights and outputs of nine slots at a time are loaded
+  // together, whatever the slot count turns out to be (every slot up to the
+  // layer's maximum is in bounds); slots past the count or with weight 0 (a
+  // slot the token does not use, whose outputs may be stale) are then
+  // skipped, the rest added in slot order
   const int ns = __ldg(q.comb_n_slots);
   float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-  // eight slots' loads in flight at a time, none for a slot the token does
-  // not use (weight 0); slots still added in order
-  constexpr int kB = 8;
-  for (int s0 = 0; s0 < ns; s0 += kB) {
+  constexpr int kB = 9;
+  for (int s0 = 0; s0 < q.comb_max_slots; s0 += kB) {
     float wt[kB];
-#pragma unroll
-    for (int k = 0; k < kB; ++k) wt[k] = s0 + k < ns ? __ldg(q.comb_cw + (s0 + k) * q.N + tok) : 0.0f;
     float4 ya[kB], yb[kB];
 #pragma unroll
     for (int k = 0; k < kB; ++k) {
-      const float4* yp = reinterpret_cast<const float4*>(q.comb_ys + ((size_t)(s0 + k) * q.N + tok) * q.d_in) + 2 * c;
-      ya[k] = wt[k] != 0.0f ? __ldg(yp) : make_float4(0.f, 0.f, 0.f, 0.f);
-      yb[k] = wt[k] != 0.0f ? __ldg(yp + 1) : make_float4(0.f, 0.f, 0.f, 0.f);
+      const int sl = s0 + k < q.comb_max_slots ? s0 + k : s0;
+      wt[k] = __ldg(q.comb_cw + sl * q.N + tok);
+      const float4* yp = reinterpret_cast<const float4*>(q.comb_ys + ((size_t)sl * q.N + tok) * q.d_in) + 2 * c;
+      ya[k] = __ldg(yp);
+      yb[k] = __ldg(yp + 1);
     }
+    if (s0 >= ns) break;
 #pragma unroll
     for (int k = 0; k < kB; ++k) {
-      if (wt[k] == 0.0f) continue;
+      if (s0 + k >= ns || wt[k] == 0.0f) continue;
       const float y8[8] = {ya[k].x, ya[k].y, ya[k].z, ya[k].w, yb[k].x, yb[k].y, yb[k].z, yb[k].w};
 #pragma unroll
       for (int i = 0; i < 8; ++i) acc[i] = __fmaf_rn(wt[k], y8[i], acc[i]);

@@ -151,6 +151,7 @@ cudaError_t prep(const Ctx& c, int mode, const uint16_t* x, int ld, const uint16
     q.comb_ys = comb->ys;
     q.comb_cw = comb->route.cw;
     q.comb_n_slots = comb->route.n_slots;
+    q.comb_max_slots = comb->route.max_slots;
   }
   if (route != nullptr) {
     q.has_route = 1;
