@@ -1,8 +1,10 @@
 // Weight-stream products fed by TMA: one producer warp per CTA streams weight
 // tiles into a ring of shared-memory stages with cp.async.bulk.tensor; eight
-// consumer warps decode them and run the MMAs. The producer starts before the
-// kernel waits on its inputs (weights never depend on earlier kernels), so the
-// ring fills while the previous kernel finishes.
+// consumer warps decode them and run the MMAs. The producer gives the first
+// stages their weights before the kernel waits on its inputs (weights never
+// depend on earlier kernels); the weight copies carry an L2 evict-first
+// policy (read once per step, they should not push out what later kernels
+// read back).
 //
 // Tiles and units. A tile is 128 output rows (8 MMA sub-tiles of 16): rows
 // [128i, 128i+128) of one matrix, or, for the fused SwiGLU, 64 gate rows and
@@ -10,8 +12,11 @@
 // weights, 128 FP8 weights) and arrives as four 32-row TMA boxes with 128-byte
 // swizzle (plus four 32 x 16-byte boxes of E4M3 block scales for NVFP4) and,
 // through 1D bulk copies, the unit's activations of every token. Units are
-// dealt to CTAs in equal contiguous ranges (stream-K); a tile cut between CTAs
-// is finished by the last CTA to arrive, adding partial sums in CTA order.
+// dealt to CTAs in contiguous ranges (stream-K, SplitK); a tile cut between
+// CTAs is finished by the last CTA to arrive, adding partial sums in CTA
+// order. In deposit mode (the layer stack) every tile piece only writes its
+// raw sums to the slot of its (tile, CTA) pair, and the prep that reads the
+// rows next finishes them the same way.
 //
 // Consumer warp w takes box b = w%4 (two sub-tiles) and half h = w/4 of every
 // unit's 128 bytes: lane (g, t) reads the 16-byte chunk c = 2t + h of rows g,
