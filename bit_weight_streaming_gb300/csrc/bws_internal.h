@@ -175,7 +175,7 @@ struct PrepParams {
   SplitK fin_split;        // the product's stream-K split and units per tile (TmaGeom)
   int fin_nks;
   int fin_epi, fin_fmt, fin_n_mats;
-  int fin_d_out[kMaxMats], fin_row_off[kMaxMats], fin_tile_begin[kMaxMats];
+  int fin_row_off[kMaxMats], fin_tile_begin[kMaxMats];   // the matrices' first output row and tile
   const float* fin_scale[kMaxMats];
   const int* fin_xexp;     // exponents of the product's input rows [N]
 };

@@ -112,7 +112,6 @@ bool deposit_setup(const bws_matrix* mats, int nm, int epi, GemvParams& p, int n
   f.fin_n_mats = nm;
   int tile = 0;
   for (int i = 0; i < nm; ++i) {
-    f.fin_d_out[i] = mats[i].d_out;
     f.fin_row_off[i] = p.mats[i].out_row_off;
     f.fin_tile_begin[i] = tile;
     f.fin_scale[i] = mats[i].scale32;
