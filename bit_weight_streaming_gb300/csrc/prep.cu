@@ -521,8 +521,8 @@ __global__ void __launch_bounds__(THREADS) prep_kernel(const __grid_constant__ P
   prep_body<CL, THREADS, MOE>(q);
 }
 
-template <int CL, int THREADS, int KB, bool RMS, bool SWI>
-__global__ void __launch_bounds__(THREADS, 2) prep_fin_kernel(const __grid_constant__ PrepParams q) {
+template <int CL, int THREADS, int KB, bool RMS, bool SWI, int MINB = 2>
+__global__ void __launch_bounds__(THREADS, MINB) prep_fin_kernel(const __grid_constant__ PrepParams q) {
   prep_fin_body<CL, THREADS, KB, RMS, SWI>(q);
 }
 
@@ -541,7 +541,9 @@ cudaError_t launch_prep(const PrepParams& q, cudaStream_t st, bool pdl) {
   // rows: one CTA of 1024 threads; 8192 on, a cluster of 8 x 256. Finishing
   // a product (one slot, no x0, status or combine): a chunk per thread, and
   // registers for a tile's slots in one batch of loads: a cluster of 4 x 256
-  // (8 x 384 from 8192 on, to 24576)
+  // (8 x 384 from 8192 on, to 24576). The residual update takes up to 13
+  // slots at once (the 5120-row products with a lighter split have up to 13
+  // CTAs per tile), at 159 registers.
   if (fin) {
     const bool rms = q.mode == kPrepRmsNorm;
     if (moe || q.n_slots != nullptr || q.x0 != nullptr || q.hdr != nullptr || q.status_clear != nullptr ||
@@ -573,7 +575,7 @@ cudaError_t launch_prep(const PrepParams& q, cudaStream_t st, bool pdl) {
     const bool swi = q.fin_epi == kEpiSwiGLU;
     if (q.mode == kPrepRmsNorm)
       return long_row ? cudaLaunchKernelEx(&cfg, prep_fin_kernel<8, 384, 4, true, false>, q)
-                      : cudaLaunchKernelEx(&cfg, prep_fin_kernel<4, 256, 10, true, false>, q);
+                      : cudaLaunchKernelEx(&cfg, prep_fin_kernel<4, 256, 13, true, false, 1>, q);
     if (swi)
       return long_row ? cudaLaunchKernelEx(&cfg, prep_fin_kernel<8, 384, 3, false, true>, q)
                       : cudaLaunchKernelEx(&cfg, prep_fin_kernel<4, 256, 4, false, true>, q);
