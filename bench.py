@@ -129,41 +129,76 @@ def parse_clock_lines(lines):
 
 # ---- CPU baseline (the oracle) ------------------------------------------------
 
-def cpu_oracle_rate(sample_matrices, budget_s=12.0):
-    """Times the oracle's NVFP4 product on host copies of some of the step's
-    matrices (N = 1), as algorithmic bytes per second of wall time. Returns
-    (GB/s, threads used, description)."""
+_ONE_THREAD = {k: "1" for k in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS")}
+
+
+def _oracle_worker(path, barrier, out):
+    """One host core (numpy with one BLAS thread): loads a matrix, waits for
+    the others, then times the oracle's NVFP4 product on it (N = 1)."""
+    os.environ.update(_ONE_THREAD)
     import numpy as np
     from oracle import products as P
-    rng = np.random.default_rng(0)
-    done_bytes = 0
-    t0, c0 = time.perf_counter(), sum(os.times()[:2])
-    n = 0
-    for codes, scales, ts in sample_matrices:
-        x = rng.standard_normal((1, codes.shape[1] * 2)).astype(np.float32)
-        P.nvfp4_gemv(codes, scales, ts, x)
-        done_bytes += codes.nbytes + scales.nbytes
-        n += 1
-        if time.perf_counter() - t0 > budget_s:
-            break
-    wall = time.perf_counter() - t0
-    cpu = sum(os.times()[:2]) - c0
-    cores = max(1, round(cpu / wall)) if wall > 0 else 1
-    return done_bytes / wall / 1e9, cores, f"oracle NVFP4 GEMV (FP64, numpy) on {n} of the step's matrices, N=1, {done_bytes/1e9:.3f} GB"
+    d = np.load(path)
+    codes, scales, ts = d["c"], d["s"], np.float32(d["t"])
+    x = np.random.default_rng(0).standard_normal((1, codes.shape[1] * 2)).astype(np.float32)
+    barrier.wait(timeout=300)
+    t0 = time.perf_counter()
+    P.nvfp4_gemv(codes, scales, ts, x)
+    t1 = time.perf_counter()
+    out.put((codes.nbytes + scales.nbytes, t0, t1))
 
 
-def host_copies(stack, max_bytes):
-    out, total = [], 0
+def cpu_oracle_rate(sample, procs):
+    """The oracle's NVFP4 product timed on `procs` host cores at once: one
+    spawned process per core, one BLAS thread each, every process running the
+    product over the same sample matrix (codes, scales, s_t). Returns
+    algorithmic bytes per second of wall time (first start to last end)."""
+    import multiprocessing as mp
+    import tempfile
+    import numpy as np
+    codes, scales, ts = sample
+    ctx = mp.get_context("spawn")
+    with tempfile.TemporaryDirectory() as tmp:
+        path = os.path.join(tmp, "m.npz")
+        np.savez(path, c=codes, s=scales, t=np.float32(ts))
+        barrier, out = ctx.Barrier(procs), ctx.Queue()
+        ps = [ctx.Process(target=_oracle_worker, args=(path, barrier, out)) for _ in range(procs)]
+        for p in ps:
+            p.start()
+        try:
+            res = [out.get(timeout=600) for _ in ps]
+        finally:
+            for p in ps:
+                p.join(timeout=30)
+                if p.is_alive():
+                    p.kill()
+    nbytes = sum(r[0] for r in res)
+    wall = max(r[2] for r in res) - min(r[1] for r in res)
+    return nbytes / wall / 1e9
+
+
+def cpu_baseline(sample):
+    """The oracle on the host cores: all cores at once (the reported value)
+    and one core, with the core counts."""
+    cores = os.cpu_count() or 1
+    all_cores = cpu_oracle_rate(sample, cores)
+    one = cpu_oracle_rate(sample, 1)
+    rows = sample[0].shape[0]
+    cols = sample[0].shape[1] * 2
+    desc = (f"oracle NVFP4 GEMV (FP64 products, numpy, one BLAS thread per process) over one of the step's "
+            f"matrices ({rows}x{cols}, N=1), once per core")
+    return {"value": round(all_cores, 4), "unit": UNIT, "cores": cores, "kind": "oracle", "sample": desc,
+            "one_core": {"value": round(one, 4), "unit": UNIT, "cores": 1}}
+
+
+def host_copy(stack, rows=8192):
+    """Host copy (codes, scales, s_t) of the first `rows` rows of the stack's
+    first MLP gate matrix: a bounded sample of the step's weights."""
     for L in stack.layers_py:
-        for name in ("gate", "up", "down"):
-            m = L.get(name)
-            if m is None or m.fmt != 1:
-                continue
-            out.append((m.codes.cpu().numpy(), m.scales.cpu().numpy(), float(m.scale32.item())))
-            total += m.nbytes()
-            if total >= max_bytes:
-                return out
-    return out
+        m = L.get("gate")
+        if m is not None and m.fmt == 1:
+            return m.codes[:rows].cpu().numpy(), m.scales[:rows].cpu().numpy(), float(m.scale32.item())
+    raise RuntimeError("no NVFP4 gate matrix in the stack")
 
 
 # ---- the GPU arm ------------------------------------------------------------------
@@ -193,8 +228,8 @@ def time_steps(fn, steps, warmup, stream):
 
 
 # DRAM bytes (read + write) per algorithmic byte of the one-token NVFP4
-# product kernel, from ncu counters on four of the step's matrix shapes
-# (profiles/gemv_tma_nvfp4_traffic_n1.md).
+# product kernel, from one ncu capture of its counters on four of the step's
+# matrix shapes.
 TRAFFIC_RATIO = 1.033
 
 
@@ -318,11 +353,7 @@ def run_gpu(args):
         del stack8
         moe = run_moe(args, dev, stream)
 
-    cpu = None
-    if rank == 0:
-        sample = host_copies(stack1, 600e6)
-        gbs, cores, desc = cpu_oracle_rate(sample)
-        cpu = {"value": round(gbs, 4), "unit": UNIT, "cores": cores, "kind": "oracle", "sample": desc}
+    cpu = cpu_baseline(host_copy(stack1)) if rank == 0 else None
 
     if rank == 0:
         line = {
@@ -348,8 +379,8 @@ def run_gpu(args):
             "roofline": {"bound": "hbm", "achieved": round(dk_bytes / dk_secs / 1e9, 1), "peak": peak,
                          "unit": "GB/s", "frac": round(dk_bytes / dk_secs / 1e9 / peak, 4),
                          "traffic": round(TRAFFIC_RATIO * dk_bytes),
-                         "traffic_basis": "ncu dram__bytes_read.sum + dram__bytes_write.sum per launch on four of "
-                                          "the step's shapes, x algorithmic bytes (profiles/gemv_tma_nvfp4_traffic_n1.md)",
+                         "traffic_basis": "ncu dram__bytes_read.sum + dram__bytes_write.sum per algorithmic byte from one "
+                                          "capture on four of the step's shapes, times the algorithmic bytes per launch",
                          "kernel": "NVFP4 weight-stream product kernel (gemv_tma_kernel, one token), activations prepared beforehand",
                          "launches_timed": dk_n, "bytes_per_launch": round(dk_bytes), "peak_kind": peak_kind},
             "clocks": clk,
@@ -408,15 +439,30 @@ def run_reference(args):
     for i, s in enumerate(shapes):
         W = synth.weight_fp32(s, seed=args.seed, index=i).numpy()
         mats.append(Q.nvfp4_quantize(W))
-    rates = []
+    from oracle import products as P
+    rng = np.random.default_rng(args.seed)
+
+    def one_step():
+        """The oracle's product over the sample, in this process (numpy uses
+        what threads its BLAS starts); returns (seconds, CPU seconds)."""
+        t0, c0 = time.perf_counter(), sum(os.times()[:2])
+        for codes, scales, ts in mats:
+            P.nvfp4_gemv(codes, scales, ts, rng.standard_normal((1, codes.shape[1] * 2)).astype(np.float32))
+        return time.perf_counter() - t0, sum(os.times()[:2]) - c0
+
     for _ in range(args.warmup):
-        cpu_oracle_rate(mats[:1], budget_s=0.0)
-    t_all = []
-    for _ in range(args.steps):
-        gbs, cores, desc = cpu_oracle_rate(mats, budget_s=1e9)
-        rates.append(gbs)
-    value = statistics.median(rates)
+        one_step()
+    rates, cpu_s, wall_s = [], 0.0, 0.0
     nbytes = sum(c.nbytes + s.nbytes for c, s, _ in mats)
+    for _ in range(args.steps):
+        w, c = one_step()
+        rates.append(nbytes / w / 1e9)
+        wall_s += w
+        cpu_s += c
+    cores = max(1, round(cpu_s / wall_s))
+    desc = (f"oracle NVFP4 GEMV (FP64 products, numpy) over the 17408x5120 gate projection, N=1, in one "
+            f"process ({cores} threads busy on average)")
+    value = statistics.median(rates)
     line = {
         "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": UNIT, "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(nbytes / (value * 1e9) * 1e3, 2),

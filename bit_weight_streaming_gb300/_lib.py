@@ -34,6 +34,7 @@ SIGNATURES = {
     "bws_decode_step_stream": (I, [P, P, P, P, Z, P]),
     "bws_decode_step_kernel_count": (I, [P]),
     "bws_status_word": (I, [P, P, P]),
+    "bws_debug_wait_flag": (I, [P, C.c_uint32, P, Z, P]),
     "bws_hbm_read_probe": (I, [P, Z, P, P]),
     "bws_l2_flush": (I, [P, Z, P]),
 }

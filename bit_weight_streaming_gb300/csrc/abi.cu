@@ -299,8 +299,27 @@ int bws_status_word(const void* workspace, uint32_t* status, void* stream) {
   uint32_t s = hdr2[1];
   for (uint32_t i = 0; i < hdr2[0] && i < (uint32_t)kMaxTokens; ++i) s |= flags[i];
   *status = s;
+  if (s & BWS_STATUS_WAIT_TIMEOUT)
+    return fail(BWS_ERR_TIMEOUT, "bws_status_word: a bounded device wait ran out (status 0x%x)", s);
   g_err[0] = 0;
   return BWS_OK;
+}
+
+int bws_debug_wait_flag(const uint32_t* flag, uint32_t max_polls, void* workspace, size_t workspace_bytes,
+                        void* stream) {
+  const char* name = "bws_debug_wait_flag";
+  if (!flag || !workspace) return fail(BWS_ERR_INVALID_ARG, "%s: null pointer", name);
+  if (max_polls == 0 || max_polls > (1u << 24))
+    return fail(BWS_ERR_INVALID_ARG, "%s: max_polls must be in [1, 2^24]", name);
+  const GemvWorkspace L = gemv_workspace_layout(1, 32, 1, 1);
+  if (workspace_bytes < L.off_hdr + 8 || !aligned(workspace, 256) || !aligned(flag, 4))
+    return fail(BWS_ERR_WORKSPACE, "%s: workspace of %zu bytes (256-byte aligned) and a 4-byte aligned flag needed",
+                name, L.off_hdr + 8);
+  uint32_t* hdr = reinterpret_cast<uint32_t*>(static_cast<char*>(workspace) + L.off_hdr);
+  cudaStream_t st = as_stream(stream);
+  cudaError_t e = cudaMemsetAsync(hdr, 0, 8, st);
+  if (e == cudaSuccess) e = launch_wait_flag(flag, max_polls, hdr, st);
+  return cuda_status(e, name);
 }
 
 int bws_hbm_read_probe(const void* src, size_t n_bytes, uint32_t* out, void* stream) {

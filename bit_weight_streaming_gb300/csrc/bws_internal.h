@@ -1,6 +1,8 @@
 // Internal launch interface between the C ABI (abi.cu, stack.cu) and the kernels.
 #pragma once
 #include <cuda_runtime.h>
+
+#include <atomic>
 #include <stddef.h>
 #include <stdint.h>
 
@@ -186,7 +188,22 @@ struct GemvWorkspace {
 };
 GemvWorkspace gemv_workspace_layout(int N, int d_in, int n_tiles, long long max_warps, int slots = 1);
 size_t align256(size_t v);
+// Devices the per-device caches below cover (ordinals 0..kMaxDevices-1).
+constexpr int kMaxDevices = 64;
+// The current device's ordinal (0 if it cannot be read or is out of range).
+int current_device();
+// SM count of the current device (cached per device).
 int num_sms();
+// Sets a kernel's dynamic shared-memory limit once per device: attribute
+// settings are per device, so a second GPU needs its own call.
+template <typename K>
+cudaError_t set_smem_once(std::atomic<unsigned long long>& done, K kernel, int bytes) {
+  const unsigned long long bit = 1ull << current_device();
+  if (done.load(std::memory_order_acquire) & bit) return cudaSuccess;
+  const cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e == cudaSuccess) done.fetch_or(bit, std::memory_order_acq_rel);
+  return e;
+}
 long long gemv_max_warps();
 
 cudaError_t launch_prep(const PrepParams& q, cudaStream_t st, bool pdl);
@@ -258,5 +275,6 @@ cudaError_t launch_fp8_rowwise_quantize(const float* W, int rows, int cols, uint
 
 cudaError_t launch_hbm_read_probe(const void* src, size_t n_bytes, uint32_t* out, cudaStream_t st);
 cudaError_t launch_l2_flush(void* buf, size_t n_bytes, cudaStream_t st);
+cudaError_t launch_wait_flag(const uint32_t* flag, uint32_t max_polls, uint32_t* hdr, cudaStream_t st);
 
 }  // namespace bws

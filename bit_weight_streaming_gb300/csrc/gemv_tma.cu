@@ -536,12 +536,10 @@ __global__ void __launch_bounds__(kThreadsTma, 2) gemv_tma_kernel(const __grid_c
 template <int FMT, int EPI, bool N1>
 cudaError_t launch_tma_one(const TmaParams& p, cudaStream_t st, bool pdl) {
   const int smem = p.n_stages * p.stage_bytes + (int)sizeof(Tail) + 1024;
-  static bool attr = false;
-  if (!attr) {
-    cudaError_t e = cudaFuncSetAttribute(gemv_tma_kernel<FMT, EPI, N1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         kSmemBudget + (int)sizeof(Tail) + 1024);
+  static std::atomic<unsigned long long> attr{0};
+  {
+    const cudaError_t e = set_smem_once(attr, gemv_tma_kernel<FMT, EPI, N1>, kSmemBudget + (int)sizeof(Tail) + 1024);
     if (e != cudaSuccess) return e;
-    attr = true;
   }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)p.n_ctas);

@@ -529,12 +529,10 @@ __global__ void __launch_bounds__(kThreadsMoe, 2) gemv_tma_moe_kernel(const __gr
 template <int EPI, bool N1>
 cudaError_t launch_moe_one(const MoeTmaParams& p, cudaStream_t st, bool pdl) {
   const int smem = p.n_stages * p.stage_bytes + (int)sizeof(MoeTail) + 1024;
-  static bool attr = false;
-  if (!attr) {
-    cudaError_t e = cudaFuncSetAttribute(gemv_tma_moe_kernel<EPI, N1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         kSmemBudgetMoe + (int)sizeof(MoeTail) + 1024);
+  static std::atomic<unsigned long long> attr{0};
+  {
+    const cudaError_t e = set_smem_once(attr, gemv_tma_moe_kernel<EPI, N1>, kSmemBudgetMoe + (int)sizeof(MoeTail) + 1024);
     if (e != cudaSuccess) return e;
-    attr = true;
   }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)p.n_ctas);

@@ -429,12 +429,10 @@ __global__ void __launch_bounds__(kUThreads, 1) gemv_umma_kernel(const __grid_co
 template <int EPI>
 cudaError_t launch_umma_one(const UParams& p, cudaStream_t st, bool pdl) {
   const int smem = p.n_stages * kUStage + (int)sizeof(UTail) + 1024;
-  static bool attr = false;
-  if (!attr) {
-    cudaError_t e = cudaFuncSetAttribute(gemv_umma_kernel<EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         kUNumStages * kUStage + (int)sizeof(UTail) + 1024);
+  static std::atomic<unsigned long long> attr{0};
+  {
+    const cudaError_t e = set_smem_once(attr, gemv_umma_kernel<EPI>, kUNumStages * kUStage + (int)sizeof(UTail) + 1024);
     if (e != cudaSuccess) return e;
-    attr = true;
   }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)p.n_ctas);

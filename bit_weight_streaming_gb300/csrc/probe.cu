@@ -50,4 +50,19 @@ cudaError_t launch_l2_flush(void* buf, size_t n_bytes, cudaStream_t st) {
   return cudaGetLastError();
 }
 
+// One CTA runs the library's bounded flag wait (the acquire poll the MoE
+// expert kernels use on their routing table's ready flag) on flag with a
+// poll limit; when the limit runs out it sets the timeout bit in status[1]
+// and returns, as every bounded wait in the library does.
+__global__ void __launch_bounds__(32) wait_flag_kernel(const uint32_t* flag, uint32_t max_polls, uint32_t* hdr) {
+  if (threadIdx.x != 0) return;
+  hdr[0] = 0u;   // no token flags to collect
+  if (!poll_acquire(flag, max_polls)) atomicOr(hdr + 1, 0x100u);
+}
+
+cudaError_t launch_wait_flag(const uint32_t* flag, uint32_t max_polls, uint32_t* hdr, cudaStream_t st) {
+  wait_flag_kernel<<<1, 32, 0, st>>>(flag, max_polls, hdr);
+  return cudaGetLastError();
+}
+
 }  // namespace bws

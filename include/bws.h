@@ -170,9 +170,10 @@ int bws_nvfp4_gemv_prepared(const uint8_t* codes, const uint8_t* scales,
  *     (d_out/32 + 16 * SMs) KiB) are rejected with BWS_ERR_WORKSPACE and a
  *     message; the call allocates nothing (no cudaMalloc, no allocating
  *     library routine).
- *   - The first call on a device looks up the scratch's device address (once
- *     per device, with that device current); make that first call before any
- *     stream capture.
+ *   - The first call in a CUDA context looks up the scratch's device address
+ *     (once per context, with that context current: a device that was reset,
+ *     or another driver-API context made current on it, gets a lookup of its
+ *     own); make that first call before any stream capture.
  *   - All calls on a device share the one scratch array and it keeps the last
  *     call's contents: calls that overlap on the GPU (different streams, or
  *     host threads without ordering) race with each other. Order them. */
@@ -329,8 +330,22 @@ int bws_decode_step_kernel_count(const bws_stack_plan* plan);
 /* ------------------------------------------------------------------------ */
 
 /* Copies the device status word of a workspace (an OR of bws_status_bits set
- * by the calls that used it) into *status (host); synchronises the stream. */
+ * by the calls that used it) into *status (host); synchronises the stream.
+ * Returns BWS_ERR_TIMEOUT (with *status filled in) when a bounded device wait
+ * of those calls ran out, else BWS_OK. */
 int bws_status_word(const void* workspace, uint32_t* status, void* stream);
+
+/* Failure-path check of the bounded device waits (no counterpart on the
+ * pages): one CTA polls *flag (device, acquire loads, a short sleep between
+ * polls) until it is non-zero, at most max_polls times (1..2^24), with the
+ * same wait the MoE expert kernels run on their routing table's ready flag.
+ * A flag that stays zero makes the wait run out: the kernel sets
+ * BWS_STATUS_WAIT_TIMEOUT in the workspace's status word and returns, so
+ * bws_status_word then reports BWS_ERR_TIMEOUT. Nothing hangs and the context
+ * stays usable. workspace: 256-byte aligned, bws_gemv_workspace_size(1, 1, 32)
+ * bytes suffice. */
+int bws_debug_wait_flag(const uint32_t* flag, uint32_t max_polls, void* workspace,
+                        size_t workspace_bytes, void* stream);
 
 /* Read-only streaming sum over n_bytes (% 16 == 0) of src; writes one u32
  * checksum to out. Used to measure the achievable HBM read bandwidth. */

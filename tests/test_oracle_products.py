@@ -1,6 +1,8 @@
 """Pins for the oracle's products and layer recipe (CPU only)."""
 from fractions import Fraction
 
+import math
+
 import numpy as np
 import pytest
 
@@ -148,18 +150,47 @@ def test_dense_stack_zero_layers_is_the_head():
     assert np.array_equal(logits, want) and np.array_equal(r, x0)
 
 
-def test_dense_layer_mixer_stand_in_takes_prefix():
-    d, dv = 32, 16
-    mk = lambda s, i: P.nvfp4_dequantize(*Q.nvfp4_quantize(synth.weight_fp32(s, seed=5, index=i).numpy()))
-    layer = {"in": [mk((48, d), 0)], "out": mk((d, dv), 1),
-             "gate": mk((64, d), 2), "up": mk((64, d), 3), "down": mk((d, 64), 4)}
-    r0 = synth.activation_bf16(1, d, seed=5).float().numpy().astype(np.float64)
-    r1 = M.dense_layer(r0, layer)
-    a = F.round_bf16(M.rmsnorm(r0))
-    v = F.round_bf16(P.matvec(layer["in"][0], a)[0])[:, :dv]
-    r_mid = r0 + P.matvec(layer["out"], v)[0]
-    want = r_mid + M.mlp(layer["gate"], layer["up"], layer["down"], F.round_bf16(M.rmsnorm(r_mid)))
-    assert np.array_equal(r1, want)
+def test_rmsnorm_eps_inside_the_root_worked_by_hand():
+    """r = [3, -4, 0, 12]: mean(r^2) = (9 + 16 + 0 + 144) / 4 = 42.25; with
+    eps = 6.75, sqrt(42.25 + 6.75) = sqrt(49) = 7, so RMSNorm(r) =
+    [3/7, -4/7, 0, 12/7]. (eps added after the root would divide by
+    6.5 + 6.75 = 13.25 instead.)"""
+    y = M.rmsnorm(np.array([[3.0, -4.0, 0.0, 12.0]]), eps=6.75)
+    assert np.allclose(y, [[3 / 7, -4 / 7, 0.0, 12 / 7]], rtol=1e-15, atol=0)
+
+
+def _silu_closed(g):
+    return g / (1.0 + math.exp(-g))
+
+
+def test_dense_layer_worked_by_hand():
+    """One dense layer on hand-chosen matrices whose every intermediate value
+    is known (hidden 4, N = 1, eps 1e-6):
+      r0 = [2, 2, 2, 2]: mean square 4, a = BF16(r0 / sqrt(4 + 1e-6)) =
+        [1, 1, 1, 1] (1 - 1.25e-7 rounds to 1 in BF16);
+      u = W_in a = row sums of W_in = [1, 1, 2, 0.5, 3, 2] (exact in BF16);
+      the mixer stand-in takes the first d_v = 2 entries: v = [1, 1];
+      W_o v = [1, 3, -1, -1], so r_mid = [3, 5, 1, 1] (mean square 9);
+      m = BF16(r_mid / 3) = [1, BF16(5/3), BF16(1/3), BF16(1/3)]
+        = [1, 213/128, 171/512, 171/512] (5/3 = 1.1010101|01..b rounds
+        down to 1.1010101b; 1/3 = 1.0101010|1010..b x 2^-2 rounds up);
+      g = W_gate m = [3 m_2, -2 m_0, m_2 - m_3] = [513/512, -2, 0];
+      up = W_up m = [3 m_1, m_0, 4 m_0] = [639/128, 1, 4];
+      h = BF16(SiLU(g) * up) with SiLU(x) = x / (1 + e^-x);
+      y = W_down h = [h0, h1, h0 + h1, h2] and r1 = r_mid + y.
+    (Taking the last d_v entries of u instead gives W_o [3, 2] =
+    [3, 7, -3, -2]; any slip in the order fails this.)"""
+    W_in = np.array([[1, 0, 0, 0], [0, 1, 0, 0], [1, 1, 0, 0], [0, 0, 0, 0.5], [3, 0, 0, 0], [0, 0, 1, 1]],
+                    dtype=np.float64)
+    W_o = np.array([[1, 0], [1, 2], [-1, 0], [0, -1]], dtype=np.float64)
+    W_g = np.array([[0, 0, 3, 0], [-2, 0, 0, 0], [0, 0, 1, -1]], dtype=np.float64)
+    W_u = np.array([[0, 3, 0, 0], [1, 0, 0, 0], [4, 0, 0, 0]], dtype=np.float64)
+    W_d = np.array([[1, 0, 0], [0, 1, 0], [1, 1, 0], [0, 0, 1]], dtype=np.float64)
+    layer = {"in": [W_in[:4], W_in[4:]], "out": W_o, "gate": W_g, "up": W_u, "down": W_d}
+    r1 = M.dense_layer(np.array([[2.0, 2.0, 2.0, 2.0]]), layer)
+    h = F.round_bf16(np.array([_silu_closed(513 / 512) * 639 / 128, _silu_closed(-2.0) * 1.0, 0.0]))
+    want = np.array([[3 + h[0], 5 + h[1], 1 + h[0] + h[1], 1 + h[2]]])
+    assert np.array_equal(r1, want), (r1, want)
 
 
 def test_tolerance_bound():

@@ -25,6 +25,29 @@ def test_nvfp4_hand_example():
     assert list(w_hat[1]) == g["w_hat_row1"]
 
 
+def _bits_f32(h):
+    return np.array([int(h, 16)], dtype=np.uint32).view(np.float32)[0]
+
+
+def test_nvfp4_hand_example_non_power_of_two_tensor_scale():
+    """A tensor scale of 29/28 in FP32: the example's scale codes and element
+    codes depend on the order of the FP32 scale arithmetic (worked by hand in
+    nvfp4_hand_st.json), so a reordered division fails here."""
+    g = load_golden("nvfp4_hand_st.json")
+    W = np.zeros(g["shape"], dtype=np.float32)
+    for e in g["nonzero"]:
+        v = _bits_f32(e["bits"])
+        assert v == np.float32(float(e["w"]))
+        W[e["at"][0], e["at"][1]] = v
+    codes, scales, s_t = Q.nvfp4_quantize(W)
+    assert np.float32(s_t).view(np.uint32) == int(g["s_t_bits"], 16)
+    assert scales.tolist() == g["scales"]
+    q = np.zeros(g["shape"], dtype=np.uint8)
+    for e in g["codes_nonzero"]:
+        q[e["at"][0], e["at"][1]] = e["code"]
+    assert codes.tolist() == Q.pack_nibbles(q).tolist()
+
+
 def test_mxfp4_hand_example():
     g, W = _golden_W("mxfp4_hand.json")
     codes, scales = Q.mxfp4_quantize(W)
@@ -135,3 +158,45 @@ def test_fp8_row_max_encodes_near_448(W_rand):
     rel = np.abs(W - w_hat) / np.maximum(np.abs(W), 1e-30)
     normal = np.abs(W) >= (2.0 ** -6) * s_r[:, None]
     assert np.all(rel[normal] <= 2.0 ** -4 + 1e-7)
+
+
+def _nvfp4_reordered(scale_order, elem_order):
+    """The oracle's NVFP4 quantizer with one step of its FP32 sequence done
+    in another order (a planted mistake)."""
+    from oracle.formats import e2m1_encode, e4m3_encode, e4m3_decode
+    f32 = np.float32
+
+    def quant(W, s_t=None):
+        W = np.asarray(W, dtype=f32)
+        d_out, d_in = W.shape
+        s_t = Q.nvfp4_tensor_scale(W) if s_t is None else f32(s_t)
+        blk = W.reshape(d_out, d_in // 16, 16)
+        amax_b = np.max(np.abs(blk), axis=2).astype(f32)
+        if scale_order:
+            sb = (amax_b / f32(f32(6.0) * s_t)).astype(f32)
+        else:
+            sb = ((amax_b / f32(6.0)).astype(f32) / s_t).astype(f32)
+        sc = e4m3_encode(sb)
+        dec = e4m3_decode(sc).astype(f32)
+        with np.errstate(divide="ignore", invalid="ignore"):
+            if elem_order:
+                ratio = ((blk / s_t).astype(f32) / dec[..., None]).astype(f32)
+            else:
+                ratio = (blk / (dec * s_t).astype(f32)[..., None]).astype(f32)
+        q = np.where((dec > 0)[..., None], e2m1_encode(ratio), 0).astype(np.uint8)
+        return Q.pack_nibbles(q.reshape(d_out, d_in)), sc, s_t
+    return quant
+
+
+@pytest.mark.parametrize("scale_order,elem_order", [(True, False), (False, True)])
+def test_reordered_scale_arithmetic_fails_the_hand_example(monkeypatch, scale_order, elem_order):
+    monkeypatch.setattr(Q, "nvfp4_quantize", _nvfp4_reordered(scale_order, elem_order))
+    with pytest.raises(AssertionError):
+        test_nvfp4_hand_example_non_power_of_two_tensor_scale()
+
+
+def test_reorder_helper_matches_the_oracle_when_not_reordered():
+    W = synth.weight_fp32((8, 64), seed=3, index=0).numpy()
+    a = Q.nvfp4_quantize(W)
+    b = _nvfp4_reordered(False, False)(W)
+    assert np.array_equal(a[0], b[0]) and np.array_equal(a[1], b[1]) and a[2] == b[2]

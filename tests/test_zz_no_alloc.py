@@ -50,15 +50,19 @@ def test_noalloc_matches_workspace_entry_point_twice():
 
 
 def test_noalloc_rejects_sizes_beyond_its_scratch():
+    """A size whose activations alone (N * d_in * 8 bytes) exceed the scratch.
+    Every buffer is allocated at its full declared size, so that a refusal
+    that stopped working would show as a wrong status, not as accesses past
+    the end of a buffer."""
     m = bws()
     lib = m.lib()
     dev = device()
-    d_out, d_in, N = 248320, 5120, 8                        # the output layer at N = 8
-    c = torch.zeros((1024, d_in // 2), dtype=torch.uint8, device=dev)
-    s = torch.zeros((1024, d_in // 16), dtype=torch.uint8, device=dev)
+    d_out, d_in, N = 32, 262144, 8
+    c = torch.zeros((d_out, d_in // 2), dtype=torch.uint8, device=dev)
+    s = torch.zeros((d_out, d_in // 16), dtype=torch.uint8, device=dev)
     t = torch.ones(1, dtype=torch.float32, device=dev)
     x = torch.zeros((N, d_in), dtype=torch.bfloat16, device=dev)
-    y = torch.zeros((1, 1), dtype=torch.bfloat16, device=dev)
+    y = torch.zeros((N, d_out), dtype=torch.bfloat16, device=dev)
     rc = lib.bws_nvfp4_gemv_noalloc(c.data_ptr(), s.data_ptr(), t.data_ptr(), x.data_ptr(), N, d_out, d_in,
                                     y.data_ptr(), torch.cuda.current_stream().cuda_stream)
     assert rc == 7
