@@ -426,9 +426,8 @@ int bws_decode_step_plan_create(const bws_stack* S, int N, bws_stack_plan** plan
   P->step = (opt && opt[0] == '1')
                 ? step_program_create(N, H, P->eps, P->layers.data(), (int)P->layers.size(), P->head)
                 : nullptr;
-  if (P->step) {
-    const size_t sb = step_program_workspace(P->step);
-    P->total = sb > P->total ? sb : P->total;
+  if (P->step) {   // the chain's buffers are not used
+    P->total = step_program_workspace(P->step);
     P->kernels = 2;
   }
   P->exec = nullptr;

@@ -24,6 +24,9 @@ void step_program_destroy(StepProgram* program);
 size_t step_program_workspace(const StepProgram* program);
 // CTAs of the persistent kernel.
 int step_program_grid(const StepProgram* program);
+// Byte offset in the workspace of the optional trace (-1: none) and the
+// number of products.
+long long step_program_trace(const StepProgram* program, int* n_prods);
 // Enqueues one step: an init kernel, then the persistent kernel (2 launches).
 cudaError_t step_program_enqueue(const StepProgram* program, const uint16_t* x0, float* logits, void* ws,
                                  cudaStream_t st);
