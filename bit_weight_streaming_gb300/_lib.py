@@ -33,6 +33,8 @@ SIGNATURES = {
     "bws_decode_step_plan_destroy": (None, [P]),
     "bws_decode_step_stream": (I, [P, P, P, P, Z, P]),
     "bws_decode_step_kernel_count": (I, [P]),
+    "bws_decode_step_tap_size": (Z, [P]),
+    "bws_decode_step_tap": (I, [P, P, P, P, Z, P, Z, P]),
     "bws_status_word": (I, [P, P, P]),
     "bws_debug_wait_flag": (I, [P, C.c_uint32, P, Z, P]),
     "bws_hbm_read_probe": (I, [P, Z, P, P]),

@@ -22,6 +22,7 @@ int enqueue_moe(const bws_moe_layer* L, const int32_t* ids, const float* route_w
 struct MoeStackView {
   MoeRoute route;
   float* ys;
+  uint16_t* h;             // SwiGLU activations of the slots [max_slots][N][inter]
   uint32_t* counters;
   int n_counters;
 };

@@ -180,6 +180,9 @@ struct PrepParams {
   int fin_row_off[kMaxMats], fin_tile_begin[kMaxMats];   // the matrices' first output row and tile
   const float* fin_scale[kMaxMats];
   const int* fin_xexp;     // exponents of the product's input rows [N]
+  // optional (one-slot rows, not the tensor-core image): the BF16 row formed,
+  // written to tap_x [N][d_in] (verification tap of the decode step)
+  uint16_t* tap_x;
 };
 
 // Workspace of one product call (all offsets 256-byte aligned).

@@ -282,6 +282,7 @@ MoeStackView moe_stack_view(const bws_moe_layer* L, const int32_t* ids, const fl
   v.route.cw = reinterpret_cast<float*>(w + (buffer ? m.off_cw_b : m.off_cw));
   v.route.status = reinterpret_cast<uint32_t*>(w + m.off_status);
   v.ys = reinterpret_cast<float*>(w + m.off_ys);
+  v.h = reinterpret_cast<uint16_t*>(w + m.off_h);
   v.counters = reinterpret_cast<uint32_t*>(w + m.off_counters);
   v.n_counters = m.n_tiles;
   return v;

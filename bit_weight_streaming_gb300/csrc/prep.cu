@@ -396,7 +396,11 @@ __device__ __forceinline__ void prep_body(const PrepParams& q) {
   uint4* lo4 = reinterpret_cast<uint4*>(q.lo + rowbase + (size_t)tok * q.d_in_pad);
   for (int c = c0 + threadIdx.x; c < c1; c += blockDim.x) {
     uint32_t w[4] = {0u, 0u, 0u, 0u};
-    if (c < nchunk) chunk_bf16<FIN>(q, c, rr, xr, inv_rms, w);
+    if (c < nchunk) {
+      chunk_bf16<FIN>(q, c, rr, xr, inv_rms, w);
+      if (q.tap_x != nullptr)   // verification tap: the BF16 row as formed
+        reinterpret_cast<uint4*>(q.tap_x + (size_t)tok * q.d_in)[c] = make_uint4(w[0], w[1], w[2], w[3]);
+    }
     store_bands(w, E, hi4, lo4, band_pos(c, q.interleave), flags);
   }
   }
@@ -503,6 +507,8 @@ __device__ __forceinline__ void prep_fin_body(const PrepParams& q) {
       for (int i = 0; i < 4; ++i)
         w[i] = (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(__fmul_rn(v[2 * i], inv_rms))) |
                ((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(__fmul_rn(v[2 * i + 1], inv_rms))) << 16);
+      if (q.tap_x != nullptr)   // verification tap: the BF16 row as formed
+        reinterpret_cast<uint4*>(q.tap_x + (size_t)tok * q.d_in)[c] = make_uint4(w[0], w[1], w[2], w[3]);
     }
     uint4* hi4 = reinterpret_cast<uint4*>(q.hi + (size_t)tok * q.d_in_pad);
     uint4* lo4 = reinterpret_cast<uint4*>(q.lo + (size_t)tok * q.d_in_pad);

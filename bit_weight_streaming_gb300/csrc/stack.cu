@@ -69,10 +69,35 @@ GemvMat gm(const bws_matrix& m, int out_row_off, int tile_begin) {
   return g;
 }
 
+// Verification tap (bws_decode_step_tap): records appended in launch order,
+// each on a 256-byte boundary. With a null base only the sizes are counted.
+struct Tap {
+  char* base;
+  size_t off;
+  cudaStream_t st;
+  cudaError_t err;
+  void* take(size_t bytes) {
+    void* d = base ? base + off : nullptr;
+    off += align256(bytes);
+    return d;
+  }
+  void copy(const void* src, size_t bytes) {
+    void* d = take(bytes);
+    if (d && err == cudaSuccess) err = cudaMemcpyAsync(d, src, bytes, cudaMemcpyDeviceToDevice, st);
+  }
+  // rows of row_bytes each, src_pitch bytes apart, packed
+  void copy_rows(const void* src, size_t src_pitch, size_t row_bytes, int rows) {
+    void* d = take(row_bytes * rows);
+    if (d && err == cudaSuccess)
+      err = cudaMemcpy2DAsync(d, row_bytes, src, src_pitch, row_bytes, rows, cudaMemcpyDeviceToDevice, st);
+  }
+};
+
 struct Ctx {
   const bws_stack_plan* P;
   char* w;
   cudaStream_t st;
+  Tap* tap;   // optional
 };
 
 XPrep xprep_of(const Ctx& c, size_t block, const GemvWorkspace& L) {
@@ -127,6 +152,9 @@ cudaError_t prep(const Ctx& c, int mode, const uint16_t* x, int ld, const uint16
                  const PrepParams* fin = nullptr) {
   PrepParams q = {};
   if (fin != nullptr) q = *fin;   // the finishing fields
+  // tap: an RMSNorm prep records the BF16 row it forms, then the residual it normalised
+  const bool tap_norm = c.tap != nullptr && mode == kPrepRmsNorm;
+  if (tap_norm) q.tap_x = static_cast<uint16_t*>(c.tap->take(2 * (size_t)c.P->N * d_in));
   q.mode = mode;
   q.x = x;
   q.ld = ld;
@@ -156,7 +184,9 @@ cudaError_t prep(const Ctx& c, int mode, const uint16_t* x, int ld, const uint16
     q.has_route = 1;
     q.route = *route;
   }
-  return launch_prep(q, c.st, true);
+  const cudaError_t e = launch_prep(q, c.st, true);
+  if (e == cudaSuccess && tap_norm) c.tap->copy(q.r, sizeof(float) * (size_t)c.P->N * d_in);
+  return e;
 }
 
 int tiles_for(const bws_matrix* mats, int nm, int epi) {
@@ -204,10 +234,14 @@ cudaError_t product(const Ctx& c, const bws_matrix* mats, int nm, int epi, const
                         true);
 }
 
-int enqueue_step(const bws_stack_plan* P, const uint16_t* x0, float* logits, void* ws, cudaStream_t st) {
-  const char* name = "bws_decode_step_stream";
-  if (P->step) return cuda_status(step_program_enqueue(P->step, x0, logits, ws, st), name);
-  Ctx c{P, static_cast<char*>(ws), st};
+int enqueue_step(const bws_stack_plan* P, const uint16_t* x0, float* logits, void* ws, cudaStream_t st,
+                 Tap* tap = nullptr) {
+  const char* name = tap ? "bws_decode_step_tap" : "bws_decode_step_stream";
+  if (P->step) {
+    if (tap) return fail(BWS_ERR_UNSUPPORTED_SHAPE, "%s: the persistent step kernel has no tap", name);
+    return cuda_status(step_program_enqueue(P->step, x0, logits, ws, st), name);
+  }
+  Ctx c{P, static_cast<char*>(ws), st, tap};
   float* r = reinterpret_cast<float*>(c.w + P->off_r);
   uint32_t* counters = reinterpret_cast<uint32_t*>(c.w + P->off_counters);
   uint16_t* u = reinterpret_cast<uint16_t*>(c.w + P->off_u);
@@ -261,6 +295,7 @@ int enqueue_step(const bws_stack_plan* P, const uint16_t* x0, float* logits, voi
       pout.split_light = late_ctas(dv);
       BWS_TRY(prep(c, kPrepCopy, u, sum_out, nullptr, dv, P->off_vp, P->vw, counters,
                    tiles_for(&L.mixer_out, 1, kEpiResidF32), layout_for(&L.mixer_out, pout), nullptr, nullptr, fin));
+      if (tap) tap->copy_rows(u, 2 * (size_t)sum_out, 2 * (size_t)dv, P->N);
       deposit(&L.mixer_out, 1, kEpiResidF32, pout, H);
       BWS_TRY(product(c, &L.mixer_out, 1, kEpiResidF32, pout));
     }
@@ -279,6 +314,7 @@ int enqueue_step(const bws_stack_plan* P, const uint16_t* x0, float* logits, voi
       pdn.split_light = late_ctas(I);
       BWS_TRY(prep(c, kPrepCopy, h, I, nullptr, I, P->off_hp, P->hw, counters, tiles_for(&L.down, 1, kEpiResidF32),
                    layout_for(&L.down, pdn), nullptr, nullptr, fin));
+      if (tap) tap->copy(h, 2 * (size_t)P->N * I);
       // the next prep finishes the down rows unless it is an MoE layer's
       // (routing and combine), which reads r as the product leaves it
       const bool next_moe = li + 1 < P->layers.size() && P->layers[li + 1].kind == BWS_LAYER_MOE;
@@ -304,6 +340,14 @@ int enqueue_step(const bws_stack_plan* P, const uint16_t* x0, float* logits, voi
       const int rc = enqueue_moe_experts(&L.moe, P->N, L.topk, v.route.n_slots, v.route.slot_expert, xa,
                                          c.w + P->off_moe, st, name, v.route.ready);
       if (rc != BWS_OK) return rc;
+      if (tap) {
+        const int ms = v.route.max_slots;
+        tap->copy(v.route.n_slots, sizeof(int));
+        tap->copy(v.route.slot_expert, sizeof(int) * (size_t)ms);
+        tap->copy(v.route.cw, sizeof(float) * (size_t)ms * P->N);
+        tap->copy(v.h, 2 * (size_t)ms * P->N * L.moe.inter);
+        tap->copy(v.ys, sizeof(float) * (size_t)ms * P->N * H);
+      }
       pend_v = v;
       pending = &pend_v;
       moe_buf ^= 1;
@@ -316,6 +360,36 @@ int enqueue_step(const bws_stack_plan* P, const uint16_t* x0, float* logits, voi
   BWS_TRY(product(c, &P->head, 1, kEpiStoreF32, ph));
 #undef BWS_TRY
   return BWS_OK;
+}
+
+// The tap's record sizes, in the order enqueue_step writes them.
+size_t tap_walk_size(const bws_stack_plan* P, Tap* t) {
+  const size_t N = P->N, H = P->hidden;
+  for (const bws_layer& L : P->layers) {
+    if (L.kind == BWS_LAYER_MIXER_MLP) {
+      t->take(2 * N * H);                            // a = BF16(RMSNorm(r))
+      t->take(4 * N * H);                            // the r it normalised
+      t->take(2 * N * (size_t)L.mixer_out.d_in);     // v = the mixer inputs' first d_v outputs
+    }
+    if (L.kind == BWS_LAYER_MIXER_MLP || L.kind == BWS_LAYER_MLP) {
+      t->take(2 * N * H);                            // m
+      t->take(4 * N * H);                            // the r it normalised
+      t->take(2 * N * (size_t)L.gate.d_out);         // h
+    }
+    if (L.kind == BWS_LAYER_MOE) {
+      const size_t ms = N * L.topk + (L.moe.shared_gate_up_codes != nullptr ? 1 : 0);
+      t->take(2 * N * H);                            // m
+      t->take(4 * N * H);                            // the r it normalised
+      t->take(sizeof(int));                          // live slots
+      t->take(sizeof(int) * ms);                     // slot experts
+      t->take(sizeof(float) * ms * N);               // combine weights
+      t->take(2 * ms * N * L.moe.inter);             // h per slot
+      t->take(sizeof(float) * ms * N * H);           // y per slot
+    }
+  }
+  t->take(2 * N * H);                                // the output layer's input
+  t->take(4 * N * H);                                // the r it normalised
+  return t->off;
 }
 
 }  // namespace
@@ -447,6 +521,29 @@ void bws_decode_step_plan_destroy(bws_stack_plan* plan) {
 size_t bws_decode_step_workspace_size(const bws_stack_plan* plan) { return plan ? plan->total : 0; }
 
 int bws_decode_step_kernel_count(const bws_stack_plan* plan) { return plan ? plan->kernels : 0; }
+
+size_t bws_decode_step_tap_size(const bws_stack_plan* plan) {
+  if (!plan || plan->step) return 0;
+  Tap t{nullptr, 0, nullptr, cudaSuccess};
+  return tap_walk_size(plan, &t);
+}
+
+int bws_decode_step_tap(bws_stack_plan* P, const uint16_t* x0, float* logits, void* ws, size_t ws_bytes, void* tap,
+                        size_t tap_bytes, void* stream) {
+  const char* name = "bws_decode_step_tap";
+  if (!P || !x0 || !logits || !ws || !tap) return fail(BWS_ERR_INVALID_ARG, "%s: null pointer", name);
+  if (P->step) return fail(BWS_ERR_UNSUPPORTED_SHAPE, "%s: the persistent step kernel has no tap", name);
+  if (ws_bytes < P->total) return fail(BWS_ERR_WORKSPACE, "%s: workspace of %zu bytes needed, %zu given", name, P->total, ws_bytes);
+  const size_t need = bws_decode_step_tap_size(P);
+  if (tap_bytes < need) return fail(BWS_ERR_WORKSPACE, "%s: tap of %zu bytes needed, %zu given", name, need, tap_bytes);
+  if (!aligned(ws, 256) || !aligned(tap, 256) || !aligned(x0, 16) || !aligned(logits, 4))
+    return fail(BWS_ERR_MISALIGNED, "%s: workspace and tap 256-byte, x0 16-byte, logits 4-byte alignment needed", name);
+  cudaStream_t st = as_stream(stream);
+  Tap t{static_cast<char*>(tap), 0, st, cudaSuccess};
+  const int rc = enqueue_step(P, x0, logits, ws, st, &t);
+  if (rc != BWS_OK) return rc;
+  return cuda_status(t.err, name);
+}
 
 int bws_decode_step_stream(bws_stack_plan* P, const uint16_t* x0, float* logits, void* ws, size_t ws_bytes,
                            void* stream) {

@@ -98,6 +98,50 @@ class DecodeStack:
                                            _stream(self.device)), "bws_decode_step_stream")
         return logits
 
+    def tap_size(self):
+        return int(lib().bws_decode_step_tap_size(self.plan))
+
+    def step_tap(self, x0, logits=None):
+        """One step through bws_decode_step_tap: returns (logits, records),
+        records being the list of device tensors (views of one tap buffer)
+        in the order the C ABI writes them (see tap_layout)."""
+        if logits is None:
+            logits = torch.empty((self.N, self.head.d_out), dtype=torch.float32, device=self.device)
+        n = self.tap_size()
+        if n == 0:
+            raise BwsError("this plan has no tap (persistent step kernel)")
+        buf = torch.empty(n, dtype=torch.uint8, device=self.device)
+        check(lib().bws_decode_step_tap(self.plan, _ptr(x0), _ptr(logits), self.ws.ptr, self.ws.nbytes, _ptr(buf), n,
+                                        _stream(self.device)), "bws_decode_step_tap")
+        recs, off = [], 0
+        for kind, dtype, shape in self.tap_layout():
+            nbytes = int(torch.Size(shape).numel()) * torch.tensor([], dtype=dtype).element_size()
+            recs.append((kind, buf[off:off + nbytes].view(dtype).view(shape)))
+            off += (nbytes + 255) // 256 * 256
+        assert off == n, (off, n)
+        return logits, recs
+
+    def tap_layout(self):
+        """(kind, dtype, shape) of each tap record, in order."""
+        N, H = self.N, self.hidden
+        out = []
+        for L in self.layers_py:
+            if L["kind"] == "mixer_mlp":
+                out += [("a", torch.bfloat16, (N, H)), ("r", torch.float32, (N, H)),
+                        ("v", torch.bfloat16, (N, L["mixer_out"].d_in))]
+            if L["kind"] in ("mixer_mlp", "mlp"):
+                out += [("m", torch.bfloat16, (N, H)), ("r", torch.float32, (N, H)),
+                        ("h", torch.bfloat16, (N, L["gate"].d_out))]
+            if L["kind"] == "moe":
+                w = L["moe"]
+                S = N * L["ids"].shape[1] + (1 if w.shared is not None else 0)
+                out += [("m", torch.bfloat16, (N, H)), ("r", torch.float32, (N, H)),
+                        ("n_slots", torch.int32, (1,)), ("slot_expert", torch.int32, (S,)),
+                        ("cw", torch.float32, (S, N)), ("h_slots", torch.bfloat16, (S, N, w.inter)),
+                        ("y_slots", torch.float32, (S, N, H))]
+        out += [("x_head", torch.bfloat16, (N, H)), ("r", torch.float32, (N, H))]
+        return out
+
     def weight_bytes(self, distinct_experts=None):
         """Algorithmic bytes of one step (codes + block/row scales). For MoE
         layers pass the number of distinct routed experts per MoE layer."""

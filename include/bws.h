@@ -325,6 +325,31 @@ int bws_decode_step_stream(bws_stack_plan* plan, const uint16_t* x0, float* logi
 /* Number of kernels one decode step launches (2 for the persistent kernel). */
 int bws_decode_step_kernel_count(const bws_stack_plan* plan);
 
+/* Verification tap of the kernel chain (not the persistent kernel): runs the
+ * same step as bws_decode_step_stream, launched directly on the stream (no
+ * graph), and also copies into `tap` (device, 256-byte aligned,
+ * bws_decode_step_tap_size bytes) what each stage of the layer recipe
+ * received or produced, as the GPU formed it, so that every stage can be
+ * checked on its own against its definition from its actual input. Records
+ * follow in launch order, each starting on a 256-byte boundary:
+ *   MIXER_MLP layer: a bf16 [N][hidden] (BF16(RMSNorm(r))), r fp32
+ *     [N][hidden] (the residual a normalised), v bf16 [N][d_v] (the first
+ *     d_v outputs of the mixer input projections, the mixer-out input), then
+ *     the MLP records below;
+ *   MIXER_MLP and MLP layers: m bf16 [N][hidden], r fp32 [N][hidden] (the
+ *     residual m normalised), h bf16 [N][inter] (the down projection input);
+ *   MOE layer: m, r as above, the slot count int32 [1], the slot experts
+ *     int32 [S] (-1: the shared expert), the combine weights fp32 [S][N], h
+ *     bf16 [S][N][inter] per slot and the slots' outputs fp32 [S][N][hidden]
+ *     (S = N * topk + 1 with a shared expert, else N * topk; slots past the
+ *     count hold stale values);
+ *   the output layer: x bf16 [N][hidden] and the r it normalised.
+ * The logits go to `logits` as with bws_decode_step_stream. */
+size_t bws_decode_step_tap_size(const bws_stack_plan* plan);
+int bws_decode_step_tap(bws_stack_plan* plan, const uint16_t* x0, float* logits,
+                        void* workspace, size_t workspace_bytes, void* tap,
+                        size_t tap_bytes, void* stream);
+
 /* ------------------------------------------------------------------------ */
 /* Status and measurement                                                    */
 /* ------------------------------------------------------------------------ */
