@@ -16,6 +16,7 @@ from .api import (  # noqa: F401
     nvfp4_gemv_prepared,
     nvfp4_gate_up_silu,
     fp8_lmhead_gemv,
+    fp8_lmhead_argmax,
     status_word,
     hbm_read_probe,
     l2_flush,

@@ -25,6 +25,7 @@ SIGNATURES = {
     "bws_nvfp4_gemv_noalloc": (I, [P, P, P, P, I, I, I, P, P]),
     "bws_nvfp4_gate_up_silu": (I, [P, P, P, P, P, P, P, I, I, I, P, P, Z, P]),
     "bws_fp8_lmhead_gemv": (I, [P, P, P, I, I, I, P, P, Z, P]),
+    "bws_fp8_lmhead_argmax": (I, [P, P, P, I, I, I, P, P, P, P, Z, P]),
     "bws_mxfp4_moe_workspace_size": (Z, [P, I, I]),
     "bws_mxfp4_moe_gemv": (I, [P, P, P, I, I, P, P, P, Z, P]),
     "bws_mxfp4_moe_inspect": (I, [P, P, I, I, P, P, P, P, P]),
@@ -32,6 +33,7 @@ SIGNATURES = {
     "bws_decode_step_plan_create": (I, [P, I, P]),
     "bws_decode_step_plan_destroy": (None, [P]),
     "bws_decode_step_stream": (I, [P, P, P, P, Z, P]),
+    "bws_decode_step_greedy": (I, [P, P, P, P, P, P, Z, P]),
     "bws_decode_step_kernel_count": (I, [P]),
     "bws_decode_step_tap_size": (Z, [P]),
     "bws_decode_step_tap": (I, [P, P, P, P, Z, P, Z, P]),

@@ -149,6 +149,24 @@ def fp8_lmhead_gemv(W, row_scale, x, logits=None, ws=None):
     return logits
 
 
+def fp8_lmhead_argmax(W, row_scale, x, logits=False, row_token=None, ws=None):
+    """Greedy next-token choice fused into the FP8 output layer: int32 [N]
+    rows of the largest logit (lowest row on ties), through row_token when
+    given. logits=True also returns the fp32 [N, V] logits (a tensor may be
+    passed to store them into)."""
+    _need_cuda(W, row_scale, x)
+    N, d = x.shape
+    V = W.shape[0]
+    if logits is True:
+        logits = torch.empty((N, V), dtype=torch.float32, device=x.device)
+    tok = torch.empty(N, dtype=torch.int32, device=x.device)
+    buf = _ws(ws, gemv_workspace_size(N, V, d), x.device)
+    check(lib().bws_fp8_lmhead_argmax(_ptr(W), _ptr(row_scale), _ptr(x), N, V, d,
+                                      _ptr(logits) if logits is not False else None, _ptr(row_token), _ptr(tok),
+                                      _ptr(buf), buf.numel(), _stream(x.device)), "bws_fp8_lmhead_argmax")
+    return (tok, logits) if logits is not False else tok
+
+
 def status_word(ws):
     """OR of the status bits set by the last product call that used ws."""
     import ctypes

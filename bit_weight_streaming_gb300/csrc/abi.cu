@@ -62,7 +62,8 @@ constexpr int kPhaseBoth = 0, kPhasePrepare = 1, kPhaseProduct = 2;
 // (phase: both, the prep alone, or the product on activations an earlier
 // prepare-only call left in the workspace).
 int run_product(int fmt, int epi, GemvParams& p, const uint16_t* x, int N, int d_in, void* ws,
-                size_t ws_bytes, void* out, int out_ld, cudaStream_t st, const char* name, int phase = kPhaseBoth) {
+                size_t ws_bytes, void* out, int out_ld, cudaStream_t st, const char* name, int phase = kPhaseBoth,
+                const int32_t* row_token = nullptr, int32_t* tokens = nullptr) {
   p.N = N;
   p.d_in = d_in;
   p.nseg = nseg_of(d_in);
@@ -90,6 +91,11 @@ int run_product(int fmt, int epi, GemvParams& p, const uint16_t* x, int N, int d
   q.status_clear = q.hdr + 1;
   q.zero_ptr = reinterpret_cast<uint32_t*>(w + L.off_counters);
   q.zero_words = p.n_tiles;
+  if (tokens != nullptr) {   // greedy argmax: the keys after the tile counters, zeroed with them
+    p.amax_key = reinterpret_cast<unsigned long long*>(q.zero_ptr + argmax_key_word(p.n_tiles));
+    p.no_store = out == nullptr;
+    q.zero_words = argmax_key_word(p.n_tiles) + 2 * N;
+  }
   p.x.hi = q.hi;
   p.x.lo = q.lo;
   p.x.exp = q.exp;
@@ -114,9 +120,13 @@ int run_product(int fmt, int epi, GemvParams& p, const uint16_t* x, int N, int d
                   name);
     return cuda_status(launch_product(fmt, epi, p, q.hdr + 1, st, true), name);
   }
+  if (tokens != nullptr && !(gemv_tma_eligible(fmt, p) && !gemv_umma_eligible(fmt, p)))
+    return fail(BWS_ERR_UNSUPPORTED_SHAPE, "%s: the fused argmax needs the TMA product kernel (d %% 128 == 0, "
+                "16-byte aligned weights)", name);
   cudaError_t e = launch_prep(q, st, true);
   if (e != cudaSuccess) return cuda_status(e, name);
   e = launch_product(fmt, epi, p, q.hdr + 1, st, true);
+  if (e == cudaSuccess && tokens != nullptr) e = launch_argmax_finish(p.amax_key, N, row_token, tokens, st, true);
   return cuda_status(e, name);
 }
 
@@ -282,6 +292,25 @@ int bws_fp8_lmhead_gemv(const uint8_t* W, const float* row_scale, const uint16_t
   p.n_tiles = tiles_rows32(V);
   return run_product(kFmtFP8, kEpiStoreF32, p, x, N, d, workspace, workspace_bytes, logits, V,
                      as_stream(stream), name);
+}
+
+int bws_fp8_lmhead_argmax(const uint8_t* W, const float* row_scale, const uint16_t* x, int N, int V, int d,
+                          float* logits, const int32_t* row_token, int32_t* token, void* workspace,
+                          size_t workspace_bytes, void* stream) {
+  const char* name = "bws_fp8_lmhead_argmax";
+  bool noop;
+  int rc = check_product_common(name, W, x, token, N, V, d, &noop);
+  if (rc || noop) return rc;
+  if (!row_scale) return fail(BWS_ERR_INVALID_ARG, "%s: null row_scale", name);
+  if (!aligned(row_scale, 4) || !aligned(token, 4) || (logits && !aligned(logits, 4)) ||
+      (row_token && !aligned(row_token, 4)))
+    return fail(BWS_ERR_MISALIGNED, "%s: row_scale, logits, row_token and token 4-byte alignment needed", name);
+  GemvParams p = {};
+  p.n_mats = 1;
+  p.mats[0] = {W, nullptr, row_scale, V, 0, 0};
+  p.n_tiles = tiles_rows32(V);
+  return run_product(kFmtFP8, kEpiStoreF32, p, x, N, d, workspace, workspace_bytes, logits, V, as_stream(stream),
+                     name, kPhaseBoth, row_token, token);
 }
 
 int bws_status_word(const void* workspace, uint32_t* status, void* stream) {

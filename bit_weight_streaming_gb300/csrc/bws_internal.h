@@ -3,6 +3,7 @@
 #include <cuda_runtime.h>
 
 #include <atomic>
+#include <cstring>
 #include <stddef.h>
 #include <stdint.h>
 
@@ -90,7 +91,29 @@ struct GemvParams {
                            // slots the prep before holds): give them a lighter share (SplitK)
   int deposit;             // TMA kernel: tile pieces leave their raw sums in partials for the
                            // next prep to finish (PrepParams::fin_*), nothing else is stored
+  unsigned long long* amax_key;   // TMA kernel, kEpiStoreF32, optional: per token the largest
+                           // argmax_key(value, row) of the outputs (zero on entry)
+  int no_store;            // with amax_key: the outputs themselves are not stored
 };
+
+// Greedy argmax over a product's outputs: the key orders by value (FP32 bits
+// mapped to an order-preserving u32), then by lower row index, so the
+// largest key over all outputs is the largest value with the lowest index
+// among equal ones, whatever order the keys are combined in.
+__host__ __device__ inline unsigned long long argmax_key(float v, int row) {
+  uint32_t b;
+  memcpy(&b, &v, 4);
+  b = (b & 0x80000000u) ? ~b : (b | 0x80000000u);
+  return ((unsigned long long)b << 32) | (uint32_t)(0xFFFFFFFFu - (uint32_t)row);
+}
+__host__ __device__ inline int argmax_row(unsigned long long key) {
+  return (int)(0xFFFFFFFFu - (uint32_t)(key & 0xFFFFFFFFull));
+}
+// Word offset of the argmax keys after n_tiles tile counters (8-byte aligned).
+inline int argmax_key_word(int n_tiles) { return (n_tiles + 1) & ~1; }
+// tokens[n] = row (or row_token[row]) of keys[n], n < N.
+cudaError_t launch_argmax_finish(const unsigned long long* keys, int N, const int32_t* row_token, int32_t* tokens,
+                                 cudaStream_t st, bool pdl);
 
 // MoE helpers.
 struct MoeRoute {

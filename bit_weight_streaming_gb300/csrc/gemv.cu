@@ -575,7 +575,8 @@ GemvWorkspace gemv_workspace_layout(int N, int d_in, int n_tiles, long long max_
   w.off_flags = o; o += align256(sizeof(uint32_t) * (size_t)kMaxTokens * slots);
   w.off_hi = o; o += align256(2 * d_pad * (size_t)(N + 1) * slots);
   w.off_lo = o; o += align256(2 * d_pad * (size_t)(N + 1) * slots);
-  w.off_counters = o; o += align256(sizeof(uint32_t) * (size_t)n_tiles);
+  w.off_counters = o;   // tile counters, then (8-byte aligned) the argmax keys of the output layer
+  o += align256(sizeof(uint32_t) * (size_t)argmax_key_word(n_tiles) + sizeof(unsigned long long) * kMaxTokens);
   w.off_partials = o; o += align256(sizeof(float) * kSlotFloats * ((size_t)n_tiles + max_warps));
   w.total = o;
   return w;

@@ -76,6 +76,8 @@ struct TmaParams {
   int n_stages, stage_bytes, x_off, x_blk, x_bytes;
   int n_prime;   // stages given their weights before the inputs are ready
   int deposit;   // 1: each tile piece writes its raw sums to its partial slot, nothing else
+  unsigned long long* amax_key;   // StoreF32, optional: greedy argmax keys [N] (GemvParams)
+  int no_store;
 };
 
 // Shared memory after the stages (which end on a 1024-byte boundary).
@@ -86,6 +88,7 @@ struct Tail {
                                 // used from element 1 on (see consume)
   uint64_t full[kMaxStages];
   uint64_t empty[kMaxStages];
+  unsigned long long akey[kMaxTokens];   // the CTA's best argmax keys
   uint32_t flag;
 };
 static_assert(offsetof(Tail, zero_x) % 128 == 0, "zero pieces must start on a 128-byte boundary");
@@ -149,7 +152,7 @@ BWS_DEV void epi_read(const TmaParams& p, int tile, int b, int g, int t, EpiIn& 
 // token 2t + (i&1)). SwiGLU: b is a gate box and vu the matching up sums.
 template <int FMT, int EPI>
 BWS_DEV void store_sub(const TmaParams& p, int tile, int b, int s, int g, int t, const float (&v)[4],
-                       const float (&vu)[4], const int (&xexp)[2], const EpiIn& in) {
+                       const float (&vu)[4], const int (&xexp)[2], const EpiIn& in, unsigned long long (&ak)[2]) {
   int mi, row_b;
   box_of<EPI>(p, tile, b, mi, row_b);
   const TmaMat& M = p.mats[mi];
@@ -170,11 +173,15 @@ BWS_DEV void store_sub(const TmaParams& p, int tile, int b, int s, int g, int t,
           __float2bfloat16_rn(silu_mul_t(val, up));
     } else {
       const size_t o = (size_t)tok * p.out_ld + M.out_row_off + row;
-      if (EPI == kEpiStoreBF16)
+      if (EPI == kEpiStoreBF16) {
         reinterpret_cast<__nv_bfloat16*>(p.out)[o] = __float2bfloat16_rn(val);
-      else if (EPI == kEpiStoreF32)
-        reinterpret_cast<float*>(p.out)[o] = val;
-      else
+      } else if (EPI == kEpiStoreF32) {
+        if (!p.no_store) reinterpret_cast<float*>(p.out)[o] = val;
+        if (p.amax_key != nullptr) {
+          const unsigned long long k = argmax_key(val, M.out_row_off + row);
+          ak[i & 1] = k > ak[i & 1] ? k : ak[i & 1];
+        }
+      } else
         reinterpret_cast<float*>(p.out)[o] = __fadd_rn(in.r[s][i], val);
     }
   }
@@ -214,6 +221,7 @@ BWS_DEV void consume(const TmaParams& p, Tail& T, uint32_t stage0, long long u0,
   // in different banks
   const uint32_t zaddr = smem_u32(&T.zero_x[1]) + c * 16;
   float acc[2][2][4] = {}, accl[2][4] = {};   // N1: acc[st][0] holds y, accl[st] the lo band's
+  unsigned long long ak[2] = {0ull, 0ull};     // StoreF32 with argmax: best keys of tokens 2t, 2t+1
   uint4 xh[kXv], xl[kXv];
   bool dead = false;   // a wait ran out: keep the control flow (barriers), skip the work
   int tile = (int)(u0 / p.nks), ks = (int)(u0 % p.nks);
@@ -405,14 +413,26 @@ BWS_DEV void consume(const TmaParams& p, Tail& T, uint32_t stage0, long long u0,
         for (int st = 0; st < 2; ++st) {
           const float4 o = T.swi[b][st][lane];
           const float vu[4] = {o.x, o.y, o.z, o.w};
-          store_sub<FMT, EPI>(p, cur_tile, b, st, g, t, v[st], vu, xexp, ein);
+          store_sub<FMT, EPI>(p, cur_tile, b, st, g, t, v[st], vu, xexp, ein, ak);
         }
       }
       named_bar_sync(3, 4 * 32);
     } else {
       const float none[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-      for (int st = 0; st < 2; ++st) store_sub<FMT, EPI>(p, cur_tile, b, st, g, t, v[st], none, xexp, ein);
+      for (int st = 0; st < 2; ++st) store_sub<FMT, EPI>(p, cur_tile, b, st, g, t, v[st], none, xexp, ein, ak);
+    }
+  }
+  if (EPI == kEpiStoreF32 && p.amax_key != nullptr) {
+    // the warp's best key per token (lanes of one t hold the same tokens), into the CTA's
+#pragma unroll
+    for (int k = 0; k < 2; ++k) {
+#pragma unroll
+      for (int o = 4; o < 32; o <<= 1) {
+        const unsigned long long q = __shfl_xor_sync(0xffffffffu, ak[k], o);
+        ak[k] = q > ak[k] ? q : ak[k];
+      }
+      if (g == 0 && 2 * t + k < p.N) atomicMax(&T.akey[2 * t + k], ak[k]);
     }
   }
 }
@@ -446,6 +466,7 @@ __global__ void __launch_bounds__(kThreadsTma, 2) gemv_tma_kernel(const __grid_c
     mbar_fence_init();
   }
   for (int i = threadIdx.x; i < 33; i += blockDim.x) T.zero_x[i] = make_uint4(0, 0, 0, 0);
+  if (threadIdx.x < kMaxTokens) T.akey[threadIdx.x] = 0ull;
   __syncthreads();
   constexpr int kUnitK = FMT == kFmtFP8 ? 128 : 256;
 
@@ -531,6 +552,11 @@ __global__ void __launch_bounds__(kThreadsTma, 2) gemv_tma_kernel(const __grid_c
     consume_lo<FMT, EPI, N1>(p, T, stage0, u0, u1, warp, lane, p.x.lo);
   else
     consume<FMT, EPI, false, N1>(p, T, stage0, u0, u1, warp, lane, p.x.lo);
+  if (EPI == kEpiStoreF32 && p.amax_key != nullptr) {
+    // the CTA's best keys into the call's, one atomic per token
+    named_bar_sync(1, kConsumerWarps * 32);
+    if (threadIdx.x < p.N) atomicMax(p.amax_key + threadIdx.x, T.akey[threadIdx.x]);
+  }
 }
 
 template <int FMT, int EPI, bool N1>
@@ -649,6 +675,8 @@ cudaError_t launch_gemv_tma(int fmt, int epi, const GemvParams& g, uint32_t* sta
   p.num = geo.split.num;
   p.den = geo.split.den;
   p.deposit = g.deposit;
+  p.amax_key = epi == kEpiStoreF32 ? g.amax_key : nullptr;
+  p.no_store = p.amax_key != nullptr && g.no_store;
   if (p.deposit && (epi == kEpiStoreF32 || !gemv_tma_deposit_fits(geo, g))) return cudaErrorInvalidValue;
   p.x = g.x;
   p.out = g.out;

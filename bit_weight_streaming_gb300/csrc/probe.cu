@@ -65,4 +65,32 @@ cudaError_t launch_wait_flag(const uint32_t* flag, uint32_t max_polls, uint32_t*
   return cudaGetLastError();
 }
 
+// tokens[n]: the row of the largest argmax key of token n (keys the product
+// kernel's epilogue combined), or row_token[row] when a map is given; -1 if
+// no output was seen.
+__global__ void __launch_bounds__(32) argmax_finish_kernel(const unsigned long long* keys, int N,
+                                                           const int32_t* row_token, int32_t* tokens) {
+  pdl_launch_dependents();
+  pdl_wait();
+  const int n = threadIdx.x;
+  if (n >= N) return;
+  const unsigned long long k = keys[n];
+  const int row = k == 0ull ? -1 : argmax_row(k);
+  tokens[n] = (row >= 0 && row_token != nullptr) ? row_token[row] : row;
+}
+
+cudaError_t launch_argmax_finish(const unsigned long long* keys, int N, const int32_t* row_token, int32_t* tokens,
+                                 cudaStream_t st, bool pdl) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(1);
+  cfg.blockDim = dim3(32);
+  cfg.stream = st;
+  cudaLaunchAttribute a[1];
+  a[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  a[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = a;
+  cfg.numAttrs = pdl ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, argmax_finish_kernel, keys, N, row_token, tokens);
+}
+
 }  // namespace bws

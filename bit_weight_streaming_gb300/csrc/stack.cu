@@ -33,7 +33,7 @@ struct bws_stack_plan {
   StepProgram* step;
   // recorded graph
   cudaGraphExec_t exec;
-  const void* key[4];
+  const void* key[6];
 };
 
 namespace {
@@ -234,11 +234,12 @@ cudaError_t product(const Ctx& c, const bws_matrix* mats, int nm, int epi, const
                         true);
 }
 
-int enqueue_step(const bws_stack_plan* P, const uint16_t* x0, float* logits, void* ws, cudaStream_t st,
-                 Tap* tap = nullptr) {
-  const char* name = tap ? "bws_decode_step_tap" : "bws_decode_step_stream";
+int enqueue_step(const bws_stack_plan* P, const uint16_t* x0, float* logits, const int32_t* row_token,
+                 int32_t* tokens, void* ws, cudaStream_t st, Tap* tap = nullptr) {
+  const char* name = tap ? "bws_decode_step_tap" : (tokens ? "bws_decode_step_greedy" : "bws_decode_step_stream");
   if (P->step) {
-    if (tap) return fail(BWS_ERR_UNSUPPORTED_SHAPE, "%s: the persistent step kernel has no tap", name);
+    if (tap || tokens)
+      return fail(BWS_ERR_UNSUPPORTED_SHAPE, "%s: the persistent step kernel has no tap or fused argmax", name);
     return cuda_status(step_program_enqueue(P->step, x0, logits, ws, st), name);
   }
   Ctx c{P, static_cast<char*>(ws), st, tap};
@@ -355,9 +356,19 @@ int enqueue_step(const bws_stack_plan* P, const uint16_t* x0, float* logits, voi
   }
   GemvParams ph = product_params(c, &P->head, 1, kEpiStoreF32, H, xa, logits, P->head.d_out);
   ph.split_light = late_ctas(H);
-  BWS_TRY(prep(c, kPrepRmsNorm, nullptr, 0, init, H, P->off_xp, P->xw, counters, tiles_for(&P->head, 1, kEpiStoreF32),
+  const int head_tiles = tiles_for(&P->head, 1, kEpiStoreF32);
+  int head_zero = head_tiles;
+  if (tokens != nullptr) {   // greedy argmax fused into the output layer: keys after its tile counters
+    if (!gemv_tma_eligible(fmt_of(P->head), ph) || gemv_umma_eligible(fmt_of(P->head), ph))
+      return fail(BWS_ERR_UNSUPPORTED_SHAPE, "%s: the fused argmax needs the TMA output-layer kernel", name);
+    ph.amax_key = reinterpret_cast<unsigned long long*>(counters + argmax_key_word(head_tiles));
+    ph.no_store = logits == nullptr;
+    head_zero = argmax_key_word(head_tiles) + 2 * P->N;
+  }
+  BWS_TRY(prep(c, kPrepRmsNorm, nullptr, 0, init, H, P->off_xp, P->xw, counters, head_zero,
                layout_for(&P->head, ph), pending, nullptr, fin));
   BWS_TRY(product(c, &P->head, 1, kEpiStoreF32, ph));
+  if (tokens != nullptr) BWS_TRY(launch_argmax_finish(ph.amax_key, P->N, row_token, tokens, st, true));
 #undef BWS_TRY
   return BWS_OK;
 }
@@ -473,7 +484,7 @@ int bws_decode_step_plan_create(const bws_stack* S, int N, bws_stack_plan** plan
     P->layers.push_back(L);
   }
   if ((rc = check_matrix(S->head, H, "head", -1))) return bad(rc);
-  const int th = (S->head.d_out + 31) / 32;
+  const int th = argmax_key_word((S->head.d_out + 31) / 32) + 2 * kMaxTokens;   // tile counters, argmax keys
   P->max_tiles = th > P->max_tiles ? th : P->max_tiles;
   // workspace layout
   size_t o = 0;
@@ -540,28 +551,27 @@ int bws_decode_step_tap(bws_stack_plan* P, const uint16_t* x0, float* logits, vo
     return fail(BWS_ERR_MISALIGNED, "%s: workspace and tap 256-byte, x0 16-byte, logits 4-byte alignment needed", name);
   cudaStream_t st = as_stream(stream);
   Tap t{static_cast<char*>(tap), 0, st, cudaSuccess};
-  const int rc = enqueue_step(P, x0, logits, ws, st, &t);
+  const int rc = enqueue_step(P, x0, logits, nullptr, nullptr, ws, st, &t);
   if (rc != BWS_OK) return rc;
   return cuda_status(t.err, name);
 }
 
-int bws_decode_step_stream(bws_stack_plan* P, const uint16_t* x0, float* logits, void* ws, size_t ws_bytes,
-                           void* stream) {
-  const char* name = "bws_decode_step_stream";
-  if (!P || !x0 || !logits || !ws) return fail(BWS_ERR_INVALID_ARG, "%s: null pointer", name);
+static int run_step(bws_stack_plan* P, const uint16_t* x0, float* logits, const int32_t* row_token, int32_t* tokens,
+                    void* ws, size_t ws_bytes, void* stream, const char* name) {
+  if (!P || !x0 || !ws || (!logits && !tokens)) return fail(BWS_ERR_INVALID_ARG, "%s: null pointer", name);
   if (ws_bytes < P->total) return fail(BWS_ERR_WORKSPACE, "%s: workspace of %zu bytes needed, %zu given", name, P->total, ws_bytes);
-  if (!aligned(ws, 256) || !aligned(x0, 16) || !aligned(logits, 4))
-    return fail(BWS_ERR_MISALIGNED, "%s: workspace 256-byte, x0 16-byte, logits 4-byte alignment needed", name);
+  if (!aligned(ws, 256) || !aligned(x0, 16) || !aligned(logits, 4) || !aligned(tokens, 4) || !aligned(row_token, 4))
+    return fail(BWS_ERR_MISALIGNED, "%s: workspace 256-byte, x0 16-byte, logits and tokens 4-byte alignment needed", name);
   cudaStream_t st = as_stream(stream);
   cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
   if (st != nullptr) {
     cudaError_t e = cudaStreamIsCapturing(st, &cs);
     if (e != cudaSuccess) return cuda_status(e, name);
   }
-  if (st == nullptr || cs != cudaStreamCaptureStatusNone) return enqueue_step(P, x0, logits, ws, st);
-  const void* key[4] = {x0, logits, ws, st};
+  if (st == nullptr || cs != cudaStreamCaptureStatusNone) return enqueue_step(P, x0, logits, row_token, tokens, ws, st);
+  const void* key[6] = {x0, logits, ws, st, row_token, tokens};
   bool same = P->exec != nullptr;
-  for (int i = 0; i < 4; ++i) same = same && key[i] == P->key[i];
+  for (int i = 0; i < 6; ++i) same = same && key[i] == P->key[i];
   if (!same) {
     if (P->exec) {
       cudaGraphExecDestroy(P->exec);
@@ -569,7 +579,7 @@ int bws_decode_step_stream(bws_stack_plan* P, const uint16_t* x0, float* logits,
     }
     cudaError_t e = cudaStreamBeginCapture(st, cudaStreamCaptureModeThreadLocal);
     if (e != cudaSuccess) return cuda_status(e, name);
-    const int rc = enqueue_step(P, x0, logits, ws, st);
+    const int rc = enqueue_step(P, x0, logits, row_token, tokens, ws, st);
     cudaGraph_t g = nullptr;
     e = cudaStreamEndCapture(st, &g);
     if (rc != BWS_OK) {
@@ -583,9 +593,21 @@ int bws_decode_step_stream(bws_stack_plan* P, const uint16_t* x0, float* logits,
       P->exec = nullptr;
       return cuda_status(e, name);
     }
-    for (int i = 0; i < 4; ++i) P->key[i] = key[i];
+    for (int i = 0; i < 6; ++i) P->key[i] = key[i];
   }
   return cuda_status(cudaGraphLaunch(P->exec, st), name);
+}
+
+int bws_decode_step_stream(bws_stack_plan* P, const uint16_t* x0, float* logits, void* ws, size_t ws_bytes,
+                           void* stream) {
+  if (!logits) return fail(BWS_ERR_INVALID_ARG, "bws_decode_step_stream: null logits");
+  return run_step(P, x0, logits, nullptr, nullptr, ws, ws_bytes, stream, "bws_decode_step_stream");
+}
+
+int bws_decode_step_greedy(bws_stack_plan* P, const uint16_t* x0, float* logits, const int32_t* row_token,
+                           int32_t* tokens, void* ws, size_t ws_bytes, void* stream) {
+  if (!tokens) return fail(BWS_ERR_INVALID_ARG, "bws_decode_step_greedy: null tokens");
+  return run_step(P, x0, logits, row_token, tokens, ws, ws_bytes, stream, "bws_decode_step_greedy");
 }
 
 }  // extern "C"

@@ -98,6 +98,17 @@ class DecodeStack:
                                            _stream(self.device)), "bws_decode_step_stream")
         return logits
 
+    def step_greedy(self, x0, tokens=None, logits=None, row_token=None):
+        """One step with the greedy next-token choice fused into the output
+        layer: returns tokens int32 [N] (logits are stored too when a tensor
+        is passed)."""
+        if tokens is None:
+            tokens = torch.empty(self.N, dtype=torch.int32, device=self.device)
+        check(lib().bws_decode_step_greedy(self.plan, _ptr(x0), _ptr(logits), _ptr(row_token), _ptr(tokens),
+                                           self.ws.ptr, self.ws.nbytes, _stream(self.device)),
+              "bws_decode_step_greedy")
+        return tokens
+
     def tap_size(self):
         return int(lib().bws_decode_step_tap_size(self.plan))
 

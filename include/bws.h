@@ -201,6 +201,25 @@ int bws_fp8_lmhead_gemv(const uint8_t* W, const float* row_scale,
                         const uint16_t* x, int N, int V, int d, float* logits,
                         void* workspace, size_t workspace_bytes, void* stream);
 
+/* The FP8 output layer with the greedy choice of the next token fused into
+ * its epilogue ([Spark27B] "MTP": the whole 248,320-row output layer is read
+ * only to pick one token; "Shaving the step": a reduced-vocabulary draft head
+ * of the 100,032 most used rows). For each token row n, token[n] = the row
+ * of the largest logit (ties: the lowest row), mapped through row_token when
+ * given (a reduced head's row -> vocabulary id), -1 if V == 0. The logits of
+ * bws_fp8_lmhead_gemv are also stored when `logits` is not NULL. Every CTA
+ * keeps the best (value, lowest row) per token over the tiles it stores and
+ * one 64-bit atomic max per CTA and token combines them: the result does not
+ * depend on the order the CTAs finish in.
+ *   W, row_scale, x, N, V, d: as bws_fp8_lmhead_gemv (d % 128 == 0, W
+ *   16-byte aligned: the TMA kernel carries the fused epilogue, else
+ *   BWS_ERR_UNSUPPORTED_SHAPE); row_token int32 [V] or NULL; token int32 [N].
+ * Workspace: bws_gemv_workspace_size(N, V, d). */
+int bws_fp8_lmhead_argmax(const uint8_t* W, const float* row_scale,
+                          const uint16_t* x, int N, int V, int d, float* logits,
+                          const int32_t* row_token, int32_t* token, void* workspace,
+                          size_t workspace_bytes, void* stream);
+
 /* One MXFP4 mixture-of-experts layer ([LingMoE] sections 3, 4 and 8: each
  * token is routed to top-k of n_experts routed experts plus one shared
  * expert; only the activated experts' weights are read; N tokens of a
@@ -320,6 +339,16 @@ size_t bws_decode_step_workspace_size(const bws_stack_plan* plan);
  * and later calls with the same (x0, logits, workspace, stream) replay it; on
  * the legacy default stream the kernels are launched directly. */
 int bws_decode_step_stream(bws_stack_plan* plan, const uint16_t* x0, float* logits,
+                           void* workspace, size_t workspace_bytes, void* stream);
+
+/* The decode step with greedy decoding fused into the output layer (see
+ * bws_fp8_lmhead_argmax): tokens int32 [N] receives each token row's
+ * next-token choice; logits (fp32 [N][vocab]) are stored too unless NULL;
+ * row_token (int32 [vocab] or NULL) maps output rows to vocabulary ids.
+ * Graph recording and replay as bws_decode_step_stream (keyed also on
+ * tokens and row_token). The kernel chain only (not the persistent kernel). */
+int bws_decode_step_greedy(bws_stack_plan* plan, const uint16_t* x0, float* logits,
+                           const int32_t* row_token, int32_t* tokens,
                            void* workspace, size_t workspace_bytes, void* stream);
 
 /* Number of kernels one decode step launches (2 for the persistent kernel). */
