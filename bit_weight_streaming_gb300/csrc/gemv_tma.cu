@@ -125,7 +125,8 @@ BWS_DEV SplitK split_of(const TmaParams& p) {
 // scale; the tensor scales of the matrices (loaded once per CTA).
 struct EpiIn {
   float r[2][4];
-  float rs[2][2];
+  float rs[2][2];    // FP8: row scales of the stored rows (SwiGLU: the gate rows)
+  float rsu[2][2];   // FP8 SwiGLU: row scales of the matching up rows
   float ts[kMaxMats];
 };
 
@@ -143,7 +144,10 @@ BWS_DEV void epi_read(const TmaParams& p, int tile, int b, int g, int t, EpiIn& 
       const bool ok = row < M.d_out && tok < p.N;
       if (EPI == kEpiResidF32)
         in.r[s][i] = ok ? reinterpret_cast<const float*>(p.out)[(size_t)tok * p.out_ld + M.out_row_off + row] : 0.0f;
-      if (FMT == kFmtFP8 && (i & 1) == 0) in.rs[s][i >> 1] = row < M.d_out ? __ldg(M.scale32 + row) : 0.0f;
+      if (FMT == kFmtFP8 && (i & 1) == 0) {
+        in.rs[s][i >> 1] = row < M.d_out ? __ldg(M.scale32 + row) : 0.0f;
+        if (EPI == kEpiSwiGLU) in.rsu[s][i >> 1] = row < p.mats[1].d_out ? __ldg(p.mats[1].scale32 + row) : 0.0f;
+      }
     }
   }
 }
@@ -168,7 +172,8 @@ BWS_DEV void store_sub(const TmaParams& p, int tile, int b, int s, int g, int t,
     if (FMT == kFmtFP8) sc = in.rs[s][i >> 1];
     const float val = ldexp_exact(__fmul_rn(v[i], sc), xexp[i & 1] - 14);
     if (EPI == kEpiSwiGLU) {
-      const float up = ldexp_exact(__fmul_rn(vu[i], in.ts[1]), xexp[i & 1] - 14);
+      const float su = FMT == kFmtFP8 ? in.rsu[s][i >> 1] : in.ts[1];
+      const float up = ldexp_exact(__fmul_rn(vu[i], su), xexp[i & 1] - 14);
       reinterpret_cast<__nv_bfloat16*>(p.out)[(size_t)tok * p.out_ld + row] =
           __float2bfloat16_rn(silu_mul_t(val, up));
     } else {

@@ -98,10 +98,15 @@ __device__ __forceinline__ void finish_chunk(const PrepParams& q, int tok, int e
   }
   const int xe = __ldg(q.fin_xexp + tok) - 14;
   if (SWI) {
-    const float tg = __ldg(q.fin_scale[0]), tu = __ldg(q.fin_scale[1]);
+    // NVFP4: the two tensor scales; FP8: the gate and up rows' own scales
+    const bool fp8 = q.fin_fmt == kFmtFP8;
+    const float tg = fp8 ? 0.0f : __ldg(q.fin_scale[0]), tu = fp8 ? 0.0f : __ldg(q.fin_scale[1]);
 #pragma unroll
-    for (int i = 0; i < 8; ++i)
-      out[i] = silu_mul_t(ldexp_exact(__fmul_rn(a[i], tg), xe), ldexp_exact(__fmul_rn(au[i], tu), xe));
+    for (int i = 0; i < 8; ++i) {
+      const float sg = fp8 ? __ldg(q.fin_scale[0] + lrow + i) : tg;
+      const float su = fp8 ? __ldg(q.fin_scale[1] + lrow + i) : tu;
+      out[i] = silu_mul_t(ldexp_exact(__fmul_rn(a[i], sg), xe), ldexp_exact(__fmul_rn(au[i], su), xe));
+    }
   } else {
 #pragma unroll
     for (int i = 0; i < 8; ++i) {

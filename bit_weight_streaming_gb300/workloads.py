@@ -62,18 +62,43 @@ def dense_layer_shapes(i, hidden=5120, inter=17408, attn=(12288, 1024, 1024, 614
 
 def dense_stack_layers(n_layers, seed=0, hidden=5120, inter=17408, attn=(12288, 1024, 1024, 6144),
                        gdn=(46336, 6144), fmt=FMT_NVFP4, quant=None, device="cuda"):
+    """fmt: one format for every matrix, or fmt(layer, part) with part
+    'mixer' or 'mlp'."""
+    fmt_of = fmt if callable(fmt) else (lambda i, part: fmt)
     layers = []
     idx = 0
     for i in range(n_layers):
         mixer_in, mixer_out, mlp = dense_layer_shapes(i, hidden, inter, attn, gdn)
         L = {"kind": "mixer_mlp", "mixer_in": []}
+        fm, fl = fmt_of(i, "mixer"), fmt_of(i, "mlp")
         for s in mixer_in:
-            L["mixer_in"].append(make_matrix(fmt, s, seed, idx, quant, device)); idx += 1
-        L["mixer_out"] = make_matrix(fmt, mixer_out, seed, idx, quant, device); idx += 1
+            L["mixer_in"].append(make_matrix(fm, s, seed, idx, quant, device)); idx += 1
+        L["mixer_out"] = make_matrix(fm, mixer_out, seed, idx, quant, device); idx += 1
         for name in ("gate", "up", "down"):
-            L[name] = make_matrix(fmt, mlp[name], seed, idx, quant, device); idx += 1
+            L[name] = make_matrix(fl, mlp[name], seed, idx, quant, device); idx += 1
         layers.append(L)
     return layers
+
+
+# The pages' mixed checkpoint ([Spark27B] "Fewer bytes per weight: NVFP4"):
+# FP8 attention and linear-attention projections in every layer, NVFP4 MLPs
+# in layers 0-55 and FP8 MLPs in the last eight; the MLPs are 59 % of the
+# layer bytes. With FP8 mixers the linear-attention projections are sized
+# down to 14336x5120 in and 5120x8192 out so that the layers total 17.77 GB
+# (the pages: 17.83 GB).
+MIXED_GDN = (14336, 8192)
+MIXED_FP8_MLP_FROM = 56
+
+
+def mixed_fmt(n_fp8_from=MIXED_FP8_MLP_FROM):
+    return lambda i, part: FMT_FP8_ROW if (part == "mixer" or i >= n_fp8_from) else FMT_NVFP4
+
+
+def dense_27b_mixed(N, seed=0, n_layers=64, hidden=5120, inter=17408, vocab=248320, attn=(12288, 1024, 1024, 6144),
+                    gdn=MIXED_GDN, n_fp8_from=MIXED_FP8_MLP_FROM, quant=None, device="cuda"):
+    layers = dense_stack_layers(n_layers, seed, hidden, inter, attn, gdn, mixed_fmt(n_fp8_from), quant, device)
+    head = make_matrix(FMT_FP8_ROW, (vocab, hidden), seed, 100000, quant, device)
+    return DecodeStack(hidden, layers, head, N, device=device)
 
 
 def dense_27b(N, seed=0, n_layers=64, hidden=5120, inter=17408, vocab=248320, attn=(12288, 1024, 1024, 6144),

@@ -292,3 +292,42 @@ def test_mixer_input_rows_the_stand_in_discards(N):
         del qm
     print(N, rep.summary())
     rep.assert_ok(expect=("codes_bit_exact", "product"))
+
+
+# ---- the mixed checkpoint: FP8 mixers, NVFP4 MLPs then FP8 in the last layers --------------
+
+@pytest.mark.parametrize("N", [1, 8])
+def test_mixed_checkpoint_stages_every_row(N):
+    from bit_weight_streaming_gb300 import workloads as W
+    bws()
+    stack = W.dense_27b_mixed(N, seed=9, n_layers=4, hidden=1024, inter=2048, vocab=1500,
+                              attn=(1536, 256, 256, 1024), gdn=(1792, 1024), n_fp8_from=2,
+                              quant=oracle_quantizers(device()), device=device())
+    fmts = [(L["mixer_out"].fmt, L["down"].fmt) for L in stack.layers_py]
+    assert fmts == [(3, 1), (3, 1), (3, 3), (3, 3)]
+    x0 = synth.activation_bf16(N, 1024, seed=120 + N, device=device())
+    logits, recs = stack.step_tap(x0)
+    torch.cuda.synchronize()
+    assert torch.equal(logits, stack.step(x0))
+    rep = SC.Report()
+    SC.check_dense_stack(rep, stack, recs, logits, x0, _dense_rows_of(stack))
+    print(rep.summary())
+    rep.assert_ok(expect=("rmsnorm", "mixer_in", "mixer_out", "swiglu", "down", "head"))
+
+
+@pytest.mark.parametrize("N", [1, 8])
+def test_mixed_checkpoint_stages_full_size(N):
+    from bit_weight_streaming_gb300 import workloads as W
+    bws()
+    stack = W.dense_27b_mixed(N, seed=0, device=device())
+    torch.cuda.synchronize()
+    x0 = synth.activation_bf16(N, stack.hidden, seed=130 + N, device=device())
+    logits, recs = stack.step_tap(x0)
+    torch.cuda.synchronize()
+    rep = SC.Report()
+    SC.check_dense_stack(rep, stack, recs, logits, x0, _dense_seeded(stack, 0, rep), k_rows=16, seed=N)
+    print(N, rep.summary())
+    rep.assert_ok(expect=("codes_bit_exact", "rmsnorm", "mixer_in", "mixer_out", "swiglu", "down", "head"))
+    assert rep.count["codes_bit_exact"] == 5 * len(stack.layers_py) + 1
+    del stack
+    torch.cuda.empty_cache()

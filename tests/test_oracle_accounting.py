@@ -74,3 +74,24 @@ def test_config4_bytes():
 def test_config2_bytes():
     assert B.config_bytes(1) == 150_405_120
     assert B.config_bytes(2) == 203_489_280
+
+
+def test_mixed_checkpoint_composition_matches_pages():
+    """The mixed-checkpoint workload (FP8 mixers everywhere, NVFP4 MLPs in
+    layers 0-55, FP8 MLPs in 56-63, linear-attention projections
+    14336x5120 / 5120x8192): its layers come within 0.5 % of the pages'
+    17.83 GB, its MLPs are 59 % of them, and the step is 19.05 GB."""
+    from bit_weight_streaming_gb300 import workloads as W
+    fmt = W.mixed_fmt()
+    size = {1: B.nvfp4_bytes, 3: B.fp8_rowwise_bytes}
+    layers = mlp = 0
+    for i in range(64):
+        mixer_in, mixer_out, mlps = W.dense_layer_shapes(i, gdn=W.MIXED_GDN)
+        mix = sum(size[fmt(i, "mixer")](*s) for s in mixer_in + [mixer_out])
+        m = sum(size[fmt(i, "mlp")](*s) for s in mlps.values())
+        layers += mix + m
+        mlp += m
+    assert abs(layers / 1e9 - G["stack_gb"]["value"]) / G["stack_gb"]["value"] < 5e-3
+    assert round(mlp / layers, 2) == G["mlp_share_of_layer_bytes"]["value"]
+    V, d = G["head_shape"]["value"]
+    assert round((layers + B.fp8_rowwise_bytes(V, d)) / 1e9, 2) == 19.05
