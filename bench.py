@@ -228,55 +228,95 @@ def time_steps(fn, steps, warmup, stream):
 
 
 # DRAM bytes (read + write) per algorithmic byte of the one-token NVFP4
-# product kernel, from one ncu capture of its counters on four of the step's
-# matrix shapes.
-TRAFFIC_RATIO = 1.033
+# product kernel in its current form, from one ncu capture of its counters
+# (None until a capture of this kernel exists: the traffic is then reported
+# as null).
+TRAFFIC_PER_BYTE = None
+TRAFFIC_BASIS = None
+
+
+def product_groups(stack):
+    """The step's NVFP4 products by type: (name, [(matrix, input width)])."""
+    g = {"mixer-in": [], "mixer-out": [], "gate/up": [], "down": []}
+    for L in stack.layers_py:
+        for m in L.get("mixer_in", []):
+            g["mixer-in"].append(m)
+        if "mixer_out" in L:
+            g["mixer-out"].append(L["mixer_out"])
+        for name in ("gate", "up"):
+            if name in L:
+                g["gate/up"].append(L[name])
+        if "down" in L:
+            g["down"].append(L["down"])
+    return [(k, [m for m in v if m.fmt == 1]) for k, v in g.items()]
 
 
 def time_dominant_kernel(stack, stream, reps=3):
-    """Average duration of the NVFP4 product kernel alone, on the stack's own
-    matrices: the activations of each input width are prepared once
-    (bws_nvfp4_prepare, outside the timed launches), then every MLP and
-    mixer matrix runs bws_nvfp4_gemv_prepared once per rep, rotating through
-    all of them (15 GB) so that every launch reads cold weights. CUDA events
-    on the launching stream around each product launch."""
+    """The NVFP4 product kernel as it runs inside the step: each type of the
+    step's products (mixer inputs, mixer outputs, gate and up, down) is
+    captured as one CUDA graph of back-to-back launches over all of the
+    stack's matrices of that type (bws_nvfp4_gemv_prepared, chained with
+    programmatic dependent launch as in the step; every launch reads cold
+    weights, the whole set being far larger than L2), on activations
+    prepared once per input width. CUDA events on the launching stream
+    around `reps` replays. Returns {type: (launches, bytes, seconds per
+    replay)}."""
     import torch
     import bit_weight_streaming_gb300 as bws
-    mats = []
-    for L in stack.layers_py:
-        for m in [L.get("gate"), L.get("up"), L.get("down")] + list(L.get("mixer_in", [])):
-            if m is not None and m.fmt == 1:
-                mats.append(m)
-    d_out_max = {}
-    for m in mats:
-        d_out_max[m.d_in] = max(d_out_max.get(m.d_in, 0), m.d_out)
-    ys = {m.d_out: torch.empty((1, m.d_out), dtype=torch.bfloat16, device=stack.device) for m in mats}
-    wss = {}
-    with torch.cuda.stream(stream):
-        for d_in, dmax in d_out_max.items():
-            wss[d_in] = bws.Workspace(stack.device)
-            x = torch.randn((1, d_in), device=stack.device).to(torch.bfloat16)
-            bws.nvfp4_prepare(x, dmax, wss[d_in])
-
-        def run(m):
-            bws.nvfp4_gemv_prepared(m.codes, m.scales, m.scale32, 1, m.d_in, wss[m.d_in], y=ys[m.d_out])
-
-        for m in mats[:8]:   # warm-up
-            run(m)
+    dev = stack.device
+    out = {}
+    for name, mats in product_groups(stack):
+        if not mats:
+            continue
+        d_in = mats[0].d_in
+        assert all(m.d_in == d_in for m in mats)
+        ws = bws.Workspace(dev)
+        ys = {m.d_out: torch.empty((stack.N, m.d_out), dtype=torch.bfloat16, device=dev) for m in mats}
+        x = torch.randn((stack.N, d_in), device=dev).to(torch.bfloat16)
+        with torch.cuda.stream(stream):
+            bws.nvfp4_prepare(x, max(m.d_out for m in mats), ws)
+            for m in mats[:4]:   # warm-up outside the graph (tensor-map encoder, attributes)
+                bws.nvfp4_gemv_prepared(m.codes, m.scales, m.scale32, stack.N, d_in, ws, y=ys[m.d_out])
         stream.synchronize()
-        events = []
-        for _ in range(reps):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
             for m in mats:
-                a = torch.cuda.Event(enable_timing=True)
-                b = torch.cuda.Event(enable_timing=True)
-                a.record(stream)
-                run(m)
-                b.record(stream)
-                events.append((m.nbytes(), a, b))
-        stream.synchronize()
-    nbytes = sum(n for n, _, _ in events)
-    secs = sum(a.elapsed_time(b) for _, a, b in events) / 1e3
-    return nbytes / len(events), secs / len(events), len(events)
+                bws.nvfp4_gemv_prepared(m.codes, m.scales, m.scale32, stack.N, d_in, ws, y=ys[m.d_out])
+        with torch.cuda.stream(stream):
+            g.replay()
+            stream.synchronize()
+            a = torch.cuda.Event(enable_timing=True)
+            b = torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            for _ in range(reps):
+                g.replay()
+            b.record(stream)
+            b.synchronize()
+        out[name] = (len(mats), sum(m.nbytes() for m in mats), a.elapsed_time(b) / 1e3 / reps)
+        del g
+    return out
+
+
+def roofline_entry(dk, peak, peak_kind, ms_per_step):
+    launches = sum(v[0] for v in dk.values())
+    nbytes = sum(v[1] for v in dk.values())
+    secs = sum(v[2] for v in dk.values())
+    achieved = nbytes / secs / 1e9
+    per_launch = nbytes / launches
+    return {
+        "bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+        "frac": round(achieved / peak, 4),
+        "traffic": round(TRAFFIC_PER_BYTE * per_launch) if TRAFFIC_PER_BYTE else None,
+        "traffic_basis": TRAFFIC_BASIS,
+        "kernel": "NVFP4 weight-stream product kernel (gemv_tma_kernel), the step's products launched back to back "
+                  "in CUDA graphs by type, activations prepared beforehand",
+        "launches_timed": launches, "bytes_per_launch": round(per_launch), "peak_kind": peak_kind,
+        "by_type": {k: {"launches": v[0], "us_per_launch": round(v[2] / v[0] * 1e6, 2),
+                        "GBs": round(v[1] / v[2] / 1e9, 1), "frac": round(v[1] / v[2] / 1e9 / peak, 4)}
+                    for k, v in dk.items()},
+        "product_ms_per_step": round(secs * 1e3, 4),
+        "product_ms_within_step": bool(secs * 1e3 <= ms_per_step),
+    }
 
 
 def run_gpu(args):
@@ -321,18 +361,29 @@ def run_gpu(args):
     value, t_max = aggregate([r[0] for r in per_rank], [r[1] for r in per_rank])
     value /= 1e9
 
-    # end to end through the public API, host buffers: H2D x0, step, D2H logits
+    # end to end through the public API, host buffers: H2D x0, the greedy
+    # step (the next token chosen inside the output layer), D2H the token ids
     x_host = x1.cpu().pin_memory()
-    out_host = torch.empty_like(logits1, device="cpu").pin_memory()
     x_dev = torch.empty_like(x1)
+    tok_dev = torch.empty(1, dtype=torch.int32, device=dev)
+    tok_host = torch.empty(1, dtype=torch.int32).pin_memory()
 
     def step_e2e():
+        x_dev.copy_(x_host, non_blocking=True)
+        stack1.step_greedy(x_dev, tokens=tok_dev)
+        tok_host.copy_(tok_dev, non_blocking=True)
+
+    # the same with the whole logits row brought back instead
+    out_host = torch.empty_like(logits1, device="cpu").pin_memory()
+
+    def step_e2e_logits():
         x_dev.copy_(x_host, non_blocking=True)
         stack1.step(x_dev, logits1)
         out_host.copy_(logits1, non_blocking=True)
 
     with torch.cuda.stream(stream):
         t_e2e = time_steps(step_e2e, args.steps, args.warmup, stream)
+        t_e2e_lg = time_steps(step_e2e_logits, args.steps, args.warmup, stream)
     per_rank_e2e = all_gather_floats([nbytes, t_e2e], world)
     e2e_val, _ = aggregate([r[0] for r in per_rank_e2e], [r[1] for r in per_rank_e2e])
 
@@ -343,14 +394,30 @@ def run_gpu(args):
         logits8 = torch.empty((8, stack1.head.d_out), dtype=torch.float32, device=dev)
         t_step8 = time_steps(lambda: stack8.step(x8, logits8), args.steps, args.warmup, stream)
 
-    # dominant kernel: the NVFP4 product
-    with torch.cuda.stream(stream):
-        dk_bytes, dk_secs, dk_n = time_dominant_kernel(stack1, stream)
+    # dominant kernel: the NVFP4 product, by product type, as in the step
     peak, peak_kind = peaks()
+    with torch.cuda.stream(stream):
+        dk1 = time_dominant_kernel(stack1, stream)
+        dk8 = time_dominant_kernel(stack8, stream)
+    del stack8
+
+    # output layers with the greedy choice fused (the full head and the
+    # reduced-vocabulary draft head of 100,032 rows), no logits stored
+    heads = {}
+    with torch.cuda.stream(stream):
+        for V, hm in ((stack1.head.d_out, stack1.head),
+                      (100032, W.make_matrix(3, (100032, stack1.hidden), args.seed, 100003, device=dev))):
+            hws = bws.Workspace(dev)
+            t = time_steps(lambda: bws.fp8_lmhead_argmax(hm.codes, hm.scale32, x1, ws=hws), args.steps, args.warmup,
+                           stream)
+            heads[str(V)] = {"us_per_call": round(t * 1e6, 1), "GBs": round(hm.nbytes() / t / 1e9, 1),
+                             "frac_of_hbm_peak": round(hm.nbytes() / t / 1e9 / peak, 4),
+                             "weight_bytes": hm.nbytes(), "note": "activation prep + product with fused argmax, N=1"}
+
+    mixed = run_mixed(args, dev, stream, peak)
 
     moe = None
     if not args.no_moe:
-        del stack8
         moe = run_moe(args, dev, stream)
 
     cpu = cpu_baseline(host_copy(stack1)) if rank == 0 else None
@@ -373,16 +440,16 @@ def run_gpu(args):
             "n8": {"value": round(nbytes / t_step8 / 1e9, 2), "unit": UNIT, "us_per_step": round(t_step8 * 1e6, 1),
                    "tokens_per_s": round(8 / t_step8, 1), "frac_of_hbm_peak": round(nbytes / t_step8 / 1e9 / peak, 4)},
             "moe": moe,
+            "mixed": mixed,
+            "heads_argmax": heads,
             "e2e": {"value": round(e2e_val / 1e9, 2), "unit": UNIT, "h2d_bytes_per_step": x_host.numel() * 2,
-                    "d2h_bytes_per_step": out_host.numel() * 4},
+                    "d2h_bytes_per_step": tok_host.numel() * 4,
+                    "path": "H2D x0, bws_decode_step_greedy (next token chosen in the output layer), D2H the token id",
+                    "with_logits": {"value": round(nbytes / t_e2e_lg / 1e9, 2), "unit": UNIT,
+                                    "d2h_bytes_per_step": out_host.numel() * 4}},
             "gpu_launches": stack1.kernel_count * args.steps,
-            "roofline": {"bound": "hbm", "achieved": round(dk_bytes / dk_secs / 1e9, 1), "peak": peak,
-                         "unit": "GB/s", "frac": round(dk_bytes / dk_secs / 1e9 / peak, 4),
-                         "traffic": round(TRAFFIC_RATIO * dk_bytes),
-                         "traffic_basis": "ncu dram__bytes_read.sum + dram__bytes_write.sum per algorithmic byte from one "
-                                          "capture on four of the step's shapes, times the algorithmic bytes per launch",
-                         "kernel": "NVFP4 weight-stream product kernel (gemv_tma_kernel, one token), activations prepared beforehand",
-                         "launches_timed": dk_n, "bytes_per_launch": round(dk_bytes), "peak_kind": peak_kind},
+            "roofline": roofline_entry(dk1, peak, peak_kind, t_max * 1e3),
+            "roofline_n8": roofline_entry(dk8, peak, peak_kind, t_step8 * 1e3),
             "clocks": clk,
             "cpu_baseline": cpu,
         }
@@ -390,6 +457,34 @@ def run_gpu(args):
     if world > 1:
         dist.barrier()
         dist.destroy_process_group()
+
+
+def run_mixed(args, dev, stream, peak, tokens=(1, 8)):
+    """The pages' mixed checkpoint: FP8 mixer projections in every layer,
+    NVFP4 MLPs in layers 0-55, FP8 MLPs in 56-63, FP8 output layer."""
+    import torch
+    from bit_weight_streaming_gb300 import workloads as W
+    import bit_weight_streaming_gb300 as bws
+    import synth
+    with torch.cuda.stream(stream):
+        base = W.dense_27b_mixed(1, seed=args.seed, device=dev)
+    stream.synchronize()
+    nbytes = base.weight_bytes()
+    out = {"workload": "27B-shape mixed checkpoint: FP8 attention and linear-attention projections (14336x5120, "
+                       "5120x8192), NVFP4 MLPs in layers 0-55, FP8 MLPs in 56-63, FP8 248320x5120 output layer",
+           "weight_bytes_per_step": nbytes}
+    for N in tokens:
+        S = base if N == 1 else bws.stack.DecodeStack(base.hidden, base.layers_py, base.head, N, device=dev)
+        x = synth.activation_bf16(N, base.hidden, seed=args.seed, device=dev)
+        lg = torch.empty((N, base.head.d_out), dtype=torch.float32, device=dev)
+        with torch.cuda.stream(stream):
+            t = time_steps(lambda: S.step(x, lg), args.steps, args.warmup, stream)
+        out[f"n{N}"] = {"value": round(nbytes / t / 1e9, 2), "unit": UNIT, "us_per_step": round(t * 1e6, 1),
+                        "frac_of_hbm_peak": round(nbytes / t / 1e9 / peak, 4)}
+        del S
+    del base
+    torch.cuda.empty_cache()
+    return out
 
 
 def run_moe(args, dev, stream, tokens=(1, 4)):
