@@ -227,35 +227,51 @@ def time_steps(fn, steps, warmup, stream):
     return s.elapsed_time(e) / 1e3 / steps
 
 
-# DRAM bytes (read + write) per algorithmic byte of the one-token NVFP4
-# product kernel in its current form, from one ncu capture of its counters
-# (None until a capture of this kernel exists: the traffic is then reported
-# as null).
-TRAFFIC_PER_BYTE = None
-TRAFFIC_BASIS = None
+# DRAM read + write bytes per algorithmic byte of the NVFP4 product kernel,
+# from ncu's dram__bytes_read.sum + dram__bytes_write.sum over two launches
+# of each of the step's five product shapes (46336x5120, 14336x5120,
+# 34816x5120, 5120x17408, 5120x6144; one token), weighted by the step's
+# launches per shape. Taken on the current kernel; reset to None when the
+# kernel changes.
+TRAFFIC_PER_BYTE = 1.0339
+TRAFFIC_BASIS = ("ncu dram__bytes_read.sum + dram__bytes_write.sum of the product kernel on the step's five shapes "
+                 "(two launches each, one token), weighted by launches per shape: 1.034 x algorithmic bytes")
 
 
 def product_groups(stack):
-    """The step's NVFP4 products by type: (name, [(matrix, input width)])."""
+    """The step's NVFP4 products by type, one entry per launch of the step:
+    (name, [matrix lists]). The step runs a layer's mixer-input matrices
+    (query, key and value of a full-attention layer) as one product and its
+    gate and up matrices as one SwiGLU product; each list is one such launch."""
     g = {"mixer-in": [], "mixer-out": [], "gate/up": [], "down": []}
     for L in stack.layers_py:
-        for m in L.get("mixer_in", []):
-            g["mixer-in"].append(m)
+        if L.get("mixer_in"):
+            g["mixer-in"].append(list(L["mixer_in"]))
         if "mixer_out" in L:
-            g["mixer-out"].append(L["mixer_out"])
-        for name in ("gate", "up"):
-            if name in L:
-                g["gate/up"].append(L[name])
+            g["mixer-out"].append([L["mixer_out"]])
+        if "gate" in L:
+            g["gate/up"].append([L["gate"], L["up"]])
         if "down" in L:
-            g["down"].append(L["down"])
-    return [(k, [m for m in v if m.fmt == 1]) for k, v in g.items()]
+            g["down"].append([L["down"]])
+    return [(k, [ms for ms in v if all(m.fmt == 1 for m in ms)]) for k, v in g.items()]
+
+
+def launch_matrix(ms):
+    """One launch's matrices as one NVFP4 matrix: rows concatenated (codes
+    and block scales), so that a single standalone product streams the same
+    bytes in the same launch as the step's product over those matrices."""
+    import torch
+    from bit_weight_streaming_gb300.stack import QMatrix
+    if len(ms) == 1:
+        return ms[0]
+    return QMatrix(ms[0].fmt, torch.cat([m.codes for m in ms]), torch.cat([m.scales for m in ms]), ms[0].scale32)
 
 
 def time_dominant_kernel(stack, stream, reps=3):
     """The NVFP4 product kernel as it runs inside the step: each type of the
     step's products (mixer inputs, mixer outputs, gate and up, down) is
-    captured as one CUDA graph of back-to-back launches over all of the
-    stack's matrices of that type (bws_nvfp4_gemv_prepared, chained with
+    captured as one CUDA graph of back-to-back launches, one per product of
+    that type in the step (bws_nvfp4_gemv_prepared, chained with
     programmatic dependent launch as in the step; every launch reads cold
     weights, the whole set being far larger than L2), on activations
     prepared once per input width. CUDA events on the launching stream
@@ -265,9 +281,10 @@ def time_dominant_kernel(stack, stream, reps=3):
     import bit_weight_streaming_gb300 as bws
     dev = stack.device
     out = {}
-    for name, mats in product_groups(stack):
-        if not mats:
+    for name, launches in product_groups(stack):
+        if not launches:
             continue
+        mats = [launch_matrix(ms) for ms in launches]
         d_in = mats[0].d_in
         assert all(m.d_in == d_in for m in mats)
         ws = bws.Workspace(dev)
@@ -293,7 +310,7 @@ def time_dominant_kernel(stack, stream, reps=3):
             b.record(stream)
             b.synchronize()
         out[name] = (len(mats), sum(m.nbytes() for m in mats), a.elapsed_time(b) / 1e3 / reps)
-        del g
+        del g, mats
     return out
 
 
@@ -308,8 +325,9 @@ def roofline_entry(dk, peak, peak_kind, ms_per_step):
         "frac": round(achieved / peak, 4),
         "traffic": round(TRAFFIC_PER_BYTE * per_launch) if TRAFFIC_PER_BYTE else None,
         "traffic_basis": TRAFFIC_BASIS,
-        "kernel": "NVFP4 weight-stream product kernel (gemv_tma_kernel), the step's products launched back to back "
-                  "in CUDA graphs by type, activations prepared beforehand",
+        "kernel": "NVFP4 weight-stream product kernel (gemv_tma_kernel): one launch per product of the step "
+                  "(a layer's q, k, v as one; its gate and up as one), launched back to back in CUDA graphs by "
+                  "type, activations prepared beforehand",
         "launches_timed": launches, "bytes_per_launch": round(per_launch), "peak_kind": peak_kind,
         "by_type": {k: {"launches": v[0], "us_per_launch": round(v[2] / v[0] * 1e6, 2),
                         "GBs": round(v[1] / v[2] / 1e9, 1), "frac": round(v[1] / v[2] / 1e9 / peak, 4)}
@@ -416,9 +434,10 @@ def run_gpu(args):
 
     mixed = run_mixed(args, dev, stream, peak)
 
-    moe = None
+    moe = moe_routed = None
     if not args.no_moe:
         moe = run_moe(args, dev, stream)
+        moe_routed = run_moe(args, dev, stream, router=True)
 
     cpu = cpu_baseline(host_copy(stack1)) if rank == 0 else None
 
@@ -440,6 +459,7 @@ def run_gpu(args):
             "n8": {"value": round(nbytes / t_step8 / 1e9, 2), "unit": UNIT, "us_per_step": round(t_step8 * 1e6, 1),
                    "tokens_per_s": round(8 / t_step8, 1), "frac_of_hbm_peak": round(nbytes / t_step8 / 1e9 / peak, 4)},
             "moe": moe,
+            "moe_routed": moe_routed,
             "mixed": mixed,
             "heads_argmax": heads,
             "e2e": {"value": round(e2e_val / 1e9, 2), "unit": UNIT, "h2d_bytes_per_step": x_host.numel() * 2,
@@ -487,7 +507,11 @@ def run_mixed(args, dev, stream, peak, tokens=(1, 8)):
     return out
 
 
-def run_moe(args, dev, stream, tokens=(1, 4)):
+def run_moe(args, dev, stream, tokens=(1, 4), router=False):
+    """The Ling-shape MoE step at each N of tokens: with seeded expert ids
+    (router=False), or routed by a BF16 512x2560 router per MoE layer inside
+    the step (router=True: the distinct experts are those the step chose,
+    the routers' bytes count)."""
     import torch
     from bit_weight_streaming_gb300 import workloads as W
     import synth
@@ -495,11 +519,9 @@ def run_moe(args, dev, stream, tokens=(1, 4)):
     for N in tokens:
         t0 = time.time()
         with torch.cuda.stream(stream):
-            st = W.moe_ling(N, seed=args.seed, device=dev)
+            st = W.moe_ling(N, seed=args.seed, device=dev, router=router)
         stream.synchronize()
         tb = time.time() - t0
-        distinct = W.distinct_per_moe_layer(st)
-        nbytes = st.weight_bytes(distinct)
         x = synth.activation_bf16(N, st.hidden, seed=args.seed, device=dev)
         lg = torch.empty((N, st.head.d_out), dtype=torch.float32, device=dev)
 
@@ -508,13 +530,17 @@ def run_moe(args, dev, stream, tokens=(1, 4)):
 
         with torch.cuda.stream(stream):
             t = time_steps(step, args.steps, args.warmup, stream)
+        distinct = W.distinct_per_moe_layer(st)   # routed: the ids the timed steps chose
+        nbytes = st.weight_bytes(distinct)
         out[f"n{N}"] = {"value": round(nbytes / t / 1e9, 2), "unit": UNIT, "us_per_step": round(t * 1e6, 1),
                         "weight_bytes_per_step": nbytes, "distinct_experts_mean": round(sum(distinct) / len(distinct), 2),
                         "build_s": round(tb, 1)}
         del st
         torch.cuda.empty_cache()
     out["workload"] = ("Ling-shape MoE decode step: 2 dense MXFP4 MLP layers (6912) + 40 MoE layers (512 experts, "
-                       "inter 768, top-8 + 1 shared, MXFP4) + FP8 157184x2560 output layer")
+                       "inter 768, top-8 + 1 shared, MXFP4) + FP8 157184x2560 output layer"
+                       + ("; each MoE layer routed in the step by a BF16 512x2560 router (top-8 of its logits, "
+                          "softmax weights)" if router else "; seeded expert ids and combine weights"))
     return out
 
 
@@ -608,7 +634,7 @@ def run_moe_only(args):
     g.build()
     dev = torch.device("cuda", 0)
     stream = torch.cuda.Stream(dev)
-    out = run_moe(args, dev, stream, tokens=(args.tokens,))
+    out = run_moe(args, dev, stream, tokens=(args.tokens,), router=args.router)
     print(json.dumps({"moe_only": out}), flush=True)
 
 
@@ -623,6 +649,7 @@ def main(argv=None):
     ap.add_argument("--product", default=None, help="ROWSxCOLS: time one NVFP4 product only (profiling)")
     ap.add_argument("--moe-only", action="store_true", help="time the MoE step alone at --tokens N (profiling)")
     ap.add_argument("--tokens", type=int, default=1)
+    ap.add_argument("--router", action="store_true", help="--moe-only: MoE layers routed inside the step")
     ap.add_argument("--copies", type=int, default=4, help="--product: distinct weight copies to rotate")
     args = ap.parse_args(argv)
     if args.warmup < 3:

@@ -17,6 +17,7 @@ from .api import (  # noqa: F401
     nvfp4_gate_up_silu,
     fp8_lmhead_gemv,
     fp8_lmhead_argmax,
+    moe_router_topk,
     status_word,
     hbm_read_probe,
     l2_flush,

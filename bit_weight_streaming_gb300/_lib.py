@@ -27,6 +27,8 @@ SIGNATURES = {
     "bws_fp8_lmhead_gemv": (I, [P, P, P, I, I, I, P, P, Z, P]),
     "bws_fp8_lmhead_argmax": (I, [P, P, P, I, I, I, P, P, P, P, Z, P]),
     "bws_mxfp4_moe_workspace_size": (Z, [P, I, I]),
+    "bws_moe_router_workspace_size": (Z, [I, I]),
+    "bws_moe_router_topk": (I, [P, P, I, I, I, I, P, P, P, P, Z, P]),
     "bws_mxfp4_moe_gemv": (I, [P, P, P, I, I, P, P, P, Z, P]),
     "bws_mxfp4_moe_inspect": (I, [P, P, I, I, P, P, P, P, P]),
     "bws_decode_step_workspace_size": (Z, [P]),

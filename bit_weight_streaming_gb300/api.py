@@ -167,6 +167,26 @@ def fp8_lmhead_argmax(W, row_scale, x, logits=False, row_token=None, ws=None):
     return (tok, logits) if logits is not False else tok
 
 
+def moe_router_topk(W_router, x, topk, logits=False, ws=None):
+    """MoE routing on the device: the top-k experts of each token by the
+    logits z = W_router x (BF16 operands, FP32 sums; lower id first on equal
+    logits) and their softmax-renormalised weights. Returns (ids int32 [N, k],
+    route_w fp32 [N, k]), largest logit first, plus the fp32 [N, E] logits
+    when logits=True (a tensor may be passed to store them into)."""
+    _need_cuda(W_router, x)
+    N, d = x.shape
+    E = W_router.shape[0]
+    if logits is True:
+        logits = torch.empty((N, E), dtype=torch.float32, device=x.device)
+    ids = torch.empty((N, topk), dtype=torch.int32, device=x.device)
+    w = torch.empty((N, topk), dtype=torch.float32, device=x.device)
+    buf = _ws(ws, lib().bws_moe_router_workspace_size(N, E), x.device)
+    check(lib().bws_moe_router_topk(_ptr(W_router), _ptr(x), N, E, d, topk,
+                                    _ptr(logits) if logits is not False else None, _ptr(ids), _ptr(w),
+                                    _ptr(buf), buf.numel(), _stream(x.device)), "bws_moe_router_topk")
+    return (ids, w, logits) if logits is not False else (ids, w)
+
+
 def status_word(ws):
     """OR of the status bits set by the last product call that used ws."""
     import ctypes

@@ -130,6 +130,27 @@ struct MoeRoute {
                            // then runs without waiting for the kernels before (it reads only
                            // ids and weights), so the experts' kernels can read the table early
 };
+// MoE router (router.cu): z = W x for the E routed experts, then each
+// token's top-k experts (largest logits, lower id first on equal logits) and
+// their softmax-renormalised combine weights.
+struct RouterParams {
+  const uint16_t* W;       // bf16 [E][d], 16-byte aligned
+  const uint16_t* x;       // bf16 [N][d], 16-byte aligned
+  int N, E, d, topk;       // d % 8 == 0
+  float* z;                // out [N][E] FP32 logits
+  uint32_t* counter;       // zero on entry; counts the CTAs that finished
+  int32_t* ids;            // out [N][topk], largest logit first
+  float* route_w;          // out [N][topk]
+  int has_route;           // also write the slot table of route (ids / route_w = the outputs above)
+  MoeRoute route;
+};
+constexpr int kRouterMaxD = 8192;
+constexpr int kRouterMaxExperts = 2048;
+constexpr int kRouterSmemMax = 131072;   // shared memory for either phase at the limits above
+size_t router_smem_bytes(int N, int E, int d);
+int router_ctas(int E);
+cudaError_t launch_router(const RouterParams& p, cudaStream_t st, bool pdl);
+
 // A stream-K split of n_units units over n_ctas CTAs into contiguous ranges:
 // CTA c takes units [splitk_begin(c), splitk_begin(c + 1)). The CTAs from lf
 // on get num/den of the others' share (uniform: lf = n_ctas, num = den = 1).

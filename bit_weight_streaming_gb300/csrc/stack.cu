@@ -26,6 +26,11 @@ struct bws_stack_plan {
   // ready flag, cleared at the start of every step
   size_t off_routes, route_stride, off_ready;
   int n_moe;
+  // MoE layers with a router: the layer's normalised input (bf16 [N][hidden])
+  // and logits (fp32 [N][max_router_e]) of the layer being routed; one
+  // counter per MoE layer follows the ready flags
+  size_t off_rx, off_rz;
+  int max_router_e;
   GemvWorkspace xw, vw, hw;    // prep-block offsets (relative to their block)
   int max_u, max_dv, max_inter, max_tiles;
   int kernels;
@@ -83,6 +88,9 @@ struct Tap {
   }
   void copy(const void* src, size_t bytes) {
     void* d = take(bytes);
+    if (d && err == cudaSuccess) err = cudaMemcpyAsync(d, src, bytes, cudaMemcpyDeviceToDevice, st);
+  }
+  void copy_to(void* d, const void* src, size_t bytes) {
     if (d && err == cudaSuccess) err = cudaMemcpyAsync(d, src, bytes, cudaMemcpyDeviceToDevice, st);
   }
   // rows of row_bytes each, src_pitch bytes apart, packed
@@ -149,12 +157,15 @@ bool deposit_setup(const bws_matrix* mats, int nm, int epi, GemvParams& p, int n
 cudaError_t prep(const Ctx& c, int mode, const uint16_t* x, int ld, const uint16_t* x0, int d_in, size_t block,
                  const GemvWorkspace& L, uint32_t* zero_ptr, int zero_words, int interleave = 0,
                  const MoeStackView* comb = nullptr, const MoeRoute* route = nullptr,
-                 const PrepParams* fin = nullptr) {
+                 const PrepParams* fin = nullptr, uint16_t* xout = nullptr) {
   PrepParams q = {};
   if (fin != nullptr) q = *fin;   // the finishing fields
+  // xout: the BF16 row formed, written out (the router's input)
   // tap: an RMSNorm prep records the BF16 row it forms, then the residual it normalised
   const bool tap_norm = c.tap != nullptr && mode == kPrepRmsNorm;
-  if (tap_norm) q.tap_x = static_cast<uint16_t*>(c.tap->take(2 * (size_t)c.P->N * d_in));
+  const size_t xbytes = 2 * (size_t)c.P->N * d_in;
+  uint16_t* tap_rec = tap_norm ? static_cast<uint16_t*>(c.tap->take(xbytes)) : nullptr;
+  q.tap_x = xout != nullptr ? xout : tap_rec;
   q.mode = mode;
   q.x = x;
   q.ld = ld;
@@ -185,7 +196,10 @@ cudaError_t prep(const Ctx& c, int mode, const uint16_t* x, int ld, const uint16
     q.route = *route;
   }
   const cudaError_t e = launch_prep(q, c.st, true);
-  if (e == cudaSuccess && tap_norm) c.tap->copy(q.r, sizeof(float) * (size_t)c.P->N * d_in);
+  if (e == cudaSuccess && tap_norm) {
+    if (xout != nullptr) c.tap->copy_to(tap_rec, xout, xbytes);
+    c.tap->copy(q.r, sizeof(float) * (size_t)c.P->N * d_in);
+  }
   return e;
 }
 
@@ -258,7 +272,7 @@ int enqueue_step(const bws_stack_plan* P, const uint16_t* x0, float* logits, con
   const MoeStackView* pending = nullptr;
   int moe_buf = 0, moe_i = 0;
   if (P->n_moe > 0) {
-    const cudaError_t e0 = cudaMemsetAsync(c.w + P->off_ready, 0, sizeof(uint32_t) * (size_t)P->n_moe, st);
+    const cudaError_t e0 = cudaMemsetAsync(c.w + P->off_ready, 0, 2 * sizeof(uint32_t) * (size_t)P->n_moe, st);
     if (e0 != cudaSuccess) return cuda_status(e0, name);
   }
   // the last product's rows, when it deposited them for the next prep
@@ -333,10 +347,35 @@ int enqueue_step(const bws_stack_plan* P, const uint16_t* x0, float* logits, con
         v.route.slot_expert = reinterpret_cast<int*>(rt + 256);
         v.route.cw = reinterpret_cast<float*>(rt + 256 + align256(sizeof(int) * (size_t)v.route.max_slots));
         v.route.ready = reinterpret_cast<uint32_t*>(c.w + P->off_ready) + moe_i;
-        ++moe_i;
       }
-      BWS_TRY(prep(c, kPrepRmsNorm, nullptr, 0, init, H, P->off_xp, P->xw, v.counters, v.n_counters,
-                   moe_x_layout(&L.moe, P->N), pending, &v.route));
+      if (L.router == nullptr) {   // ids known before the layer: routed by an extra CTA of the prep
+        BWS_TRY(prep(c, kPrepRmsNorm, nullptr, 0, init, H, P->off_xp, P->xw, v.counters, v.n_counters,
+                     moe_x_layout(&L.moe, P->N), pending, &v.route));
+      } else {   // the router reads the prep's BF16 row, then writes ids, weights and the slot table
+        uint16_t* rx = reinterpret_cast<uint16_t*>(c.w + P->off_rx);
+        BWS_TRY(prep(c, kPrepRmsNorm, nullptr, 0, init, H, P->off_xp, P->xw, v.counters, v.n_counters,
+                     moe_x_layout(&L.moe, P->N), pending, nullptr, nullptr, rx));
+        RouterParams rp = {};
+        rp.W = L.router;
+        rp.x = rx;
+        rp.N = P->N;
+        rp.E = L.moe.n_experts;
+        rp.d = H;
+        rp.topk = L.topk;
+        rp.z = reinterpret_cast<float*>(c.w + P->off_rz);
+        rp.counter = reinterpret_cast<uint32_t*>(c.w + P->off_ready) + P->n_moe + moe_i;
+        rp.ids = const_cast<int32_t*>(L.ids);
+        rp.route_w = const_cast<float*>(L.route_w);
+        rp.has_route = 1;
+        rp.route = v.route;
+        BWS_TRY(launch_router(rp, st, true));
+        if (tap) {
+          tap->copy(rp.z, sizeof(float) * (size_t)P->N * rp.E);
+          tap->copy(L.ids, sizeof(int32_t) * (size_t)P->N * L.topk);
+          tap->copy(L.route_w, sizeof(float) * (size_t)P->N * L.topk);
+        }
+      }
+      ++moe_i;
       init = nullptr;
       const int rc = enqueue_moe_experts(&L.moe, P->N, L.topk, v.route.n_slots, v.route.slot_expert, xa,
                                          c.w + P->off_moe, st, name, v.route.ready);
@@ -391,6 +430,11 @@ size_t tap_walk_size(const bws_stack_plan* P, Tap* t) {
       const size_t ms = N * L.topk + (L.moe.shared_gate_up_codes != nullptr ? 1 : 0);
       t->take(2 * N * H);                            // m
       t->take(4 * N * H);                            // the r it normalised
+      if (L.router != nullptr) {
+        t->take(4 * N * (size_t)L.moe.n_experts);    // router logits
+        t->take(4 * N * (size_t)L.topk);             // chosen ids
+        t->take(4 * N * (size_t)L.topk);             // their weights
+      }
       t->take(sizeof(int));                          // live slots
       t->take(sizeof(int) * ms);                     // slot experts
       t->take(sizeof(float) * ms * N);               // combine weights
@@ -428,6 +472,7 @@ int bws_decode_step_plan_create(const bws_stack* S, int N, bws_stack_plan** plan
   P->kernels = 2;
   size_t moe_bytes = 0, route_bytes = 256;
   P->n_moe = 0;
+  P->max_router_e = 0;
   auto bad = [&](int code) {
     delete P;
     return code;
@@ -471,6 +516,16 @@ int bws_decode_step_plan_create(const bws_stack* S, int N, bws_stack_plan** plan
       if ((rc = check_moe_layer(&L.moe, N, L.topk, name))) return bad(rc);
       if (L.moe.hidden != H) return bad(fail(BWS_ERR_UNSUPPORTED_SHAPE, "%s: layer %d: MoE hidden != stack hidden", name, li));
       if (!L.ids || !L.route_w) return bad(fail(BWS_ERR_INVALID_ARG, "%s: layer %d: null routing", name, li));
+      if (L.router != nullptr) {
+        if (!aligned(L.router, 16) || !aligned(L.ids, 4) || !aligned(L.route_w, 4))
+          return bad(fail(BWS_ERR_MISALIGNED, "%s: layer %d: router 16-byte, ids and route_w 4-byte alignment needed",
+                          name, li));
+        if (L.moe.n_experts > kRouterMaxExperts || H % 8 || H > kRouterMaxD || L.topk > L.moe.n_experts)
+          return bad(fail(BWS_ERR_UNSUPPORTED_SHAPE, "%s: layer %d: router needs n_experts <= %d, hidden %% 8 == 0, "
+                          "hidden <= %d, topk <= n_experts", name, li, kRouterMaxExperts, kRouterMaxD));
+        P->max_router_e = L.moe.n_experts > P->max_router_e ? L.moe.n_experts : P->max_router_e;
+        ++P->kernels;
+      }
       const size_t b = moe_workspace_bytes(&L.moe, N, L.topk);
       moe_bytes = b > moe_bytes ? b : moe_bytes;
       const size_t slots = (size_t)N * L.topk + (L.moe.shared_gate_up_codes != nullptr ? 1 : 0);
@@ -501,7 +556,9 @@ int bws_decode_step_plan_create(const bws_stack* S, int N, bws_stack_plan** plan
   P->off_moe = o; o += align256(moe_bytes);
   P->route_stride = route_bytes;
   P->off_routes = o; o += route_bytes * (size_t)P->n_moe;
-  P->off_ready = o; o += align256(sizeof(uint32_t) * (size_t)(P->n_moe > 0 ? P->n_moe : 1));
+  P->off_ready = o; o += align256(2 * sizeof(uint32_t) * (size_t)(P->n_moe > 0 ? P->n_moe : 1));
+  P->off_rx = o; o += P->max_router_e > 0 ? align256(2 * (size_t)N * H) : 0;
+  P->off_rz = o; o += align256(sizeof(float) * (size_t)N * P->max_router_e);
   P->off_counters = o; o += align256(sizeof(uint32_t) * (size_t)P->max_tiles);
   P->off_partials = o; o += align256(sizeof(float) * kSlotFloats * ((size_t)P->max_tiles + gemv_max_warps()));
   P->total = o;

@@ -19,7 +19,8 @@ class Matrix(C.Structure):
 class Layer(C.Structure):
     _fields_ = [("kind", C.c_int), ("n_mixer_in", C.c_int), ("mixer_in", Matrix * 4),
                 ("mixer_out", Matrix), ("gate", Matrix), ("up", Matrix), ("down", Matrix),
-                ("moe", MoeLayer), ("ids", C.c_void_p), ("route_w", C.c_void_p), ("topk", C.c_int)]
+                ("moe", MoeLayer), ("ids", C.c_void_p), ("route_w", C.c_void_p), ("topk", C.c_int),
+                ("router", C.c_void_p)]
 
 
 class Stack(C.Structure):
@@ -50,7 +51,9 @@ class QMatrix:
 class DecodeStack:
     """Layers: dicts with kind 'mixer_mlp' (mixer_in: [QMatrix], mixer_out,
     gate, up, down), 'mlp' (gate, up, down) or 'moe' (moe: MoeWeights, ids,
-    route_w device tensors). head: QMatrix (FP8)."""
+    route_w device tensors [N][topk]; optional 'router': bf16 [n_experts]
+    [hidden], with which the step routes the layer itself and writes the
+    chosen ids and weights into ids / route_w). head: QMatrix (FP8)."""
 
     def __init__(self, hidden, layers, head, N, rms_eps=1e-6, device="cuda"):
         self.hidden, self.layers_py, self.head, self.N = hidden, layers, head, N
@@ -70,6 +73,10 @@ class DecodeStack:
                 s.kind = LAYER_MOE
                 s.moe = L["moe"].descriptor()
                 s.ids, s.route_w, s.topk = _ptr(L["ids"]), _ptr(L["route_w"]), L["ids"].shape[1]
+                if L.get("router") is not None:
+                    r = L["router"]
+                    assert r.dtype == torch.bfloat16 and r.is_contiguous() and tuple(r.shape) == (L["moe"].n_experts, hidden)
+                    s.router = _ptr(r)
             else:
                 raise BwsError(f"unknown layer kind {L['kind']}")
             if L["kind"] in ("mixer_mlp", "mlp"):
@@ -146,16 +153,21 @@ class DecodeStack:
             if L["kind"] == "moe":
                 w = L["moe"]
                 S = N * L["ids"].shape[1] + (1 if w.shared is not None else 0)
-                out += [("m", torch.bfloat16, (N, H)), ("r", torch.float32, (N, H)),
-                        ("n_slots", torch.int32, (1,)), ("slot_expert", torch.int32, (S,)),
+                out += [("m", torch.bfloat16, (N, H)), ("r", torch.float32, (N, H))]
+                if L.get("router") is not None:
+                    k = L["ids"].shape[1]
+                    out += [("z", torch.float32, (N, w.n_experts)), ("ids", torch.int32, (N, k)),
+                            ("route_w", torch.float32, (N, k))]
+                out += [("n_slots", torch.int32, (1,)), ("slot_expert", torch.int32, (S,)),
                         ("cw", torch.float32, (S, N)), ("h_slots", torch.bfloat16, (S, N, w.inter)),
                         ("y_slots", torch.float32, (S, N, H))]
         out += [("x_head", torch.bfloat16, (N, H)), ("r", torch.float32, (N, H))]
         return out
 
     def weight_bytes(self, distinct_experts=None):
-        """Algorithmic bytes of one step (codes + block/row scales). For MoE
-        layers pass the number of distinct routed experts per MoE layer."""
+        """Algorithmic bytes of one step (codes + block/row scales, and the
+        BF16 routers). For MoE layers pass the number of distinct routed
+        experts per MoE layer."""
         b = self.head.nbytes()
         k = 0
         for L in self.layers_py:
@@ -168,6 +180,8 @@ class DecodeStack:
                 per = (w.gu_c[0].numel() + w.gu_s[0].numel() + w.dn_c[0].numel() + w.dn_s[0].numel())
                 n = distinct_experts[k] + (1 if w.shared is not None else 0)
                 b += n * per
+                if L.get("router") is not None:
+                    b += L["router"].numel() * 2
                 k += 1
         return b
 

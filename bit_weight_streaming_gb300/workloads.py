@@ -135,8 +135,17 @@ def moe_weights(n_experts, hidden, inter, seed, layer, with_shared=True, quant=N
     return api.MoeWeights(gu_c[:n_experts], gu_s[:n_experts], dn_c[:n_experts], dn_s[:n_experts], shared)
 
 
+def router_weights(n_experts, hidden, seed, layer, device="cuda"):
+    """A BF16 [n_experts][hidden] router: seeded N(0, 0.02) FP32 rounded to
+    BF16 (nearest, ties to even)."""
+    return synth.weight_fp32((n_experts, hidden), seed=seed, index=3000000 + layer, device=device).to(torch.bfloat16)
+
+
 def moe_stack_layers(N, seed=0, n_dense=2, n_moe=40, hidden=2560, inter=768, n_experts=512, topk=8,
-                     dense_inter=6912, quant=None, device="cuda"):
+                     dense_inter=6912, quant=None, device="cuda", router=False):
+    """router=False: seeded expert ids and combine weights (inputs); True: a
+    BF16 router per MoE layer, the step choosing ids and weights itself and
+    writing them into the layer's ids / route_w tensors."""
     layers = []
     for i in range(n_dense):
         L = {"kind": "mlp"}
@@ -146,19 +155,29 @@ def moe_stack_layers(N, seed=0, n_dense=2, n_moe=40, hidden=2560, inter=768, n_e
         layers.append(L)
     for j in range(n_moe):
         li = n_dense + j
+        w = moe_weights(n_experts, hidden, inter, seed, li, True, quant, device)
+        if router:
+            layers.append({"kind": "moe", "moe": w, "router": router_weights(n_experts, hidden, seed, li, device),
+                           "ids": torch.zeros((N, topk), dtype=torch.int32, device=device),
+                           "route_w": torch.zeros((N, topk), dtype=torch.float32, device=device)})
+            continue
         ids = synth.expert_ids(N, topk, n_experts, seed=seed, layer=li)
         rw = synth.route_weights(N, topk, seed=seed, layer=li)
-        layers.append({"kind": "moe", "moe": moe_weights(n_experts, hidden, inter, seed, li, True, quant, device),
-                       "ids": ids.to(device), "route_w": rw.to(device), "ids_host": ids, "route_w_host": rw})
+        layers.append({"kind": "moe", "moe": w, "ids": ids.to(device), "route_w": rw.to(device), "ids_host": ids,
+                       "route_w_host": rw})
     return layers
 
 
 def moe_ling(N, seed=0, n_dense=2, n_moe=40, hidden=2560, inter=768, n_experts=512, topk=8, dense_inter=6912,
-             vocab=157184, quant=None, device="cuda"):
-    layers = moe_stack_layers(N, seed, n_dense, n_moe, hidden, inter, n_experts, topk, dense_inter, quant, device)
+             vocab=157184, quant=None, device="cuda", router=False):
+    layers = moe_stack_layers(N, seed, n_dense, n_moe, hidden, inter, n_experts, topk, dense_inter, quant, device,
+                              router)
     head = make_matrix(FMT_FP8_ROW, (vocab, hidden), seed, 100001, quant, device)
     return DecodeStack(hidden, layers, head, N, device=device)
 
 
 def distinct_per_moe_layer(stack):
-    return [len(set(L["ids_host"].reshape(-1).tolist())) for L in stack.layers_py if L["kind"] == "moe"]
+    """Distinct routed experts per MoE layer (a routed stack: those of the
+    ids its last step wrote)."""
+    return [len(set((L["ids_host"] if "ids_host" in L else L["ids"].cpu()).reshape(-1).tolist()))
+            for L in stack.layers_py if L["kind"] == "moe"]

@@ -253,6 +253,27 @@ int bws_mxfp4_moe_gemv(const bws_moe_layer* L, const int32_t* ids,
                        uint16_t* y, void* workspace, size_t workspace_bytes,
                        void* stream);
 
+/* MoE router ([LingMoE] section 3: each MoE layer sends every token to 8 of
+ * its 512 routed experts, plus one shared expert). The pages name the routing
+ * but not its arithmetic; this library reads it as
+ *   z[n][e] = sum_j W[e][j] * x[n][j]   (BF16 operands, FP32 accumulation)
+ *   ids[n][0..topk) = the topk largest z[n][.], largest first; on equal
+ *                     logits the lower expert id ranks first; NaN ranks last
+ *   route_w[n][i]   = exp(z_i - z_0) / sum_j exp(z_j - z_0) over the chosen
+ *                     (the softmax over all experts renormalised over them)
+ *   W_router bf16 [n_experts][d], x bf16 [N][d]: device, 16-byte aligned
+ *   logits fp32 [N][n_experts] device or NULL (then kept in the workspace)
+ *   ids int32 [N][topk], route_w fp32 [N][topk]: device outputs
+ * N in [1, 8], n_experts in [1, 2048], topk in [1, min(8, n_experts)],
+ * d % 8 == 0 and d <= 8192. Workspace: bws_moe_router_workspace_size(N,
+ * n_experts) bytes, 256-byte aligned (returns 0 for sizes out of range).
+ * One kernel on the stream; the ids feed bws_mxfp4_moe_gemv directly. */
+size_t bws_moe_router_workspace_size(int N, int n_experts);
+int bws_moe_router_topk(const uint16_t* W_router, const uint16_t* x, int N,
+                        int n_experts, int d, int topk, float* logits,
+                        int32_t* ids, float* route_w, void* workspace,
+                        size_t workspace_bytes, void* stream);
+
 /* Verification tap: copies to HOST memory, from the workspace of the last
  * bws_mxfp4_moe_gemv call with the same (L, N, topk), the number of live
  * expert slots, the expert of every slot (-1 = shared expert; shared first,
@@ -298,6 +319,11 @@ typedef struct bws_layer {
   const int32_t* ids;            /* MOE: device [N][topk]                       */
   const float* route_w;          /* MOE: device [N][topk]                       */
   int topk;                      /* MOE                                         */
+  const uint16_t* router;        /* MOE, optional: bf16 [n_experts][hidden], 16-byte aligned. When set,
+                                    the step routes the layer itself (bws_moe_router_topk on the layer's
+                                    normalised input, then the experts) and WRITES the chosen ids and
+                                    weights to ids / route_w, which must then be writable device buffers.
+                                    NULL: ids / route_w are inputs, read on the device every step. */
 } bws_layer;
 
 typedef struct bws_stack {
@@ -367,7 +393,9 @@ int bws_decode_step_kernel_count(const bws_stack_plan* plan);
  *     the MLP records below;
  *   MIXER_MLP and MLP layers: m bf16 [N][hidden], r fp32 [N][hidden] (the
  *     residual m normalised), h bf16 [N][inter] (the down projection input);
- *   MOE layer: m, r as above, the slot count int32 [1], the slot experts
+ *   MOE layer: m, r as above; with a router, its logits fp32
+ *     [N][n_experts], then the ids int32 [N][topk] and weights fp32
+ *     [N][topk] it chose; then the slot count int32 [1], the slot experts
  *     int32 [S] (-1: the shared expert), the combine weights fp32 [S][N], h
  *     bf16 [S][N][inter] per slot and the slots' outputs fp32 [S][N][hidden]
  *     (S = N * topk + 1 with a shared expert, else N * topk; slots past the

@@ -11,8 +11,9 @@ the token-mixing operation reads no weights. They give no normalisation,
 mixer arithmetic, shared-expert width or combine weights; the readings used
 for those (weightless RMSNorm, eps 1e-6; the mixer replaced by taking the
 first d_in(W_o) entries of its input projection; combine weights normalised
-to sum to 1; a shared expert of the routed experts' shape with weight 1) are
-this project's readings, not the pages'.
+to sum to 1; a shared expert of the routed experts' shape with weight 1; a
+BF16 router whose k largest logits choose the experts, weighted by their
+softmax) are this project's readings, not the pages'.
 """
 import numpy as np
 
@@ -60,6 +61,32 @@ def expected_distinct(n_experts, topk, n_tokens):
     topk distinct experts chosen uniformly: E * (1 - (1 - k/E)^n)
     ([LingMoE] §八)."""
     return n_experts * (1.0 - (1.0 - topk / n_experts) ** n_tokens)
+
+
+def router_topk(w_router, X, topk):
+    """Routing of an MoE layer ([LingMoE] section 3: every token goes to 8 of
+    the 512 routed experts, plus the shared one). The pages give no router
+    arithmetic; the reading taken here:
+
+    z[n, e]   = sum_j W_r[e, j] * x[n, j]   (exact, FP64; W_r and x BF16)
+    ids[n]    = the topk experts with the largest z[n, .], largest first;
+                of two equal logits the lower expert id ranks first
+    route_w[n, i] = exp(z_i) / sum over the chosen j of exp(z_j)
+                (the softmax over all experts, renormalised over the chosen)
+
+    Returns (ids int64 [N, k], route_w [N, k], z [N, E], A [N, E]) with A the
+    absolute sums the product bound uses."""
+    z, A = matvec(w_router, X)
+    N, E = z.shape
+    if not 1 <= topk <= E:
+        raise ValueError("topk must be in [1, n_experts]")
+    ids = np.zeros((N, topk), dtype=np.int64)
+    for n in range(N):
+        # descending by logit; a stable sort keeps equal logits in id order
+        ids[n] = np.argsort(-z[n], kind="stable")[:topk]
+    zc = np.take_along_axis(z, ids, axis=1)
+    e = np.exp(zc - zc[:, :1])
+    return ids, e / e.sum(axis=1, keepdims=True), z, A
 
 
 def moe(X, ids, route_w, expert, shared=None):
@@ -117,11 +144,17 @@ def dense_layer(r, layer):
 def moe_layer(r, layer):
     """One layer of the MoE stack: r += FFN(BF16(RMSNorm(r))), the FFN being
     a dense SwiGLU MLP ('gate','up','down') or a MoE ('moe' dict with
-    'ids', 'route_w', 'expert', 'shared')."""
+    'expert', 'shared', and either 'ids' and 'route_w' given, or 'router'
+    (W_r FP64 [E, d]) and 'topk', routed by router_topk on the layer's
+    normalised input)."""
     m = round_bf16(rmsnorm(r))
     if "moe" in layer:
         L = layer["moe"]
-        return r + moe(m, L["ids"], L["route_w"], L["expert"], L["shared"])
+        if "router" in L:
+            ids, route_w, _, _ = router_topk(L["router"], m, L["topk"])
+        else:
+            ids, route_w = L["ids"], L["route_w"]
+        return r + moe(m, ids, route_w, L["expert"], L["shared"])
     return r + mlp(layer["gate"], layer["up"], layer["down"], m)
 
 

@@ -66,7 +66,7 @@ class Report:
 
     def summary(self):
         """kind -> (checks, worst |err| / bound)."""
-        return {k: (self.count[k], round(self.worst[k][0], 4)) for k in sorted(self.count)}
+        return {k: (self.count[k], round(self.worst[k][0], 4) if k in self.worst else None) for k in sorted(self.count)}
 
 
 def check_norm(rep, where, x_gpu, r_gpu, eps=RMS_EPS):
@@ -132,6 +132,34 @@ def check_slot_table(rep, where, ids, route_w, has_shared, n_slots, slot_expert,
             w = 1.0 if e == -1 else float(np.sum(np.where(ids[t] == e, route_w[t], 0.0)))
             ok = ok and np.float32(cw[s, t]) == np.float32(w)
     rep.add("slot_table", where, ok, 0.0 if ok else math.inf, None)
+
+
+def check_router(rep, where, W_r, X, z_gpu, ids_gpu, rw_gpu):
+    """The router stage: logits z = W_r x at the product bound over every
+    expert; each token's chosen experts an acceptable top-k for the exact
+    logits within those bounds, listed largest first; their weights within
+    the softmax's interval for logits anywhere in their bounds
+    (tests/topk_rule.py). Also counts the tokens whose set is the oracle's
+    own top-k exactly."""
+    from topk_rule import acceptable_set, ordered, weight_interval
+    z, A = P.matvec(W_r, X)
+    rep.add("router", where, *T.check(z, z_gpu, A))
+    b = T.bound(z, z_gpu, A)
+    k = ids_gpu.shape[1]
+    ok, worst = True, 0.0
+    for n in range(z.shape[0]):
+        ids = np.asarray(ids_gpu[n], dtype=np.int64)
+        if not (acceptable_set(z[n], b[n], ids) and ordered(z[n], b[n], ids)):
+            ok, worst = False, math.inf
+            continue
+        lo, hi = weight_interval(z[n], b[n], ids)
+        mid, half = (lo + hi) / 2, (hi - lo) / 2
+        r = float(np.max(np.abs(rw_gpu[n] - mid) / half))
+        worst = max(worst, r)
+        ok = ok and r <= 1.0
+        own = set(np.argsort(-z[n], kind="stable")[:k].tolist())
+        rep.count["router_oracle_set"] = rep.count.get("router_oracle_set", 0) + (own == set(ids.tolist()))
+    rep.add("router_topk", where, ok, worst, None)
 
 
 def sample_rows(n, k, seed):
@@ -202,7 +230,8 @@ def check_moe_stack(rep, stack, recs, logits, x0, rows_of, expert_rows, k_rows=N
     """All stages of an MoE stack (dense MLP layers, then MoE layers).
 
     expert_rows(layer, e, name) -> provider of expert e's (-1: shared) gate,
-    up or down rows."""
+    up or down rows. A layer with a router is checked at the router stage
+    (check_router), then from the ids and weights the GPU chose."""
     it = iter(recs)
 
     def nxt(kind):
@@ -230,12 +259,17 @@ def check_moe_stack(rep, stack, recs, logits, x0, rows_of, expert_rows, k_rows=N
                 rows = pick(stack.hidden, 10 * li + 4)
                 check_residual(rep, "down", (li,), rows_of(li, "down")(rows), h, r_m[:, rows], r_next[:, rows])
             continue
+        if L.get("router") is not None:
+            z_g = f64(nxt("z"))
+            ids, rw = nxt("ids").cpu().numpy(), nxt("route_w").cpu().numpy()
+            check_router(rep, (li,), f64(L["router"]), m, z_g, ids, rw.astype(np.float64))
+        else:
+            ids, rw = L["ids_host"].numpy(), L["route_w_host"].numpy()
         n_slots = int(nxt("n_slots").item())
         slot_expert = nxt("slot_expert").cpu().numpy()
         cw = nxt("cw").cpu().numpy().astype(np.float64)
         hs, ys = f64(nxt("h_slots")), f64(nxt("y_slots"))
         w = L["moe"]
-        ids, rw = L["ids_host"].numpy(), L["route_w_host"].numpy()
         check_slot_table(rep, (li,), ids, rw, w.shared is not None, n_slots, slot_expert, cw)
         for s in range(n_slots):
             e = int(slot_expert[s])

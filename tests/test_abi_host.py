@@ -71,3 +71,28 @@ def test_workspace_size_monotone(lib):
     b = lib.bws_gemv_workspace_size(8, 17408, 5120)
     assert 0 < a < b
     assert lib.bws_gemv_workspace_size(0, 10, 10) == 0
+
+
+def test_router_argument_checks_without_gpu(lib):
+    f = lib.bws_moe_router_topk
+    ws = 1 << 20
+
+    # (W, x, N, n_experts, d, topk, logits, ids, route_w, workspace, workspace_bytes, stream)
+    def call(W=16, x=16, N=1, E=8, d=64, k=2, logits=None, ids=16, w=16, buf=256, nbytes=ws):
+        return f(W, x, N, E, d, k, logits, ids, w, buf, nbytes, None)
+
+    assert call(W=None) == 1 and b"null" in lib.bws_last_error()
+    assert call(N=0) == 1 and call(N=9) == 1
+    assert call(k=0) == 1 and call(k=9) == 1
+    assert call(E=4, k=5) == 1                      # more experts chosen than exist
+    assert call(E=0) == 2 and call(E=2049) == 2
+    assert call(d=60) == 2 and call(d=8200) == 2
+    assert call(W=24) == 3 and call(x=40) == 3      # 16-byte alignment
+    assert call(ids=None) == 1 and call(w=None) == 1
+    assert call(ids=18) == 3 and call(logits=18) == 3
+    assert call(nbytes=16) == 7 and call(buf=None) == 7
+    assert call(buf=260) == 3                       # 256-byte aligned workspace
+    assert lib.bws_moe_router_workspace_size(1, 512) == 256 + 2048
+    assert lib.bws_moe_router_workspace_size(8, 512) == 256 + 16384
+    assert lib.bws_moe_router_workspace_size(0, 512) == 0
+    assert lib.bws_moe_router_workspace_size(1, 4096) == 0

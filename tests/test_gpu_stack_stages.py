@@ -221,6 +221,34 @@ def test_moe_stages_every_row(N):
     rep.assert_ok(expect=("slot_table", "rmsnorm", "swiglu", "expert_down", "combine", "down", "head"))
 
 
+@pytest.mark.parametrize("N", [1, 4])
+def test_routed_moe_stages_every_row(N):
+    # the MoE layers route themselves: a BF16 router per layer, the step
+    # writing the chosen ids and weights that the experts then use
+    from bit_weight_streaming_gb300 import workloads as W
+    m = bws()
+    layers = W.moe_stack_layers(N, seed=7, n_dense=1, n_moe=3, hidden=512, inter=256, n_experts=64, topk=8,
+                                dense_inter=768, quant=oracle_quantizers(device()), device=device(), router=True)
+    head = W.make_matrix(3, (1200, 512), 7, 9, oracle_quantizers(device()), device())
+    stack = m.stack.DecodeStack(512, layers, head, N, device=device())
+    x0 = synth.activation_bf16(N, 512, seed=90 + N, device=device())
+    logits, recs = stack.step_tap(x0)
+    torch.cuda.synchronize()
+    assert torch.equal(logits, stack.step(x0)), "the tap must not change the step"
+    # the ids and weights the step wrote into each layer's tensors are the ones its tap recorded
+    tap_ids = [t for k, t in recs if k == "ids"]
+    tap_w = [t for k, t in recs if k == "route_w"]
+    assert len(tap_ids) == len(tap_w) == 3
+    for L, i, w in zip(layers[1:], tap_ids, tap_w):
+        assert torch.equal(L["ids"], i) and torch.equal(L["route_w"], w)
+    rep = SC.Report()
+    SC.check_moe_stack(rep, stack, recs, logits, x0, _dense_rows_of(stack), _expert_rows_small(stack))
+    print(rep.summary())
+    rep.assert_ok(expect=("router", "router_topk", "slot_table", "rmsnorm", "swiglu", "expert_down", "combine",
+                          "down", "head"))
+    assert rep.count["router_topk"] == 3 and rep.count["router_oracle_set"] == 3 * N
+
+
 # ---- full size ---------------------------------------------------------------------
 
 @pytest.fixture(scope="module")
@@ -267,6 +295,28 @@ def test_ling_shape_moe_stack_stages_full_size(N):
     rep.assert_ok(expect=("codes_bit_exact", "slot_table", "rmsnorm", "swiglu", "expert_down", "combine", "down",
                           "head"))
     assert rep.count["slot_table"] == 40 and rep.count["combine"] == 40
+    del stack
+    torch.cuda.empty_cache()
+
+
+@pytest.mark.parametrize("N", [1, 4])
+def test_routed_ling_shape_moe_stack_stages_full_size(N):
+    # the Ling-shape stack with a 512 x 2560 BF16 router in each of its 40 MoE layers
+    from bit_weight_streaming_gb300 import workloads as W
+    bws()
+    stack = W.moe_ling(N, seed=0, device=device(), router=True)
+    torch.cuda.synchronize()
+    x0 = synth.activation_bf16(N, stack.hidden, seed=75 + N, device=device())
+    logits, recs = stack.step_tap(x0)
+    torch.cuda.synchronize()
+    rep = SC.Report()
+    rows_of, expert_rows = _moe_seeded(stack, 0, rep, n_dense=2)
+    SC.check_moe_stack(rep, stack, recs, logits, x0, rows_of, expert_rows, k_rows=24, seed=N)
+    print(N, rep.summary())
+    rep.assert_ok(expect=("codes_bit_exact", "router", "router_topk", "slot_table", "rmsnorm", "swiglu",
+                          "expert_down", "combine", "down", "head"))
+    assert rep.count["router_topk"] == 40 and rep.count["combine"] == 40
+    assert rep.count["router_oracle_set"] == 40 * N
     del stack
     torch.cuda.empty_cache()
 
