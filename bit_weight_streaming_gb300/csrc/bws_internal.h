@@ -144,9 +144,9 @@ struct RouterParams {
   int has_route;           // also write the slot table of route (ids / route_w = the outputs above)
   MoeRoute route;
 };
-constexpr int kRouterMaxD = 8192;
+constexpr int kRouterMaxD = 7168;
 constexpr int kRouterMaxExperts = 2048;
-constexpr int kRouterSmemMax = 131072;   // shared memory for either phase at the limits above
+constexpr int kRouterSmemMax = 16 * 2 * kRouterMaxD;   // 8 rows and 8 tokens of x at the largest d (224 KB)
 size_t router_smem_bytes(int N, int E, int d);
 int router_ctas(int E);
 cudaError_t launch_router(const RouterParams& p, cudaStream_t st, bool pdl);

@@ -12,11 +12,13 @@
 // One kernel: CTA b computes the logits of experts [8b, 8b + 8) for every
 // token, one warp per expert. Each warp copies its router row into shared
 // memory before griddepcontrol.wait (the rows do not depend on the kernels
-// before), so the copy overlaps the input's producer. The last CTA to finish
+// before), so the copy overlaps the input's producer; after the wait the CTA
+// copies x into shared memory in one round, and the dot products read only
+// shared memory. The last CTA to finish
 // (an acquire-release count) reads all logits back from L2 and chooses each
 // token's experts, one warp per token, by k rounds of a warp-wide maximum of
-// 64-bit keys (the order-preserving logit bits, then the complemented expert
-// id). In the decode stack it also writes the layer's slot table and raises
+// the logits' order-preserving bit patterns, then of the lowest expert id
+// holding that maximum. In the decode stack it also writes the layer's slot table and raises
 // the table's ready flag for the expert kernels.
 #include "bws_abi_util.h"
 #include "bws_common.cuh"
@@ -32,10 +34,10 @@ constexpr int kRouterThreads = 32 * kRouterRows;
 __device__ __forceinline__ float bf16_lo(uint32_t v) { return __uint_as_float(v << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t v) { return __uint_as_float(v & 0xFFFF0000u); }
 
-__device__ __forceinline__ unsigned long long shfl_xor_u64(unsigned long long v, int o) {
-  const uint32_t lo = __shfl_xor_sync(0xffffffffu, (uint32_t)v, o);
-  const uint32_t hi = __shfl_xor_sync(0xffffffffu, (uint32_t)(v >> 32), o);
-  return ((unsigned long long)hi << 32) | lo;
+// The logit a key (argmax_key) was made from.
+__device__ __forceinline__ float key_value(unsigned long long key) {
+  const uint32_t b = (uint32_t)(key >> 32);
+  return __uint_as_float((b & 0x80000000u) ? (b & 0x7FFFFFFFu) : ~b);
 }
 
 __global__ void __launch_bounds__(kRouterThreads) router_kernel(RouterParams p) {
@@ -47,77 +49,95 @@ __global__ void __launch_bounds__(kRouterThreads) router_kernel(RouterParams p) 
   const int e = blockIdx.x * kRouterRows + warp;
   const int n16 = p.d / 8;   // 16-byte chunks of a row
   uint16_t* row = reinterpret_cast<uint16_t*>(smem) + (size_t)warp * p.d;
+  uint16_t* xs = reinterpret_cast<uint16_t*>(smem) + (size_t)kRouterRows * p.d;   // x [N][d]
   if (e < p.E) {
     const uint16_t* src = p.W + (size_t)e * p.d;
     for (int c = lane; c < n16; c += 32) cp_async16(smem_u32(row + (size_t)c * 8), src + (size_t)c * 8);
   }
   cp_async_commit();
   pdl_launch_dependents();
-  pdl_wait();   // x is the previous kernel's output
+  pdl_wait();   // x is the previous kernel's output: one round of copies into shared memory
+  for (int i = threadIdx.x; i < p.N * n16; i += blockDim.x) cp_async16(smem_u32(xs + (size_t)i * 8), p.x + (size_t)i * 8);
+  cp_async_commit();
   cp_async_wait<0>();
-  __syncwarp();
+  __syncthreads();
   if (e < p.E) {
-    float acc[kMaxTokens];
+    // two independent FMA chains per token (even and odd K positions)
+    float acc0[kMaxTokens], acc1[kMaxTokens];
 #pragma unroll
-    for (int n = 0; n < kMaxTokens; ++n) acc[n] = 0.0f;
+    for (int n = 0; n < kMaxTokens; ++n) acc0[n] = acc1[n] = 0.0f;
+#pragma unroll 2
     for (int c = lane; c < n16; c += 32) {
       const uint4 w = lds_v4(smem_u32(row + (size_t)c * 8));
       const uint32_t wv[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
       for (int n = 0; n < kMaxTokens; ++n) {
         if (n < p.N) {
-          const uint4 xv = ld_act_v4(p.x + (size_t)n * p.d + (size_t)c * 8);
+          const uint4 xv = lds_v4(smem_u32(xs + (size_t)n * p.d + (size_t)c * 8));
           const uint32_t xw[4] = {xv.x, xv.y, xv.z, xv.w};
-          float a = acc[n];
+          float a0 = acc0[n], a1 = acc1[n];
 #pragma unroll
           for (int i = 0; i < 4; ++i) {   // BF16 x BF16 products are exact in FP32
-            a = fmaf(bf16_lo(wv[i]), bf16_lo(xw[i]), a);
-            a = fmaf(bf16_hi(wv[i]), bf16_hi(xw[i]), a);
+            a0 = fmaf(bf16_lo(wv[i]), bf16_lo(xw[i]), a0);
+            a1 = fmaf(bf16_hi(wv[i]), bf16_hi(xw[i]), a1);
           }
-          acc[n] = a;
+          acc0[n] = a0;
+          acc1[n] = a1;
         }
       }
     }
 #pragma unroll
     for (int n = 0; n < kMaxTokens; ++n) {
       if (n < p.N) {
-        const float s = warp_sum(acc[n]);
+        const float s = warp_sum(acc0[n] + acc1[n]);
         if (lane == 0) p.z[(size_t)n * p.E + e] = s;
       }
     }
-    if (lane == 0) __threadfence();
   }
-  __syncthreads();
+  __syncthreads();   // the CTA's logits are written; thread 0's release below covers them
   if (threadIdx.x == 0) s_last = atom_add_acq_rel_gpu(p.counter, 1u) == gridDim.x - 1;
   __syncthreads();
   if (!s_last) return;
 
-  // the last CTA: every token's top-k over the logits in L2
-  unsigned long long* keys = reinterpret_cast<unsigned long long*>(smem);   // [N][E], rows no longer needed
+  // the last CTA: every token's top-k over the logits in L2, one warp per
+  // token. Each logit becomes its order-preserving 32-bit pattern; a lane
+  // keeps the best of its experts (i = lane mod 32, the lowest i among equal
+  // patterns), and each round takes the warp's largest pattern, then the
+  // lowest expert id holding it, and the lane that held it rescans.
+  uint32_t* vb = reinterpret_cast<uint32_t*>(smem);   // [N][E], rows no longer needed
   for (int i = threadIdx.x; i < p.N * p.E; i += blockDim.x) {
     float v = __ldcg(p.z + i);
     if (v != v) v = -INFINITY;   // a NaN logit ranks last
-    keys[i] = argmax_key(v, i % p.E);
+    vb[i] = (uint32_t)(argmax_key(v, 0) >> 32);   // > 0 for every value: 0 marks a taken expert
   }
   __syncthreads();
   if (warp < p.N) {
-    unsigned long long* kt = keys + (size_t)warp * p.E;
+    uint32_t* vt = vb + (size_t)warp * p.E;
+    uint32_t bv = 0u;
+    int bi = -1;
+    auto rescan = [&]() {
+      bv = 0u;
+      bi = -1;
+      for (int i = lane; i < p.E; i += 32)
+        if (vt[i] > bv) {
+          bv = vt[i];
+          bi = i;
+        }
+    };
+    rescan();
     for (int j = 0; j < p.topk; ++j) {
-      unsigned long long best = 0ull;
-      for (int i = lane; i < p.E; i += 32) best = kt[i] > best ? kt[i] : best;
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) {
-        const unsigned long long other = shfl_xor_u64(best, o);
-        best = other > best ? other : best;
-      }
-      const int id = argmax_row(best);
+      const uint32_t vmax = __reduce_max_sync(0xffffffffu, bv);
+      const int id = (int)__reduce_min_sync(0xffffffffu, (bv == vmax && bi >= 0) ? (uint32_t)bi : 0xffffffffu);
       if (lane == 0) {
         s_id[warp][j] = id;
-        s_z[warp][j] = __ldcg(p.z + (size_t)warp * p.E + id);
-        kt[id] = 0ull;   // taken
+        s_z[warp][j] = key_value((unsigned long long)vmax << 32);
       }
-      __syncwarp();
+      if ((id & 31) == lane) {   // the owner takes it out and finds its next best
+        vt[id] = 0u;
+        rescan();
+      }
     }
+    __syncwarp();
     // softmax over the chosen logits; the first is the largest
     float ex = 0.0f;
     if (lane < p.topk) ex = expf(s_z[warp][lane] - s_z[warp][0]);
@@ -136,8 +156,8 @@ __global__ void __launch_bounds__(kRouterThreads) router_kernel(RouterParams p) 
 }  // namespace
 
 size_t router_smem_bytes(int N, int E, int d) {
-  const size_t rows = (size_t)kRouterRows * d * 2;
-  const size_t keys = (size_t)N * E * 8;
+  const size_t rows = (size_t)(kRouterRows + N) * d * 2;   // the CTA's router rows, then x
+  const size_t keys = (size_t)N * E * 4;
   return rows > keys ? rows : keys;
 }
 

@@ -265,7 +265,7 @@ int bws_mxfp4_moe_gemv(const bws_moe_layer* L, const int32_t* ids,
  *   logits fp32 [N][n_experts] device or NULL (then kept in the workspace)
  *   ids int32 [N][topk], route_w fp32 [N][topk]: device outputs
  * N in [1, 8], n_experts in [1, 2048], topk in [1, min(8, n_experts)],
- * d % 8 == 0 and d <= 8192. Workspace: bws_moe_router_workspace_size(N,
+ * d % 8 == 0 and d <= 7168. Workspace: bws_moe_router_workspace_size(N,
  * n_experts) bytes, 256-byte aligned (returns 0 for sizes out of range).
  * One kernel on the stream; the ids feed bws_mxfp4_moe_gemv directly. */
 size_t bws_moe_router_workspace_size(int N, int n_experts);

@@ -86,7 +86,7 @@ def test_router_argument_checks_without_gpu(lib):
     assert call(k=0) == 1 and call(k=9) == 1
     assert call(E=4, k=5) == 1                      # more experts chosen than exist
     assert call(E=0) == 2 and call(E=2049) == 2
-    assert call(d=60) == 2 and call(d=8200) == 2
+    assert call(d=60) == 2 and call(d=7176) == 2
     assert call(W=24) == 3 and call(x=40) == 3      # 16-byte alignment
     assert call(ids=None) == 1 and call(w=None) == 1
     assert call(ids=18) == 3 and call(logits=18) == 3

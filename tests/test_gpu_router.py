@@ -57,7 +57,7 @@ def test_router_ling_shape(N):
     assert same == N
 
 
-@pytest.mark.parametrize("E,d,N,k", [(37, 256, 3, 5), (8, 64, 2, 8), (1, 8, 1, 1), (2048, 8192, 8, 8),
+@pytest.mark.parametrize("E,d,N,k", [(37, 256, 3, 5), (8, 64, 2, 8), (1, 8, 1, 1), (2048, 7168, 8, 8),
                                      (100, 2568, 5, 3)])
 def test_router_shapes_and_edges(E, d, N, k):
     # a partial last CTA (37, 100 experts), every expert chosen (8 of 8), a
