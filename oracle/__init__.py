@@ -10,7 +10,7 @@ makes a rounding decision, FP64 for every product and sum):
 
 * ``formats``   E2M1 / E4M3 / E8M0 codecs and round-to-nearest-even encoders,
                 BF16 rounding.
-* ``quant``     NVFP4, MXFP4 and row-wise FP8 quantizers.
+* ``quant``     NVFP4, MXFP4 and row-wise FP8 quantizers; MXFP8 activations.
 * ``products``  dequantization and exact (FP64) matrix-vector products.
 * ``model``     SwiGLU MLP, top-k MoE with a shared expert, weightless RMSNorm,
                 and the layer recipe of the dense and MoE stacks.

@@ -9,7 +9,7 @@ sums the products in FP64 with a library matmul.
 import numpy as np
 
 from .formats import e2m1_decode, e4m3_decode, e8m0_decode
-from .quant import unpack_nibbles, NVFP4_BLOCK, MXFP4_BLOCK
+from .quant import unpack_nibbles, NVFP4_BLOCK, MXFP4_BLOCK, MXFP8_BLOCK
 
 
 def nvfp4_dequantize(codes, scales, s_t):
@@ -28,6 +28,15 @@ def mxfp4_dequantize(codes, scales):
     sb = e8m0_decode(scales)
     w = q.reshape(rows, d_in // MXFP4_BLOCK, MXFP4_BLOCK) * sb[..., None]
     return w.reshape(rows, d_in)
+
+
+def mxfp8_dequantize(codes, scales):
+    """x_hat = 2^(scale-127) * dec_E4M3(code), FP64 (MXFP8 activations)."""
+    q = e4m3_decode(codes)
+    n, d = q.shape
+    sb = e8m0_decode(scales)
+    x = q.reshape(n, d // MXFP8_BLOCK, MXFP8_BLOCK) * sb[..., None]
+    return x.reshape(n, d)
 
 
 def fp8_dequantize(codes, row_scale):
@@ -51,6 +60,12 @@ def nvfp4_gemv(codes, scales, s_t, X):
 
 def mxfp4_gemv(codes, scales, X):
     return matvec(mxfp4_dequantize(codes, scales), X)
+
+
+def w4a8_gemv(w_codes, w_scales, x_codes, x_scales):
+    """W4A8: MXFP4 weights times MXFP8 activations, Y = X_hat W_hat^T with both
+    operands dequantized exactly ([LingMoE] §三, the W4A8 baseline)."""
+    return matvec(mxfp4_dequantize(w_codes, w_scales), mxfp8_dequantize(x_codes, x_scales))
 
 
 def fp8_gemv(codes, row_scale, X):

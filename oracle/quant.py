@@ -1,4 +1,4 @@
-"""Quantizers: NVFP4, MXFP4, row-wise FP8.
+"""Quantizers: NVFP4, MXFP4, row-wise FP8, and MXFP8 activations.
 
 Every rounding decision is taken in FP32 (numpy float32 arithmetic is IEEE
 round-to-nearest-even), in the order written below, so that codes can be
@@ -103,6 +103,35 @@ def mxfp4_quantize(W):
     q = e2m1_encode(scaled)
     q = np.where(nz[..., None], q, 0).astype(np.uint8)
     return pack_nibbles(q.reshape(rows, d_in)), (e + 127).astype(np.uint8)
+
+
+MXFP8_BLOCK = 32
+
+
+def mxfp8_quantize(X):
+    """MXFP8 activations for the W4A8 product: E4M3 elements with one E8M0
+    (power-of-two) scale per 32 consecutive values along the row. [LingMoE]
+    §三 runs the MoE baseline as W4A8 (MXFP4 weights, 8-bit activations) and
+    does not give the activation quantizer; it is read, as for MXFP4, from
+    the OCP MX specification, with E4M3's largest exponent 8:
+      e    = clamp(floor(log2 amax_b) - 8, -127, 127)
+      code = e + 127
+      q_j  = E4M3_rne_satfinite(x_j * 2^-e)             (exact scaling)
+    A block with amax_b = 0 gets scale code 0 and all-zero codes.
+    X: [N, d] values (BF16 activations held in any float type).
+    Returns (codes uint8 [N, d] E4M3, scales uint8 [N, d/32] E8M0)."""
+    X = np.atleast_2d(np.asarray(X, dtype=_F32))
+    n, d = X.shape
+    assert d % MXFP8_BLOCK == 0
+    blk = X.reshape(n, d // MXFP8_BLOCK, MXFP8_BLOCK).astype(np.float64)
+    amax_b = np.max(np.abs(blk), axis=2)
+    nz = amax_b > 0
+    e = np.where(nz, floor_log2(np.where(nz, amax_b, 1.0)) - 8, -127)
+    e = np.clip(e, -127, 127)
+    scaled = np.ldexp(blk, -e[..., None])
+    q = e4m3_encode(scaled.astype(_F32))
+    q = np.where(nz[..., None], q, 0).astype(np.uint8)
+    return q.reshape(n, d), (e + 127).astype(np.uint8)
 
 
 def fp8_rowwise_quantize(W):

@@ -73,6 +73,28 @@ def test_fp8_and_mxfp4_products_match_numpy_dot():
     assert np.allclose(y4, X @ wd4.T, rtol=1e-14)
 
 
+def test_w4a8_brute_force_exact_rationals():
+    # MXFP4 weights times MXFP8 activations, every product and sum in exact
+    # rationals from the decoded codes and the power-of-two scales
+    W = synth.weight_fp32((8, 64), seed=12).numpy()
+    X = synth.activation_bf16(3, 64, seed=12).float().numpy()
+    wc, ws = Q.mxfp4_quantize(W)
+    xc, xs = Q.mxfp8_quantize(X)
+    Y, A = P.w4a8_gemv(wc, ws, xc, xs)
+    q = Q.unpack_nibbles(wc)
+    for n in range(3):
+        for i in range(8):
+            acc = Fraction(0)
+            acc_abs = Fraction(0)
+            for j in range(64):
+                w = Fraction(float(F.e2m1_decode(q[i, j]))) * Fraction(2) ** (int(ws[i, j // 32]) - 127)
+                x = Fraction(float(F.e4m3_decode(xc[n, j]))) * Fraction(2) ** (int(xs[n, j // 32]) - 127)
+                acc += w * x
+                acc_abs += abs(w * x)
+            assert abs(Fraction(float(Y[n, i])) - acc) <= abs(acc) * Fraction(1, 2 ** 50)
+            assert abs(Fraction(float(A[n, i])) - acc_abs) <= acc_abs * Fraction(1, 2 ** 50)
+
+
 def test_silu_identities():
     g = np.linspace(-30, 30, 1001)
     s = M.silu(g)

@@ -9,9 +9,9 @@ from tests.conftest import load_golden, golden_float
 import synth
 
 
-def _golden_W(name):
+def _golden_W(name, key="W"):
     g = load_golden(name)
-    W = np.array([[golden_float(v) for v in row] for row in g["W"]], dtype=np.float32)
+    W = np.array([[golden_float(v) for v in row] for row in g[key]], dtype=np.float32)
     return g, W
 
 
@@ -53,6 +53,54 @@ def test_mxfp4_hand_example():
     codes, scales = Q.mxfp4_quantize(W)
     assert scales.tolist() == g["scales"]
     assert codes.tolist() == g["codes"]
+
+
+def test_mxfp8_hand_example():
+    # five rows worked by hand: ordinary values, ties to the even mantissa, a
+    # subnormal, signed zero, saturation at 448, an all-zero block, a large
+    # exponent and the scale's clamp at 2^-127
+    g, X = _golden_W("mxfp8_hand.json", "X")
+    codes, scales = Q.mxfp8_quantize(X)
+    assert scales.tolist() == g["scales"]
+    assert codes.tolist() == g["codes"]
+
+
+def test_mxfp8_invariants():
+    X = synth.weight_fp32((16, 512), seed=3, index=1, std=1.0).numpy()
+    X[2, :32] = 0.0
+    X[4, 32:64] *= 1e-30
+    codes, scales = Q.mxfp8_quantize(X)
+    x_hat = P.mxfp8_dequantize(codes, scales)
+    blk = np.abs(X.astype(np.float64)).reshape(16, 16, 32)
+    amax = blk.max(axis=2)
+    X_scale = F.e8m0_decode(scales)
+    nz = amax > 0
+    # the block's largest value lands in [256, 448] after scaling (448 when it saturates)
+    top = np.abs(x_hat).reshape(16, 16, 32).max(axis=2)
+    assert np.all(top[nz] / X_scale[nz] >= 256) and np.all(top[nz] / X_scale[nz] <= 448)
+    assert np.all(scales[~nz] == 0) and np.all(x_hat.reshape(16, 16, 32)[~nz] == 0)
+    # every value within half an E4M3 step of its block: 2^-4 relative for
+    # normals, half the subnormal step 2^-10 X below them; saturated ones
+    # lose at most (512 - 448) / 512 of the block maximum
+    err = np.abs(x_hat - X.astype(np.float64)).reshape(16, 16, 32)
+    bound = np.maximum(2.0 ** -4 * blk, 2.0 ** -10 * X_scale[..., None]) + (blk * X_scale[..., None] ** -1 > 448) * blk
+    assert np.all(err <= bound)
+    # quantizing the dequantized values again changes nothing
+    c2, s2 = Q.mxfp8_quantize(x_hat.astype(np.float32))
+    assert np.array_equal(c2, codes) and np.array_equal(s2, scales)
+
+
+def test_mxfp8_exact_round_trip():
+    # values that are E4M3 numbers times the block's power of two come back exactly
+    rng = np.random.default_rng(0)
+    vals = F.e4m3_decode(np.arange(0, 0x7F, dtype=np.uint8))
+    vals = vals[vals >= 2.0 ** -6]
+    x = rng.choice(vals, size=(3, 64)) * rng.choice([-1.0, 1.0], size=(3, 64))
+    x[:, 0] = 448.0   # fixes the block exponent at 0 (floor(log2 448) - 8 = 0)
+    x[:, 32] = -448.0
+    codes, scales = Q.mxfp8_quantize(x.astype(np.float32))
+    assert np.all(scales == 127)
+    assert np.array_equal(P.mxfp8_dequantize(codes, scales), x)
 
 
 def test_fp8_hand_example():
