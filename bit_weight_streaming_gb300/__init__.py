@@ -18,6 +18,8 @@ from .api import (  # noqa: F401
     fp8_lmhead_gemv,
     fp8_lmhead_argmax,
     moe_router_topk,
+    mxfp8_quantize,
+    mxfp4_w4a8_gemv,
     status_word,
     hbm_read_probe,
     l2_flush,

@@ -28,6 +28,9 @@ SIGNATURES = {
     "bws_fp8_lmhead_argmax": (I, [P, P, P, I, I, I, P, P, P, P, Z, P]),
     "bws_mxfp4_moe_workspace_size": (Z, [P, I, I]),
     "bws_moe_router_workspace_size": (Z, [I, I]),
+    "bws_mxfp8_quantize": (I, [P, I, I, P, P, P]),
+    "bws_w4a8_workspace_size": (Z, [I, I, I]),
+    "bws_mxfp4_w4a8_gemv": (I, [P, P, P, I, I, I, P, P, Z, P]),
     "bws_moe_router_topk": (I, [P, P, I, I, I, I, P, P, P, P, Z, P]),
     "bws_mxfp4_moe_gemv": (I, [P, P, P, I, I, P, P, P, Z, P]),
     "bws_mxfp4_moe_inspect": (I, [P, P, I, I, P, P, P, P, P]),

@@ -187,6 +187,33 @@ def moe_router_topk(W_router, x, topk, logits=False, ws=None):
     return (ids, w, logits) if logits is not False else (ids, w)
 
 
+def mxfp8_quantize(x):
+    """MXFP8 activations: x bf16 [N, d] -> (codes u8 [N, d] E4M3, scales u8
+    [N, d/32] E8M0), one power-of-two scale per 32 values."""
+    _need_cuda(x)
+    N, d = x.shape
+    codes = torch.empty((N, d), dtype=torch.uint8, device=x.device)
+    scales = torch.empty((N, d // 32), dtype=torch.uint8, device=x.device)
+    check(lib().bws_mxfp8_quantize(_ptr(x), N, d, _ptr(codes), _ptr(scales), _stream(x.device)),
+          "bws_mxfp8_quantize")
+    return codes, scales
+
+
+def mxfp4_w4a8_gemv(codes, scales, x, y=None, ws=None):
+    """W4A8 on the tensor cores: MXFP4 weights (codes u8 [d_out, d_in/2],
+    E8M0 scales u8 [d_out, d_in/32]) times the MXFP8 quantization of x bf16
+    [N, d_in] (N <= 8), FP32 accumulation; returns y bf16 [N, d_out]."""
+    _need_cuda(codes, scales, x)
+    N, d_in = x.shape
+    d_out = codes.shape[0]
+    if y is None:
+        y = torch.empty((N, d_out), dtype=torch.bfloat16, device=x.device)
+    buf = _ws(ws, lib().bws_w4a8_workspace_size(N, d_out, d_in), x.device)
+    check(lib().bws_mxfp4_w4a8_gemv(_ptr(codes), _ptr(scales), _ptr(x), N, d_out, d_in, _ptr(y), _ptr(buf),
+                                    buf.numel(), _stream(x.device)), "bws_mxfp4_w4a8_gemv")
+    return y
+
+
 def status_word(ws):
     """OR of the status bits set by the last product call that used ws."""
     import ctypes

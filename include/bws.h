@@ -253,6 +253,36 @@ int bws_mxfp4_moe_gemv(const bws_moe_layer* L, const int32_t* ids,
                        uint16_t* y, void* workspace, size_t workspace_bytes,
                        void* stream);
 
+/* W4A8: MXFP4 weights times MXFP8 activations on the tensor cores
+ * ([LingMoE] section 3: the MoE baseline runs W4A8, 4-bit MXFP4 weights with
+ * 8-bit activations; the pages do not give the activation quantizer, which is
+ * read from the OCP MX rule).
+ *
+ * bws_mxfp8_quantize: x bf16 [N][d] (device, finite) -> codes u8 [N][d] E4M3
+ * and scales u8 [N][d/32] E8M0, per block of 32 values along the row:
+ *   e = clamp(floor(log2 amax) - 8, -127, 127), scale code e + 127,
+ *   code_j = E4M3(x_j * 2^-e), nearest even, saturating at 448, sign kept;
+ * an all-zero block gets scale code 0 and zero codes. N >= 0 (0: no-op),
+ * d % 32 == 0. One kernel on the stream, no workspace.
+ *
+ * bws_mxfp4_w4a8_gemv: y[n][i] = sum_j w_ij * xq[n][j], w the MXFP4 weights
+ * (codes and scales as bws_mxfp4_quantize writes them) and xq the MXFP8
+ * quantization of x above; FP32 accumulation, y rounded to BF16.
+ *   codes u8 [d_out][d_in/2] (32-byte aligned), scales u8 [d_out][d_in/32]
+ *   (8-byte aligned), x bf16 [N][d_in], y bf16 [N][d_out]: device pointers
+ *   N in [1, 8], d_in % 256 == 0; N == 0 or d_out == 0 is a no-op.
+ *   Workspace: bws_w4a8_workspace_size(N, d_out, d_in) bytes, 256-byte
+ *   aligned (0 for sizes out of range); its status word (bws_status_word)
+ *   reports a bounded wait that ran out. Two kernels on the stream: the
+ *   activation quantizer, then the product (one CTA per SM). */
+int bws_mxfp8_quantize(const uint16_t* x, int N, int d, uint8_t* codes,
+                       uint8_t* scales, void* stream);
+size_t bws_w4a8_workspace_size(int N, int d_out, int d_in);
+int bws_mxfp4_w4a8_gemv(const uint8_t* codes, const uint8_t* scales,
+                        const uint16_t* x, int N, int d_out, int d_in,
+                        uint16_t* y, void* workspace, size_t workspace_bytes,
+                        void* stream);
+
 /* MoE router ([LingMoE] section 3: each MoE layer sends every token to 8 of
  * its 512 routed experts, plus one shared expert). The pages name the routing
  * but not its arithmetic; this library reads it as

@@ -96,3 +96,27 @@ def test_router_argument_checks_without_gpu(lib):
     assert lib.bws_moe_router_workspace_size(8, 512) == 256 + 16384
     assert lib.bws_moe_router_workspace_size(0, 512) == 0
     assert lib.bws_moe_router_workspace_size(1, 4096) == 0
+
+
+def test_w4a8_argument_checks_without_gpu(lib):
+    f = lib.bws_mxfp4_w4a8_gemv
+    ws = 1 << 24
+
+    # (codes, scales, x, N, d_out, d_in, y, workspace, workspace_bytes, stream)
+    def call(c=32, s=32, x=32, N=1, d_out=64, d_in=256, y=32, buf=256, nbytes=ws):
+        return f(c, s, x, N, d_out, d_in, y, buf, nbytes, None)
+
+    assert call(N=0) == 0 and call(d_out=0) == 0           # no-ops
+    assert call(c=None) == 1 and b"null" in lib.bws_last_error()
+    assert call(N=9) == 1
+    assert call(d_in=128) == 2 and call(d_in=320) == 2
+    assert call(c=48) == 3 and call(s=36) == 3 and call(x=33) == 3
+    assert call(nbytes=256) == 7 and call(buf=None) == 7
+    assert call(buf=272) == 3
+    assert lib.bws_w4a8_workspace_size(9, 64, 256) == 0
+    assert lib.bws_w4a8_workspace_size(1, 64, 320) == 0
+    assert 0 < lib.bws_w4a8_workspace_size(1, 64, 256) < lib.bws_w4a8_workspace_size(8, 17408, 5120)
+    q = lib.bws_mxfp8_quantize
+    assert q(None, 0, 32, None, None, None) == 0
+    assert q(None, 1, 32, 16, 16, None) == 1
+    assert q(16, 1, 48, 16, 16, None) == 2 and q(17, 1, 32, 16, 16, None) == 3
