@@ -433,6 +433,7 @@ def run_gpu(args):
                              "weight_bytes": hm.nbytes(), "note": "activation prep + product with fused argmax, N=1"}
 
     mixed = run_mixed(args, dev, stream, peak)
+    w4a8 = run_w4a8(args, dev, stream, peak)
 
     moe = moe_routed = None
     if not args.no_moe:
@@ -461,6 +462,7 @@ def run_gpu(args):
             "moe": moe,
             "moe_routed": moe_routed,
             "mixed": mixed,
+            "w4a8": w4a8,
             "heads_argmax": heads,
             "e2e": {"value": round(e2e_val / 1e9, 2), "unit": UNIT, "h2d_bytes_per_step": x_host.numel() * 2,
                     "d2h_bytes_per_step": tok_host.numel() * 4,
@@ -504,6 +506,56 @@ def run_mixed(args, dev, stream, peak, tokens=(1, 8)):
         del S
     del base
     torch.cuda.empty_cache()
+    return out
+
+
+def run_w4a8(args, dev, stream, peak, shapes=((46336, 5120), (17408, 5120)), tokens=(1, 8), copies=4):
+    """W4A8 products (MXFP4 weights, MXFP8 activations, tensor cores) on two
+    of the 27B-shape step's matrix shapes held in MXFP4: each call quantizes
+    the activations, then streams the weights; a CUDA graph of back-to-back
+    calls over four weight copies (each read cold), CUDA events around it."""
+    import torch
+    import bit_weight_streaming_gb300 as bws
+    from bit_weight_streaming_gb300 import workloads as W
+    import synth
+    out = {}
+    for d_out, d_in in shapes:
+        with torch.cuda.stream(stream):
+            mats = [W.make_matrix(2, (d_out, d_in), args.seed, 500 + i, device=dev) for i in range(copies)]
+        stream.synchronize()
+        nbytes = mats[0].nbytes()
+        for N in tokens:
+            x = synth.activation_bf16(N, d_in, seed=args.seed, device=dev)
+            y = torch.empty((N, d_out), dtype=torch.bfloat16, device=dev)
+            ws = bws.Workspace(dev)
+            with torch.cuda.stream(stream):
+                for m in mats:
+                    bws.mxfp4_w4a8_gemv(m.codes, m.scales, x, y=y, ws=ws)
+                stream.synchronize()
+                g = torch.cuda.CUDAGraph()
+                reps = 5
+                with torch.cuda.graph(g, stream=stream):
+                    for _ in range(reps):
+                        for m in mats:
+                            bws.mxfp4_w4a8_gemv(m.codes, m.scales, x, y=y, ws=ws)
+                g.replay()
+                stream.synchronize()
+                a = torch.cuda.Event(enable_timing=True)
+                b = torch.cuda.Event(enable_timing=True)
+                a.record(stream)
+                for _ in range(3):
+                    g.replay()
+                b.record(stream)
+                b.synchronize()
+            t = a.elapsed_time(b) / 1e3 / (3 * reps * copies)
+            out[f"{d_out}x{d_in}_n{N}"] = {"us_per_call": round(t * 1e6, 2), "GBs": round(nbytes / t / 1e9, 1),
+                                          "frac_of_hbm_peak": round(nbytes / t / 1e9 / peak, 4),
+                                          "weight_bytes": nbytes}
+            del g
+        del mats
+        torch.cuda.empty_cache()
+    out["note"] = ("bws_mxfp4_w4a8_gemv: activation quantizer + tcgen05 product per call; weight bytes = MXFP4 codes "
+                   "+ E8M0 scales")
     return out
 
 
