@@ -678,6 +678,35 @@ def run_product_only(args):
                       "us_per_call": round(t * 1e6, 2), "GB/s": round(nb / t / 1e9, 1)}), flush=True)
 
 
+def run_w4a8_only(args):
+    """Times repeated W4A8 calls on one MXFP4 matrix shape (a small,
+    two-kernel workload for profiler captures): --w4a8 ROWSxCOLS --tokens N."""
+    import torch
+    import __graft_entry__ as g
+    g.build()
+    import bit_weight_streaming_gb300 as bws
+    from bit_weight_streaming_gb300 import workloads as W
+    import synth
+    rows, cols = (int(v) for v in args.w4a8.lower().split("x"))
+    dev = torch.device("cuda", 0)
+    mats = [W.make_matrix(2, (rows, cols), args.seed, 500 + i, device=dev) for i in range(args.copies)]
+    x = synth.activation_bf16(args.tokens, cols, seed=args.seed, device=dev)
+    y = torch.empty((args.tokens, rows), dtype=torch.bfloat16, device=dev)
+    ws = bws.Workspace(dev)
+    k = [0]
+
+    def call():
+        m = mats[k[0] % len(mats)]
+        k[0] += 1
+        bws.mxfp4_w4a8_gemv(m.codes, m.scales, x, y=y, ws=ws)
+
+    stream = torch.cuda.current_stream(dev)
+    t = time_steps(call, args.steps, args.warmup, stream)
+    nb = mats[0].nbytes()
+    print(json.dumps({"w4a8": f"{rows}x{cols}", "tokens": args.tokens, "copies": args.copies,
+                      "us_per_call": round(t * 1e6, 2), "GB/s": round(nb / t / 1e9, 1)}), flush=True)
+
+
 def run_moe_only(args):
     """The MoE step alone at --tokens N (a short workload for profiler launch
     lists): one JSON line with its timing."""
@@ -700,6 +729,7 @@ def main(argv=None):
     ap.add_argument("--no-moe", action="store_true")
     ap.add_argument("--product", default=None, help="ROWSxCOLS: time one NVFP4 product only (profiling)")
     ap.add_argument("--moe-only", action="store_true", help="time the MoE step alone at --tokens N (profiling)")
+    ap.add_argument("--w4a8", default=None, help="ROWSxCOLS: time one W4A8 product only (profiling)")
     ap.add_argument("--tokens", type=int, default=1)
     ap.add_argument("--router", action="store_true", help="--moe-only: MoE layers routed inside the step")
     ap.add_argument("--copies", type=int, default=4, help="--product: distinct weight copies to rotate")
@@ -708,6 +738,8 @@ def main(argv=None):
         args.warmup = 3
     if args.product:
         run_product_only(args)
+    elif args.w4a8:
+        run_w4a8_only(args)
     elif args.moe_only:
         run_moe_only(args)
     elif args.impl == "reference":
