@@ -622,10 +622,11 @@ cudaError_t launch_gemv_tma_moe(int epi, const GemvParams& g, uint32_t* status, 
   p.n_stages = kSmemBudgetMoe / p.stage_bytes;
   if (p.n_stages > kMaxStagesMoe) p.n_stages = kMaxStagesMoe;
   if (p.n_stages < 2) return cudaErrorInvalidValue;
-  // weights ahead of the inputs: two stages at one token; with more tokens
-  // none (measured at 4 tokens: 0 / 1 / 2 / 3 stages 2.43 / 2.47 / 2.46 /
-  // 2.47 ms per step, the table still read early)
-  p.n_prime = g.N == 1 ? 2 : 0;
+  // weights ahead of the inputs: one stage at one token; with more tokens
+  // none (measured, MoE step at one token, 0 / 1 / 2 / 3 / 5 stages: 1.329 /
+  // 1.277 / 1.292 / 1.308 / 1.307 ms; at four tokens 0 / 1 / 2: 2.450 /
+  // 2.482 / 2.477 ms; the table still read early)
+  p.n_prime = g.N == 1 ? 1 : 0;
   if (p.n_prime > p.n_stages) p.n_prime = p.n_stages;
   const bool n1 = g.N == 1;
   if (epi == kEpiSwiGLU) return n1 ? launch_moe_one<kEpiSwiGLU, true>(p, st, pdl) : launch_moe_one<kEpiSwiGLU, false>(p, st, pdl);
