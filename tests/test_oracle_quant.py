@@ -248,3 +248,30 @@ def test_reorder_helper_matches_the_oracle_when_not_reordered():
     a = Q.nvfp4_quantize(W)
     b = _nvfp4_reordered(False, False)(W)
     assert np.array_equal(a[0], b[0]) and np.array_equal(a[1], b[1]) and a[2] == b[2]
+
+
+@pytest.mark.parametrize("bad", ["emax7", "no_clamp", "ceil_log2", "no_saturation"])
+def test_mxfp8_planted_mistakes_fail_the_hand_rows(monkeypatch, bad):
+    """Plausible slips in the MXFP8 rule must fail the hand-worked rows."""
+    def broken(X):
+        X = np.atleast_2d(np.asarray(X, dtype=np.float32))
+        n, d = X.shape
+        blk = X.reshape(n, d // 32, 32).astype(np.float64)
+        amax = np.max(np.abs(blk), axis=2)
+        nz = amax > 0
+        fl = Q.floor_log2(np.where(nz, amax, 1.0))
+        if bad == "ceil_log2":
+            fl = np.ceil(np.log2(np.where(nz, amax, 1.0))).astype(np.int64)
+        e = np.where(nz, fl - (7 if bad == "emax7" else 8), -127)
+        if bad != "no_clamp":
+            e = np.clip(e, -127, 127)
+        scaled = np.ldexp(blk, -e[..., None]).astype(np.float32)
+        q = F.e4m3_encode(scaled)
+        if bad == "no_saturation":   # wraps past 448 into the NaN pattern
+            q = np.where(np.abs(scaled) > 448, (q & 0x80) | 0x7F, q)
+        q = np.where(nz[..., None], q, 0).astype(np.uint8)
+        return q.reshape(n, d), (e + 127).astype(np.uint8)
+
+    monkeypatch.setattr(Q, "mxfp8_quantize", broken)
+    with pytest.raises(AssertionError):
+        test_mxfp8_hand_example()

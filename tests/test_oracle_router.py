@@ -140,3 +140,36 @@ def test_rule_weight_interval():
     # a logit bound of 0.01 moves a weight by about 1 % at most
     lo, hi = weight_interval(z, np.full(4, 0.01), [1, 2, 0])
     assert np.all(lo < w * 0.995) and np.all(hi > w * 1.005) and np.all(hi < w * 1.03)
+
+
+@pytest.mark.parametrize("bad", ["ascending", "ties_high", "unnormalised"])
+def test_router_planted_mistakes_are_caught(monkeypatch, bad):
+    """Plausible slips in the routing rule must fail the hand-worked pins."""
+    def broken(w_router, X, topk):
+        from oracle.products import matvec
+        z, A = matvec(w_router, X)
+        N, E = z.shape
+        ids = np.zeros((N, topk), dtype=np.int64)
+        for n in range(N):
+            if bad == "ascending":
+                ids[n] = np.argsort(z[n], kind="stable")[:topk]
+            elif bad == "ties_high":
+                ids[n] = (E - 1 - np.argsort(-z[n][::-1], kind="stable"))[:topk]
+            else:
+                ids[n] = np.argsort(-z[n], kind="stable")[:topk]
+        zc = np.take_along_axis(z, ids, axis=1)
+        if bad == "unnormalised":   # the full softmax, not renormalised over the chosen
+            e = np.exp(z - z.max(axis=1, keepdims=True))
+            return ids, np.take_along_axis(e / e.sum(axis=1, keepdims=True), ids, axis=1), z, A
+        e = np.exp(zc - zc[:, :1])
+        return ids, e / e.sum(axis=1, keepdims=True), z, A
+
+    monkeypatch.setattr(M, "router_topk", broken)
+    failed = 0
+    for pin in (test_hand_worked_two_of_four_with_a_tie, test_hand_worked_three_of_four,
+                test_all_equal_logits_pick_the_lowest_ids_evenly):
+        try:
+            pin()
+        except AssertionError:
+            failed += 1
+    assert failed > 0, f"planted mistake {bad} passed every pin"
