@@ -706,9 +706,10 @@ cudaError_t launch_gemv_tma(int fmt, int epi, const GemvParams& g, uint32_t* sta
   // starts while the previous kernels finish, and a full ring of weight
   // copies from all of them (about 30 MB) queues ahead of those kernels'
   // last loads and stores, which decide when the inputs are ready. A stage
-  // or two keeps the overlap without the queue (measured: 1 token best with
-  // 2, 2-4 tokens with 1, 8 tokens with none).
-  p.n_prime = p.N == 1 ? 2 : (p.N <= 4 ? 1 : 0);
+  // keeps the overlap without the queue (measured on the 27B-shape step,
+  // one token, 1 / 2 / 3 / 4 stages: 5.16 / 5.23 / 5.31 / 5.37 ms; eight
+  // tokens, 0 / 1 / 2: 6.90 / 6.99 / 7.07 ms; 2-4 tokens best with 1).
+  p.n_prime = p.N <= 4 ? 1 : 0;
   if (p.n_ctas <= 0) return cudaSuccess;
   // one NVFP4 token: the block-diagonal operand (block scales on the accumulators)
   const bool n1 = fmt == kFmtNVFP4 && p.N == 1;
