@@ -228,14 +228,14 @@ def time_steps(fn, steps, warmup, stream):
 
 
 # DRAM read + write bytes per algorithmic byte of the NVFP4 product kernel,
-# from ncu's dram__bytes_read.sum + dram__bytes_write.sum over two launches
-# of each of the step's five product shapes (46336x5120, 14336x5120,
-# 34816x5120, 5120x17408, 5120x6144; one token), weighted by the step's
-# launches per shape. Taken on the current kernel; reset to None when the
+# by token count, from ncu's dram__bytes_read.sum + dram__bytes_write.sum
+# over two launches of each of the step's five product shapes (46336x5120,
+# 14336x5120, 34816x5120, 5120x17408, 5120x6144), weighted by the step's
+# launches per shape. Taken on the current kernel; to be dropped when the
 # kernel changes.
-TRAFFIC_PER_BYTE = 1.0339
+TRAFFIC_PER_BYTE = {1: 1.0339, 8: 1.0366}
 TRAFFIC_BASIS = ("ncu dram__bytes_read.sum + dram__bytes_write.sum of the product kernel on the step's five shapes "
-                 "(two launches each, one token), weighted by launches per shape: 1.034 x algorithmic bytes")
+                 "(two launches each), weighted by launches per shape: {r} x algorithmic bytes at {n} token(s)")
 
 
 def product_groups(stack):
@@ -314,7 +314,7 @@ def time_dominant_kernel(stack, stream, reps=3):
     return out
 
 
-def roofline_entry(dk, peak, peak_kind, ms_per_step):
+def roofline_entry(dk, peak, peak_kind, ms_per_step, tokens=1):
     launches = sum(v[0] for v in dk.values())
     nbytes = sum(v[1] for v in dk.values())
     secs = sum(v[2] for v in dk.values())
@@ -323,8 +323,8 @@ def roofline_entry(dk, peak, peak_kind, ms_per_step):
     return {
         "bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
         "frac": round(achieved / peak, 4),
-        "traffic": round(TRAFFIC_PER_BYTE * per_launch) if TRAFFIC_PER_BYTE else None,
-        "traffic_basis": TRAFFIC_BASIS,
+        "traffic": round(TRAFFIC_PER_BYTE[tokens] * per_launch) if tokens in TRAFFIC_PER_BYTE else None,
+        "traffic_basis": TRAFFIC_BASIS.format(r=TRAFFIC_PER_BYTE[tokens], n=tokens) if tokens in TRAFFIC_PER_BYTE else None,
         "kernel": "NVFP4 weight-stream product kernel (gemv_tma_kernel): one launch per product of the step "
                   "(a layer's q, k, v as one; its gate and up as one), launched back to back in CUDA graphs by "
                   "type, activations prepared beforehand",
@@ -471,7 +471,7 @@ def run_gpu(args):
                                     "d2h_bytes_per_step": out_host.numel() * 4}},
             "gpu_launches": stack1.kernel_count * args.steps,
             "roofline": roofline_entry(dk1, peak, peak_kind, t_max * 1e3),
-            "roofline_n8": roofline_entry(dk8, peak, peak_kind, t_step8 * 1e3),
+            "roofline_n8": roofline_entry(dk8, peak, peak_kind, t_step8 * 1e3, tokens=8),
             "clocks": clk,
             "cpu_baseline": cpu,
         }
