@@ -126,6 +126,8 @@ struct MoeRoute {
   int* slot_expert;        // out [max_slots]
   float* cw;               // out [max_slots][N] combine weights
   uint32_t* status;        // out [1]: bit 4 set if an id was out of range
+  int* tok_slots;          // optional out [N][topk]: each token's routed slots in ascending order
+                           // (-1 for an id out of range), so that a combine reads only them
   uint32_t* ready;         // optional: set to 1 (release) once the table is written; the routing
                            // then runs without waiting for the kernels before (it reads only
                            // ids and weights), so the experts' kernels can read the table early
@@ -208,6 +210,10 @@ struct PrepParams {
   const float* comb_cw;
   const int* comb_n_slots;
   int comb_max_slots;      // the layer's most slots (the arrays' extent)
+  // optional: each token's routed slots, ascending (MoeRoute::tok_slots); the
+  // combine then reads the shared slot and these only, in slot order
+  const int* comb_tok_slots;
+  int comb_topk, comb_has_shared;
   // optional: one extra CTA computes an MoE layer's slot table (one-CTA rows only)
   int has_route;
   MoeRoute route;

@@ -48,6 +48,19 @@ static BWS_DEV void moe_route_body(const MoeRoute& m) {
   __syncthreads();   // cw zeroing above is complete
   // ids are distinct per token, so each (slot, token) cell gets one weight
   if (i < n && ids[i] >= 0) m.cw[slot * m.N + i / m.topk] = m.route_w[i];
+  if (m.tok_slots != nullptr && i < n) {
+    // the token's slots in ascending order (slot order is id order); ids out
+    // of range after the valid ones, as -1
+    const int t0 = (i / m.topk) * m.topk;
+    int pos = 0;
+    if (ids[i] >= 0) {
+      for (int j = t0; j < t0 + m.topk; ++j) pos += (ids[j] >= 0 && ids[j] < ids[i]) ? 1 : 0;
+    } else {
+      for (int j = t0; j < t0 + m.topk; ++j) pos += ids[j] >= 0 ? 1 : 0;
+      for (int j = t0; j < i; ++j) pos += ids[j] < 0 ? 1 : 0;
+    }
+    m.tok_slots[t0 + pos] = ids[i] >= 0 ? slot : -1;
+  }
   if (m.has_shared && i < m.N) m.cw[i] = 1.0f;
   if (m.ready != nullptr) {   // the table is complete: raise the flag (cumulative over the barrier)
     __syncthreads();

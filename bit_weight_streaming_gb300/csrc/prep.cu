@@ -126,9 +126,43 @@ __device__ __noinline__ void combine_chunk(const PrepParams& q, int tok, int c, 
   // layer's maximum is in bounds); slots past the count or with weight 0 (a
   // slot the token does not use, whose outputs may be stale) are then
   // skipped, the rest added in slot order
-  const int ns = __ldg(q.comb_n_slots);
   float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
   constexpr int kB = 9;
+  if (q.comb_tok_slots != nullptr && q.comb_max_slots > kB) {
+    // more slots than one batch (several tokens): the token's own slots, the
+    // shared one, then its routed ones ascending (at most 1 + 8 = kB), their
+    // weights and outputs loaded together; the slots it does not use have
+    // weight 0, so the sum equals the one over every live slot in slot order.
+    // (With one batch of slots in all, the loads below need no slot list.)
+    const int nk = q.comb_has_shared + q.comb_topk;
+    float wt[kB];
+    float4 ya[kB], yb[kB];
+    int live[kB];
+#pragma unroll
+    for (int k = 0; k < kB; ++k) {
+      int sl = -1;
+      if (k < nk) sl = (q.comb_has_shared && k == 0) ? 0 : __ldg(q.comb_tok_slots + tok * q.comb_topk + k - q.comb_has_shared);
+      live[k] = sl >= 0;
+      const int s2 = sl >= 0 ? sl : 0;
+      wt[k] = __ldg(q.comb_cw + s2 * q.N + tok);
+      const float4* yp = reinterpret_cast<const float4*>(q.comb_ys + ((size_t)s2 * q.N + tok) * q.d_in) + 2 * c;
+      ya[k] = __ldg(yp);
+      yb[k] = __ldg(yp + 1);
+    }
+#pragma unroll
+    for (int k = 0; k < kB; ++k) {
+      if (!live[k] || wt[k] == 0.0f) continue;
+      const float y8[8] = {ya[k].x, ya[k].y, ya[k].z, ya[k].w, yb[k].x, yb[k].y, yb[k].z, yb[k].w};
+#pragma unroll
+      for (int i = 0; i < 8; ++i) acc[i] = __fmaf_rn(wt[k], y8[i], acc[i]);
+    }
+#pragma unroll
+    for (int i = 0; i < 8; ++i) v[i] = __fadd_rn(v[i], acc[i]);
+    reinterpret_cast<float4*>(rr)[2 * c] = make_float4(v[0], v[1], v[2], v[3]);
+    reinterpret_cast<float4*>(rr)[2 * c + 1] = make_float4(v[4], v[5], v[6], v[7]);
+    return;
+  }
+  const int ns = __ldg(q.comb_n_slots);
   for (int s0 = 0; s0 < q.comb_max_slots; s0 += kB) {
     float wt[kB];
     float4 ya[kB], yb[kB];

@@ -190,6 +190,9 @@ cudaError_t prep(const Ctx& c, int mode, const uint16_t* x, int ld, const uint16
     q.comb_cw = comb->route.cw;
     q.comb_n_slots = comb->route.n_slots;
     q.comb_max_slots = comb->route.max_slots;
+    q.comb_tok_slots = comb->route.tok_slots;
+    q.comb_topk = comb->route.topk;
+    q.comb_has_shared = comb->route.has_shared;
   }
   if (route != nullptr) {
     q.has_route = 1;
@@ -346,6 +349,8 @@ int enqueue_step(const bws_stack_plan* P, const uint16_t* x0, float* logits, con
         v.route.n_slots = reinterpret_cast<int*>(rt);
         v.route.slot_expert = reinterpret_cast<int*>(rt + 256);
         v.route.cw = reinterpret_cast<float*>(rt + 256 + align256(sizeof(int) * (size_t)v.route.max_slots));
+        v.route.tok_slots = reinterpret_cast<int*>(reinterpret_cast<char*>(v.route.cw) +
+                                                   align256(sizeof(float) * (size_t)v.route.max_slots * P->N));
         v.route.ready = reinterpret_cast<uint32_t*>(c.w + P->off_ready) + moe_i;
       }
       if (L.router == nullptr) {   // ids known before the layer: routed by an extra CTA of the prep
@@ -529,7 +534,8 @@ int bws_decode_step_plan_create(const bws_stack* S, int N, bws_stack_plan** plan
       const size_t b = moe_workspace_bytes(&L.moe, N, L.topk);
       moe_bytes = b > moe_bytes ? b : moe_bytes;
       const size_t slots = (size_t)N * L.topk + (L.moe.shared_gate_up_codes != nullptr ? 1 : 0);
-      const size_t rb = 256 + align256(sizeof(int) * slots) + align256(sizeof(float) * slots * N);
+      const size_t rb = 256 + align256(sizeof(int) * slots) + align256(sizeof(float) * slots * N) +
+                        align256(sizeof(int) * (size_t)N * L.topk);
       route_bytes = rb > route_bytes ? rb : route_bytes;
       ++P->n_moe;
       P->kernels += 4;
