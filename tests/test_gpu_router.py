@@ -88,3 +88,21 @@ def test_router_tie_picks_the_lower_id():
     torch.cuda.synchronize()
     assert ids1.cpu().tolist() == [[3], [3]] and w1.cpu().tolist() == [[1.0], [1.0]]
     assert ids2.cpu().tolist() == [[3, 7], [3, 7]] and w2.cpu().tolist() == [[0.5, 0.5], [0.5, 0.5]]
+
+
+def test_router_near_ties_are_acceptable():
+    # experts whose rows differ by one BF16 ulp in a single weight: their
+    # logits lie within each other's bounds, so either may be chosen, and the
+    # choice must still pass the acceptance rule with its weights in range
+    m = bws()
+    E, d, N = 64, 1024, 4
+    W = _router(E, d, seed=21)
+    x = synth.activation_bf16(N, d, seed=22, device=device()).abs()
+    base = torch.full((d,), 0.0625, dtype=torch.bfloat16, device=device())
+    for e in (5, 9, 40):
+        W[e] = base
+    W[9, 0] = torch.tensor(0.0625 + 2.0 ** -11, dtype=torch.bfloat16)   # one BF16 ulp above 2^-4
+    ids, w, z = m.moe_router_topk(W, x, 2, logits=True)
+    torch.cuda.synchronize()
+    _check(W, x, ids, w, z)
+    assert set(ids[:, 0].cpu().tolist()) <= {5, 9, 40}

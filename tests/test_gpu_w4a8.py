@@ -78,6 +78,8 @@ def test_w4a8_product(d_out, d_in, N):
     m = bws()
     c, s, cd, sd = _mxfp4(d_out, d_in, seed=d_out + N)
     x = synth.activation_bf16(N, d_in, seed=d_in + N, device=device())
+    x[0, 32:64] = 0.0                     # a zero activation block (scale code 0)
+    x[-1, 64:96] *= 2.0 ** -60            # a tiny block
     y = m.mxfp4_w4a8_gemv(cd, sd, x)
     torch.cuda.synchronize()
     _check_product(c, s, cd, sd, x, y)
