@@ -204,7 +204,7 @@ def test_dense_stages_every_row(N):
     rep.assert_ok(expect=("rmsnorm", "mixer_in", "mixer_out", "swiglu", "down", "head"))
 
 
-@pytest.mark.parametrize("N", [1, 4])
+@pytest.mark.parametrize("N", [1, 4, 8])
 def test_moe_stages_every_row(N):
     from bit_weight_streaming_gb300 import workloads as W
     m = bws()
@@ -221,7 +221,7 @@ def test_moe_stages_every_row(N):
     rep.assert_ok(expect=("slot_table", "rmsnorm", "swiglu", "expert_down", "combine", "down", "head"))
 
 
-@pytest.mark.parametrize("N", [1, 4])
+@pytest.mark.parametrize("N", [1, 4, 8])
 def test_routed_moe_stages_every_row(N):
     # the MoE layers route themselves: a BF16 router per layer, the step
     # writing the chosen ids and weights that the experts then use
