@@ -707,6 +707,28 @@ def run_w4a8_only(args):
                       "us_per_call": round(t * 1e6, 2), "GB/s": round(nb / t / 1e9, 1)}), flush=True)
 
 
+def run_dense_only(args):
+    """The 27B-shape dense step alone at --tokens N (a workload for profiler
+    launch lists): one JSON line with its timing."""
+    import torch
+    import __graft_entry__ as g
+    g.build()
+    from bit_weight_streaming_gb300 import workloads as W
+    import synth
+    dev = torch.device("cuda", 0)
+    stream = torch.cuda.Stream(dev)
+    with torch.cuda.stream(stream):
+        st = W.dense_27b(args.tokens, seed=args.seed, device=dev)
+    stream.synchronize()
+    x = synth.activation_bf16(args.tokens, st.hidden, seed=args.seed, device=dev)
+    lg = torch.empty((args.tokens, st.head.d_out), dtype=torch.float32, device=dev)
+    with torch.cuda.stream(stream):
+        t = time_steps(lambda: st.step(x, lg), args.steps, args.warmup, stream)
+    nbytes = st.weight_bytes()
+    print(json.dumps({"dense_only": {f"n{args.tokens}": {"value": round(nbytes / t / 1e9, 2), "unit": UNIT,
+                                                         "us_per_step": round(t * 1e6, 1)}}}), flush=True)
+
+
 def run_moe_only(args):
     """The MoE step alone at --tokens N (a short workload for profiler launch
     lists): one JSON line with its timing."""
@@ -729,6 +751,7 @@ def main(argv=None):
     ap.add_argument("--no-moe", action="store_true")
     ap.add_argument("--product", default=None, help="ROWSxCOLS: time one NVFP4 product only (profiling)")
     ap.add_argument("--moe-only", action="store_true", help="time the MoE step alone at --tokens N (profiling)")
+    ap.add_argument("--dense-only", action="store_true", help="time the dense step alone at --tokens N (profiling)")
     ap.add_argument("--w4a8", default=None, help="ROWSxCOLS: time one W4A8 product only (profiling)")
     ap.add_argument("--tokens", type=int, default=1)
     ap.add_argument("--router", action="store_true", help="--moe-only: MoE layers routed inside the step")
@@ -742,6 +765,8 @@ def main(argv=None):
         run_w4a8_only(args)
     elif args.moe_only:
         run_moe_only(args)
+    elif args.dense_only:
+        run_dense_only(args)
     elif args.impl == "reference":
         run_reference(args)
     else:
