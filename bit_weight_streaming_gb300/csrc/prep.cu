@@ -631,6 +631,13 @@ cudaError_t launch_prep(const PrepParams& q, cudaStream_t st, bool pdl) {
     return moe ? cudaLaunchKernelEx(&cfg, prep_kernel<8, 256, true>, q)
                : cudaLaunchKernelEx(&cfg, prep_kernel<8, 256, false>, q);
   if (moe) return cudaLaunchKernelEx(&cfg, prep_kernel<1, 512, true>, q);
+  // the rows of an MoE layer's expert slots (768 values): one 256-thread CTA
+  // each, whose reductions are cheaper (measured, MoE step at four tokens
+  // 2.288 -> 2.263 ms, one token 1.290 -> 1.287 ms)
+  if (q.n_slots != nullptr && q.d_in_pad <= 2048) {
+    cfg.blockDim = dim3(256);
+    return cudaLaunchKernelEx(&cfg, prep_kernel<1, 256, false>, q);
+  }
   return cudaLaunchKernelEx(&cfg, prep_kernel<1, 1024, false>, q);
 }
 
