@@ -741,6 +741,141 @@ def run_moe_only(args):
     print(json.dumps({"moe_only": out}), flush=True)
 
 
+# ---- opt-in timestamp trace of one step (profiling aid) ---------------------
+#
+# With --trace dense|moe the library is rebuilt with -DBWS_TRACE: every CTA of
+# the product, MoE expert and prep kernels records global-timer readings
+# (kernel start, its waits returning, first stage, loop done, end; for preps:
+# wait, loads done, statistics, stores, end). One step is recorded after
+# warm-up and summarised per product boundary. Timing runs never use this
+# build (the build script rebuilds when the flags change).
+
+TRACE_DTYPE = [("kind", "<u8"), ("cta", "<u8"), ("t", "<u8", (6,))]
+
+
+def trace_read(lib):
+    import ctypes as C
+    import numpy as np
+    cap = 1 << 17
+    buf = np.zeros(cap, dtype=np.dtype(TRACE_DTYPE))
+    out = []
+    for fn in ("bws_trace_read_tma", "bws_trace_read_prep", "bws_trace_read_moe"):
+        f = getattr(lib, fn)
+        f.restype = C.c_int
+        n = f(C.c_void_p(buf.ctypes.data), cap)
+        if n < 0:
+            raise RuntimeError(f"{fn} failed")
+        out.append(buf[:n].copy())
+    return np.concatenate(out)
+
+
+def trace_launches(rec):
+    """The step's launches in start order: (kind, record indices), a new
+    launch wherever the kernel kind changes (consecutive launches of the
+    step's chain always differ in kind)."""
+    import numpy as np
+    t0 = rec["t"][:, 0]
+    order = np.argsort(t0, kind="stable")
+    segs, cur, ck = [], [], None
+    for i in order:
+        k = int(rec["kind"][i])
+        if ck is not None and k != ck:
+            segs.append((ck, np.array(cur)))
+            cur = []
+        cur.append(i)
+        ck = k
+    if cur:
+        segs.append((ck, np.array(cur)))
+    return segs
+
+
+def trace_summary_dense(rec):
+    """Per product kind (kind 1000 + 100 fmt + 10 epilogue + deposit), the
+    average microseconds of each piece of a product and the boundary after it."""
+    import numpy as np
+    t = rec["t"].astype(np.int64)
+    segs = trace_launches(rec)
+    P = [s for s in segs if s[0] // 1000 == 1]
+    Q = [s for s in segs if s[0] // 1000 in (2, 3)]
+    med = lambda a: float(np.median(a))
+    names = ["wait->first stage", "stream (median CTA)", "CTA spread", "last CTA -> prep wait", "prep loads",
+             "prep statistics barrier", "prep bands and stores", "prep end -> next wait", "next wait -> first stage"]
+    agg = {}
+    for k in range(min(len(P) - 1, len(Q) - 1)):
+        (pk, p), (_, q), (_, pn) = P[k], Q[k + 1], P[k + 1]
+        v = [med(t[p, 3]) - med(t[p, 2]), med(t[p, 4]) - med(t[p, 3]), t[p, 4].max() - med(t[p, 4]),
+             t[q, 1].min() - t[p, 5].max(), t[q, 2].max() - t[q, 1].min(), t[q, 3].max() - t[q, 2].max(),
+             t[q, 4].max() - t[q, 3].max(), med(t[pn, 2]) - t[q, 5].max(), med(t[pn, 3]) - med(t[pn, 2])]
+        agg.setdefault(pk, []).append(v)
+    out = {}
+    for pk, v in agg.items():
+        a = np.mean(np.array(v), axis=0) / 1e3
+        out[str(pk)] = {"launches": len(v), **{n: round(float(x), 2) for n, x in zip(names, a)}}
+    span = (t[:, 5].max() - t[:, 0].min()) / 1e3
+    return {"span_us": round(float(span), 1), "by_product_kind_us": out}
+
+
+def trace_summary_moe(rec):
+    """Per MoE layer (prep 3100 + CL, gate/up 403x, h prep 3001, down 401x),
+    the average microseconds of each kernel's pieces and the hops between."""
+    import numpy as np
+    t = rec["t"].astype(np.int64)
+    segs = trace_launches(rec)
+    med = lambda a: float(np.median(a))
+    names = ["prev end -> prep wait", "MoE prep", "-> gate/up wait", "gate/up wait -> first stage",
+             "gate/up stream (median CTA)", "gate/up CTA spread", "-> h prep wait", "h prep",
+             "-> down wait", "down wait -> first stage", "down stream (median CTA)", "down CTA spread",
+             "-> next prep wait", "layer"]
+    rows = []
+    for i in range(1, len(segs) - 4):
+        ks = [segs[i + j][0] for j in range(5)]
+        if not (ks[0] // 100 == 31 and ks[1] // 10 == 403 and ks[2] == 3001 and ks[3] // 10 == 401
+                and ks[4] // 100 == 31):
+            continue
+        pv, p, g, h, d, p2 = (segs[i + j][1] for j in range(-1, 5))
+        rows.append([t[p, 1].min() - t[pv, 5].max(), t[p, 5].max() - t[p, 1].min(),
+                     med(t[g, 2]) - t[p, 5].max(), med(t[g, 3]) - med(t[g, 2]), med(t[g, 4]) - med(t[g, 3]),
+                     t[g, 4].max() - med(t[g, 4]), t[h, 1].min() - t[g, 5].max(), t[h, 5].max() - t[h, 1].min(),
+                     med(t[d, 2]) - t[h, 5].max(), med(t[d, 3]) - med(t[d, 2]), med(t[d, 4]) - med(t[d, 3]),
+                     t[d, 4].max() - med(t[d, 4]), t[p2, 1].min() - t[d, 5].max(), t[p2, 0].min() - t[p, 0].min()])
+    a = np.mean(np.array(rows), axis=0) / 1e3 if rows else []
+    span = (t[:, 5].max() - t[:, 0].min()) / 1e3
+    return {"span_us": round(float(span), 1), "moe_layers": len(rows),
+            "per_layer_us": {n: round(float(x), 2) for n, x in zip(names, a)}}
+
+
+def run_trace(args):
+    """One step of the dense (--trace dense) or MoE (--trace moe) stack at
+    --tokens N, recorded with the opt-in timestamp trace."""
+    os.environ["BWS_NVCC_FLAGS"] = (os.environ.get("BWS_NVCC_FLAGS", "") + " -DBWS_TRACE").strip()
+    import torch
+    import __graft_entry__ as g
+    g.build()
+    from bit_weight_streaming_gb300._lib import lib
+    from bit_weight_streaming_gb300 import workloads as W
+    import synth
+    L = lib()
+    dev = torch.device("cuda", 0)
+    stream = torch.cuda.Stream(dev)
+    N = args.tokens
+    with torch.cuda.stream(stream):
+        st = W.dense_27b(N, seed=args.seed, device=dev) if args.trace == "dense" else \
+            W.moe_ling(N, seed=args.seed, device=dev)
+    stream.synchronize()
+    x = synth.activation_bf16(N, st.hidden, seed=args.seed, device=dev)
+    lg = torch.empty((N, st.head.d_out), dtype=torch.float32, device=dev)
+    with torch.cuda.stream(stream):
+        for _ in range(max(args.warmup, 3)):
+            st.step(x, lg)
+        stream.synchronize()
+        trace_read(L)            # drop the warm-up steps' records
+        st.step(x, lg)
+        stream.synchronize()
+    rec = trace_read(L)
+    summ = trace_summary_dense(rec) if args.trace == "dense" else trace_summary_moe(rec)
+    print(json.dumps({"trace": args.trace, "tokens": N, "records": int(len(rec)), **summ}), flush=True)
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
@@ -754,12 +889,16 @@ def main(argv=None):
     ap.add_argument("--dense-only", action="store_true", help="time the dense step alone at --tokens N (profiling)")
     ap.add_argument("--w4a8", default=None, help="ROWSxCOLS: time one W4A8 product only (profiling)")
     ap.add_argument("--tokens", type=int, default=1)
+    ap.add_argument("--trace", choices=["dense", "moe"], default=None,
+                    help="record one step of the dense or MoE stack with the opt-in timestamp trace (profiling)")
     ap.add_argument("--router", action="store_true", help="--moe-only: MoE layers routed inside the step")
     ap.add_argument("--copies", type=int, default=4, help="--product: distinct weight copies to rotate")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         args.warmup = 3
-    if args.product:
+    if args.trace:
+        run_trace(args)
+    elif args.product:
         run_product_only(args)
     elif args.w4a8:
         run_w4a8_only(args)

@@ -15,8 +15,11 @@ CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libbws.so")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
-FLAGS = ["-std=c++17", "-O3", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", "-O2",
-         "-I", os.path.join(ROOT, "include")] + os.environ.get("BWS_NVCC_FLAGS", "").split()
+def _flags():
+    """nvcc flags of every translation unit; BWS_NVCC_FLAGS adds to them (read
+    at each build, e.g. -DBWS_TRACE for the opt-in timestamp trace)."""
+    return (["-std=c++17", "-O3", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", "-O2",
+             "-I", os.path.join(ROOT, "include")] + os.environ.get("BWS_NVCC_FLAGS", "").split())
 
 
 def _nvcc():
@@ -40,6 +43,12 @@ def _stale(out, deps):
 def build(verbose=False, force=False):
     nvcc = _nvcc()
     os.makedirs(BUILD, exist_ok=True)
+    # objects built with other flags (e.g. the opt-in -DBWS_TRACE) are rebuilt
+    stamp = os.path.join(BUILD, "flags.txt")
+    FLAGS = _flags()
+    flags = " ".join(ARCH + FLAGS)
+    if not os.path.exists(stamp) or open(stamp).read() != flags:
+        force = True
     headers = [os.path.join(CSRC, f) for f in os.listdir(CSRC) if f.endswith((".h", ".cuh"))]
     headers.append(os.path.join(ROOT, "include", "bws.h"))
     objs, jobs = [], []
@@ -62,6 +71,8 @@ def build(verbose=False, force=False):
         tmp = LIB + ".tmp"
         run([nvcc] + ARCH + ["-shared", "-o", tmp] + objs + ["-lcudart"])
         os.replace(tmp, LIB)
+        with open(stamp, "w") as f:
+            f.write(flags)
     return LIB
 
 

@@ -35,6 +35,7 @@
 #include "bws_common.cuh"
 #include "bws_internal.h"
 #include "stream_tile.cuh"
+#include "trace.cuh"
 
 namespace bws {
 
@@ -90,6 +91,9 @@ struct Tail {
   uint64_t empty[kMaxStages];
   unsigned long long akey[kMaxTokens];   // the CTA's best argmax keys
   uint32_t flag;
+#ifdef BWS_TRACE
+  unsigned long long tr[4];   // producer's wait returned, consumers' wait returned, first stage, loop done
+#endif
 };
 static_assert(offsetof(Tail, zero_x) % 128 == 0, "zero pieces must start on a 128-byte boundary");
 
@@ -245,6 +249,9 @@ BWS_DEV void consume(const TmaParams& p, Tail& T, uint32_t stage0, long long u0,
       if (lane == 0) atomicOr(p.status, kStatusTimeout);
       dead = true;
     }
+#ifdef BWS_TRACE
+    if (u == u0 && threadIdx.x == 0) T.tr[2] = trace_now();
+#endif
     const uint32_t base = stage0 + (uint32_t)s * p.stage_bytes;
     uint4 cw[4];
     uint32_t sc[4];
@@ -428,6 +435,9 @@ BWS_DEV void consume(const TmaParams& p, Tail& T, uint32_t stage0, long long u0,
       for (int st = 0; st < 2; ++st) store_sub<FMT, EPI>(p, cur_tile, b, st, g, t, v[st], none, xexp, ein, ak);
     }
   }
+#ifdef BWS_TRACE
+  if (threadIdx.x == 0) T.tr[3] = trace_now();
+#endif
   if (EPI == kEpiStoreF32 && p.amax_key != nullptr) {
     // the warp's best key per token (lanes of one t hold the same tokens), into the CTA's
 #pragma unroll
@@ -453,6 +463,9 @@ __device__ __noinline__ void consume_lo(const TmaParams& p, Tail& T, uint32_t st
 template <int FMT, int EPI, bool N1>
 __global__ void __launch_bounds__(kThreadsTma, 2) gemv_tma_kernel(const __grid_constant__ TmaParams p) {
   extern __shared__ __align__(16) uint8_t smem_raw[];
+#ifdef BWS_TRACE
+  const unsigned long long tr_start = trace_now();
+#endif
   // 128-byte swizzled TMA boxes need 1024-byte aligned destinations
   const uint32_t mis = smem_u32(smem_raw) & 1023u;
   uint8_t* sbase = smem_raw + ((1024u - mis) & 1023u);
@@ -518,6 +531,9 @@ __global__ void __launch_bounds__(kThreadsTma, 2) gemv_tma_kernel(const __grid_c
           if (++ks == p.nks) { ks = 0; ++tile; }
         }
         pdl_wait();
+#ifdef BWS_TRACE
+        T.tr[0] = trace_now();
+#endif
         tile = (int)(u0 / p.nks);
         ks = (int)(u0 % p.nks);
         for (int k = 0; k < n_ring; ++k) {
@@ -551,6 +567,9 @@ __global__ void __launch_bounds__(kThreadsTma, 2) gemv_tma_kernel(const __grid_c
 
   // ---- consumers ----
   pdl_wait();
+#ifdef BWS_TRACE
+  if (threadIdx.x == 0) T.tr[1] = trace_now();
+#endif
   uint32_t fl = 0u;
   for (int tok = 0; tok < p.N; ++tok) fl |= __ldg(p.x.flags + tok);
   if (fl & 1u)
@@ -562,6 +581,13 @@ __global__ void __launch_bounds__(kThreadsTma, 2) gemv_tma_kernel(const __grid_c
     named_bar_sync(1, kConsumerWarps * 32);
     if (threadIdx.x < p.N) atomicMax(p.amax_key + threadIdx.x, T.akey[threadIdx.x]);
   }
+#ifdef BWS_TRACE
+  named_bar_sync(1, kConsumerWarps * 32);
+  if (threadIdx.x == 0) {
+    const unsigned long long t[6] = {tr_start, T.tr[0], T.tr[1], T.tr[2], T.tr[3], trace_now()};
+    trace_put(1000u + 100u * FMT + 10u * EPI + (p.deposit ? 1u : 0u), t);
+  }
+#endif
 }
 
 template <int FMT, int EPI, bool N1>
@@ -729,3 +755,7 @@ cudaError_t launch_gemv_tma(int fmt, int epi, const GemvParams& g, uint32_t* sta
 }
 
 }  // namespace bws
+
+#ifdef BWS_TRACE
+extern "C" int bws_trace_read_tma(void* host, int cap) { return bws::trace_read(host, cap); }
+#endif

@@ -26,6 +26,7 @@
 #include "bws_common.cuh"
 #include "bws_internal.h"
 #include "stream_tile.cuh"
+#include "trace.cuh"
 
 namespace bws {
 
@@ -76,6 +77,9 @@ struct MoeTail {
   int slot_expert[kMaxTokens * kMaxTopk + 1];
   uint32_t flag;
   int n_slots;
+#ifdef BWS_TRACE
+  unsigned long long tr[4];   // table read, consumers' wait returned, first stage, loop done
+#endif
 };
 static_assert(offsetof(MoeTail, zero_x) % 128 == 0, "zero pieces must start on a 128-byte boundary");
 
@@ -243,6 +247,9 @@ BWS_DEV void consume_moe(const MoeTmaParams& p, MoeTail& T, uint32_t stage0, lon
       if (lane == 0) atomicOr(p.status, kStatusTimeoutMoe);
       dead = true;
     }
+#ifdef BWS_TRACE
+    if (u == u0 && threadIdx.x == 0) T.tr[2] = trace_now();
+#endif
     const uint32_t base = stage0 + (uint32_t)s * p.stage_bytes;
     uint4 cw[4];
     uint32_t sc = 0u;
@@ -372,6 +379,9 @@ BWS_DEV void consume_moe(const MoeTmaParams& p, MoeTail& T, uint32_t stage0, lon
       for (int st = 0; st < 2; ++st) store_moe<EPI>(p, cur_tile, b, st, g, t, v[st], none);
     }
   }
+#ifdef BWS_TRACE
+  if (threadIdx.x == 0) T.tr[3] = trace_now();
+#endif
 }
 
 template <int EPI, bool N1>
@@ -383,6 +393,9 @@ __device__ __noinline__ void consume_moe_lo(const MoeTmaParams& p, MoeTail& T, u
 template <int EPI, bool N1>
 __global__ void __launch_bounds__(kThreadsMoe, 2) gemv_tma_moe_kernel(const __grid_constant__ MoeTmaParams p) {
   extern __shared__ __align__(16) uint8_t smem_raw[];
+#ifdef BWS_TRACE
+  const unsigned long long tr_start = trace_now();
+#endif
   const uint32_t mis = smem_u32(smem_raw) & 1023u;
   uint8_t* sbase = smem_raw + ((1024u - mis) & 1023u);
   MoeTail& T = *reinterpret_cast<MoeTail*>(sbase + (size_t)p.n_stages * p.stage_bytes);
@@ -418,6 +431,9 @@ __global__ void __launch_bounds__(kThreadsMoe, 2) gemv_tma_moe_kernel(const __gr
   for (int i = threadIdx.x; i < p.max_slots; i += blockDim.x)
     T.slot_expert[i] = early ? __ldcg(p.slot_expert + i) : __ldg(p.slot_expert + i);
   __syncthreads();
+#ifdef BWS_TRACE
+  if (threadIdx.x == 0) T.tr[0] = trace_now();
+#endif
   // units dealt over G = min(CTAs, units) CTAs, so that every CTA that
   // shares a tile holds at least one unit of it; the rest have none
   const long long U = (long long)T.n_slots * p.tiles_per_slot * p.nks;
@@ -512,6 +528,9 @@ __global__ void __launch_bounds__(kThreadsMoe, 2) gemv_tma_moe_kernel(const __gr
 
   // ---- consumers ----
   if (early) pdl_wait();   // the activations are the previous kernel's output
+#ifdef BWS_TRACE
+  if (threadIdx.x == 0) T.tr[1] = trace_now();
+#endif
   // the lo band is needed if any activation row this CTA reads has one
   uint32_t fl = 0u;
   if (u0 < u1) {
@@ -524,6 +543,12 @@ __global__ void __launch_bounds__(kThreadsMoe, 2) gemv_tma_moe_kernel(const __gr
     consume_moe_lo<EPI, N1>(p, T, stage0, u0, u1, U, G, warp, lane);
   else
     consume_moe<EPI, false, N1>(p, T, stage0, u0, u1, U, G, warp, lane);
+#ifdef BWS_TRACE
+  if (threadIdx.x == 0) {
+    const unsigned long long t[6] = {tr_start, T.tr[0], T.tr[1], T.tr[2], T.tr[3], trace_now()};
+    trace_put(4000u + 10u * EPI + (early ? 1u : 0u), t);
+  }
+#endif
 }
 
 template <int EPI, bool N1>
@@ -636,3 +661,7 @@ cudaError_t launch_gemv_tma_moe(int epi, const GemvParams& g, uint32_t* status, 
 }
 
 }  // namespace bws
+
+#ifdef BWS_TRACE
+extern "C" int bws_trace_read_moe(void* host, int cap) { return bws::trace_read(host, cap); }
+#endif

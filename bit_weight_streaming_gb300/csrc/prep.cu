@@ -16,6 +16,7 @@
 #include "bws_internal.h"
 #include "moe_route.cuh"
 #include "stream_tile.cuh"
+#include "trace.cuh"
 
 namespace cg = cooperative_groups;
 
@@ -118,9 +119,13 @@ __device__ __forceinline__ void finish_chunk(const PrepParams& q, int tok, int e
 
 
 // The previous MoE layer's combine for chunk c of token tok, in slot order,
-// added to r (v: the chunk's residual values, updated). Out of line: its
-// registers stay out of the prep's main path.
+// added to the residual r, which it writes back (v: the updated chunk). The
+// residual is loaded here, in the same round of loads as the slots' outputs.
+// Out of line: its registers stay out of the prep's main path.
 __device__ __noinline__ void combine_chunk(const PrepParams& q, int tok, int c, float (&v)[8], float* rr) {
+  const float4 ra = reinterpret_cast<const float4*>(rr)[2 * c];
+  const float4 rb = reinterpret_cast<const float4*>(rr)[2 * c + 1];
+  const float r8[8] = {ra.x, ra.y, ra.z, ra.w, rb.x, rb.y, rb.z, rb.w};
   // the slot count, weights and outputs of nine slots at a time are loaded
   // together, whatever the slot count turns out to be (every slot up to the
   // layer's maximum is in bounds); slots past the count or with weight 0 (a
@@ -157,7 +162,7 @@ __device__ __noinline__ void combine_chunk(const PrepParams& q, int tok, int c, 
       for (int i = 0; i < 8; ++i) acc[i] = __fmaf_rn(wt[k], y8[i], acc[i]);
     }
 #pragma unroll
-    for (int i = 0; i < 8; ++i) v[i] = __fadd_rn(v[i], acc[i]);
+    for (int i = 0; i < 8; ++i) v[i] = __fadd_rn(r8[i], acc[i]);
     reinterpret_cast<float4*>(rr)[2 * c] = make_float4(v[0], v[1], v[2], v[3]);
     reinterpret_cast<float4*>(rr)[2 * c + 1] = make_float4(v[4], v[5], v[6], v[7]);
     return;
@@ -184,7 +189,7 @@ __device__ __noinline__ void combine_chunk(const PrepParams& q, int tok, int c, 
     }
   }
 #pragma unroll
-  for (int i = 0; i < 8; ++i) v[i] = __fadd_rn(v[i], acc[i]);
+  for (int i = 0; i < 8; ++i) v[i] = __fadd_rn(r8[i], acc[i]);
   reinterpret_cast<float4*>(rr)[2 * c] = make_float4(v[0], v[1], v[2], v[3]);
   reinterpret_cast<float4*>(rr)[2 * c + 1] = make_float4(v[4], v[5], v[6], v[7]);
 }
@@ -327,22 +332,30 @@ BWS_DEV int band_pos(int c, int interleave) {
 template <int CL, int THREADS, bool MOE>
 __device__ __forceinline__ void prep_body(const PrepParams& q) {
   constexpr bool FIN = false;
+#ifdef BWS_TRACE
+  unsigned long long tr[6] = {trace_now(), 0, 0, 0, 0, 0};
+#endif
   pdl_launch_dependents();
-  // the routing CTA: with a ready flag it reads only ids and weights, so it
-  // need not wait for the kernels before
-  const bool route = MOE && CL == 1 && q.has_route && blockIdx.x == gridDim.x - 1;
-  const bool early = route && q.route.ready != nullptr;
+  // the routing CTA, the last of the grid (with clusters, the last cluster
+  // holds it and CL - 1 CTAs that only pad the cluster): with a ready flag it
+  // reads only ids and weights, so it need not wait for the kernels before
+  const bool rcl = MOE && q.has_route && (int)blockIdx.x >= (int)gridDim.x - CL;
+  const bool route = rcl && blockIdx.x == gridDim.x - 1;
+  const bool early = rcl && q.route.ready != nullptr;
   if (early) {
-    route_cta(q.route);
+    if (route) route_cta(q.route);
     return;
   }
   pdl_wait();
+#ifdef BWS_TRACE
+  tr[1] = trace_now();
+#endif
   const int rank = CL == 1 ? 0 : (int)cg::this_cluster().block_rank();
-  const int zctas = gridDim.x - (MOE && q.has_route && q.route.ready != nullptr ? 1 : 0);
+  const int zctas = gridDim.x - (MOE && q.has_route && q.route.ready != nullptr ? CL : 0);
   for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < q.zero_words; i += zctas * blockDim.x)
     q.zero_ptr[i] = 0u;
-  if (route) {
-    route_cta(q.route);
+  if (rcl) {
+    if (route) route_cta(q.route);
     return;
   }
   const int row = blockIdx.x / CL;
@@ -397,11 +410,12 @@ __device__ __forceinline__ void prep_body(const PrepParams& q) {
         }
         reinterpret_cast<float4*>(rr)[2 * c] = make_float4(v[0], v[1], v[2], v[3]);
         reinterpret_cast<float4*>(rr)[2 * c + 1] = make_float4(v[4], v[5], v[6], v[7]);
+      } else if (MOE && q.comb_ys != nullptr) {
+        combine_chunk(q, tok, c, v, rr);
       } else {
         const float4 a = reinterpret_cast<const float4*>(rr)[2 * c];
         const float4 b = reinterpret_cast<const float4*>(rr)[2 * c + 1];
         v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w; v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
-        if (MOE && q.comb_ys != nullptr) combine_chunk(q, tok, c, v, rr);
       }
 #pragma unroll
       for (int i = 0; i < 8; ++i) {
@@ -419,7 +433,13 @@ __device__ __forceinline__ void prep_body(const PrepParams& q) {
         ma = fmaxf(ma, fmaxf(fabsf(bf16_bits_to_f32(w[i] & 0xFFFF)), fabsf(bf16_bits_to_f32(w[i] >> 16))));
     }
   }
+#ifdef BWS_TRACE
+  tr[2] = trace_now();
+#endif
   const float2 st = cluster_sum_max<CL, THREADS>(&xch, ss, ma, warp_part);
+#ifdef BWS_TRACE
+  tr[3] = trace_now();
+#endif
   float mx = st.y;
   if (q.mode == kPrepRmsNorm) {
     const float ms = __fdiv_rn(st.x, (float)q.d_in);
@@ -446,7 +466,16 @@ __device__ __forceinline__ void prep_body(const PrepParams& q) {
   const uint32_t wf = __reduce_or_sync(0xffffffffu, flags);
   if (wf != 0u && (threadIdx.x & 31) == 0) atomicOr(q.flags + slot * q.N + tok, wf);
   if (rank == 0 && threadIdx.x == 0) q.exp[slot * q.N + tok] = E;
+#ifdef BWS_TRACE
+  tr[4] = trace_now();
+#endif
   if (CL > 1) asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+#ifdef BWS_TRACE
+  if (threadIdx.x == 0) {
+    tr[5] = trace_now();
+    trace_put(3000u + (MOE ? 100u : 0u) + CL, tr);
+  }
+#endif
 }
 
 // The prep that finishes the previous product's rows (one slot; a cluster of
@@ -459,8 +488,14 @@ __device__ __forceinline__ void prep_body(const PrepParams& q) {
 template <int CL, int THREADS, int KB, bool RMS, bool SWI>
 __device__ __forceinline__ void prep_fin_body(const PrepParams& q) {
   constexpr int kW = THREADS / 32;
+#ifdef BWS_TRACE
+  unsigned long long tr[6] = {trace_now(), 0, 0, 0, 0, 0};
+#endif
   pdl_launch_dependents();
   pdl_wait();
+#ifdef BWS_TRACE
+  tr[1] = trace_now();
+#endif
   cg::cluster_group cl = cg::this_cluster();
   const int rank = (int)cl.block_rank();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -516,10 +551,16 @@ __device__ __forceinline__ void prep_fin_body(const PrepParams& q) {
   // the statistics: each warp's into rank 0's table, one cluster barrier,
   // then every warp adds the table in the same fixed order
   __shared__ float2 parts[CL * kW];
+#ifdef BWS_TRACE
+  tr[2] = trace_now();
+#endif
   ss = warp_sum(ss);
   ma = warp_max(ma);
   if (lane == 0) *cl.map_shared_rank(&parts[rank * kW + warp], 0) = make_float2(ss, ma);
   cl.sync();
+#ifdef BWS_TRACE
+  tr[3] = trace_now();
+#endif
   const float2* tab = cl.map_shared_rank(parts, 0);
   float ts = 0.0f, tm = 0.0f;
   for (int i = lane; i < CL * kW; i += 32) {
@@ -556,7 +597,16 @@ __device__ __forceinline__ void prep_fin_body(const PrepParams& q) {
   const uint32_t wf = __reduce_or_sync(0xffffffffu, flags);
   if (wf != 0u && lane == 0) atomicOr(q.flags + tok, wf);
   if (rank == 0 && threadIdx.x == 0) q.exp[tok] = E;
+#ifdef BWS_TRACE
+  tr[4] = trace_now();
+#endif
   asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+#ifdef BWS_TRACE
+  if (threadIdx.x == 0) {
+    tr[5] = trace_now();
+    trace_put(2000u + (RMS ? 10u : 0u) + (SWI ? 1u : 0u) + 100u * CL, tr);
+  }
+#endif
 }
 
 // The plain instantiations keep few registers, so that they fit beside
@@ -582,7 +632,7 @@ cudaError_t launch_prep(const PrepParams& q, cudaStream_t st, bool pdl) {
   const bool long_row = q.d_in_pad > kLongRow;
   const bool moe = q.has_route || q.comb_ys != nullptr;
   const bool fin = q.fin_partials != nullptr;
-  if (q.has_route && long_row) return cudaErrorInvalidValue;   // the routing CTA needs one-CTA rows
+  if (q.has_route && long_row) return cudaErrorInvalidValue;   // an MoE prep row is one cluster of 4
   // rows: one CTA of 1024 threads; 8192 on, a cluster of 8 x 256. Finishing
   // a product (one slot, no x0, status or combine): a chunk per thread, and
   // registers for a tile's slots in one batch of loads: a cluster of 4 x 256
@@ -595,10 +645,15 @@ cudaError_t launch_prep(const PrepParams& q, cudaStream_t st, bool pdl) {
         rms != (q.fin_epi == kEpiResidF32) || q.d_in_pad > 3 * kLongRow)
       return cudaErrorInvalidValue;
   }
-  const int cl = long_row ? 8 : (fin ? 4 : 1);
+  // An MoE layer's prep (the previous layer's combine, RMSNorm, the routing
+  // CTA): a cluster of 4 x 128, so that the combine's loads of every slot's
+  // outputs are spread over four SMs (measured, MoE step at one token 1.266
+  // -> 1.250 ms; four tokens unchanged); the routing CTA is the last of one
+  // more cluster, whose other CTAs return at once.
+  const int cl = long_row ? 8 : (fin || moe ? 4 : 1);
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((unsigned)(slots * q.N * cl + (q.has_route ? 1 : 0)));
-  cfg.blockDim = dim3(long_row ? (fin ? 384 : 256) : (fin ? 256 : (moe ? 512 : 1024)));
+  cfg.gridDim = dim3((unsigned)(slots * q.N * cl + (q.has_route ? cl : 0)));
+  cfg.blockDim = dim3(long_row ? (fin ? 384 : 256) : (fin ? 256 : (moe ? 128 : 1024)));
   cfg.stream = st;
   cudaLaunchAttribute a[2];
   int na = 0;
@@ -630,7 +685,7 @@ cudaError_t launch_prep(const PrepParams& q, cudaStream_t st, bool pdl) {
   if (long_row)
     return moe ? cudaLaunchKernelEx(&cfg, prep_kernel<8, 256, true>, q)
                : cudaLaunchKernelEx(&cfg, prep_kernel<8, 256, false>, q);
-  if (moe) return cudaLaunchKernelEx(&cfg, prep_kernel<1, 512, true>, q);
+  if (moe) return cudaLaunchKernelEx(&cfg, prep_kernel<4, 128, true>, q);
   // the rows of an MoE layer's expert slots (768 values): one 256-thread CTA
   // each, whose reductions are cheaper (measured, MoE step at four tokens
   // 2.288 -> 2.263 ms, one token 1.290 -> 1.287 ms)
@@ -642,3 +697,7 @@ cudaError_t launch_prep(const PrepParams& q, cudaStream_t st, bool pdl) {
 }
 
 }  // namespace bws
+
+#ifdef BWS_TRACE
+extern "C" int bws_trace_read_prep(void* host, int cap) { return bws::trace_read(host, cap); }
+#endif
