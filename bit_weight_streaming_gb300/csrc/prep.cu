@@ -369,6 +369,8 @@ __device__ __forceinline__ void prep_body(const PrepParams& q) {
   }
   __shared__ float2 warp_part[THREADS / 32];
   __shared__ float2 xch;     // this CTA's values in the cluster exchange
+  __shared__ uint32_t cta_flags;
+  if (threadIdx.x == 0) cta_flags = 0u;   // ordered before its use by the statistics' barriers
   // the row's band flags are OR-ed into global memory by the warps that find
   // any; the cluster barrier below orders this clearing store before them
   if (rank == 0 && threadIdx.x == 0) q.flags[slot * q.N + tok] = 0u;
@@ -463,8 +465,11 @@ __device__ __forceinline__ void prep_body(const PrepParams& q) {
     store_bands(w, E, hi4, lo4, band_pos(c, q.interleave), flags);
   }
   }
+  // the band flags: the warps' into the CTA's word, then one atomic per CTA
   const uint32_t wf = __reduce_or_sync(0xffffffffu, flags);
-  if (wf != 0u && (threadIdx.x & 31) == 0) atomicOr(q.flags + slot * q.N + tok, wf);
+  if (wf != 0u && (threadIdx.x & 31) == 0) atomicOr(&cta_flags, wf);
+  __syncthreads();
+  if (threadIdx.x == 0 && cta_flags != 0u) atomicOr(q.flags + slot * q.N + tok, cta_flags);
   if (rank == 0 && threadIdx.x == 0) q.exp[slot * q.N + tok] = E;
 #ifdef BWS_TRACE
   tr[4] = trace_now();
@@ -482,7 +487,8 @@ __device__ __forceinline__ void prep_body(const PrepParams& q) {
 // CL CTAs, one 8-value chunk per thread): RMS, the RMSNorm of r += y (the
 // product a residual update), else a copy of y (SWI: SiLU(g) * u). Each
 // thread keeps its chunk in registers from the statistics to the bands, and
-// the cluster's statistics meet in rank 0's shared memory in one barrier.
+// each warp's statistics are pushed into every CTA's table before one cluster
+// barrier, after which each CTA reads only its own shared memory.
 // KB: slots per batch of loads (a tile of the product's split has about
 // nks * CTAs / units + 1 slots).
 template <int CL, int THREADS, int KB, bool RMS, bool SWI>
@@ -548,30 +554,32 @@ __device__ __forceinline__ void prep_fin_body(const PrepParams& q) {
         ma = fmaxf(ma, fmaxf(fabsf(bf16_bits_to_f32(w[i] & 0xFFFF)), fabsf(bf16_bits_to_f32(w[i] >> 16))));
     }
   }
-  // the statistics: each warp's into rank 0's table, one cluster barrier,
-  // then every warp adds the table in the same fixed order
+  // the statistics: each warp's pushed into the table of every CTA of the
+  // cluster (remote stores, posted), one cluster barrier, then every warp adds
+  // its own CTA's table in the same fixed order
   __shared__ float2 parts[CL * kW];
+  __shared__ uint32_t cta_flags;
+  if (threadIdx.x == 0) cta_flags = 0u;
 #ifdef BWS_TRACE
   tr[2] = trace_now();
 #endif
   ss = warp_sum(ss);
   ma = warp_max(ma);
-  if (lane == 0) *cl.map_shared_rank(&parts[rank * kW + warp], 0) = make_float2(ss, ma);
+  if (lane < CL) *cl.map_shared_rank(&parts[rank * kW + warp], lane) = make_float2(ss, ma);
   cl.sync();
 #ifdef BWS_TRACE
   tr[3] = trace_now();
 #endif
-  const float2* tab = cl.map_shared_rank(parts, 0);
+  // every remote store into this CTA's table came before the barrier: from
+  // here on no CTA of the cluster touches another's shared memory
   float ts = 0.0f, tm = 0.0f;
   for (int i = lane; i < CL * kW; i += 32) {
-    const float2 o = tab[i];
+    const float2 o = parts[i];
     ts += o.x;
     tm = fmaxf(tm, o.y);
   }
   ts = warp_sum(ts);
   tm = warp_max(tm);
-  // done with rank 0's table; the wait at the end keeps rank 0 alive until all have read
-  asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
   float inv_rms = 1.0f, mx = tm;
   if (RMS) {
     inv_rms = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(__fdiv_rn(ts, (float)q.d_in), q.eps)));
@@ -594,13 +602,17 @@ __device__ __forceinline__ void prep_fin_body(const PrepParams& q) {
     uint4* lo4 = reinterpret_cast<uint4*>(q.lo + (size_t)tok * q.d_in_pad);
     store_bands(w, E, hi4, lo4, band_pos(c, q.interleave), flags);
   }
+  // the band flags: the warps' into the CTA's word, then one atomic per CTA
+  // (rows of small values set them in most warps; one global address for
+  // every warp of the cluster would serialise their atomics)
   const uint32_t wf = __reduce_or_sync(0xffffffffu, flags);
-  if (wf != 0u && lane == 0) atomicOr(q.flags + tok, wf);
+  if (wf != 0u && lane == 0) atomicOr(&cta_flags, wf);
+  __syncthreads();
+  if (threadIdx.x == 0 && cta_flags != 0u) atomicOr(q.flags + tok, cta_flags);
   if (rank == 0 && threadIdx.x == 0) q.exp[tok] = E;
 #ifdef BWS_TRACE
   tr[4] = trace_now();
 #endif
-  asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
 #ifdef BWS_TRACE
   if (threadIdx.x == 0) {
     tr[5] = trace_now();
