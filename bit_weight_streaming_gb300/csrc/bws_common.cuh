@@ -59,6 +59,12 @@ BWS_DEV uint32_t atom_add_acq_rel_gpu(uint32_t* p, uint32_t v) {
   asm volatile("atom.add.acq_rel.gpu.global.u32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
   return old;
 }
+// 32 bytes (eight floats, 32-byte aligned) through L2 in one request.
+BWS_DEV void ld_cg_f8(const float* p, float4& a, float4& b) {
+  asm volatile("ld.global.cg.v8.f32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+               : "=f"(a.x), "=f"(a.y), "=f"(a.z), "=f"(a.w), "=f"(b.x), "=f"(b.y), "=f"(b.z), "=f"(b.w)
+               : "l"(p));
+}
 BWS_DEV float4 ld_cg_f4(const float4* p) {
   float4 v;
   asm volatile("ld.global.cg.v4.f32 {%0,%1,%2,%3}, [%4];"

@@ -77,11 +77,16 @@ __device__ __forceinline__ void finish_chunk(const PrepParams& q, int tok, int e
     float4 o[kB][kV];
 #pragma unroll
     for (int k = 0; k < kB; ++k) {
-      const float4* base =
-          reinterpret_cast<const float4*>(q.fin_partials + ((size_t)(tile + cb + k) * q.N + tok) * 128 + rit);
+      // the chunk's 8 values (32 bytes) in one request; SwiGLU: gate, then up 64 rows on
+      const float* base = q.fin_partials + ((size_t)(tile + cb + k) * q.N + tok) * 128 + rit;
 #pragma unroll
-      for (int j = 0; j < kV; ++j)   // gate pieces at 0, 1; up pieces at 16, 17 (64 rows on)
-        o[k][j] = cb + k <= cc1 ? __ldcg(base + (j & 1) + 16 * (j >> 1)) : make_float4(0.f, 0.f, 0.f, 0.f);
+      for (int j = 0; j < kV; j += 2) {
+        if (cb + k <= cc1) {
+          ld_cg_f8(base + 64 * (j >> 1), o[k][j], o[k][j + 1]);
+        } else {
+          o[k][j] = o[k][j + 1] = make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+      }
     }
 #pragma unroll
     for (int k = 0; k < kB; ++k) {
@@ -528,8 +533,8 @@ __device__ __forceinline__ void prep_fin_body(const PrepParams& q) {
   float ss = 0.0f, ma = 0.0f;
   if (live) {
     if (RMS) {   // r += y
-      const float4 a = reinterpret_cast<const float4*>(rr)[2 * c];
-      const float4 b = reinterpret_cast<const float4*>(rr)[2 * c + 1];
+      float4 a, b;
+      ld_cg_f8(rr + 8 * c, a, b);
       float f[8];
       finish_chunk<false, KB>(q, tok, 8 * c, f);
       v[0] = __fadd_rn(a.x, f[0]); v[1] = __fadd_rn(a.y, f[1]); v[2] = __fadd_rn(a.z, f[2]);
