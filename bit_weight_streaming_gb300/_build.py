@@ -15,6 +15,8 @@ CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libbws.so")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
+
+
 def _flags():
     """nvcc flags of every translation unit; BWS_NVCC_FLAGS adds to them (read
     at each build, e.g. -DBWS_TRACE for the opt-in timestamp trace)."""

@@ -178,9 +178,6 @@ __host__ __device__ inline SlabPos slab_pos(int T, int K, int S, int c, int G) {
   return q;
 }
 
-// Position of k-unit kl in the CTA's slab.
-__host__ __device__ inline int slab_slot(const SlabPos& q, int kl) { return kl >= q.kl0 ? kl - q.kl0 : kl + q.nk - q.kl0; }
-
 // The deposit slots of tile t, in the order they are added: slabs in order,
 // each slab's CTAs in order. Returns their number (at most cap written).
 __host__ __device__ inline int tile_slots(int T, int K, int S, int G, long long stride, int t, int* out, int cap) {
