@@ -148,8 +148,9 @@ def test_nvfp4_requantize_is_identity(W_rand):
     w_hat = P.nvfp4_dequantize(codes, scales, s_t).astype(np.float32)
     # re-encode w_hat under the same scales: w_hat / d_b is the grid value
     d_b = (F.e4m3_decode(scales).astype(np.float32) * s_t).astype(np.float32)
-    ratio = (w_hat.reshape(96, 32, 16) / d_b[..., None]).astype(np.float32)
-    q2 = np.where((d_b > 0)[..., None], F.e2m1_encode(ratio), 0)
+    live = d_b > 0                                   # zero blocks: scale 0, codes 0
+    ratio = (w_hat.reshape(96, 32, 16) / np.where(live, d_b, 1)[..., None]).astype(np.float32)
+    q2 = np.where(live[..., None], F.e2m1_encode(ratio), 0)
     q1 = Q.unpack_nibbles(codes).reshape(96, 32, 16)
     same = (q1 & 7) == (q2 & 7)
     assert np.all(same)
