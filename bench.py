@@ -707,6 +707,31 @@ def run_w4a8_only(args):
                       "us_per_call": round(t * 1e6, 2), "GB/s": round(nb / t / 1e9, 1)}), flush=True)
 
 
+def run_moe_layer_only(args):
+    """Times repeated calls of one Ling-shape MoE layer (512 MXFP4 experts,
+    hidden 2560, inter 768, top-8 + shared; 1.6 GB on the device) through
+    bws_mxfp4_moe_gemv at --tokens N: a small workload for profiler captures
+    of the expert kernels."""
+    import torch
+    import __graft_entry__ as g
+    g.build()
+    import bit_weight_streaming_gb300 as bws
+    from bit_weight_streaming_gb300 import workloads as W
+    import synth
+    dev = torch.device("cuda", 0)
+    N, topk = args.tokens, 8
+    w = W.moe_weights(512, 2560, 768, args.seed, 2, True, device=dev)
+    ids = synth.expert_ids(N, topk, 512, seed=args.seed, layer=2).to(dev)
+    rw = synth.route_weights(N, topk, seed=args.seed, layer=2).to(dev)
+    x = synth.activation_bf16(N, 2560, seed=args.seed, device=dev)
+    y = torch.empty((N, 2560), dtype=torch.bfloat16, device=dev)
+    ws = bws.Workspace(dev)
+    stream = torch.cuda.current_stream(dev)
+    t = time_steps(lambda: bws.mxfp4_moe_gemv(w, ids, rw, x, y=y, ws=ws), args.steps, args.warmup, stream)
+    print(json.dumps({"moe_layer": "512 experts, 2560 x 768, top-8 + shared", "tokens": N,
+                      "us_per_call": round(t * 1e6, 2)}), flush=True)
+
+
 def run_dense_only(args):
     """The 27B-shape dense step alone at --tokens N (a workload for profiler
     launch lists): one JSON line with its timing."""
@@ -888,6 +913,8 @@ def main(argv=None):
     ap.add_argument("--moe-only", action="store_true", help="time the MoE step alone at --tokens N (profiling)")
     ap.add_argument("--dense-only", action="store_true", help="time the dense step alone at --tokens N (profiling)")
     ap.add_argument("--w4a8", default=None, help="ROWSxCOLS: time one W4A8 product only (profiling)")
+    ap.add_argument("--moe-layer", action="store_true",
+                    help="time one Ling-shape MoE layer call at --tokens N (profiling)")
     ap.add_argument("--tokens", type=int, default=1)
     ap.add_argument("--trace", choices=["dense", "moe"], default=None,
                     help="record one step of the dense or MoE stack with the opt-in timestamp trace (profiling)")
@@ -902,6 +929,8 @@ def main(argv=None):
         run_product_only(args)
     elif args.w4a8:
         run_w4a8_only(args)
+    elif args.moe_layer:
+        run_moe_layer_only(args)
     elif args.moe_only:
         run_moe_only(args)
     elif args.dense_only:
