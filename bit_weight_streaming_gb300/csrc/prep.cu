@@ -663,14 +663,19 @@ cudaError_t launch_prep(const PrepParams& q, cudaStream_t st, bool pdl) {
       return cudaErrorInvalidValue;
   }
   // An MoE layer's prep (the previous layer's combine, RMSNorm, the routing
-  // CTA): a cluster of 4 x 128, so that the combine's loads of every slot's
-  // outputs are spread over four SMs (measured, MoE step at one token 1.266
-  // -> 1.250 ms; four tokens unchanged); the routing CTA is the last of one
-  // more cluster, whose other CTAs return at once.
-  const int cl = long_row ? 8 : (fin || moe ? 4 : 1);
+  // CTA): a cluster per token row, so that the combine's loads of every
+  // slot's outputs are spread over several SMs; the routing CTA is the last
+  // of one more cluster, whose other CTAs return at once. Several tokens: 4
+  // x 128 (measured, MoE step at one token 1.266 -> 1.250 ms against one CTA
+  // of 512; four tokens unchanged). One token: 8 x 64, whose CTAs (126
+  // registers) also fit beside two expert-product CTAs on an SM, so that
+  // neither waits for the other (one token 1.258-1.274 -> 1.236 ms; at four
+  // tokens 2.267 -> 2.275 ms).
+  const bool moe8 = moe && !long_row && q.N == 1;
+  const int cl = long_row ? 8 : (moe8 ? 8 : (fin || moe ? 4 : 1));
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)(slots * q.N * cl + (q.has_route ? cl : 0)));
-  cfg.blockDim = dim3(long_row ? (fin ? 384 : 256) : (fin ? 256 : (moe ? 128 : 1024)));
+  cfg.blockDim = dim3(long_row ? (fin ? 384 : 256) : (fin ? 256 : (moe ? (moe8 ? 64 : 128) : 1024)));
   cfg.stream = st;
   cudaLaunchAttribute a[2];
   int na = 0;
@@ -702,6 +707,7 @@ cudaError_t launch_prep(const PrepParams& q, cudaStream_t st, bool pdl) {
   if (long_row)
     return moe ? cudaLaunchKernelEx(&cfg, prep_kernel<8, 256, true>, q)
                : cudaLaunchKernelEx(&cfg, prep_kernel<8, 256, false>, q);
+  if (moe8) return cudaLaunchKernelEx(&cfg, prep_kernel<8, 64, true>, q);
   if (moe) return cudaLaunchKernelEx(&cfg, prep_kernel<4, 128, true>, q);
   // the rows of an MoE layer's expert slots (768 values): one 256-thread CTA
   // each, whose reductions are cheaper (measured, MoE step at four tokens
