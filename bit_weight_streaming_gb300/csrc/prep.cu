@@ -667,11 +667,12 @@ cudaError_t launch_prep(const PrepParams& q, cudaStream_t st, bool pdl) {
   // slot's outputs are spread over several SMs; the routing CTA is the last
   // of one more cluster, whose other CTAs return at once. Several tokens: 4
   // x 128 (measured, MoE step at one token 1.266 -> 1.250 ms against one CTA
-  // of 512; four tokens unchanged). One token: 8 x 64, whose CTAs (126
-  // registers) also fit beside two expert-product CTAs on an SM, so that
-  // neither waits for the other (one token 1.258-1.274 -> 1.236 ms; at four
-  // tokens 2.267 -> 2.275 ms).
-  const bool moe8 = moe && !long_row && q.N == 1;
+  // of 512; four tokens unchanged). One token with its routing CTA: 8 x 64,
+  // whose CTAs (126 registers) also fit beside two expert-product CTAs on an
+  // SM, so that neither waits for the other (one token 1.254-1.274 ->
+  // 1.236-1.250 ms; at four tokens 2.267 -> 2.275 ms; with a router kernel
+  // after the prep instead of the routing CTA 1.749 -> 1.778 ms, so not there).
+  const bool moe8 = moe && !long_row && q.N == 1 && q.has_route;
   const int cl = long_row ? 8 : (moe8 ? 8 : (fin || moe ? 4 : 1));
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)(slots * q.N * cl + (q.has_route ? cl : 0)));
